@@ -1,0 +1,449 @@
+"""LOCKS oracle: a plain, slow float64 CPU statement of the LOCKS decode path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports, calls or links
+this module: only the tests, `__graft_entry__.smoke()` and `bench.py`'s CPU
+baseline / reference arm use it.  It shares no code with the CUDA library and
+never imports it.
+
+Sources (cited by page title and section, equation or algorithm):
+  [notes]  "LOCKS 阅读笔记：为什么 KV Cache 摘要要按「页」而不是按「序列」或
+           「全局」来建" (Zhongzhu Zhou, zhongzhuzhou.org, 2026-07-29):
+           §3.1 Eq.(1); §4.1 Eq.(2), Eq.(3) and the "存储" (storage)
+           paragraph; §4.2 Eq.(4), Eq.(5) and the sink/recent rule;
+           §4.3 Algorithm 1; §4.4 Algorithm 2; §5 Eq.(6)-(7); §5.1 toy example.
+  [gist]   "Resumo Técnico: LOCKS – Sumários de Chaves Compactos por Página
+           para Decodificação Eficiente de Contexto Longo" (gist.science), §2.
+
+Readings where the pages are silent (each is listed in the design doc):
+  * quantiser: symmetric, fp16 scales (basis: one per column; coefficients:
+    one per row; centroid: one per page), scale = fp16_rn(fp32(absmax)/qmax),
+    code = clamp(rint_fp32(fp32(x)/fp32(scale)), -qmax, qmax), qmax = 7 for
+    int4 and 127 for int8; a zero scale gives zero codes; a scale that
+    overflows fp16 saturates to 65504.  The quantiser decides integers, so it
+    runs in the kernel's precision (fp32), on fp32 copies of the float64
+    basis/coefficients.
+  * the centroid that is quantised is the fp32 mean with the 16 tokens summed
+    in order 0..15, then scaled by 1/16 (the kernel's precision); centring for
+    the eigenproblem uses the exact float64 mean of Eq.(2).
+  * eigenpairs in descending order; each kept eigenvector u_k is signed so its
+    entry of largest magnitude is positive (lowest index on exact ties);
+    components with eigenvalue <= 1e-6 * lambda_1 (or lambda_1 == 0) are zeroed.
+  * page mass fractions are normalised over all summarised (full) pages of the
+    sequence, sink included; sink = logical page 0, recent = the page holding
+    the last token; ties in the share-average go to the lower page index.
+
+Pins (tests/test_oracle_pins.py): the §5.1 toy example in closed form, an SVD
+cross-check, orthonormal bases, exactness at r = rank, the Eckart-Young tail,
+Eq.(1) identity, Eq.(7) bound, brute-force top-k, k >= pages giving dense
+attention, and hand-written record fixtures.  Parity unpinned by the pages:
+the quantiser's scale dtype/granularity, rounding and sign rule are readings
+(pinned only by their own invariants and by hand-written byte fixtures).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+PAGE = 16
+HEAD_DIM = 128
+RANK = 8
+RECORD_BYTES = 832          # 818 B payload + 14 B zero padding
+OFF_V4, OFF_C8, OFF_MU8 = 0, 512, 640
+OFF_SV, OFF_SC, OFF_SMU = 768, 784, 816
+PAYLOAD_BYTES = 818
+ZERO_TOL = 1e-6
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+def logsumexp(x, axis=-1):
+    x = np.asarray(x, dtype=np.float64)
+    m = np.max(x, axis=axis, keepdims=True)
+    m = np.where(np.isfinite(m), m, 0.0)
+    with np.errstate(divide="ignore"):
+        out = np.log(np.sum(np.exp(x - m), axis=axis, keepdims=True)) + m
+    return np.squeeze(out, axis=axis)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """uint16 bf16 bit patterns -> float64 (exact)."""
+    u = bits.astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+# ----------------------------------------------------------------------------
+# Build: notes §4.1 Eq.(2)-(3), §4.3 Algorithm 1
+# ----------------------------------------------------------------------------
+def page_summary(keys: np.ndarray, r: int = RANK):
+    """Unquantised per-page summary of Algorithm 1 for keys [..., B, d].
+
+    Returns dict with
+      mu   [..., d]     page centroid (Eq.(2))
+      D    [..., B, d]  centred deviations delta_i = k_i - mu
+      lam  [..., B]     eigenvalues of D D^T, descending (Eq.(3)), >= 0
+      U    [..., B, B]  matching eigenvectors (columns), sign-canonicalised
+      V    [..., d, r]  basis V = D^T U_r Sigma_r^{-1}
+      C    [..., B, r]  coefficients C = U_r Sigma_r  (c_i = V^T delta_i)
+      tau  [...]        spectral tail sum_{k>r} sigma_k^2
+    """
+    K = np.asarray(keys, dtype=np.float64)
+    mu = K.mean(axis=-2)                                  # Eq.(2)
+    D = K - mu[..., None, :]                              # delta_i rows
+    gram = D @ np.swapaxes(D, -1, -2)                     # D D^T, B x B
+    lam, U = np.linalg.eigh(gram)                         # Eq.(3), ascending
+    lam = np.maximum(lam[..., ::-1], 0.0)
+    U = U[..., ::-1].copy()
+    # sign: entry of largest magnitude positive, lowest index on exact ties
+    piv = np.argmax(np.abs(U), axis=-2)                   # [..., B]
+    pv = np.take_along_axis(U, piv[..., None, :], axis=-2)[..., 0, :]
+    U = U * np.where(pv < 0, -1.0, 1.0)[..., None, :]
+    sigma = np.sqrt(lam)
+    lam1 = lam[..., :1]
+    keep = (lam[..., :r] > ZERO_TOL * lam1) & (lam1 > 0)  # [..., r]
+    Ur, sr = U[..., :r], sigma[..., :r]
+    safe = np.where(keep, sr, 1.0)
+    V = (np.swapaxes(D, -1, -2) @ Ur) / safe[..., None, :]
+    V = np.where(keep[..., None, :], V, 0.0)
+    C = np.where(keep[..., None, :], Ur * sr[..., None, :], 0.0)
+    tau = lam[..., r:].sum(axis=-1)
+    return dict(mu=mu, D=D, lam=lam, U=U, V=V, C=C, tau=tau)
+
+
+def centroid_f32(keys_f32: np.ndarray) -> np.ndarray:
+    """fp32 mean with tokens summed in order 0..15 then scaled by 1/16."""
+    k = np.asarray(keys_f32, dtype=np.float32)
+    acc = np.zeros(k.shape[:-2] + k.shape[-1:], dtype=np.float32)
+    for t in range(k.shape[-2]):
+        acc = (acc + k[..., t, :]).astype(np.float32)
+    return (acc * np.float32(1.0 / k.shape[-2])).astype(np.float32)
+
+
+def _scale(absmax_f32: np.ndarray, qmax: int) -> np.ndarray:
+    s = (np.asarray(absmax_f32, np.float32) / np.float32(qmax)).astype(
+        np.float32)
+    with np.errstate(over="ignore"):
+        s16 = s.astype(np.float16)
+    return np.where(np.isinf(s16), np.float16(65504.0), s16).astype(np.float16)
+
+
+def _codes(x_f32: np.ndarray, s16: np.ndarray, qmax: int) -> np.ndarray:
+    s = s16.astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = (np.asarray(x_f32, np.float32) / s).astype(np.float32)
+    c = np.rint(y)
+    c = np.where(s == 0, 0.0, c)
+    return np.clip(c, -qmax, qmax).astype(np.int8)
+
+
+def quantize_summary(mu32, V32, C32):
+    """Storage paragraph of §4.1 / Algorithm 1: int4 basis with a per-column
+    scale, int8 coefficients with a per-row scale, int8 centroid."""
+    mu32 = np.asarray(mu32, np.float32)
+    V32 = np.asarray(V32, np.float32)
+    C32 = np.asarray(C32, np.float32)
+    smu = _scale(np.abs(mu32).max(axis=-1), 127)
+    mu8 = _codes(mu32, smu[..., None], 127)
+    sV = _scale(np.abs(V32).max(axis=-2), 7)
+    V4 = _codes(V32, sV[..., None, :], 7)
+    sC = _scale(np.abs(C32).max(axis=-1), 127)
+    C8 = _codes(C32, sC[..., :, None], 127)
+    return dict(V4=V4, C8=C8, mu8=mu8, sV=sV, sC=sC, smu=smu)
+
+
+def dequantize(q):
+    """(mu_hat [..., d], V_hat [..., d, r], C_hat [..., B, r]) in float64."""
+    mu = q["smu"].astype(np.float64)[..., None] * q["mu8"].astype(np.float64)
+    V = q["sV"].astype(np.float64)[..., None, :] * q["V4"].astype(np.float64)
+    C = q["sC"].astype(np.float64)[..., :, None] * q["C8"].astype(np.float64)
+    return mu, V, C
+
+
+def build_page(keys_bf16_as_f32: np.ndarray):
+    """Algorithm 1 for full pages, keys [..., 16, 128] holding bf16 values.
+
+    Returns (quantised summary dict, unquantised summary dict)."""
+    s = page_summary(keys_bf16_as_f32, RANK)
+    q = quantize_summary(centroid_f32(keys_bf16_as_f32),
+                         s["V"].astype(np.float32), s["C"].astype(np.float32))
+    return q, s
+
+
+# ----------------------------------------------------------------------------
+# Record layout (include/locks.h documents the same bytes)
+# ----------------------------------------------------------------------------
+def _v4_positions():
+    d = np.arange(HEAD_DIM)[:, None]
+    n = np.arange(RANK)[None, :]
+    c = (d % 8) // 2
+    e = d % 2
+    hi8 = (d % 16) // 8
+    s = d // 16
+    w, sp = s // 2, s % 2
+    word = (4 * n + c) * 4 + w                 # u32 word index 0..127
+    shift = 16 * e + 8 * sp + 4 * hi8
+    return np.broadcast_to(word, (HEAD_DIM, RANK)), \
+        np.broadcast_to(shift, (HEAD_DIM, RANK))
+
+
+def _c8_offsets():
+    i = np.arange(PAGE)[:, None]
+    k = np.arange(RANK)[None, :]
+    return OFF_C8 + 4 * (4 * (i % 8) + k // 2) + 2 * (i // 8) + k % 2
+
+
+def _mu8_offsets():
+    d = np.arange(HEAD_DIM)
+    o = d % 16
+    c = (o % 8) // 2
+    j = (o % 2) + 2 * (o // 8)
+    return OFF_MU8 + 32 * c + 4 * (d // 16) + j
+
+
+V4_WORD, V4_SHIFT = _v4_positions()
+V4_WORD_COLS = np.argsort(V4_WORD.reshape(-1), kind="stable").reshape(128, 8)
+C8_OFF = _c8_offsets()
+MU8_OFF = _mu8_offsets()
+
+
+def encode_records(q) -> np.ndarray:
+    """Quantised summaries [...] -> uint8 records [..., 832]."""
+    lead = q["mu8"].shape[:-1]
+    n = int(np.prod(lead)) if lead else 1
+    V4 = q["V4"].reshape(n, HEAD_DIM, RANK).astype(np.int64) & 0xF
+    flat_s = V4_SHIFT.reshape(-1).astype(np.uint64)
+    vals = V4.reshape(n, -1).astype(np.uint64) << flat_s[None, :]
+    # each u32 word gathers exactly 8 non-overlapping nibbles
+    words = vals[:, V4_WORD_COLS].sum(axis=-1)            # [n][128]
+    rec = np.zeros((n, RECORD_BYTES), dtype=np.uint8)
+    rec[:, OFF_V4:OFF_V4 + 512] = np.ascontiguousarray(
+        words.astype("<u4")).view(np.uint8).reshape(n, 512)
+    C8 = np.ascontiguousarray(q["C8"].reshape(n, PAGE, RANK)).view(np.uint8)
+    rec[:, C8_OFF.reshape(-1)] = C8.reshape(n, -1)
+    mu8 = np.ascontiguousarray(q["mu8"].reshape(n, HEAD_DIM)).view(np.uint8)
+    rec[:, MU8_OFF] = mu8
+    for off, key, cnt in ((OFF_SV, "sV", RANK), (OFF_SC, "sC", PAGE),
+                          (OFF_SMU, "smu", 1)):
+        f16 = np.ascontiguousarray(q[key].reshape(n, cnt).astype("<f2"))
+        rec[:, off:off + 2 * cnt] = f16.view(np.uint8).reshape(n, 2 * cnt)
+    return rec.reshape(lead + (RECORD_BYTES,))
+
+
+def decode_records(rec: np.ndarray):
+    """uint8 records [..., 832] -> quantised summary dict."""
+    rec = np.asarray(rec, dtype=np.uint8)
+    lead = rec.shape[:-1]
+    n = int(np.prod(lead)) if lead else 1
+    r = rec.reshape(n, RECORD_BYTES)
+    words = r[:, :512].copy().view("<u4").astype(np.int64)     # [n][128]
+    nib = (words[:, V4_WORD] >> V4_SHIFT) & 0xF                 # [n][128][8]
+    V4 = np.where(nib >= 8, nib - 16, nib).astype(np.int8)
+    C8 = r[:, C8_OFF.reshape(-1)].view(np.int8).reshape(n, PAGE, RANK)
+    mu8 = r[:, MU8_OFF].view(np.int8).reshape(n, HEAD_DIM)
+    sV = r[:, OFF_SV:OFF_SV + 16].copy().view("<f2").reshape(n, RANK)
+    sC = r[:, OFF_SC:OFF_SC + 32].copy().view("<f2").reshape(n, PAGE)
+    smu = r[:, OFF_SMU:OFF_SMU + 2].copy().view("<f2").reshape(n)
+    return dict(V4=V4.reshape(lead + (HEAD_DIM, RANK)),
+                C8=C8.reshape(lead + (PAGE, RANK)),
+                mu8=mu8.reshape(lead + (HEAD_DIM,)),
+                sV=sV.reshape(lead + (RANK,)).astype(np.float16),
+                sC=sC.reshape(lead + (PAGE,)).astype(np.float16),
+                smu=smu.reshape(lead).astype(np.float16))
+
+
+def build_summaries(k_cache, page_table, seq_ids, page_ids, batch, max_pages,
+                    store=None):
+    """Algorithm 1 over listed (sequence, logical page) pairs, every KV head.
+
+    k_cache [P][h_kv][16][128] (float32 holding bf16 values), page_table
+    [batch][max_pages].  Writes records into store [batch][h_kv][max_pages]
+    [832] (zero-initialised if None); returns (store, tau [n][h_kv])."""
+    k_cache = np.asarray(k_cache, dtype=np.float32)
+    h_kv = k_cache.shape[1]
+    if store is None:
+        store = np.zeros((batch, h_kv, max_pages, RECORD_BYTES), np.uint8)
+    seq_ids = np.asarray(seq_ids, dtype=np.int64)
+    page_ids = np.asarray(page_ids, dtype=np.int64)
+    phys = np.asarray(page_table)[seq_ids, page_ids].astype(np.int64)
+    keys = k_cache[phys]                                 # [n][h_kv][16][128]
+    q, s = build_page(keys)
+    rec = encode_records(q)                              # [n][h_kv][832]
+    for h in range(h_kv):
+        store[seq_ids, h, page_ids] = rec[:, h]
+    return store, s["tau"]
+
+
+# ----------------------------------------------------------------------------
+# Score: notes §4.2 Eq.(4), Algorithm 2
+# ----------------------------------------------------------------------------
+def score_from_summaries(q, mu_hat, V_hat, C_hat):
+    """Eq.(4) for query heads q [G][d] against pages [n] of one KV head:
+    s_hat[g][j] = log sum_i exp((q.mu_j + (V_j^T q).c_i) / sqrt(d))."""
+    q = np.asarray(q, dtype=np.float64)
+    d = q.shape[-1]
+    qmu = np.einsum("gd,nd->gn", q, mu_hat)
+    proj = np.einsum("gd,ndr->gnr", q, V_hat)                # V_j^T q
+    logits = (qmu[..., None] + np.einsum("gnr,nir->gni", proj, C_hat)) \
+        / math.sqrt(d)
+    return logsumexp(logits, axis=-1)
+
+
+def score_store(q, store, seq_lens):
+    """s_hat [batch][h_kv][G][max_pages] (NaN where a page has no summary),
+    q [batch][h_q][128] holding bf16 values, store as build_summaries."""
+    q = np.asarray(q, dtype=np.float64)
+    batch, h_kv, max_pages, _ = store.shape
+    G = q.shape[1] // h_kv
+    out = np.full((batch, h_kv, G, max_pages), np.nan)
+    for b in range(batch):
+        nf = int(seq_lens[b]) // PAGE
+        if nf == 0:
+            continue
+        for h in range(h_kv):
+            mu, V, C = dequantize(decode_records(store[b, h, :nf]))
+            out[b, h, :, :nf] = score_from_summaries(
+                q[b, h * G:(h + 1) * G], mu, V, C)
+    return out
+
+
+def exact_page_lse(q, keys):
+    """s_j(q) = log sum_{i in P_j} exp(q.k_i / sqrt(d)) (the target of Eq.(4)),
+    q [G][d], keys [n][B][d] -> [G][n]."""
+    q = np.asarray(q, np.float64)
+    keys = np.asarray(keys, np.float64)
+    return logsumexp(np.einsum("gd,nid->gni", q, keys)
+                     / math.sqrt(q.shape[-1]), axis=-1)
+
+
+# ----------------------------------------------------------------------------
+# Select: notes §4.2 Eq.(5) and sink/recent rule, Algorithm 2
+# ----------------------------------------------------------------------------
+def mass_fractions(s_hat_g, n_full):
+    """m_hat_g(j) = exp(s_hat_j(q_g)) / sum_{j'} exp(s_hat_j'(q_g)) over the
+    n_full summarised pages; s_hat_g [G][>= n_full] -> [G][n_full]."""
+    s = np.asarray(s_hat_g, np.float64)[:, :n_full]
+    Z = logsumexp(s, axis=1)
+    return np.exp(s - Z[:, None])
+
+
+def select_one(s_hat_g, seq_len, k):
+    """Selected logical pages (ascending) for one (sequence, KV head):
+    the sink page 0, the recent page n-1 and the top-(k-2) remaining pages by
+    the share-average m_bar_j = (1/G) sum_g m_hat_g(j) (Eq.(5))."""
+    n = -(-int(seq_len) // PAGE)
+    if n == 0:
+        return []
+    if n <= k:
+        return list(range(n))
+    nf = int(seq_len) // PAGE
+    m_bar = mass_fractions(s_hat_g, nf).mean(axis=0)
+    cand = np.arange(1, n - 1)
+    order = np.lexsort((cand, -m_bar[cand]))       # mass desc, index asc
+    top = cand[order[:k - 2]]
+    return sorted([0, n - 1] + top.tolist())
+
+
+def select_store(s_hat, seq_lens, k):
+    """idx [batch][h_kv][k] int32, ascending, -1 padded."""
+    batch, h_kv = s_hat.shape[:2]
+    idx = np.full((batch, h_kv, k), -1, dtype=np.int32)
+    for b in range(batch):
+        for h in range(h_kv):
+            sel = select_one(s_hat[b, h], seq_lens[b], k)
+            idx[b, h, :len(sel)] = sel
+    return idx
+
+
+def share_average(s_hat_g, n_full):
+    return mass_fractions(s_hat_g, n_full).mean(axis=0)
+
+
+# ----------------------------------------------------------------------------
+# Attention over selected pages: notes §2, Algorithm 2
+# ----------------------------------------------------------------------------
+def attend(q, K, V):
+    """Softmax attention of query heads q [G][d] over tokens K, V [T][d].
+    Returns (o [G][d], lse [G]) with natural-log LSE of the logits."""
+    q = np.asarray(q, np.float64)
+    if K.shape[0] == 0:
+        return np.zeros_like(q), np.full(q.shape[0], -np.inf)
+    logits = q @ np.asarray(K, np.float64).T / math.sqrt(q.shape[-1])
+    lse = logsumexp(logits, axis=1)
+    p = np.exp(logits - lse[:, None])
+    return p @ np.asarray(V, np.float64), lse
+
+
+def gather_tokens(k_cache, v_cache, page_table, b, h, pages, seq_len):
+    Ks, Vs = [], []
+    for p in pages:
+        if p < 0:
+            continue
+        ntok = min(PAGE, int(seq_len) - PAGE * int(p))
+        if ntok <= 0:
+            continue
+        phys = int(page_table[b][p])
+        Ks.append(np.asarray(k_cache[phys, h, :ntok], np.float64))
+        Vs.append(np.asarray(v_cache[phys, h, :ntok], np.float64))
+    if not Ks:
+        d = k_cache.shape[-1]
+        return np.zeros((0, d)), np.zeros((0, d))
+    return np.concatenate(Ks), np.concatenate(Vs)
+
+
+def sparse_decode(q, k_cache, v_cache, page_table, seq_lens, idx):
+    """o [batch][h_q][d], lse [batch][h_q] over the selected pages' tokens;
+    idx None means every page (dense decode)."""
+    q = np.asarray(q, np.float64)
+    batch, h_q, d = q.shape
+    h_kv = k_cache.shape[1]
+    G = h_q // h_kv
+    o = np.zeros((batch, h_q, d))
+    lse = np.full((batch, h_q), -np.inf)
+    for b in range(batch):
+        n = -(-int(seq_lens[b]) // PAGE)
+        for h in range(h_kv):
+            pages = range(n) if idx is None else idx[b][h]
+            K, V = gather_tokens(k_cache, v_cache, page_table, b, h, pages,
+                                 seq_lens[b])
+            ob, lb = attend(q[b, h * G:(h + 1) * G], K, V)
+            o[b, h * G:(h + 1) * G] = ob
+            lse[b, h * G:(h + 1) * G] = lb
+    return o, lse
+
+
+def dense_decode(q, k_cache, v_cache, page_table, seq_lens):
+    return sparse_decode(q, k_cache, v_cache, page_table, seq_lens, None)
+
+
+# ----------------------------------------------------------------------------
+# Output-error identity and retention bound: notes §3.1 Eq.(1), §5 Eq.(6)-(7)
+# ----------------------------------------------------------------------------
+def identity_terms(q, K, V, keep_mask):
+    """For one query q [d] and tokens K, V [T][d], a keep mask over tokens:
+    returns (o, o_S, eps, vbar_S, vbar_Sc): o over every token, o_S over the
+    kept tokens only, eps = 1 - gamma_S(q) the attention mass outside S, and
+    the attention-weighted means of the kept / dropped values.  (o_S and
+    vbar_S coincide by definition; both are returned so a check of Eq.(1)
+    reads term by term.)"""
+    q = np.asarray(q, np.float64)
+    logits = np.asarray(K, np.float64) @ q / math.sqrt(q.shape[-1])
+    p = np.exp(logits - logsumexp(logits))
+    V = np.asarray(V, np.float64)
+    o = p @ V
+    pS, pC = p[keep_mask], p[~keep_mask]
+    gamma = pS.sum()
+    lS = logits[keep_mask]
+    wS = np.exp(lS - logsumexp(lS))
+    o_S = wS @ V[keep_mask]                 # attention restricted to S
+    vS = pS @ V[keep_mask] / gamma
+    vC = pC @ V[~keep_mask] / pC.sum()
+    return o, o_S, 1.0 - gamma, vS, vC
+
+
+def eq7_bound(q, V, tau):
+    """||q_perp|| sqrt(tau) / sqrt(d), q_perp = q minus its projection on the
+    span of the orthonormal basis V [d][r] (Eq.(7), one query, one page)."""
+    q = np.asarray(q, np.float64)
+    qp = q - V @ (V.T @ q)
+    return np.linalg.norm(qp) * math.sqrt(max(tau, 0.0)) / math.sqrt(q.size)

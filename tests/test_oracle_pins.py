@@ -1,0 +1,386 @@
+"""Pins of the float64 oracle against what the LOCKS pages and mathematics fix.
+
+None of these checks retypes an oracle formula: each compares the oracle with
+a closed form, an independent library routine (SVD instead of the Gram
+eigensolver), brute force on tiny inputs, an identity of the pages, or a
+hand-derived byte fixture.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import locks_oracle as O
+
+
+def _rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+def _pages(rng, n, B=16, d=128, rank=8, noise=0.05):
+    mu = rng.normal(0, 0.5, (n, 1, d))
+    W = np.linalg.qr(rng.normal(size=(n, d, rank)))[0]
+    A = rng.normal(size=(n, B, rank))
+    A = np.linalg.qr(A - A.mean(axis=1, keepdims=True))[0]
+    s = 4.0 * 0.6 ** np.arange(rank)
+    return mu + (A * s) @ np.swapaxes(W, 1, 2) + rng.normal(0, noise, (n, B, d))
+
+
+# --------------------------------------------------------------------------
+# §5.1 toy example (closed form derived by hand from the printed deltas)
+# --------------------------------------------------------------------------
+def test_toy_example_closed_form(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "toy_example_5_1.json")))
+    deltas = np.array(g["deltas"])
+    offset = np.array([0.3, -0.2, 0.5, 1.0])          # any centroid
+    keys = deltas + offset
+    s = O.page_summary(keys, r=g["r"])
+    tr, det = 3.64, 3.62 * 0.02 - 0.18 ** 2
+    lam1 = (tr + math.sqrt(tr * tr - 4 * det)) / 2
+    lam2 = (tr - math.sqrt(tr * tr - 4 * det)) / 2
+    assert s["mu"] == pytest.approx(offset, abs=1e-14)
+    assert s["lam"][0] == pytest.approx(lam1, rel=1e-12)
+    assert s["lam"][1] == pytest.approx(lam2, rel=1e-10)
+    assert np.abs(s["lam"][2:]).max() < 1e-12
+    assert lam1 == pytest.approx(3.628978, abs=1e-6)
+    assert lam2 == pytest.approx(0.011022, abs=1e-6)
+    assert s["tau"] == pytest.approx(lam2, rel=1e-10)   # tau_{j,1} = sigma_2^2
+    v = np.array([0.18, lam1 - 3.62, 0.0, 0.0])
+    v /= np.linalg.norm(v)
+    assert abs(s["V"][:, 0] @ v) == pytest.approx(1.0, abs=1e-12)
+    # c_i = V^T delta_i
+    assert s["C"][:, 0] == pytest.approx(deltas @ s["V"][:, 0], abs=1e-12)
+    # query along the dropped axis: the rank-1 logits cannot tell delta_1
+    # from delta_2 (nor delta_3 from delta_4), the exact logits can
+    q = np.array(g["query"])
+    exact = keys @ q / 2.0
+    recon = (q @ s["mu"] + (s["V"].T @ q) @ s["C"].T) / 2.0
+    assert abs(exact[1] - exact[0]) == pytest.approx(0.05, abs=1e-12)
+    assert abs(recon[1] - recon[0]) < 0.1 * abs(exact[1] - exact[0])
+    # Eq.(7): |s_hat - s| <= ||q_perp|| sqrt(tau) / sqrt(d)
+    s_hat = O.logsumexp(recon)
+    s_ex = O.logsumexp(exact)
+    bound = O.eq7_bound(q, s["V"], s["tau"])
+    assert abs(s_hat - s_ex) <= bound + 1e-12
+
+
+# --------------------------------------------------------------------------
+# Eq.(3) against an independent routine (SVD of D) and basis properties
+# --------------------------------------------------------------------------
+def test_gram_eigen_matches_svd():
+    rng = _rng(1)
+    keys = _pages(rng, 24)
+    s = O.page_summary(keys, r=8)
+    for j in range(keys.shape[0]):
+        D = keys[j] - keys[j].mean(axis=0)
+        U_, S_, Vt_ = np.linalg.svd(D, full_matrices=False)
+        # eigenvalues of D D^T are the squared singular values of D (the zero
+        # one only to rounding of the squared scale)
+        assert s["lam"][j] == pytest.approx(S_ ** 2, rel=1e-9,
+                                            abs=1e-13 * S_[0] ** 2)
+        gaps = np.diff(S_[:9] ** 2)
+        for k in range(8):
+            if min(abs(gaps[k]) if k < 8 else 1, abs(gaps[k - 1]) if k else 1) \
+                    < 1e-6 * S_[0] ** 2:
+                continue
+            assert abs(s["V"][j][:, k] @ Vt_[k]) == pytest.approx(1, abs=1e-9)
+        # C = U_r Sigma_r equals D V (c_i = V^T delta_i)
+        assert s["C"][j] == pytest.approx(D @ s["V"][j], abs=1e-10)
+
+
+def test_basis_orthonormal():
+    s = O.page_summary(_pages(_rng(2), 16), r=8)
+    VtV = np.swapaxes(s["V"], 1, 2) @ s["V"]
+    assert np.abs(VtV - np.eye(8)).max() < 1e-10
+
+
+def test_exact_when_rank_reached():
+    """r = 15 = rank of 16 centred keys: reconstructed logits equal the exact
+    logits, so s_hat equals the exact page LSE."""
+    rng = _rng(3)
+    keys = _pages(rng, 12)
+    s = O.page_summary(keys, r=15)
+    q = rng.normal(size=(4, 128))
+    s_hat = O.score_from_summaries(q, s["mu"], s["V"], s["C"])
+    s_ex = O.exact_page_lse(q, keys)
+    assert np.abs(s_hat - s_ex).max() < 1e-10
+    # a planted rank-3 page is exact already at r = 3
+    W = np.linalg.qr(rng.normal(size=(128, 3)))[0]
+    A = rng.normal(size=(16, 3))
+    page = (A - A.mean(0)) @ W.T + rng.normal(size=128)
+    s3 = O.page_summary(page[None], r=3)
+    assert s3["tau"][0] < 1e-13 * s3["lam"][0, 0]
+    assert np.abs(O.score_from_summaries(q, s3["mu"], s3["V"], s3["C"])
+                  - O.exact_page_lse(q, page[None])).max() < 1e-10
+
+
+@pytest.mark.parametrize("r", [1, 2, 4, 8, 12, 15])
+def test_eckart_young_tail(r):
+    """Retained reconstruction error equals the spectral tail tau_{j,r}."""
+    rng = _rng(4 + r)
+    keys = _pages(rng, 10)
+    s = O.page_summary(keys, r=r)
+    for j in range(keys.shape[0]):
+        D = keys[j] - keys[j].mean(axis=0)
+        err = ((D - s["C"][j] @ s["V"][j].T) ** 2).sum()
+        assert err == pytest.approx(s["tau"][j], rel=1e-8, abs=1e-12)
+        # and no other orthonormal rank-r basis does better
+        Q = np.linalg.qr(rng.normal(size=(128, r)))[0]
+        assert ((D - D @ Q @ Q.T) ** 2).sum() >= err - 1e-9
+
+
+# --------------------------------------------------------------------------
+# Eq.(1) identity and Eq.(7) bound
+# --------------------------------------------------------------------------
+def test_output_error_identity():
+    rng = _rng(5)
+    for trial in range(20):
+        T = 48
+        K = rng.normal(size=(T, 128)) * 1.5
+        V = rng.normal(size=(T, 128))
+        q = rng.normal(size=128)
+        keep = rng.random(T) < 0.4
+        keep[0] = True
+        keep[-1] = False
+        o, o_S, eps, vS, vC = O.identity_terms(q, K, V, keep)
+        assert np.abs((o - o_S) - eps * (vC - vS)).max() < 1e-12
+
+
+def test_eq7_bound_unquantised():
+    rng = _rng(6)
+    keys = _pages(rng, 32)
+    s = O.page_summary(keys, r=8)
+    q = rng.normal(size=(8, 128)) * 1.3
+    s_hat = O.score_from_summaries(q, s["mu"], s["V"], s["C"])
+    s_ex = O.exact_page_lse(q, keys)
+    for g in range(q.shape[0]):
+        for j in range(keys.shape[0]):
+            b = O.eq7_bound(q[g], s["V"][j], s["tau"][j])
+            assert abs(s_hat[g, j] - s_ex[g, j]) <= b + 1e-12
+
+
+# --------------------------------------------------------------------------
+# Selection: brute force, ties, degenerate cases (Eq.(5) and sink/recent)
+# --------------------------------------------------------------------------
+def _brute_select(s_hat, L, k):
+    n = -(-L // 16)
+    if n <= k:
+        return list(range(n))
+    nf = L // 16
+    G = len(s_hat)
+    m = []
+    for j in range(nf):
+        acc = 0.0
+        for g in range(G):
+            z = sum(math.exp(s_hat[g][jj]) for jj in range(nf))
+            acc += math.exp(s_hat[g][j]) / z
+        m.append(acc / G)
+    best, best_key = None, None
+    for sub in itertools.combinations(range(1, n - 1), k - 2):
+        key = (sum(m[j] for j in sub), tuple(-j for j in sub))
+        if best_key is None or key > best_key:
+            best, best_key = sub, key
+    return sorted([0, n - 1] + list(best))
+
+
+@pytest.mark.parametrize("G", [1, 3])
+def test_select_matches_brute_force(G):
+    rng = _rng(7 + G)
+    for trial in range(40):
+        n = int(rng.integers(3, 13))
+        L = 16 * n - int(rng.integers(0, 16))
+        k = int(rng.integers(2, n + 1))
+        s_hat = rng.normal(0, 2.0, (G, n))
+        assert O.select_one(s_hat, L, k) == _brute_select(s_hat, L, k)
+
+
+def test_select_ties_and_degenerate():
+    s = np.zeros((2, 10))
+    assert O.select_one(s, 160, 5) == [0, 1, 2, 3, 9]   # equal mass: low index
+    assert O.select_one(s, 0, 4) == []
+    assert O.select_one(s, 5, 4) == [0]                 # one partial page
+    assert O.select_one(s, 17, 4) == [0, 1]
+    assert O.select_one(s, 160, 10) == list(range(10))
+    assert O.select_one(s, 160, 2) == [0, 9]
+
+
+def test_group_of_one_ranks_by_score():
+    rng = _rng(9)
+    s_hat = rng.normal(size=(1, 40))
+    sel = O.select_one(s_hat, 640, 10)
+    mid = [j for j in sel if j not in (0, 39)]
+    order = sorted(range(1, 39), key=lambda j: (-s_hat[0, j], j))
+    assert sorted(order[:8]) == mid
+
+
+def test_mass_fractions_sum_to_one():
+    rng = _rng(10)
+    s_hat = rng.normal(0, 3, (4, 50))
+    assert O.mass_fractions(s_hat, 50).sum(axis=1) == pytest.approx(1, abs=1e-12)
+    assert O.share_average(s_hat, 50).sum() == pytest.approx(1, abs=1e-12)
+
+
+# --------------------------------------------------------------------------
+# Attention
+# --------------------------------------------------------------------------
+def test_attend_brute_force():
+    rng = _rng(11)
+    q = rng.normal(size=(2, 8))
+    K = rng.normal(size=(5, 8))
+    V = rng.normal(size=(5, 8))
+    o, lse = O.attend(q, K, V)
+    for g in range(2):
+        logits = [sum(q[g][i] * K[t][i] for i in range(8)) / math.sqrt(8)
+                  for t in range(5)]
+        z = sum(math.exp(x) for x in logits)
+        assert lse[g] == pytest.approx(math.log(z), abs=1e-12)
+        for i in range(8):
+            ref = sum(math.exp(logits[t]) / z * V[t][i] for t in range(5))
+            assert o[g][i] == pytest.approx(ref, abs=1e-12)
+
+
+def test_all_pages_selected_equals_dense():
+    rng = _rng(12)
+    P, h_kv, G = 10, 2, 2
+    kc = rng.normal(size=(P, h_kv, 16, 128))
+    vc = rng.normal(size=(P, h_kv, 16, 128))
+    pt = np.array([[3, 7, 1, 0, -1], [2, 9, 8, 5, 4]])
+    lens = np.array([55, 80])
+    q = rng.normal(size=(2, h_kv * G, 128))
+    s_hat = rng.normal(size=(2, h_kv, G, 5))
+    idx = O.select_store(s_hat, lens, 8)
+    o1, l1 = O.sparse_decode(q, kc, vc, pt, lens, idx)
+    o2, l2 = O.dense_decode(q, kc, vc, pt, lens)
+    assert np.abs(o1 - o2).max() < 1e-12 and np.abs(l1 - l2).max() < 1e-12
+
+
+# --------------------------------------------------------------------------
+# Quantiser invariants and the byte layout fixture
+# --------------------------------------------------------------------------
+def test_quantiser_invariants():
+    rng = _rng(13)
+    V = rng.normal(size=(20, 128, 8)).astype(np.float32)
+    V[3, :, 5] = 0.0
+    q = O.quantize_summary(np.ones((20, 128), np.float32), V,
+                           np.ones((20, 16, 8), np.float32))
+    s = q["sV"].astype(np.float32)
+    assert q["V4"].min() >= -7 and q["V4"].max() <= 7
+    assert (q["sV"][3, 5] == 0) and (q["V4"][3, :, 5] == 0).all()
+    amax = np.abs(V).argmax(axis=1)
+    for j in range(20):
+        for k in range(8):
+            if s[j, k] == 0:
+                continue
+            assert abs(q["V4"][j, amax[j, k], k]) == 7
+            err = np.abs(V[j, :, k] - s[j, k] * q["V4"][j, :, k])
+            assert err.max() <= 0.5 * s[j, k] * (1 + 1e-3) + 1e-3 * s[j, k]
+    assert (q["mu8"] == 127).all() and (q["C8"] == 127).all()
+    # overflowing scale saturates at the largest finite fp16
+    big = O._scale(np.array([1e9], np.float32), 127)
+    assert big[0] == np.float16(65504)
+
+
+def test_centroid_fp32_sequential():
+    rng = _rng(14)
+    k = (rng.integers(-64, 64, (5, 16, 128)) / 8.0).astype(np.float32)
+    assert O.centroid_f32(k) == pytest.approx(k.mean(axis=1), abs=0)
+    # sequential order is what is stated: one value that rounds away
+    x = np.zeros((1, 16, 1), np.float32)
+    x[0, 0, 0] = 1.0
+    x[0, 1:, 0] = 2.0 ** -25
+    seq = np.float32(1.0)
+    for t in range(1, 16):
+        seq = np.float32(seq + np.float32(2.0 ** -25))
+    assert O.centroid_f32(x)[0, 0] == np.float32(seq / 16)
+
+
+def test_record_fixture(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "record_fixture.json")))
+    e = g["entries"]
+    q = dict(V4=np.zeros((128, 8), np.int8), C8=np.zeros((16, 8), np.int8),
+             mu8=np.zeros(128, np.int8), sV=np.zeros(8, np.float16),
+             sC=np.zeros(16, np.float16), smu=np.float16(e["smu"]))
+    for d, k, v in e["V4"]:
+        q["V4"][d, k] = v
+    for i, k, v in e["C8"]:
+        q["C8"][i, k] = v
+    for d, v in e["mu8"]:
+        q["mu8"][d] = v
+    for k, v in e["sV"]:
+        q["sV"][k] = v
+    for i, v in e["sC"]:
+        q["sC"][i] = v
+    q["smu"] = np.array(q["smu"], np.float16)
+    rec = O.encode_records(q)
+    expect = np.zeros(O.RECORD_BYTES, np.uint8)
+    for off, val in g["expected_bytes"]:
+        expect[off] = val
+    assert (rec == expect).all(), np.nonzero(rec != expect)
+    back = O.decode_records(rec)
+    for key in q:
+        assert (np.asarray(back[key]) == np.asarray(q[key])).all(), key
+
+
+def test_record_byte_accounting():
+    """768 B logical payload per page-head at r=8, B=16, d=128, i.e. 9.4% of
+    the page's 8 KB of bf16 K/V; with the fp16 scales about one tenth."""
+    payload = 128 * 8 // 2 + 16 * 8 + 128
+    assert payload == 768
+    assert round(100 * payload / (2 * 16 * 128 * 2), 1) == 9.4
+    assert O.PAYLOAD_BYTES == payload + 2 * (8 + 16 + 1)
+    assert abs(O.PAYLOAD_BYTES / 8192 - 0.1) < 0.001
+    assert O.RECORD_BYTES % 16 == 0 and O.RECORD_BYTES >= O.PAYLOAD_BYTES
+
+
+def test_quantised_score_close_to_exact():
+    """End to end on the synthetic key model: quantised r=8 scores track the
+    exact page LSE (the page's claim that the summary ranks like exact LSE)."""
+    rng = _rng(15)
+    keys = _pages(rng, 64)
+    kb = keys.astype(np.float32)
+    q8, s = O.build_page(kb)
+    mu, V, C = O.dequantize(O.decode_records(O.encode_records(q8)))
+    qv = rng.normal(size=(4, 128))
+    err = np.abs(O.score_from_summaries(qv, mu, V, C)
+                 - O.exact_page_lse(qv, kb.astype(np.float64)))
+    assert err.max() < 0.1
+
+
+# --------------------------------------------------------------------------
+# Planted mistakes in the oracle are caught by the pins above
+# --------------------------------------------------------------------------
+def test_planted_mistakes_are_caught(monkeypatch):
+    orig = O.score_from_summaries
+
+    def no_centroid(q, mu, V, C):                    # dropped q.mu term
+        return orig(q, 0 * mu, V, C)
+    monkeypatch.setattr(O, "score_from_summaries", no_centroid)
+    with pytest.raises(AssertionError):
+        test_exact_when_rank_reached()
+    monkeypatch.setattr(O, "score_from_summaries", orig)
+
+    def select_variant(s_hat, L, k, merge, tie_high):
+        n = -(-L // 16)
+        if n <= k:
+            return list(range(n))
+        nf = L // 16
+        s = np.asarray(s_hat, np.float64)
+        m = merge(s, nf)
+        cand = np.arange(1, n - 1)
+        tie = -cand if tie_high else cand
+        top = cand[np.lexsort((tie, -m[cand]))[:k - 2]]
+        return sorted([0, n - 1] + top.tolist())
+
+    # ties to the higher index instead of the lower one
+    monkeypatch.setattr(O, "select_one", lambda s, L, k: select_variant(
+        s, L, k, O.share_average, True))
+    with pytest.raises(AssertionError):
+        test_select_ties_and_degenerate()
+    # averaging raw scores over the group instead of mass fractions (Eq.(5))
+    monkeypatch.setattr(O, "select_one", lambda s, L, k: select_variant(
+        s, L, k, lambda x, nf: x[:, :nf].mean(axis=0), False))
+    with pytest.raises(AssertionError):
+        test_select_matches_brute_force(3)
