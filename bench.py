@@ -1,0 +1,520 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the LOCKS sparse decode path on one GB300.
+
+A step is one layer's decode step for the whole batch: score every full page
+from its summary, select the GQA-shared page set, attend over the selected
+pages.  Summaries are built once before timing (the build is reported
+separately).  Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W]
+                    [--impl locks|reference] [--workload NAME] [--batch B]
+                    [--quick]
+
+Under torchrun every rank runs its own replica of the workload (the path
+shards by sequence with no exchange step), so `value` is the sum over ranks
+and scaling is weak.  `--impl reference` times the float64 oracle on the
+host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("decode tokens/s per layer (score+select+sparse attn) @128K; "
+          "% HBM roofline")
+RECORD_PAYLOAD = 818          # algorithmic bytes of one page summary
+KV_PAGE_HEAD = 2 * 16 * 128 * 2  # K + V bytes of one full page-head (bf16)
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="locks", choices=["locks", "reference"])
+    p.add_argument("--workload", default="llama8b_128k")
+    p.add_argument("--batch", type=int, default=0,
+                   help="override the workload's batch (profiling cases)")
+    p.add_argument("--quick", action="store_true",
+                   help="skip e2e, dense context, build timing and CPU "
+                        "baseline (profiling runs)")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# ranks
+# ---------------------------------------------------------------------------
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_max(x: float) -> float:
+    """Max of a scalar over ranks (the slowest rank sets the job time)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_spec(spec, rank: int, batch: int = 0):
+    """Each rank runs its own replica: same shape, its own seed."""
+    kw = {"seed": spec.seed + 7919 * rank}
+    if batch:
+        kw["batch"] = batch
+    return dataclasses.replace(spec, **kw)
+
+
+# ---------------------------------------------------------------------------
+# measurement helpers
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}",
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"),
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_step(O, recs, keys, vals, q, seq_len, k, heads):
+    """One oracle decode step of one sequence for the listed KV heads:
+    score every summarised page, select, attend.  recs [h][n][832]."""
+    import numpy as np
+    G = q.shape[0] // keys.shape[1]
+    for h in heads:
+        mu, V, C = O.dequantize(O.decode_records(recs[h]))
+        s_hat = O.score_from_summaries(q[h * G:(h + 1) * G], mu, V, C)
+        sel = O.select_one(s_hat, seq_len, k)
+        toks_k, toks_v = [], []
+        for p in sel:
+            nt = min(16, seq_len - 16 * p)
+            toks_k.append(keys[p, h, :nt])
+            toks_v.append(vals[p, h, :nt])
+        O.attend(q[h * G:(h + 1) * G], np.concatenate(toks_k),
+                 np.concatenate(toks_v))
+
+
+def oracle_records(O, keys, seq_len):
+    """Oracle summaries [h][n_full][832] of one sequence's full pages."""
+    nf = seq_len // 16
+    q8, _ = O.build_page(keys[:nf])                    # [n][h][...]
+    rec = O.encode_records(q8)                          # [n][h][832]
+    return rec.transpose(1, 0, 2).copy()
+
+
+def cpu_baseline(O, keys, vals, queries, seq_len, k, steps=4):
+    """Time `steps` oracle decode steps of one sequence (all KV heads)."""
+    import numpy as np
+    recs = oracle_records(O, keys, seq_len)
+    h_kv = keys.shape[1]
+    t0 = time.perf_counter()
+    for s in range(steps):
+        oracle_step(O, recs, keys, vals, queries[s % len(queries)].astype(
+            np.float64), seq_len, k, range(h_kv))
+    dt = time.perf_counter() - t0
+    return steps / dt, dt
+
+
+# ---------------------------------------------------------------------------
+# the LOCKS arm
+# ---------------------------------------------------------------------------
+def run_locks(args):
+    import numpy as np
+    import torch
+
+    from sparse_paged_kv_locks_gb300 import binding as B
+    from sparse_paged_kv_locks_gb300 import workload as W
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist_init(world, "nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    spec = rank_spec(W.SPECS[args.workload], rank, args.batch)
+    B.lib()
+
+    wl = W.generate(spec, dev)
+    lens = [int(x) for x in wl.seq_lens]
+    batch, max_pages = wl.page_table.shape
+    h_kv, G, k = spec.h_kv, spec.group, spec.k
+    seq = torch.tensor([b for b in range(batch) for _ in range(lens[b] // 16)],
+                       dtype=torch.int32, device=dev)
+    pgs = torch.tensor([p for b in range(batch) for p in range(lens[b] // 16)],
+                       dtype=torch.int32, device=dev)
+    n_records = int(seq.numel()) * h_kv
+    store = B.new_summary_store(batch, h_kv, max_pages, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
+        enable_timing=True)
+    e0.record()
+    B.locks_build_summaries(wl.k_cache, wl.page_table, seq, pgs, store,
+                            status=status)
+    e1.record()
+    torch.cuda.synchronize()
+    build_ms = e0.elapsed_time(e1)
+    if not args.quick:   # rebuild once warm for a steady number
+        e0.record()
+        B.locks_build_summaries(wl.k_cache, wl.page_table, seq, pgs, store,
+                                status=status)
+        e1.record()
+        torch.cuda.synchronize()
+        build_ms = e0.elapsed_time(e1)
+    assert int(status.item()) == 0, "build reported a device error"
+
+    ws = B.new_workspace(batch, spec.h_q, h_kv, max_pages, max_pages, dev)
+    scores = ws[256:256 + 4 * batch * h_kv * G * max_pages].view(
+        torch.float32).view(batch, h_kv, G, max_pages)
+    idx = torch.empty(batch, h_kv, k, dtype=torch.int32, device=dev)
+    o = torch.empty(batch, spec.h_q, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(batch, spec.h_q, dtype=torch.float32, device=dev)
+    qs = wl.queries
+    n_q = qs.shape[0]
+
+    def step(i, evs=None):
+        q = qs[i % n_q]
+        if evs:
+            evs[0].record()
+        B.locks_score_pages(q, store, wl.seq_lens, scores, ws[:4].view(
+            torch.int32))
+        if evs:
+            evs[1].record()
+        B.locks_select_pages(scores, wl.seq_lens, spec.h_q, k, idx, ws)
+        if evs:
+            evs[2].record()
+        B.locks_sparse_decode(q, wl.k_cache, wl.v_cache, wl.page_table,
+                              wl.seq_lens, idx, k, o, lse, ws)
+        if evs:
+            evs[3].record()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == 0, "decode reported a device error"
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+           for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
+        enable_timing=True)
+    t_start.record()
+    for i in range(args.steps):
+        step(args.warmup + i, evs[i])
+    t_end.record()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    score_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    select_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    decode_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    job_ms = reduce_max(total_ms)
+    value = world * batch * args.steps / (job_ms / 1e3)
+
+    # algorithmic bytes: summaries of every full page + selected K/V (valid
+    # tokens) + q + o
+    idx_h = idx.cpu().numpy()
+    kv_bytes = 0
+    for b in range(batch):
+        for h in range(h_kv):
+            for p in idx_h[b, h]:
+                if p >= 0:
+                    kv_bytes += min(16, lens[b] - 16 * int(p)) * 2 * 128 * 2
+    q_bytes = batch * spec.h_q * 128 * 2
+    score_bytes = n_records * RECORD_PAYLOAD
+    step_bytes = score_bytes + kv_bytes + 2 * q_bytes
+    peak, peak_src = measured_peaks()
+    score_gbs = score_bytes / (score_ms / 1e3) / 1e9
+    step_gbs = step_bytes / (total_ms / args.steps / 1e3) / 1e9
+    decode_gbs = kv_bytes / (decode_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": job_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "precision": "bf16 K/V and queries, int4/int8 summaries with fp16 "
+                     "scales, fp16/bf16 tensor-core operands, fp32 "
+                     "accumulation",
+        "data": "synthetic (seeded generator, no datasets or weights)",
+        "config": {
+            "workload": f"{spec.name}: batch {batch} x {spec.ctx} tokens, "
+                        f"{spec.h_q} query / {h_kv} KV heads, d=128, page 16, "
+                        f"rank 8, budget k={k} pages",
+            "batch": batch, "context": spec.ctx, "h_q": spec.h_q,
+            "h_kv": h_kv, "k": k,
+            "l2": "inputs larger than L2: every step streams "
+                  f"{score_bytes / 1e9:.2f} GB of summaries and "
+                  f"{kv_bytes / 1e6:.0f} MB of selected K/V",
+            "parallelism": f"replicas x{world}"},
+        "roofline": {
+            "bound": "hbm", "kernel": "score (summary stream)",
+            "achieved": round(score_gbs, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(score_gbs / peak, 4), "traffic": None,
+            "peak_source": peak_src,
+            "algorithmic_bytes": score_bytes},
+        "step_roofline": {
+            "achieved": round(step_gbs, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(step_gbs / peak, 4),
+            "frac_of_8tbs": round(step_gbs / 8000.0, 4),
+            "algorithmic_bytes": step_bytes},
+        "kernels_ms": {"score": round(score_ms, 4),
+                       "select": round(select_ms, 4),
+                       "sparse_decode": round(decode_ms, 4),
+                       "sparse_decode_gbs": round(decode_gbs, 1)},
+        "gpu_launches": None, "clocks": clk,
+    }
+    # launches per step: score, select, decode (+ split combine)
+    pps = _decode_pages_per_split(k, batch * h_kv)
+    launches = 3 + (1 if math.ceil(k / pps) > 1 else 0)
+    line["gpu_launches"] = launches * args.steps
+    line["build"] = {"page_heads": n_records, "ms": round(build_ms, 3),
+                     "page_heads_per_s": round(n_records / (build_ms / 1e3))}
+
+    if not args.quick:
+        # e2e: pinned host query in, pinned host (o, lse) out, every step
+        dec = B.LocksDecoder(wl.k_cache, wl.v_cache, wl.page_table, store,
+                             spec.h_q, k)
+        q_host = qs.cpu().pin_memory()
+        o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        lse_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        n_e2e = max(10, min(args.steps, 500))
+        for i in range(3):
+            dec.step_host(q_host[i % n_q], wl.seq_lens, o_host, lse_host)
+        barrier()
+        t0 = time.perf_counter()
+        for i in range(n_e2e):
+            dec.step_host(q_host[i % n_q], wl.seq_lens, o_host, lse_host)
+        dt = reduce_max(time.perf_counter() - t0)
+        line["e2e"] = {"value": world * batch * n_e2e / dt, "unit": "tokens/s",
+                       "steps": n_e2e,
+                       "h2d_bytes_per_step": q_bytes,
+                       "d2h_bytes_per_step": q_bytes + batch * spec.h_q * 4}
+        # dense full-cache decode of the same shape, as context
+        for _ in range(2):
+            B.locks_sparse_decode(qs[0], wl.k_cache, wl.v_cache,
+                                  wl.page_table, wl.seq_lens, None, 0, o, lse,
+                                  ws)
+        torch.cuda.synchronize()
+        n_dense = 10
+        t_start.record()
+        for i in range(n_dense):
+            B.locks_sparse_decode(qs[i % n_q], wl.k_cache, wl.v_cache,
+                                  wl.page_table, wl.seq_lens, None, 0, o, lse,
+                                  ws)
+        t_end.record()
+        torch.cuda.synchronize()
+        dms = t_start.elapsed_time(t_end) / n_dense
+        dense_bytes = sum(lens) * h_kv * 2 * 128 * 2
+        line["dense_context"] = {
+            "value": batch / (dms / 1e3), "unit": "tokens/s",
+            "ms_per_step": round(dms, 4),
+            "gbs": round(dense_bytes / (dms / 1e3) / 1e9, 1)}
+        if rank == 0 and world == 1:
+            from oracle import locks_oracle as O
+            b0 = 0
+            n0 = math.ceil(lens[b0] / 16)
+            phys = wl.page_table[b0, :n0].long()
+            keys = wl.k_cache[phys].float().cpu().numpy()
+            vals = wl.v_cache[phys].float().cpu().numpy()
+            qn = qs[:, b0].float().cpu().numpy()
+            steps_cpu = 4
+            v_cpu, dt_cpu = cpu_baseline(O, keys, vals, qn, lens[b0], k,
+                                         steps_cpu)
+            line["cpu_baseline"] = {
+                "value": v_cpu, "unit": "tokens/s", "cores": host_cores(),
+                "kind": "oracle",
+                "sample": f"sequence 0 of {batch} ({lens[b0]} tokens), all "
+                          f"{h_kv} KV heads, {steps_cpu} decode steps (score "
+                          "+ select + sparse attention) in "
+                          f"{dt_cpu:.1f} s; oracle summaries built outside "
+                          "the timed region; numpy default threading"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _decode_pages_per_split(list_len, units):
+    """Mirror of the library's split rule, for the launch count only."""
+    import torch
+    sms = torch.cuda.get_device_properties(
+        torch.cuda.current_device()).multi_processor_count
+    pps = 16
+    while pps < list_len and math.ceil(list_len / pps) > 64:
+        pps *= 2
+    while pps > 4 and units * math.ceil(list_len / pps) < 4 * sms and \
+            math.ceil(list_len / (pps // 2)) <= 64:
+        pps //= 2
+    return pps
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the float64 oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    import numpy as np
+
+    from oracle import locks_oracle as O
+    from sparse_paged_kv_locks_gb300 import workload as W
+
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    spec = rank_spec(W.SPECS[args.workload], 0, args.batch)
+    one = W.generate_sequence(spec, 0, "cpu", steps=min(spec.steps, 8))
+    keys = one["keys"].float().numpy()
+    vals = one["values"].float().numpy()
+    qs = one["queries"].float().numpy().astype(np.float64)
+    L = one["seq_len"]
+    h_kv, k = spec.h_kv, spec.k
+    n_full = L // 16
+    # per-step sample: one KV head (rotating) over the first P pages, P sized
+    # so warm-up + timed steps take about two minutes
+    recs = oracle_records(O, keys, L)
+    t0 = time.perf_counter()
+    oracle_step(O, recs, keys, vals, qs[0], L, k, [0])
+    t_head = time.perf_counter() - t0
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    P = int(min(n_full, max(4 * k, n_full * budget / max(t_head, 1e-6))))
+    P = min(P, n_full)
+    Ls = 16 * P
+    sub = recs[:, :P]
+
+    def one_step(i):
+        h = i % h_kv
+        oracle_step(O, sub, keys[:P], vals[:P], qs[i % len(qs)], Ls, k, [h])
+
+    for i in range(args.warmup):
+        one_step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one_step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    frac = P / math.ceil(L / 16) / h_kv        # of one token's decode step
+    value = frac * args.steps / dt
+    sample = (f"per step: sequence 0 ({L} tokens), one KV head of {h_kv} "
+              f"(rotating), first {P} of {math.ceil(L / 16)} pages with the "
+              f"budget k={k}; counted as {frac:.4f} of a token")
+    line = {"impl": "reference", "metric": METRIC, "value": value,
+            "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded generator)",
+            "config": {"workload": f"{spec.name}: batch {spec.batch} x "
+                                   f"{spec.ctx} tokens, {spec.h_q} query / "
+                                   f"{h_kv} KV heads, d=128, page 16, rank 8, "
+                                   f"budget k={k} pages",
+                       "batch": spec.batch, "context": spec.ctx},
+            "cpu_baseline": {"value": value, "unit": "tokens/s",
+                             "cores": host_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_locks(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,226 @@
+/*
+ * locks.h - C ABI of the LOCKS page-local key-summary sparse decode library
+ * (liblocks.so, sm_103a).
+ *
+ * The method: "LOCKS: Page-Local Compact Key Summaries for Efficient
+ * Long-Context Decoding", as restated in the LOCKS reading notes
+ * (zhongzhuzhou.org, 2026-07-29) and the gist.science technical summary.
+ * Every entry point below names the passage that defines its operation.
+ *
+ * Conventions for every call
+ *  - All array pointers are CUDA device pointers owned by the caller unless a
+ *    comment says "host".  The library allocates no memory, never
+ *    synchronises the stream (except locks_read_status, which says so) and
+ *    launches its kernels on `stream` (NULL = the legacy default stream).
+ *  - Shapes: page size B = 16 tokens, head dim d = 128, summary rank r = 8.
+ *    K/V caches are bf16, laid out [num_phys_pages][h_kv][16][128] so that
+ *    each (page, KV head) is one contiguous 4 KB run.
+ *    page_table is int32 [batch][max_pages] (logical page -> physical page).
+ *    Queries are bf16 [batch][h_q][128]; query head hq belongs to KV head
+ *    hq / G with G = h_q / h_kv (1 <= G <= 16).
+ *  - Host-detectable argument errors return a locks_status_t before anything
+ *    is launched.  Data errors found on the device (a page id outside the
+ *    cache, a selected index outside the sequence, a length above
+ *    16*max_pages) never trap: the kernel skips the offending access and ORs
+ *    a LOCKS_DEV_* bit into a device status word (first int32 of the
+ *    workspace, or the explicit `status` pointer), which the caller reads
+ *    with locks_read_status and clears with locks_clear_status.
+ *  - Numerics: the fast paths feed the tensor cores fp16 operands (query
+ *    converted from bf16, summary codes exact) with fp32 accumulation, so
+ *    query entries must satisfy |q| < 65504.
+ *
+ * Summary record (one per (sequence, KV head, logical page)), 832 bytes,
+ * 16-byte aligned, laid out so that the scoring kernel's tensor-core
+ * fragments load with one 16-byte read per lane:
+ *   [  0, 512)  V4  int4 basis codes, two's complement, in [-7, 7].
+ *               128 little-endian u32 words.  The code of V[d][n] (d < 128,
+ *               component n < 8) sits in word (4n + c)*4 + w at bit
+ *               16e + 8sp + 4h, where c = (d%8)/2, e = d%2, h = (d%16)/8,
+ *               s = d/16, w = s/2, sp = s%2.
+ *   [512, 640)  C8  int8 coefficient codes C[i][n] (token i < 16), byte
+ *               512 + 4*(4*(i%8) + n/2) + 2*(i/8) + n%2, in [-127, 127].
+ *   [640, 768)  MU8 int8 centroid codes mu[d], byte
+ *               640 + 32*((d%8)/2) + 4*(d/16) + (d%2) + 2*((d%16)/8).
+ *   [768, 784)  sV  fp16[8]  per-column basis scales.
+ *   [784, 816)  sC  fp16[16] per-row coefficient scales.
+ *   [816, 818)  sMU fp16     centroid scale.
+ *   [818, 832)  zero padding.
+ * Dequantised: mu = sMU*MU8, V[:,n] = sV[n]*V4[:,n], c_i = sC[i]*C8[i,:].
+ * The summary store is [batch][h_kv][max_pages] records in logical page
+ * order, so one (sequence, KV head) is a contiguous stream.
+ */
+#ifndef LOCKS_H
+#define LOCKS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *locks_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  LOCKS_OK = 0,
+  LOCKS_ERR_INVALID_ARG = 1, /* null pointer, bad size, k < 2, ...      */
+  LOCKS_ERR_UNSUPPORTED = 2, /* G outside 1..16, size above a limit      */
+  LOCKS_ERR_WORKSPACE = 3,   /* workspace smaller than locks_workspace_size */
+  LOCKS_ERR_CUDA = 4         /* a CUDA call failed: locks_last_cuda_error */
+} locks_status_t;
+
+/* device status bits (OR-ed into the status word) */
+#define LOCKS_DEV_BAD_PAGE_ID 0x1 /* page_table entry outside the cache   */
+#define LOCKS_DEV_BAD_INDEX 0x2   /* selected page outside the sequence   */
+#define LOCKS_DEV_BAD_SEQ_LEN 0x4 /* seq_len < 0 or > 16*max_pages        */
+#define LOCKS_DEV_BAD_PAIR 0x8    /* build pair outside batch/max_pages   */
+#define LOCKS_DEV_TIMEOUT 0x10    /* an on-chip copy wait gave up         */
+
+#define LOCKS_PAGE_TOKENS 16
+#define LOCKS_HEAD_DIM 128
+#define LOCKS_RANK 8
+#define LOCKS_RECORD_BYTES 832
+#define LOCKS_RECORD_PAYLOAD_BYTES 818
+#define LOCKS_UNQUANTISED_FLOATS 1296 /* 16 + 128 + 128*8 + 16*8 */
+
+/* Human-readable name of a status code (static string). */
+const char *locks_status_string(locks_status_t s);
+
+/* cudaError_t of the last failing CUDA call in this thread (0 if none). */
+int locks_last_cuda_error(void);
+
+/* Bytes per summary record (832: 818 B payload + 14 B padding). */
+size_t locks_summary_record_bytes(void);
+
+/* Workspace bytes needed by locks_score_select, locks_select_pages and
+ * locks_sparse_decode for these sizes (k = max_pages covers dense decode).
+ * One workspace may serve those calls in stream order.  Its first int32 is
+ * the device status word: clear it once (locks_clear_status) before use. */
+locks_status_t locks_workspace_size(int batch, int h_q, int h_kv,
+                                    int max_pages, int k, size_t *bytes);
+
+/* Page summary build, LOCKS reading notes §4.1 Eq.(2)-(3), storage
+ * paragraph, and §4.3 Algorithm 1: for each listed (seq_ids[i], page_ids[i])
+ * pair and every KV head, centre the page's 16 keys on their mean, take the
+ * top r = 8 eigenpairs of the 16x16 Gram matrix D D^T (descending; each
+ * eigenvector signed so its largest-magnitude entry is positive), form
+ * V = D^T U_r Sigma_r^{-1} and C = U_r Sigma_r, quantise (int4 V with a
+ * per-column fp16 scale, int8 C with a per-row scale, int8 mean with one
+ * scale; scale = fp16(absmax/qmax), code = round-half-even(x/scale)) and
+ * write the record at summaries[seq][h][page].  Components with eigenvalue
+ * <= 1e-6 * lambda_1 are stored as zero.  Only full pages should be listed
+ * (the pages build a summary when a page fills).
+ *   k_cache       bf16 [num_phys_pages][h_kv][16][128]
+ *   page_table    int32 [batch][max_pages]
+ *   seq_ids, page_ids  int32 [n_pairs]
+ *   summaries     records [batch][h_kv][max_pages] (written for the pairs)
+ *   tau_out       optional float [n_pairs][h_kv]: spectral tail
+ *                 sum_{k>8} sigma_k^2 (the diagnostic of Algorithm 1)
+ *   unquantised_out  optional float [n_pairs][h_kv][1296]: the fp32 values
+ *                 before quantisation, per page-head in this order:
+ *                 eigenvalues [16] (descending, clipped at 0), centroid
+ *                 [128], basis V [128][8], coefficients C [16][8]
+ *   status        optional int32 device status word (LOCKS_DEV_* bits) */
+locks_status_t locks_build_summaries(
+    const void *k_cache, int64_t num_phys_pages, int h_kv,
+    const int32_t *page_table, int batch, int max_pages,
+    const int32_t *seq_ids, const int32_t *page_ids, int n_pairs,
+    void *summaries, float *tau_out, float *unquantised_out, int32_t *status,
+    locks_stream_t stream);
+
+/* Quantise and pack n given fp32 summaries into records with the same rule
+ * as locks_build_summaries (the storage paragraph of §4.1).
+ *   mu [n][128], basis [n][128][8] (V), coeffs [n][16][8] (C): float32
+ *   records [n][832] */
+locks_status_t locks_pack_summaries(const float *mu, const float *basis,
+                                    const float *coeffs, int n,
+                                    void *records, locks_stream_t stream);
+
+/* Score and select, LOCKS reading notes §4.2 Eq.(4)-(5) and §4.4
+ * Algorithm 2, one decode step: for every full page j of every (sequence b,
+ * KV head h) and each query head g of its group,
+ *   s_hat[g][j] = log sum_i exp((q_g.mu_j + (V_j^T q_g).c_i) / sqrt(128)),
+ * from the summary records alone; then mass fractions
+ * m_g(j) = exp(s_hat[g][j]) / sum_{j' full} exp(s_hat[g][j']), their group
+ * average m_bar_j (Eq.(5)), and the selection: the sink page 0, the recent
+ * page ceil(L/16)-1 and the k-2 other pages of largest m_bar (ties to the
+ * lower page); all pages when ceil(L/16) <= k.
+ *   q          bf16 [batch][h_q][128]
+ *   summaries  records [batch][h_kv][max_pages], built for every full page
+ *   seq_lens   int32 [batch] (tokens; a partial last page has no summary)
+ *   idx_out    int32 [batch][h_kv][k]: selected logical pages, ascending,
+ *              -1 padded when a sequence has fewer than k pages
+ *   workspace  >= locks_workspace_size bytes; after the call, bytes
+ *              [256, 256 + 4*batch*h_kv*G*max_pages) hold the scores s_hat
+ *              as float [batch][h_kv][G][max_pages] (full pages only) */
+locks_status_t locks_score_select(const void *q, const void *summaries,
+                                  const int32_t *seq_lens, int batch, int h_q,
+                                  int h_kv, int max_pages, int k,
+                                  int32_t *idx_out, void *workspace,
+                                  size_t workspace_bytes,
+                                  locks_stream_t stream);
+
+/* Scoring alone (§4.2 Eq.(4)): writes the natural-log page scores
+ * s_hat[g][j] of every full page to scores_out, float
+ * [batch][h_kv][G][max_pages] (entries of pages that are not full are left
+ * untouched).  locks_score_select = locks_score_pages + locks_select_pages.
+ *   status  optional int32 device status word */
+locks_status_t locks_score_pages(const void *q, const void *summaries,
+                                 const int32_t *seq_lens, int batch, int h_q,
+                                 int h_kv, int max_pages, float *scores_out,
+                                 int32_t *status, locks_stream_t stream);
+
+/* Selection alone (Eq.(5) and the sink/recent rule of §4.2) from given
+ * natural-log page scores scores[batch][h_kv][G][max_pages] (entries of
+ * full pages are read; a score of exact LSE turns this into the exact-mass
+ * selector).  Arguments as locks_score_select. */
+locks_status_t locks_select_pages(const float *scores, const int32_t *seq_lens,
+                                  int batch, int h_q, int h_kv, int max_pages,
+                                  int k, int32_t *idx_out, void *workspace,
+                                  size_t workspace_bytes,
+                                  locks_stream_t stream);
+
+/* Attention over the selected pages, LOCKS reading notes §2 (fetch full
+ * K/V only for the selected pages, then standard softmax attention for all
+ * G heads of the group) and §4.4 Algorithm 2: for each (b, query head),
+ *   o = sum_t softmax_t(q.k_t / sqrt(128)) v_t,  lse = log sum_t exp(...)
+ * over the tokens t = 16p + s (p in idx[b][h], s < 16, t < seq_lens[b]).
+ *   idx      int32 [batch][h_kv][k] (-1 entries skipped); NULL means every
+ *            page of the sequence (dense decode, used as a baseline)
+ *   o_out    bf16 [batch][h_q][128];  lse_out float [batch][h_q] (natural
+ *            log; -inf and o = 0 for a sequence with no tokens) */
+locks_status_t locks_sparse_decode(
+    const void *q, const void *k_cache, const void *v_cache,
+    int64_t num_phys_pages, const int32_t *page_table,
+    const int32_t *seq_lens, const int32_t *idx, int k, int batch, int h_q,
+    int h_kv, int max_pages, void *o_out, float *lse_out, void *workspace,
+    size_t workspace_bytes, locks_stream_t stream);
+
+/* Append one generated token per sequence and build the summary of every
+ * page this append fills (the build runs "when a page fills", LOCKS reading
+ * notes §2, Fig. 1): token position L = seq_lens[b] is written to page
+ * L/16 slot L%16 for every KV head, then, if (L+1) % 16 == 0, the record of
+ * that page is built as in locks_build_summaries; seq_lens[b] becomes L+1.
+ *   k_new, v_new  bf16 [batch][h_kv][128]
+ *   seq_lens      int32 [batch], updated in place on the device
+ *   tau_out       optional float [batch][h_kv] (written for built pages) */
+locks_status_t locks_append_kv(const void *k_new, const void *v_new,
+                               void *k_cache, void *v_cache,
+                               int64_t num_phys_pages, int h_kv,
+                               const int32_t *page_table, int batch,
+                               int max_pages, int32_t *seq_lens,
+                               void *summaries, float *tau_out,
+                               int32_t *status, locks_stream_t stream);
+
+/* Zero the device status word (the first int32 of `status_word`). */
+locks_status_t locks_clear_status(void *status_word, locks_stream_t stream);
+
+/* Copy the device status word to *host_out; synchronises `stream`. */
+locks_status_t locks_read_status(const void *status_word, int32_t *host_out,
+                                 locks_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOCKS_H */

@@ -1,0 +1,584 @@
+// Page summary build (LOCKS reading notes §4.1 Eq.(2)-(3), §4.3 Algorithm 1),
+// summary packing and append-with-incremental-build.
+//
+// One warp per (page, KV head).  Lane l owns head dims 4l..4l+3 of all 16
+// tokens, so centring, the basis V = D^T U_r Sigma_r^{-1} and the
+// quantisation of the centroid are lane-local.  The 16x16 Gram matrix is
+// accumulated as per-lane partials and reduce-scattered across the warp; the
+// symmetric eigenproblem runs as a cyclic two-sided Jacobi iteration with the
+// round-robin (circle) ordering, eight disjoint rotations per step, on a
+// per-warp shared-memory copy of the matrix.
+#include <utility>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace locks {
+
+constexpr int kBuildWarps = 4;
+constexpr int kMaxSweeps = 15;
+constexpr float kJacobiRelTol = 1e-7f;
+
+struct BuildSmem {
+  float A[16][17];
+  float U[16][17];
+  float rc[8], rs[8];
+  int rp[8], rq[8];
+  float lam[16];
+  int perm[16];
+  float cv[8], cc[8];
+  float Cf[16][8];
+  int8_t v8[128][8];
+  int8_t c8[16][8];
+  int8_t m8[128];
+  __half sv[8], sc[16], smu;
+};
+
+// Upper-triangle pair (i <= j) enumeration of the 16x16 Gram matrix.
+__host__ __device__ constexpr int pair_i(int p) {
+  int i = 0;
+  while (i < 16 && p >= 16 - i) {
+    p -= 16 - i;
+    ++i;
+  }
+  return i;
+}
+__host__ __device__ constexpr int pair_j(int p) {
+  int i = 0;
+  while (i < 16 && p >= 16 - i) {
+    p -= 16 - i;
+    ++i;
+  }
+  return i + p;
+}
+
+template <int P>
+__device__ __forceinline__ float gram_partial(const float (&D)[16][4]) {
+  if constexpr (P >= 136) {
+    return 0.f;
+  } else {
+    constexpr int i = pair_i(P), j = pair_j(P);
+    return D[i][0] * D[j][0] + D[i][1] * D[j][1] + D[i][2] * D[j][2] +
+           D[i][3] * D[j][3];
+  }
+}
+
+template <int BLK, int... L>
+__device__ __forceinline__ void gram_block(float (&v)[32],
+                                           const float (&D)[16][4],
+                                           std::integer_sequence<int, L...>) {
+  ((v[L] = gram_partial<32 * BLK + L>(D)), ...);
+}
+
+// Reduce-scatter of 32 per-lane partials: lane l ends with the warp sum of
+// element l in v[0].
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool hi = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      float send = hi ? v[i] : v[i + o];
+      float keep = hi ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0];
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1)
+    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+// Quantise (storage paragraph of §4.1) and write one 832-byte record.
+// V: lane-owned rows 4l..4l+3 of the fp32 basis; mu: lane-owned centroid
+// entries; sm.Cf: fp32 coefficients [16][8].
+__device__ void write_record(const float (&V)[4][8], const float (&mu)[4],
+                             BuildSmem &sm, uint8_t *rec, int lane) {
+  // basis: one scale per column, int4 codes
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    float a = fmaxf(fmaxf(fabsf(V[0][k]), fabsf(V[1][k])),
+                    fmaxf(fabsf(V[2][k]), fabsf(V[3][k])));
+    a = warp_max(a);
+    __half h = quant_scale(a, 7.f);
+    float s = __half2float(h);
+    if (lane == 0) sm.sv[k] = h;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      sm.v8[4 * lane + j][k] = (int8_t)quant_code(V[j][k], s, 7);
+  }
+  // centroid: one scale, int8 codes
+  {
+    float a = fmaxf(fmaxf(fabsf(mu[0]), fabsf(mu[1])),
+                    fmaxf(fabsf(mu[2]), fabsf(mu[3])));
+    a = warp_max(a);
+    __half h = quant_scale(a, 127.f);
+    float s = __half2float(h);
+    if (lane == 0) sm.smu = h;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      sm.m8[4 * lane + j] = (int8_t)quant_code(mu[j], s, 127);
+  }
+  __syncwarp();
+  // coefficients: one scale per row (token), int8 codes
+  if (lane < 16) {
+    float a = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a = fmaxf(a, fabsf(sm.Cf[lane][k]));
+    __half h = quant_scale(a, 127.f);
+    float s = __half2float(h);
+    sm.sc[lane] = h;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      sm.c8[lane][k] = (int8_t)quant_code(sm.Cf[lane][k], s, 127);
+  }
+  __syncwarp();
+  // V4: lane t = 4n + c owns words (4n + c)*4 + w, w = 0..3
+  {
+    const int n = lane >> 2, c = lane & 3;
+    uint32_t wv[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int sp = 0; sp < 2; ++sp)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int d = 32 * w + 16 * sp + 8 * h + 2 * c + e;
+            const uint32_t nib = (uint32_t)(sm.v8[d][n]) & 0xFu;
+            word |= nib << (16 * e + 8 * sp + 4 * h);
+          }
+      wv[w] = word;
+    }
+    *reinterpret_cast<uint4 *>(rec + kOffV4 + 16 * lane) =
+        make_uint4(wv[0], wv[1], wv[2], wv[3]);
+  }
+  // C8: lane t = 4*gi + c
+  {
+    const int gi = lane >> 2, c = lane & 3;
+    uint32_t b0 = (uint8_t)sm.c8[gi][2 * c], b1 = (uint8_t)sm.c8[gi][2 * c + 1];
+    uint32_t b2 = (uint8_t)sm.c8[gi + 8][2 * c];
+    uint32_t b3 = (uint8_t)sm.c8[gi + 8][2 * c + 1];
+    *reinterpret_cast<uint32_t *>(rec + kOffC8 + 4 * lane) =
+        b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  }
+  // MU8: lane l = 8c + s holds bytes d = 16s + 2c + {0, 1, 8, 9}
+  {
+    const int c = lane >> 3, s = lane & 7;
+    const int d0 = 16 * s + 2 * c;
+    uint32_t b0 = (uint8_t)sm.m8[d0], b1 = (uint8_t)sm.m8[d0 + 1];
+    uint32_t b2 = (uint8_t)sm.m8[d0 + 8], b3 = (uint8_t)sm.m8[d0 + 9];
+    *reinterpret_cast<uint32_t *>(rec + kOffMu8 + 4 * lane) =
+        b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  }
+  // scales and padding: 16 words from byte 768
+  if (lane < 16) {
+    uint32_t word = 0;
+    if (lane < 4) {
+      word = (uint32_t)__half_as_ushort(sm.sv[2 * lane]) |
+             ((uint32_t)__half_as_ushort(sm.sv[2 * lane + 1]) << 16);
+    } else if (lane < 12) {
+      const int i = 2 * (lane - 4);
+      word = (uint32_t)__half_as_ushort(sm.sc[i]) |
+             ((uint32_t)__half_as_ushort(sm.sc[i + 1]) << 16);
+    } else if (lane == 12) {
+      word = (uint32_t)__half_as_ushort(sm.smu);
+    }
+    *reinterpret_cast<uint32_t *>(rec + kOffSV + 4 * lane) = word;
+  }
+  __syncwarp();
+}
+
+// Algorithm 1 on one page-head held as kx[token][4 dims of this lane]
+// (bf16 values widened to fp32).  Writes the record and returns tau (valid
+// on every lane).
+__device__ float summarize_page(float (&kx)[16][4], BuildSmem &sm,
+                                uint8_t *rec, int lane,
+                                float *unq = nullptr) {
+  // Eq.(2): centroid (fp32, tokens summed in order, then /16) and deviations
+  float mu[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float acc = 0.f;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) acc = __fadd_rn(acc, kx[t][j]);
+    mu[j] = __fmul_rn(acc, 0.0625f);
+  }
+#pragma unroll
+  for (int t = 0; t < 16; ++t)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) kx[t][j] = __fsub_rn(kx[t][j], mu[j]);
+
+  // Eq.(3): Gram matrix D D^T, 136 unique entries in 5 blocks of 32
+  float g[5];
+  {
+    float v[32];
+    gram_block<0>(v, kx, std::make_integer_sequence<int, 32>{});
+    g[0] = reduce_scatter32(v, lane);
+    gram_block<1>(v, kx, std::make_integer_sequence<int, 32>{});
+    g[1] = reduce_scatter32(v, lane);
+    gram_block<2>(v, kx, std::make_integer_sequence<int, 32>{});
+    g[2] = reduce_scatter32(v, lane);
+    gram_block<3>(v, kx, std::make_integer_sequence<int, 32>{});
+    g[3] = reduce_scatter32(v, lane);
+    gram_block<4>(v, kx, std::make_integer_sequence<int, 32>{});
+    g[4] = reduce_scatter32(v, lane);
+  }
+#pragma unroll
+  for (int blk = 0; blk < 5; ++blk) {
+    const int p = 32 * blk + lane;
+    if (p < 136) {
+      const int i = pair_i(p), j = pair_j(p);
+      sm.A[i][j] = g[blk];
+      sm.A[j][i] = g[blk];
+    }
+  }
+  for (int e = lane; e < 256; e += 32)
+    sm.U[e >> 4][e & 15] = ((e >> 4) == (e & 15)) ? 1.f : 0.f;
+  __syncwarp();
+
+  // cyclic Jacobi, round-robin pairs: round r pairs position m with 15-m
+  for (int sweep = 0; sweep < kMaxSweeps; ++sweep) {
+    int rotated = 0;
+    for (int r = 0; r < 15; ++r) {
+      if (lane < 8) {
+        const int m = lane;
+        const int p = (m == 0) ? 0 : 1 + (m - 1 + r) % 15;
+        const int q = 1 + (14 - m + r) % 15;
+        const float app = sm.A[p][p], aqq = sm.A[q][q], apq = sm.A[p][q];
+        float c = 1.f, s = 0.f;
+        if (fabsf(apq) > kJacobiRelTol * sqrtf(fabsf(app) * fabsf(aqq)) &&
+            fabsf(apq) > 1e-30f) {
+          const float theta = (aqq - app) / (2.f * apq);
+          float t;
+          if (fabsf(theta) > 1e15f)
+            t = 0.5f / theta;
+          else
+            t = copysignf(1.f, theta) /
+                (fabsf(theta) + sqrtf(1.f + theta * theta));
+          c = 1.f / sqrtf(1.f + t * t);
+          s = t * c;
+          rotated = 1;
+        }
+        sm.rc[m] = c;
+        sm.rs[m] = s;
+        sm.rp[m] = p;
+        sm.rq[m] = q;
+      }
+      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {  // rows: A <- J^T A
+        const int task = lane + 32 * u, m = task >> 4, j = task & 15;
+        const int p = sm.rp[m], q = sm.rq[m];
+        const float c = sm.rc[m], s = sm.rs[m];
+        const float ap = sm.A[p][j], aq = sm.A[q][j];
+        sm.A[p][j] = c * ap - s * aq;
+        sm.A[q][j] = s * ap + c * aq;
+      }
+      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {  // columns: A <- A J, U <- U J
+        const int task = lane + 32 * u, m = task >> 4, i = task & 15;
+        const int p = sm.rp[m], q = sm.rq[m];
+        const float c = sm.rc[m], s = sm.rs[m];
+        const float ap = sm.A[i][p], aq = sm.A[i][q];
+        sm.A[i][p] = c * ap - s * aq;
+        sm.A[i][q] = s * ap + c * aq;
+        const float up = sm.U[i][p], uq = sm.U[i][q];
+        sm.U[i][p] = c * up - s * uq;
+        sm.U[i][q] = s * up + c * uq;
+      }
+      __syncwarp();
+      if (lane < 8 && sm.rs[lane] != 0.f) {
+        sm.A[sm.rp[lane]][sm.rq[lane]] = 0.f;
+        sm.A[sm.rq[lane]][sm.rp[lane]] = 0.f;
+      }
+      __syncwarp();
+    }
+    if (!__any_sync(0xffffffffu, rotated)) break;
+  }
+
+  // eigenvalues descending (ties: lower index first), clipped at zero
+  if (lane < 16) {
+    const float li = sm.A[lane][lane];
+    int rank = 0;
+    for (int j = 0; j < 16; ++j) {
+      const float lj = sm.A[j][j];
+      rank += (lj > li) || (lj == li && j < lane);
+    }
+    sm.perm[rank] = lane;
+    sm.lam[rank] = fmaxf(li, 0.f);
+  }
+  __syncwarp();
+  // sign rule and per-component factors
+  if (lane < 8) {
+    const int col = sm.perm[lane];
+    float best = -1.f;
+    int bi = 0;
+    for (int i = 0; i < 16; ++i) {
+      const float a = fabsf(sm.U[i][col]);
+      if (a > best) {
+        best = a;
+        bi = i;
+      }
+    }
+    const float sg = sm.U[bi][col] < 0.f ? -1.f : 1.f;
+    const float lam = sm.lam[lane], lam1 = sm.lam[0];
+    const bool keep = lam1 > 0.f && lam > 1e-6f * lam1;
+    const float sig = sqrtf(lam);
+    sm.cv[lane] = keep ? sg / sig : 0.f;
+    sm.cc[lane] = keep ? sg * sig : 0.f;
+  }
+  __syncwarp();
+  float tau = 0.f;
+#pragma unroll
+  for (int k = kRank; k < 16; ++k) tau += sm.lam[k];
+
+  // V = D^T U_r Sigma_r^{-1} (lane rows) and C = U_r Sigma_r (shared)
+  float V[4][8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int col = sm.perm[k];
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float u = sm.U[i][col];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[j] = fmaf(kx[i][j], u, acc[j]);
+    }
+    const float f = sm.cv[k];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) V[j][k] = acc[j] * f;
+  }
+  {
+    const int i = lane >> 1, k0 = (lane & 1) * 4;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const int k = k0 + kk;
+      sm.Cf[i][k] = sm.U[i][sm.perm[k]] * sm.cc[k];
+    }
+  }
+  __syncwarp();
+  if (unq) {  // fp32 values before quantisation: lam, mu, V, C
+    if (lane < 16) unq[lane] = sm.lam[lane];
+    reinterpret_cast<float4 *>(unq + 16)[lane] =
+        make_float4(mu[0], mu[1], mu[2], mu[3]);
+    float4 *vo = reinterpret_cast<float4 *>(unq + 16 + kDim) + lane * 8;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      vo[2 * j] = make_float4(V[j][0], V[j][1], V[j][2], V[j][3]);
+      vo[2 * j + 1] = make_float4(V[j][4], V[j][5], V[j][6], V[j][7]);
+    }
+    const int i = lane >> 1, k0 = (lane & 1) * 4;
+    reinterpret_cast<float4 *>(unq + 16 + kDim + kDim * kRank)[lane] =
+        make_float4(sm.Cf[i][k0], sm.Cf[i][k0 + 1], sm.Cf[i][k0 + 2],
+                    sm.Cf[i][k0 + 3]);
+  }
+  write_record(V, mu, sm, rec, lane);
+  return tau;
+}
+
+__device__ __forceinline__ void load_page_keys(const __nv_bfloat16 *page,
+                                               float (&kx)[16][4], int lane) {
+  const uint2 *src = reinterpret_cast<const uint2 *>(page);
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    const uint2 raw = src[t * 32 + lane];
+    kx[t][0] = bf16_lo(raw.x);
+    kx[t][1] = bf16_hi(raw.x);
+    kx[t][2] = bf16_lo(raw.y);
+    kx[t][3] = bf16_hi(raw.y);
+  }
+}
+
+__global__ void __launch_bounds__(32 * kBuildWarps)
+    build_kernel(const __nv_bfloat16 *__restrict__ k_cache,
+                 int64_t num_phys, int h_kv, const int32_t *__restrict__ pt,
+                 int batch, int max_pages, const int32_t *__restrict__ seq_ids,
+                 const int32_t *__restrict__ page_ids, int n_pairs,
+                 uint8_t *__restrict__ summaries, float *__restrict__ tau_out,
+                 float *__restrict__ unq_out, int32_t *status) {
+  __shared__ BuildSmem smem[kBuildWarps];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  BuildSmem &sm = smem[wid];
+  const long long total = (long long)n_pairs * h_kv;
+  for (long long w = (long long)blockIdx.x * kBuildWarps + wid; w < total;
+       w += (long long)gridDim.x * kBuildWarps) {
+    const int pair = (int)(w / h_kv), h = (int)(w % h_kv);
+    const int b = seq_ids[pair], pg = page_ids[pair];
+    if (b < 0 || b >= batch || pg < 0 || pg >= max_pages) {
+      if (lane == 0) set_status(status, LOCKS_DEV_BAD_PAIR);
+      continue;
+    }
+    const int phys = pt[(size_t)b * max_pages + pg];
+    if (phys < 0 || phys >= num_phys) {
+      if (lane == 0) set_status(status, LOCKS_DEV_BAD_PAGE_ID);
+      continue;
+    }
+    float kx[16][4];
+    load_page_keys(k_cache + ((size_t)phys * h_kv + h) * kPage * kDim, kx,
+                   lane);
+    uint8_t *rec =
+        summaries + (((size_t)b * h_kv + h) * max_pages + pg) * (size_t)kRec;
+    const float tau = summarize_page(
+        kx, sm, rec, lane,
+        unq_out ? unq_out + (size_t)w * LOCKS_UNQUANTISED_FLOATS : nullptr);
+    if (tau_out && lane == 0) tau_out[w] = tau;
+  }
+}
+
+__global__ void __launch_bounds__(32 * kBuildWarps)
+    pack_kernel(const float *__restrict__ mu, const float *__restrict__ basis,
+                const float *__restrict__ coeffs, int n,
+                uint8_t *__restrict__ records) {
+  __shared__ BuildSmem smem[kBuildWarps];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  BuildSmem &sm = smem[wid];
+  for (long long w = (long long)blockIdx.x * kBuildWarps + wid; w < n;
+       w += (long long)gridDim.x * kBuildWarps) {
+    float m[4], V[4][8];
+    const float4 mv = reinterpret_cast<const float4 *>(mu + w * kDim)[lane];
+    m[0] = mv.x;
+    m[1] = mv.y;
+    m[2] = mv.z;
+    m[3] = mv.w;
+    const float4 *vb =
+        reinterpret_cast<const float4 *>(basis + w * kDim * kRank) + lane * 8;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 a = vb[2 * j], c = vb[2 * j + 1];
+      V[j][0] = a.x;
+      V[j][1] = a.y;
+      V[j][2] = a.z;
+      V[j][3] = a.w;
+      V[j][4] = c.x;
+      V[j][5] = c.y;
+      V[j][6] = c.z;
+      V[j][7] = c.w;
+    }
+    const float4 cv =
+        reinterpret_cast<const float4 *>(coeffs + w * kPage * kRank)[lane];
+    const int i = lane >> 1, k0 = (lane & 1) * 4;
+    sm.Cf[i][k0] = cv.x;
+    sm.Cf[i][k0 + 1] = cv.y;
+    sm.Cf[i][k0 + 2] = cv.z;
+    sm.Cf[i][k0 + 3] = cv.w;
+    __syncwarp();
+    write_record(V, m, sm, records + w * (size_t)kRec, lane);
+  }
+}
+
+// One CTA per sequence, one warp per KV head.
+__global__ void append_kernel(const __nv_bfloat16 *__restrict__ k_new,
+                              const __nv_bfloat16 *__restrict__ v_new,
+                              __nv_bfloat16 *k_cache, __nv_bfloat16 *v_cache,
+                              int64_t num_phys, int h_kv,
+                              const int32_t *__restrict__ pt, int max_pages,
+                              int32_t *seq_lens, uint8_t *summaries,
+                              float *tau_out, int32_t *status) {
+  extern __shared__ __align__(16) unsigned char append_smem[];
+  BuildSmem *smem = reinterpret_cast<BuildSmem *>(append_smem);
+  const int b = blockIdx.x;
+  const int lane = threadIdx.x & 31, h = threadIdx.x >> 5;
+  const int pos = seq_lens[b];
+  __syncthreads();
+  bool ok = pos >= 0 && pos < max_pages * kPage;
+  int phys = -1;
+  if (ok) {
+    phys = pt[(size_t)b * max_pages + pos / kPage];
+    if (phys < 0 || phys >= num_phys) {
+      if (lane == 0 && h == 0) set_status(status, LOCKS_DEV_BAD_PAGE_ID);
+      ok = false;
+    }
+  } else if (lane == 0 && h == 0) {
+    set_status(status, LOCKS_DEV_BAD_SEQ_LEN);
+  }
+  if (ok) {
+    const size_t page_off = ((size_t)phys * h_kv + h) * kPage * kDim;
+    const size_t tok_off = page_off + (size_t)(pos % kPage) * kDim;
+    const uint2 kv = reinterpret_cast<const uint2 *>(
+        k_new + ((size_t)b * h_kv + h) * kDim)[lane];
+    const uint2 vv = reinterpret_cast<const uint2 *>(
+        v_new + ((size_t)b * h_kv + h) * kDim)[lane];
+    reinterpret_cast<uint2 *>(k_cache + tok_off)[lane] = kv;
+    reinterpret_cast<uint2 *>(v_cache + tok_off)[lane] = vv;
+    if ((pos + 1) % kPage == 0) {
+      // each lane re-reads exactly the bytes it wrote, so program order
+      // makes the new token visible to this warp's build
+      float kx[16][4];
+      load_page_keys(k_cache + page_off, kx, lane);
+      uint8_t *rec = summaries +
+                     (((size_t)b * h_kv + h) * max_pages + pos / kPage) *
+                         (size_t)kRec;
+      const float tau = summarize_page(kx, smem[h], rec, lane);
+      if (tau_out && lane == 0) tau_out[(size_t)b * h_kv + h] = tau;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && ok) seq_lens[b] = pos + 1;
+}
+
+// --------------------------------------------------------------------------
+// launchers
+// --------------------------------------------------------------------------
+static int grid_for(long long warps, int warps_per_cta) {
+  long long g = (warps + warps_per_cta - 1) / warps_per_cta;
+  if (g > 65535LL * 32) g = 65535LL * 32;
+  return (int)(g < 1 ? 1 : g);
+}
+
+cudaError_t launch_build(const void *k_cache, int64_t num_phys, int h_kv,
+                         const int32_t *pt, int batch, int max_pages,
+                         const int32_t *seq_ids, const int32_t *page_ids,
+                         int n_pairs, void *summaries, float *tau_out,
+                         float *unq_out, int32_t *status,
+                         cudaStream_t stream) {
+  const long long warps = (long long)n_pairs * h_kv;
+  if (warps == 0) return cudaSuccess;
+  build_kernel<<<grid_for(warps, kBuildWarps), 32 * kBuildWarps, 0, stream>>>(
+      static_cast<const __nv_bfloat16 *>(k_cache), num_phys, h_kv, pt, batch,
+      max_pages, seq_ids, page_ids, n_pairs,
+      static_cast<uint8_t *>(summaries), tau_out, unq_out, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack(const float *mu, const float *basis,
+                        const float *coeffs, int n, void *records,
+                        cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  pack_kernel<<<grid_for(n, kBuildWarps), 32 * kBuildWarps, 0, stream>>>(
+      mu, basis, coeffs, n, static_cast<uint8_t *>(records));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const void *k_new, const void *v_new, void *k_cache,
+                          void *v_cache, int64_t num_phys, int h_kv,
+                          const int32_t *pt, int batch, int max_pages,
+                          int32_t *seq_lens, void *summaries, float *tau_out,
+                          int32_t *status, cudaStream_t stream) {
+  if (batch == 0) return cudaSuccess;
+  const size_t smem = sizeof(BuildSmem) * (size_t)h_kv;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(
+        append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (int)(sizeof(BuildSmem) * 32));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  append_kernel<<<batch, 32 * h_kv, smem, stream>>>(
+      static_cast<const __nv_bfloat16 *>(k_new),
+      static_cast<const __nv_bfloat16 *>(v_new),
+      static_cast<__nv_bfloat16 *>(k_cache),
+      static_cast<__nv_bfloat16 *>(v_cache), num_phys, h_kv, pt, max_pages,
+      seq_lens, static_cast<uint8_t *>(summaries), tau_out, status);
+  return cudaGetLastError();
+}
+
+}  // namespace locks

@@ -1,0 +1,48 @@
+// Internal launchers of the LOCKS kernels (called by the C ABI in api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace locks {
+
+cudaError_t launch_build(const void *k_cache, int64_t num_phys, int h_kv,
+                         const int32_t *pt, int batch, int max_pages,
+                         const int32_t *seq_ids, const int32_t *page_ids,
+                         int n_pairs, void *summaries, float *tau_out,
+                         float *unq_out, int32_t *status,
+                         cudaStream_t stream);
+
+cudaError_t launch_pack(const float *mu, const float *basis,
+                        const float *coeffs, int n, void *records,
+                        cudaStream_t stream);
+
+cudaError_t launch_append(const void *k_new, const void *v_new, void *k_cache,
+                          void *v_cache, int64_t num_phys, int h_kv,
+                          const int32_t *pt, int batch, int max_pages,
+                          int32_t *seq_lens, void *summaries, float *tau_out,
+                          int32_t *status, cudaStream_t stream);
+
+cudaError_t launch_score(const void *q, const void *summaries,
+                         const int32_t *seq_lens, int batch, int h_kv, int G,
+                         int max_pages, float *s_hat, int32_t *status,
+                         cudaStream_t stream);
+
+cudaError_t launch_select(const float *scores, const int32_t *seq_lens,
+                          int batch, int h_kv, int G, int max_pages, int k,
+                          int32_t *idx, uint32_t *keybuf, int32_t *status,
+                          cudaStream_t stream);
+
+cudaError_t launch_decode(const void *q, const void *k_cache,
+                          const void *v_cache, int64_t num_phys,
+                          const int32_t *pt, const int32_t *seq_lens,
+                          const int32_t *idx, int k, int batch, int h_kv,
+                          int G, int max_pages, void *o_out, float *lse_out,
+                          float *o_part, float *lse_part, int32_t *status,
+                          cudaStream_t stream);
+
+int score_max_batch();
+int decode_pages_per_split(int list_len, long long units);
+
+}  // namespace locks

@@ -181,27 +181,89 @@ def seq_lengths(spec: WorkloadSpec) -> list:
     return [L if L % PAGE else L - 1 for L in lens]
 
 
+def _layout(spec: WorkloadSpec):
+    """Prompt lengths, pages per sequence (appended tokens included)."""
+    lens = seq_lengths(spec)
+    n_pages = [math.ceil((L + spec.append_steps) / PAGE) for L in lens]
+    return lens, n_pages
+
+
+def _needles(spec: WorkloadSpec, b: int, full_prompt: int):
+    """Needle pages [h_kv][needles], unit directions [h_kv][needles][128]
+    and token slots [h_kv][needles] of sequence b (CPU sub-stream)."""
+    gn = _gen("cpu", spec.seed, 2000 + b)
+    nn = spec.needles
+    pages = torch.zeros(spec.h_kv, nn, dtype=torch.int64)
+    dirs = torch.zeros(spec.h_kv, nn, HEAD_DIM)
+    for h in range(spec.h_kv):
+        lo, hi = 1, max(1, full_prompt - 2)
+        cand = torch.randperm(hi - lo + 1, generator=gn)[:nn] + lo
+        pages[h, :len(cand)] = cand
+        d = torch.randn(nn, HEAD_DIM, generator=gn)
+        dirs[h] = d / d.norm(dim=-1, keepdim=True)
+    toks = torch.randint(0, PAGE, (spec.h_kv, nn), generator=gn)
+    return pages, dirs, toks
+
+
+def sequence_chunks(spec: WorkloadSpec, b: int, device, chunk_pages=2048):
+    """Yield (p0, p1, keys, values) for logical pages [p0, p1) of sequence b,
+    float32 [p1-p0][h_kv][16][128], needles planted."""
+    lens, n_pages = _layout(spec)
+    n = n_pages[b]
+    pages, dirs, toks = _needles(spec, b, lens[b] // PAGE)
+    gk = _gen(device, spec.seed, 1000 + b)
+    for p0 in range(0, n, chunk_pages):
+        p1 = min(n, p0 + chunk_pages)
+        cnt = (p1 - p0) * spec.h_kv
+        keys = page_keys(gk, cnt, _rho(spec, gk, cnt, device), device)
+        keys = keys.view(p1 - p0, spec.h_kv, PAGE, HEAD_DIM)
+        for h in range(spec.h_kv):
+            for t in range(spec.needles):
+                pg = int(pages[h, t])
+                if p0 <= pg < p1:
+                    row = keys[pg - p0, h, int(toks[h, t])]
+                    keys[pg - p0, h, int(toks[h, t])] = row.norm() * \
+                        dirs[h, t].to(device)
+        vals = torch.randn(p1 - p0, spec.h_kv, PAGE, HEAD_DIM, generator=gk,
+                           device=device)
+        yield p0, p1, keys, vals
+
+
+def _queries(spec: WorkloadSpec, device, n_steps, needle_dirs):
+    """[steps][batch][h_q][128] N(0, I), re-aimed at the needles."""
+    gq = _gen(device, spec.seed, 3000)
+    q = torch.randn(n_steps, spec.batch, spec.h_q, HEAD_DIM, generator=gq,
+                    device=device)
+    nn = spec.needles
+    if nn:
+        G = spec.group
+        dirs = needle_dirs.to(device)
+        for h in range(spec.h_kv):
+            for g in range(G):
+                nd = dirs[:, h, g % nn]                       # [batch][128]
+                z = q[:, :, h * G + g]                        # [steps][batch][128]
+                zn = z.norm(dim=-1, keepdim=True)
+                u = z - (z * nd).sum(-1, keepdim=True) * nd
+                u = u / u.norm(dim=-1, keepdim=True)
+                q[:, :, h * G + g] = zn * (0.6 * nd + 0.8 * u)
+    return q.to(torch.bfloat16)
+
+
 def generate(spec: WorkloadSpec, device="cpu",
              seqs: Optional[Sequence[int]] = None,
              chunk_pages: int = 2048,
              steps: Optional[int] = None) -> Workload:
-    """Draw the workload on `device`.
+    """Draw the whole workload on `device`.
 
-    `seqs` restricts generation to a subset of sequences (the others keep a
-    zero cache); every sequence draws from its own seeded sub-stream, so a
-    sequence's contents do not depend on which others are generated on the
-    same device type.  `steps` overrides the number of query steps drawn.
+    Every sequence draws from its own seeded sub-stream, so a sequence's
+    contents do not depend on which others are generated (on one device
+    type).  `seqs` restricts generation to a subset (the others keep a zero
+    cache); `steps` overrides the number of query steps drawn.
     """
     device = torch.device(device)
-    lens = seq_lengths(spec)
-    extra = math.ceil(spec.append_steps / PAGE) if spec.append_steps else 0
-    n_pages = [math.ceil(L / PAGE) + extra for L in lens]
-    if spec.append_steps and any(L % PAGE for L in lens):
-        # appended tokens fill the partial page first
-        n_pages = [math.ceil((L + spec.append_steps) / PAGE) for L in lens]
+    lens, n_pages = _layout(spec)
     max_pages = max(n_pages)
     total = sum(n_pages)
-    # physical page assignment
     pg = _gen("cpu", spec.seed, 7)
     phys = torch.arange(total) if spec.contiguous else torch.randperm(
         total, generator=pg)
@@ -216,82 +278,55 @@ def generate(spec: WorkloadSpec, device="cpu",
     nn = spec.needles
     needle_pages = torch.zeros(spec.batch, spec.h_kv, nn, dtype=torch.int64)
     needle_dirs = torch.zeros(spec.batch, spec.h_kv, nn, HEAD_DIM)
-    n_steps = spec.steps if steps is None else steps
     k_app = v_app = None
     if spec.append_steps:
         k_app = torch.zeros(spec.append_steps, spec.batch, spec.h_kv,
                             HEAD_DIM, dtype=torch.bfloat16, device=device)
         v_app = torch.zeros_like(k_app)
-    todo = range(spec.batch) if seqs is None else seqs
     pt_dev = page_table.to(device)
-    for b in todo:
-        gk = _gen(device, spec.seed, 1000 + b)
-        gn = _gen("cpu", spec.seed, 2000 + b)
-        n = n_pages[b]
-        prompt_pages = math.ceil(lens[b] / PAGE)
-        full_prompt = lens[b] // PAGE
-        # needles: distinct pages in [1, full_prompt - 2], one token each
-        for h in range(spec.h_kv):
-            lo, hi = 1, max(1, full_prompt - 2)
-            cand = torch.randperm(hi - lo + 1, generator=gn)[:nn] + lo
-            needle_pages[b, h, :len(cand)] = cand
-            d = torch.randn(nn, HEAD_DIM, generator=gn)
-            needle_dirs[b, h] = d / d.norm(dim=-1, keepdim=True)
-        needle_tok = torch.randint(0, PAGE, (spec.h_kv, nn), generator=gn)
-        for p0 in range(0, n, chunk_pages):
-            p1 = min(n, p0 + chunk_pages)
-            cnt = (p1 - p0) * spec.h_kv
-            keys = page_keys(gk, cnt, _rho(spec, gk, cnt, device), device)
-            keys = keys.view(p1 - p0, spec.h_kv, PAGE, HEAD_DIM)
-            for h in range(spec.h_kv):
-                for t in range(nn):
-                    pg_id = int(needle_pages[b, h, t])
-                    if p0 <= pg_id < p1:
-                        tok = int(needle_tok[h, t])
-                        row = keys[pg_id - p0, h, tok]
-                        keys[pg_id - p0, h, tok] = row.norm() * \
-                            needle_dirs[b, h, t].to(device)
-            vals = torch.randn(p1 - p0, spec.h_kv, PAGE, HEAD_DIM,
-                               generator=gk, device=device)
+    for b in (range(spec.batch) if seqs is None else seqs):
+        needle_pages[b], needle_dirs[b], _ = _needles(spec, b,
+                                                      lens[b] // PAGE)
+        for p0, p1, keys, vals in sequence_chunks(spec, b, device,
+                                                  chunk_pages):
             ids = pt_dev[b, p0:p1].long()
             k_cache.index_copy_(0, ids, keys.to(torch.bfloat16))
             v_cache.index_copy_(0, ids, vals.to(torch.bfloat16))
-        if spec.append_steps:
-            # the appended tokens are the positions lens[b] .. lens[b]+T-1;
-            # their keys were drawn above with the page generator, move them
-            # out of the cache into the per-step append stream.
-            for s in range(spec.append_steps):
-                pos = lens[b] + s
-                pid = int(page_table[b, pos // PAGE])
-                k_app[s, b] = k_cache[pid, :, pos % PAGE]
-                v_app[s, b] = v_cache[pid, :, pos % PAGE]
-            for s in range(spec.append_steps):
-                pos = lens[b] + s
-                pid = int(page_table[b, pos // PAGE])
-                k_cache[pid, :, pos % PAGE] = 0
-                v_cache[pid, :, pos % PAGE] = 0
-        del prompt_pages
-    # queries: one N(0, I) draw per (step, seq, head), needles re-aimed
-    gq = _gen(device, spec.seed, 3000)
-    q = torch.randn(n_steps, spec.batch, spec.h_q, HEAD_DIM, generator=gq,
-                    device=device)
-    if nn:
-        G = spec.group
-        dirs = needle_dirs.to(device)
-        for h in range(spec.h_kv):
-            for g in range(G):
-                nd = dirs[:, h, g % nn]                       # [batch][128]
-                z = q[:, :, h * G + g]                        # [steps][batch][128]
-                zn = z.norm(dim=-1, keepdim=True)
-                u = z - (z * nd).sum(-1, keepdim=True) * nd
-                u = u / u.norm(dim=-1, keepdim=True)
-                q[:, :, h * G + g] = zn * (0.6 * nd + 0.8 * u)
+        # appended tokens (positions lens[b] ..) leave the cache for the
+        # per-step append stream
+        for s in range(spec.append_steps):
+            pos = lens[b] + s
+            pid = int(page_table[b, pos // PAGE])
+            k_app[s, b] = k_cache[pid, :, pos % PAGE]
+            v_app[s, b] = v_cache[pid, :, pos % PAGE]
+            k_cache[pid, :, pos % PAGE] = 0
+            v_cache[pid, :, pos % PAGE] = 0
+    n_steps = spec.steps if steps is None else steps
+    q = _queries(spec, device, n_steps, needle_dirs)
     return Workload(spec=spec, k_cache=k_cache, v_cache=v_cache,
                     page_table=page_table.to(device),
                     seq_lens=torch.tensor(lens, dtype=torch.int32,
                                           device=device),
-                    queries=q.to(torch.bfloat16), needle_pages=needle_pages,
+                    queries=q, needle_pages=needle_pages,
                     needle_dirs=needle_dirs, k_append=k_app, v_append=v_app)
+
+
+def generate_sequence(spec: WorkloadSpec, b: int, device="cpu",
+                      steps: Optional[int] = None):
+    """One sequence in logical page order (no page table): dict with keys and
+    values bf16 [n_pages][h_kv][16][128], its prompt length and its queries
+    bf16 [steps][h_q][128]."""
+    lens, n_pages = _layout(spec)
+    ks, vs = [], []
+    for _, _, keys, vals in sequence_chunks(spec, b, device):
+        ks.append(keys.to(torch.bfloat16))
+        vs.append(vals.to(torch.bfloat16))
+    needle_dirs = torch.zeros(spec.batch, spec.h_kv, spec.needles, HEAD_DIM)
+    needle_dirs[b] = _needles(spec, b, lens[b] // PAGE)[1]
+    n_steps = spec.steps if steps is None else steps
+    q = _queries(spec, device, n_steps, needle_dirs)[:, b]
+    return dict(keys=torch.cat(ks), values=torch.cat(vs), seq_len=lens[b],
+                queries=q)
 
 
 def custom_spec(**kw) -> WorkloadSpec:

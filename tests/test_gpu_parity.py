@@ -1,0 +1,486 @@
+"""GPU parity: every step of the CUDA path against the float64 oracle.
+
+Tolerances (from the LOCKS decode specification, the design doc lists them):
+  * quantised bytes: bit-exact where both sides quantise the same fp32
+    values (the pack entry point, the centroid); after the eigensolver,
+    codes may differ by one step only where the oracle's value lies near a
+    rounding boundary, up to eigenvector sign
+  * reconstructions C V^T (fp32, before quantisation): relative Frobenius
+    error <= 1e-3, up to sign, on pages whose kept spectrum is separated
+  * page scores from the same records: absolute error <= 1e-3
+  * selections: identical except pages whose oracle log share-average lies
+    within the window of the k-th boundary
+  * attention: max |o - o_ref| <= 2e-2 * max |o_ref|; |lse - lse_ref| <= 1e-3
+Inputs flow only oracle -> GPU (records, indices), never the other way.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import locks_oracle as O
+from sparse_paged_kv_locks_gb300 import binding as B
+from sparse_paged_kv_locks_gb300 import workload as W
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+S_TOL = 1e-3
+O_TOL = 2e-2
+LSE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.lib()
+
+
+def full_pairs(lens):
+    seq, pg = [], []
+    for b, L in enumerate(lens):
+        for p in range(int(L) // 16):
+            seq.append(b)
+            pg.append(p)
+    return np.array(seq, np.int32), np.array(pg, np.int32)
+
+
+def i32(x):
+    return torch.as_tensor(np.asarray(x), dtype=torch.int32, device=DEV)
+
+
+def gpu_build(wl_dev, lens, want_unq=False):
+    seq, pg = full_pairs(lens)
+    batch, max_pages = wl_dev.page_table.shape
+    h_kv = wl_dev.k_cache.shape[1]
+    store = B.new_summary_store(batch, h_kv, max_pages, DEV)
+    tau = torch.zeros(len(seq) * h_kv, dtype=torch.float32, device=DEV)
+    unq = torch.zeros(len(seq) * h_kv * B.UNQUANTISED_FLOATS,
+                      dtype=torch.float32, device=DEV) if want_unq else None
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.locks_build_summaries(wl_dev.k_cache, wl_dev.page_table, i32(seq),
+                            i32(pg), store, tau, unq, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return store, tau, unq, seq, pg
+
+
+class Dev:
+    """A workload moved to the GPU."""
+
+    def __init__(self, wl):
+        self.k_cache = wl.k_cache.to(DEV)
+        self.v_cache = wl.v_cache.to(DEV)
+        self.page_table = wl.page_table.to(DEV)
+        self.seq_lens = wl.seq_lens.to(DEV)
+        self.queries = wl.queries.to(DEV)
+
+
+def host(wl):
+    return (wl.k_cache.float().numpy(), wl.v_cache.float().numpy(),
+            wl.page_table.numpy(), [int(x) for x in wl.seq_lens])
+
+
+def s_hat_from_ws(ws, batch, h_kv, G, max_pages):
+    n = batch * h_kv * G * max_pages
+    return ws[256:256 + 4 * n].view(torch.float32).view(
+        batch, h_kv, G, max_pages).cpu().numpy()
+
+
+def log_share_average(s_hat_bh, L):
+    nf = L // 16
+    return np.log(O.share_average(s_hat_bh, nf))
+
+
+def selection_agrees(idx_gpu, idx_orc, s_hat_bh, L, k, window):
+    """Sets equal except pages whose oracle log share-average lies within
+    `window` of the (k-2)-th candidate's."""
+    a = set(int(x) for x in idx_gpu if x >= 0)
+    b = set(int(x) for x in idx_orc if x >= 0)
+    if a == b:
+        return True, 0
+    n = -(-L // 16)
+    lm = log_share_average(s_hat_bh, L)
+    cand = np.arange(1, n - 1)
+    order = cand[np.lexsort((cand, -lm[cand]))]
+    boundary = lm[order[k - 3]]
+    for p in a ^ b:
+        if p in (0, n - 1) or abs(lm[p] - boundary) > window:
+            return False, len(a ^ b)
+    return True, len(a ^ b)
+
+
+# ---------------------------------------------------------------------------
+# quantiser and record layout: bit-exact
+# ---------------------------------------------------------------------------
+def test_pack_is_bit_exact():
+    rng = np.random.default_rng(0)
+    n = 300
+    mu = rng.normal(0, 0.5, (n, 128)).astype(np.float32)
+    V = np.linalg.qr(rng.normal(size=(n, 128, 8)))[0].astype(np.float32)
+    C = (rng.normal(size=(n, 16, 8)) * 3).astype(np.float32)
+    # edge cases: zero column / row / centroid, tiny values, saturation,
+    # exact half-way codes (scale 0.0625 with values k.5 * scale)
+    V[0, :, 3] = 0.0
+    C[1, 5, :] = 0.0
+    mu[2, :] = 0.0
+    V[3] *= 1e-30
+    C[4] *= 1e9
+    V[5, :, 0] = 0.0
+    V[5, 0, 0] = 7 * 0.0625
+    V[5, 1:8, 0] = np.array([3.5, 2.5, -2.5, -3.5, 0.5, -0.5, 1.5]) * 0.0625
+    q = O.quantize_summary(mu, V, C)
+    expect = O.encode_records(q)
+    rec = torch.zeros(n * 832, dtype=torch.uint8, device=DEV)
+    B.locks_pack_summaries(torch.from_numpy(mu).to(DEV),
+                           torch.from_numpy(V).to(DEV),
+                           torch.from_numpy(C).to(DEV), rec)
+    got = rec.view(n, 832).cpu().numpy()
+    bad = np.nonzero((got != expect).any(axis=1))[0]
+    assert bad.size == 0, f"records differ: {bad[:10]}"
+
+
+# ---------------------------------------------------------------------------
+# build (Algorithm 1)
+# ---------------------------------------------------------------------------
+def _degenerate_workload():
+    spec = W.custom_spec(batch=2, h_q=4, h_kv=2, ctx=16 * 24, k=6, needles=0,
+                         seed=5)
+    wl = W.generate(spec, "cpu")
+    kc = wl.k_cache
+    pt = wl.page_table
+    # page 3 of seq 0: 16 identical keys (D = 0); page 4: exact rank 2 with
+    # small integers, so bf16 holds it exactly and the centring is exact
+    p3 = int(pt[0, 3])
+    kc[p3] = kc[p3, :, :1].clone().expand(-1, 16, -1)
+    p4 = int(pt[0, 4])
+    g = torch.Generator().manual_seed(3)
+    base = torch.randint(-4, 5, (2, 1, 128), generator=g).float()
+    dirs = torch.randint(-1, 2, (2, 2, 128), generator=g).float()
+    coef = torch.randint(-3, 4, (2, 16, 2), generator=g).float()
+    kc[p4] = (base + coef @ dirs).to(torch.bfloat16)
+    return wl
+
+
+@pytest.mark.parametrize("which", ["tiny_4k", "degenerate"])
+def test_build_matches_oracle(which):
+    wl = W.generate(W.SPECS["tiny_4k"], "cpu") if which == "tiny_4k" \
+        else _degenerate_workload()
+    d = Dev(wl)
+    kc, vc, pt, lens = host(wl)
+    batch, max_pages = pt.shape
+    store, tau, unq, seq, pg = gpu_build(d, lens, want_unq=True)
+    h_kv = kc.shape[1]
+    # oracle, same pages
+    keys = kc[pt[seq, pg]]                                  # [n][h_kv][16][128]
+    q8, s = O.build_page(keys)
+    orc = O.encode_records(q8)                               # [n][h_kv][832]
+    got = store.cpu().numpy()[seq, :, pg]                    # [n][h_kv][832]
+    gq = O.decode_records(got)
+    # centroid codes and scale: bit-exact (same fp32 rule on both sides)
+    assert (gq["mu8"] == q8["mu8"]).all()
+    assert (gq["smu"] == q8["smu"]).all()
+    # eigenvalues, basis, reconstructions
+    u = unq.view(len(seq), h_kv, -1).cpu().numpy().astype(np.float64)
+    lam_g = u[..., :16]
+    mu_g = u[..., 16:144]
+    V_g = u[..., 144:144 + 1024].reshape(len(seq), h_kv, 128, 8)
+    C_g = u[..., 1168:].reshape(len(seq), h_kv, 16, 8)
+    lam1 = s["lam"][..., :1]
+    assert np.abs(lam_g - s["lam"]).max() <= 1e-5 * max(1.0, lam1.max())
+    assert np.abs(mu_g - s["mu"]).max() < 1e-6
+    assert np.abs(tau.view(len(seq), h_kv).cpu().numpy() - s["tau"]).max() \
+        <= 1e-4 * max(1.0, lam1.max())
+    R_g = C_g @ np.swapaxes(V_g, -1, -2)
+    R_o = s["C"] @ np.swapaxes(s["V"], -1, -2)
+    gap = (s["lam"][..., 7] - s["lam"][..., 8]) / np.maximum(lam1[..., 0],
+                                                              1e-30)
+    nrm = np.linalg.norm(R_o, axis=(-2, -1))
+    err = np.linalg.norm(R_g - R_o, axis=(-2, -1)) / np.maximum(nrm, 1e-30)
+    zero = nrm < 1e-12
+    assert (np.linalg.norm(R_g, axis=(-2, -1))[zero] < 1e-6).all()
+    # the rank-8 subspace is determined to ~eps/gap: pages whose kept
+    # spectrum separates by >= 1e-3 lambda_1 meet 1e-3; closer gaps get the
+    # bound scaled by 1e-3/gap
+    ok = (gap > 1e-3) & ~zero
+    near = (gap > 1e-5) & (gap <= 1e-3) & ~zero
+    assert err[ok].max(initial=0) <= 1e-3, float(err[ok].max())
+    assert (err[near] <= 1e-3 * (1e-3 / gap[near])).all()
+    assert ok.mean() > 0.8 if which == "tiny_4k" else ok.sum() > 0
+    # kept basis columns orthonormal
+    keep = s["lam"][..., :8] > 1e-6 * lam1
+    VtV = np.swapaxes(V_g, -1, -2) @ V_g
+    for i, j in zip(*np.nonzero(keep.all(axis=-1))):
+        assert np.abs(VtV[i, j] - np.eye(8)).max() < 1e-4
+    # codes after sign alignment: off by at most one, only near a boundary
+    sgn = np.sign(np.einsum("nhdk,nhdk->nhk", V_g, s["V"]))
+    sgn[sgn == 0] = 1
+    lam = s["lam"]
+    above = np.concatenate([np.full(lam[..., :1].shape, np.inf),
+                            lam[..., :7]], -1)
+    rel_gap = np.minimum(above - lam[..., :8], lam[..., :8] - lam[..., 1:9])
+    rel_gap = rel_gap / np.maximum(lam1, 1e-30)
+    comp_ok = (rel_gap > 1e-3) & keep                       # [n][h][8]
+    V4g = gq["V4"].astype(np.int64) * sgn[..., None, :].astype(np.int64)
+    dv = np.abs(V4g - q8["V4"])
+    sv = q8["sV"].astype(np.float32)
+    xs = s["V"].astype(np.float32) / np.where(sv == 0, 1, sv)[..., None, :]
+    near = np.abs(np.abs(xs - np.floor(xs)) - 0.5) < 0.05
+    m = comp_ok[..., None, :] & np.ones_like(dv, bool)
+    assert dv[m].max(initial=0) <= 1
+    assert not ((dv > 0) & m & ~near).any()
+    assert (dv[m] > 0).mean() < 0.01
+    # coefficient codes on page-heads whose kept components all separate
+    full = comp_ok.all(axis=-1)
+    C8g = gq["C8"].astype(np.int64) * sgn[..., None, :].astype(np.int64)
+    dc = np.abs(C8g - q8["C8"])[full]
+    assert dc.max(initial=0) <= 1 and (dc > 0).mean() < 0.01
+
+
+# ---------------------------------------------------------------------------
+# score (Eq.(4)) from identical records
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("G,h_kv", [(4, 2), (1, 4), (8, 1), (16, 1), (5, 2)])
+def test_score_matches_oracle_on_same_records(G, h_kv):
+    spec = W.custom_spec(batch=3, h_q=G * h_kv, h_kv=h_kv, ctx=16 * 70 + 9,
+                         k=10, needles=0, seed=20 + G)
+    wl = W.generate(spec, "cpu")
+    kc, vc, pt, lens = host(wl)
+    lens = [16 * 70 + 9, 16 * 3, 16 * 45 + 1]
+    batch, max_pages = pt.shape
+    seq, pg = full_pairs(lens)
+    store, _ = O.build_summaries(kc, pt, seq, pg, batch, max_pages)
+    q = wl.queries[0].float().numpy()
+    s_orc = O.score_store(q, store, lens)
+    ws = B.new_workspace(batch, spec.h_q, h_kv, max_pages, spec.k, DEV)
+    idx = torch.zeros(batch, h_kv, spec.k, dtype=torch.int32, device=DEV)
+    B.locks_score_select(wl.queries[0].to(DEV), torch.from_numpy(store).to(DEV),
+                         i32(lens), spec.k, idx, ws)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == 0
+    s_gpu = s_hat_from_ws(ws, batch, h_kv, G, max_pages)
+    for b in range(batch):
+        nf = lens[b] // 16
+        d = np.abs(s_gpu[b, :, :, :nf] - s_orc[b, :, :, :nf])
+        assert d.max(initial=0) <= S_TOL, (b, float(d.max()))
+    idx_o = O.select_store(s_orc, lens, spec.k)
+    ig = idx.cpu().numpy()
+    for b in range(batch):
+        for h in range(h_kv):
+            ok, _ = selection_agrees(ig[b, h], idx_o[b, h], s_orc[b, h],
+                                     lens[b], spec.k, 1e-3)
+            assert ok, (b, h, ig[b, h], idx_o[b, h])
+
+
+# ---------------------------------------------------------------------------
+# select (Eq.(5) + sink/recent) from identical scores
+# ---------------------------------------------------------------------------
+def test_select_matches_oracle_on_same_scores():
+    rng = np.random.default_rng(7)
+    batch, h_kv, G, max_pages, k = 7, 3, 4, 300, 12
+    lens = [0, 5, 16, 16 * 12, 16 * 12 + 3, 16 * 300, 16 * 257 + 15]
+    scores = rng.normal(0, 3, (batch, h_kv, G, max_pages)).astype(np.float32)
+    scores[5, 1, :, :] = 1.0                      # all equal: lowest index
+    ws = B.new_workspace(batch, G * h_kv, h_kv, max_pages, k, DEV)
+    idx = torch.zeros(batch, h_kv, k, dtype=torch.int32, device=DEV)
+    B.locks_select_pages(torch.from_numpy(scores).to(DEV), i32(lens),
+                         G * h_kv, k, idx, ws)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == 0
+    ig = idx.cpu().numpy()
+    io = O.select_store(scores.astype(np.float64), lens, k)
+    for b in range(batch):
+        for h in range(h_kv):
+            ok, nd = selection_agrees(ig[b, h], io[b, h],
+                                      scores[b, h].astype(np.float64),
+                                      lens[b], k, 1e-4)
+            assert ok, (b, h, ig[b, h], io[b, h])
+    assert (ig[0] == -1).all()
+    assert (ig[1, :, 0] == 0).all() and (ig[1, :, 1:] == -1).all()
+    assert list(ig[3, 0]) == list(range(12))        # 12 pages = k: all
+    assert list(ig[5, 1]) == list(range(11)) + [299]
+    for b in range(batch):
+        for h in range(h_kv):
+            v = [x for x in ig[b, h] if x >= 0]
+            assert v == sorted(v) and len(set(v)) == len(v)
+
+
+# ---------------------------------------------------------------------------
+# sparse attention over the oracle's selection
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("G,h_kv,k", [(4, 2, 8), (8, 1, 5), (16, 1, 16),
+                                      (1, 3, 4), (3, 2, 64)])
+def test_sparse_decode_matches_oracle(G, h_kv, k):
+    spec = W.custom_spec(batch=4, h_q=G * h_kv, h_kv=h_kv, ctx=16 * 40,
+                         k=k, needles=0, seed=40 + G + k)
+    wl = W.generate(spec, "cpu")
+    kc, vc, pt, _ = host(wl)
+    lens = [16 * 40, 16 * 33 + 7, 0, 9]
+    batch, max_pages = pt.shape
+    rng = np.random.default_rng(G + k)
+    s_hat = rng.normal(0, 2, (batch, h_kv, G, max_pages))
+    idx_o = O.select_store(s_hat, lens, k)
+    q = wl.queries[0].float().numpy()
+    o_ref, lse_ref = O.sparse_decode(q, kc, vc, pt, lens, idx_o)
+    d = Dev(wl)
+    ws = B.new_workspace(batch, spec.h_q, h_kv, max_pages,
+                         max(k, max_pages), DEV)
+    o = torch.empty(batch, spec.h_q, 128, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(batch, spec.h_q, dtype=torch.float32, device=DEV)
+    for mode in ("sparse", "dense"):
+        if mode == "sparse":
+            B.locks_sparse_decode(d.queries[0], d.k_cache, d.v_cache,
+                                  d.page_table, i32(lens), i32(idx_o), k, o,
+                                  lse, ws)
+            ro, rl = o_ref, lse_ref
+        else:
+            B.locks_sparse_decode(d.queries[0], d.k_cache, d.v_cache,
+                                  d.page_table, i32(lens), None, 0, o, lse,
+                                  ws)
+            ro, rl = O.dense_decode(q, kc, vc, pt, lens)
+        torch.cuda.synchronize()
+        assert B.locks_read_status(ws) == 0
+        og, lg = o.float().cpu().numpy(), lse.cpu().numpy()
+        for b in range(batch):
+            if lens[b] == 0:
+                assert (og[b] == 0).all() and np.isneginf(lg[b]).all()
+                continue
+            assert np.abs(og[b] - ro[b]).max() <= O_TOL * np.abs(ro[b]).max()
+            assert np.abs(lg[b] - rl[b]).max() <= LSE_TOL
+
+
+# ---------------------------------------------------------------------------
+# the whole step on the 4K-context workload, 8 decode steps
+# ---------------------------------------------------------------------------
+def test_end_to_end_tiny_workload():
+    spec = W.SPECS["tiny_4k"]
+    wl = W.generate(spec, "cpu")
+    d = Dev(wl)
+    kc, vc, pt, lens = host(wl)
+    batch, max_pages = pt.shape
+    store, _, _, seq, pg = gpu_build(d, lens)
+    ostore, _ = O.build_summaries(kc, pt, seq, pg, batch, max_pages)
+    dec = B.LocksDecoder(d.k_cache, d.v_cache, d.page_table, store, spec.h_q,
+                         spec.k)
+    n_same = 0
+    for step in range(spec.steps):
+        o, lse = dec.step(d.queries[step], d.seq_lens)
+        torch.cuda.synchronize()
+        assert dec.status() == 0
+        q = wl.queries[step].float().numpy()
+        s_orc = O.score_store(q, ostore, lens)
+        s_gpu = s_hat_from_ws(dec.workspace, batch, spec.h_kv, spec.group,
+                              max_pages)
+        idx_o = O.select_store(s_orc, lens, spec.k)
+        ig = dec.idx.cpu().numpy()
+        o_ref, lse_ref = O.sparse_decode(q, kc, vc, pt, lens, idx_o)
+        og, lg = o.float().cpu().numpy(), lse.cpu().numpy()
+        for h in range(spec.h_kv):
+            nf = lens[0] // 16
+            window = 2 * np.abs(s_gpu[0, h, :, :nf] - s_orc[0, h, :, :nf]).max() \
+                + 1e-3
+            ok, _ = selection_agrees(ig[0, h], idx_o[0, h], s_orc[0, h],
+                                     lens[0], spec.k, window)
+            assert ok
+            if set(ig[0, h]) == set(idx_o[0, h]):
+                n_same += 1
+                sl = slice(h * spec.group, (h + 1) * spec.group)
+                assert np.abs(og[0, sl] - o_ref[0, sl]).max() <= \
+                    O_TOL * np.abs(o_ref[0, sl]).max()
+                assert np.abs(lg[0, sl] - lse_ref[0, sl]).max() <= LSE_TOL
+    assert n_same >= spec.steps * spec.h_kv // 2
+
+
+# ---------------------------------------------------------------------------
+# append + incremental build
+# ---------------------------------------------------------------------------
+def test_append_builds_filled_pages():
+    spec = W.custom_spec(batch=3, h_q=8, h_kv=2, ctx=16 * 6 + 13, k=4,
+                         steps=20, needles=0, seed=9, append_steps=20)
+    wl = W.generate(spec, "cpu")
+    d = Dev(wl)
+    batch, max_pages = wl.page_table.shape
+    store = B.new_summary_store(batch, spec.h_kv, max_pages, DEV)
+    lens0 = [int(x) for x in wl.seq_lens]
+    seq, pg = full_pairs(lens0)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.locks_build_summaries(d.k_cache, d.page_table, i32(seq), i32(pg), store,
+                            status=status)
+    seq_lens = d.seq_lens.clone()
+    for s in range(spec.append_steps):
+        B.locks_append_kv(wl.k_append[s].to(DEV), wl.v_append[s].to(DEV),
+                          d.k_cache, d.v_cache, d.page_table, seq_lens, store,
+                          status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert seq_lens.cpu().tolist() == [L + 20 for L in lens0]
+    # the host applies the same appends to its own copy of the cache
+    pt = wl.page_table.numpy()
+    kc = wl.k_cache.float().numpy().copy()
+    for s in range(spec.append_steps):
+        for b in range(batch):
+            pos = lens0[b] + s
+            kc[pt[b, pos // 16], :, pos % 16] = wl.k_append[s, b].float().numpy()
+    assert np.array_equal(d.k_cache.float().cpu().numpy(), kc)
+    # every page full after the appends has the record Algorithm 1 gives
+    lens1 = [L + 20 for L in lens0]
+    seq1, pg1 = full_pairs(lens1)
+    ostore, _ = O.build_summaries(kc, pt, seq1, pg1, batch, max_pages)
+    got = store.cpu().numpy()
+    for b, p in zip(seq1, pg1):
+        gq = O.decode_records(got[b, :, p])
+        oq = O.decode_records(ostore[b, :, p])
+        assert (gq["mu8"] == oq["mu8"]).all() and (gq["smu"] == oq["smu"]).all()
+        mu, V, C = O.dequantize(gq)
+        mo, Vo, Co = O.dequantize(oq)
+        R, Ro = C @ np.swapaxes(V, -1, -2), Co @ np.swapaxes(Vo, -1, -2)
+        rel = np.linalg.norm(R - Ro) / np.linalg.norm(Ro)
+        assert rel < 0.05, (b, p, rel)
+    # appended tokens are in the cache
+    for s in (0, 7, 19):
+        for b in range(batch):
+            pos = lens0[b] + s
+            got_k = d.k_cache[int(pt[b, pos // 16]), :, pos % 16].cpu()
+            assert torch.equal(got_k, wl.k_append[s, b])
+
+
+# ---------------------------------------------------------------------------
+# device-detected data errors set status bits, never trap
+# ---------------------------------------------------------------------------
+def test_device_status_flags():
+    spec = W.custom_spec(batch=2, h_q=4, h_kv=1, ctx=16 * 10, k=4, needles=0,
+                         seed=3)
+    wl = W.generate(spec, "cpu")
+    d = Dev(wl)
+    batch, max_pages = wl.page_table.shape
+    P = d.k_cache.shape[0]
+    bad_pt = d.page_table.clone()
+    bad_pt[0, 2] = P + 5
+    store = B.new_summary_store(batch, 1, max_pages, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.locks_build_summaries(d.k_cache, bad_pt, i32([0, 0, 1]), i32([1, 2, 99]),
+                            store, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == B.DEV_BAD_PAGE_ID | B.DEV_BAD_PAIR
+    ws = B.new_workspace(batch, 4, 1, max_pages, max_pages, DEV)
+    o = torch.empty(batch, 4, 128, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(batch, 4, dtype=torch.float32, device=DEV)
+    idx = i32([[[0, 3, 50, -1]], [[0, 1, 2, 9]]])
+    B.locks_sparse_decode(d.queries[0], d.k_cache, d.v_cache, bad_pt,
+                          d.seq_lens, idx, 4, o, lse, ws)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == B.DEV_BAD_INDEX
+    B.locks_clear_status(ws)
+    long = i32([16 * max_pages + 1, 16])
+    B.locks_sparse_decode(d.queries[0], d.k_cache, d.v_cache, d.page_table,
+                          long, idx, 4, o, lse, ws)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) & B.DEV_BAD_SEQ_LEN
+    B.locks_clear_status(ws)
+    idx2 = i32([[[0, 2, 5, 9]], [[0, 1, 2, 9]]])
+    B.locks_sparse_decode(d.queries[0], d.k_cache, d.v_cache, bad_pt,
+                          d.seq_lens, idx2, 4, o, lse, ws)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == B.DEV_BAD_PAGE_ID
