@@ -41,10 +41,13 @@
  *               512 + 4*(4*(i%8) + n/2) + 2*(i/8) + n%2, in [-127, 127].
  *   [640, 768)  MU8 int8 centroid codes mu[d], byte
  *               640 + 32*((d%8)/2) + 4*(d/16) + (d%2) + 2*((d%16)/8).
- *   [768, 784)  sV  fp16[8]  per-column basis scales.
- *   [784, 816)  sC  fp16[16] per-row coefficient scales.
- *   [816, 818)  sMU fp16     centroid scale.
- *   [818, 832)  zero padding.
+ *   [768, 832)  fp16 scales, four 16-byte groups: group t (0..3) at
+ *               768 + 16t holds sV[2t], sV[2t+1] (per-column basis
+ *               scales), sC[2t], sC[2t+1], sC[8+2t], sC[9+2t] (per-row
+ *               coefficient scales), then the centroid scale sMU in group 0
+ *               (byte 780) and zero padding elsewhere: each scoring lane
+ *               reads all its scales with one 16-byte load.  25 scales =
+ *               50 payload bytes; 14 bytes are padding.
  * Dequantised: mu = sMU*MU8, V[:,n] = sV[n]*V4[:,n], c_i = sC[i]*C8[i,:].
  * The summary store is [batch][h_kv][max_pages] records in logical page
  * order, so one (sequence, KV head) is a contiguous stream.

@@ -50,7 +50,7 @@ HEAD_DIM = 128
 RANK = 8
 RECORD_BYTES = 832          # 818 B payload + 14 B zero padding
 OFF_V4, OFF_C8, OFF_MU8 = 0, 512, 640
-OFF_SV, OFF_SC, OFF_SMU = 768, 784, 816
+OFF_SV = 768                # start of the 64-byte scale block
 PAYLOAD_BYTES = 818
 ZERO_TOL = 1e-6
 
@@ -193,6 +193,16 @@ def _c8_offsets():
     return OFF_C8 + 4 * (4 * (i % 8) + k // 2) + 2 * (i // 8) + k % 2
 
 
+def _scale_offsets():
+    """Byte offsets of the fp16 scales: the 64-byte scale block holds, for
+    t = 0..3, 16 bytes at 768 + 16t: sV[2t], sV[2t+1], sC[2t], sC[2t+1],
+    sC[8+2t], sC[9+2t], then sMU (t = 0 only) and zero padding."""
+    sv = np.array([OFF_SV + 16 * (n // 2) + 2 * (n % 2) for n in range(RANK)])
+    sc = np.array([OFF_SV + 16 * ((i % 8) // 2) + 4 + 2 * (i % 2) + 4 * (i // 8)
+                   for i in range(PAGE)])
+    return sv, sc, OFF_SV + 12
+
+
 def _mu8_offsets():
     d = np.arange(HEAD_DIM)
     o = d % 16
@@ -201,6 +211,7 @@ def _mu8_offsets():
     return OFF_MU8 + 32 * c + 4 * (d // 16) + j
 
 
+SV_OFF, SC_OFF, SMU_OFF = _scale_offsets()
 V4_WORD, V4_SHIFT = _v4_positions()
 V4_WORD_COLS = np.argsort(V4_WORD.reshape(-1), kind="stable").reshape(128, 8)
 C8_OFF = _c8_offsets()
@@ -223,10 +234,12 @@ def encode_records(q) -> np.ndarray:
     rec[:, C8_OFF.reshape(-1)] = C8.reshape(n, -1)
     mu8 = np.ascontiguousarray(q["mu8"].reshape(n, HEAD_DIM)).view(np.uint8)
     rec[:, MU8_OFF] = mu8
-    for off, key, cnt in ((OFF_SV, "sV", RANK), (OFF_SC, "sC", PAGE),
-                          (OFF_SMU, "smu", 1)):
+    for offs, key, cnt in ((SV_OFF, "sV", RANK), (SC_OFF, "sC", PAGE),
+                           (np.array([SMU_OFF]), "smu", 1)):
         f16 = np.ascontiguousarray(q[key].reshape(n, cnt).astype("<f2"))
-        rec[:, off:off + 2 * cnt] = f16.view(np.uint8).reshape(n, 2 * cnt)
+        b = f16.view(np.uint8).reshape(n, cnt, 2)
+        rec[:, offs] = b[..., 0]
+        rec[:, offs + 1] = b[..., 1]
     return rec.reshape(lead + (RECORD_BYTES,))
 
 
@@ -241,9 +254,13 @@ def decode_records(rec: np.ndarray):
     V4 = np.where(nib >= 8, nib - 16, nib).astype(np.int8)
     C8 = r[:, C8_OFF.reshape(-1)].view(np.int8).reshape(n, PAGE, RANK)
     mu8 = r[:, MU8_OFF].view(np.int8).reshape(n, HEAD_DIM)
-    sV = r[:, OFF_SV:OFF_SV + 16].copy().view("<f2").reshape(n, RANK)
-    sC = r[:, OFF_SC:OFF_SC + 32].copy().view("<f2").reshape(n, PAGE)
-    smu = r[:, OFF_SMU:OFF_SMU + 2].copy().view("<f2").reshape(n)
+    def halves(offs):
+        lo = r[:, offs].astype(np.uint16)
+        hi = r[:, offs + 1].astype(np.uint16)
+        return (lo | (hi << 8)).view(np.float16)
+    sV = halves(SV_OFF)
+    sC = halves(SC_OFF)
+    smu = halves(np.array([SMU_OFF]))[:, 0]
     return dict(V4=V4.reshape(lead + (HEAD_DIM, RANK)),
                 C8=C8.reshape(lead + (PAGE, RANK)),
                 mu8=mu8.reshape(lead + (HEAD_DIM,)),

@@ -177,20 +177,24 @@ __device__ void write_record(const float (&V)[4][8], const float (&mu)[4],
     *reinterpret_cast<uint32_t *>(rec + kOffMu8 + 4 * lane) =
         b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
   }
-  // scales and padding: 16 words from byte 768
+  // scale block: 16 bytes per t = 0..3 at 768 + 16t holding sV[2t..2t+1],
+  // sC[2t..2t+1], sC[8+2t..9+2t], then sMU (t = 0) or zero
   if (lane < 16) {
-    uint32_t word = 0;
-    if (lane < 4) {
-      word = (uint32_t)__half_as_ushort(sm.sv[2 * lane]) |
-             ((uint32_t)__half_as_ushort(sm.sv[2 * lane + 1]) << 16);
-    } else if (lane < 12) {
-      const int i = 2 * (lane - 4);
-      word = (uint32_t)__half_as_ushort(sm.sc[i]) |
-             ((uint32_t)__half_as_ushort(sm.sc[i + 1]) << 16);
-    } else if (lane == 12) {
-      word = (uint32_t)__half_as_ushort(sm.smu);
+    const int t = lane >> 2, q = lane & 3;
+    uint32_t lo = 0, hi = 0;
+    if (q == 0) {
+      lo = __half_as_ushort(sm.sv[2 * t]);
+      hi = __half_as_ushort(sm.sv[2 * t + 1]);
+    } else if (q == 1) {
+      lo = __half_as_ushort(sm.sc[2 * t]);
+      hi = __half_as_ushort(sm.sc[2 * t + 1]);
+    } else if (q == 2) {
+      lo = __half_as_ushort(sm.sc[8 + 2 * t]);
+      hi = __half_as_ushort(sm.sc[9 + 2 * t]);
+    } else if (t == 0) {
+      lo = __half_as_ushort(sm.smu);
     }
-    *reinterpret_cast<uint32_t *>(rec + kOffSV + 4 * lane) = word;
+    *reinterpret_cast<uint32_t *>(rec + kOffSV + 4 * lane) = lo | (hi << 16);
   }
   __syncwarp();
 }

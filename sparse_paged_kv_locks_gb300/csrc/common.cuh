@@ -15,7 +15,8 @@ constexpr int kDim = LOCKS_HEAD_DIM;      // d
 constexpr int kRank = LOCKS_RANK;         // r
 constexpr int kRec = LOCKS_RECORD_BYTES;  // record stride
 constexpr int kOffV4 = 0, kOffC8 = 512, kOffMu8 = 640;
-constexpr int kOffSV = 768, kOffSC = 784, kOffSMu = 816;
+constexpr int kOffSV = 768;   // 64-byte scale block (see include/locks.h)
+constexpr int kOffSMu = 780;
 constexpr int kMaxGroup = 16;
 constexpr int kMaxSplits = 64;     // split-K partials per (b, query head)
 constexpr size_t kWsHeader = 256;  // status word + reserved

@@ -32,40 +32,104 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   return h2_as_u32(__floats2half2_rn(lo, hi));
 }
 
+// Two int4 codes at bits [0,4) and [16,20) -> bf16x2 holding 136 + code
+// (exact); the constant 136 is cancelled through the accumulator's initial
+// value, so no subtraction is spent per element.
+__device__ __forceinline__ uint32_t nib_bf16_off(uint32_t x) {
+  return lop3_and_xor(x, 0x000F000Fu, 0x43084308u);
+}
+
+// Four int8 codes -> two fp16x2 holding 1152 + code (exact); the constant is
+// cancelled through the accumulator's initial value.
+__device__ __forceinline__ void i8x4_to_h2_off(uint32_t x, uint32_t &lo,
+                                               uint32_t &hi) {
+  const uint32_t f = x ^ 0x80808080u;
+  asm("prmt.b32 %0, %1, %2, 0x7170;\n" : "=r"(lo) : "r"(f), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x7372;\n" : "=r"(hi) : "r"(f), "r"(0x64646464u));
+}
+
+// Four int8 codes -> two fp16x2 holding the codes exactly.
+__device__ __forceinline__ void i8x4_to_h2(uint32_t x, uint32_t &lo,
+                                           uint32_t &hi) {
+  uint32_t a, b;
+  i8x4_to_h2_off(x, a, b);
+  const __half2 k = __half2half2(__ushort_as_half((unsigned short)0x6480));
+  lo = h2_as_u32(__hsub2(u32_as_h2(a), k));
+  hi = h2_as_u32(__hsub2(u32_as_h2(b), k));
+}
+
+// Hardware base-2 exponential and logarithm (PTX approximate forms, relative
+// error ~2^-22), used for the 16-token log-sum-exp of a page.
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2_fast(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// D = A * B (zero accumulator), m16n8k16 fp16
+__device__ __forceinline__ void mma_f16_z(float (&d)[4],
+                                          const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1),
+        "f"(0.f));
+}
+
+// log2-sum-exp2 of 16 logits spread 4 per lane over a quad
 __device__ __forceinline__ float lse2_quad(float a, float b, float c,
                                            float d) {
   float m = fmaxf(fmaxf(a, b), fmaxf(c, d));
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-  float e = exp2f(a - m) + exp2f(b - m) + exp2f(c - m) + exp2f(d - m);
+  float e = (ex2_fast(a - m) + ex2_fast(b - m)) +
+            (ex2_fast(c - m) + ex2_fast(d - m));
   e += __shfl_xor_sync(0xffffffffu, e, 1);
   e += __shfl_xor_sync(0xffffffffu, e, 2);
-  return m + log2f(e);
+  return m + lg2_fast(e);
 }
 
-struct TileInfo {
-  int b, h, page0, npg;
+// position of a warp in its contiguous range of tiles
+struct Cursor {
+  int b, h, j;
 };
 
-// tile t -> (sequence, KV head, first page, pages) from the per-sequence
-// prefix of tile counts (already multiplied by h_kv)
-__device__ __forceinline__ TileInfo decode_tile(long long t, const int *prefix,
-                                                const int *nfull, int batch,
-                                                int h_kv) {
-  int lo = 0, hi = batch;  // largest b with prefix[b] <= t
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (prefix[mid] <= t) lo = mid; else hi = mid;
+__device__ __forceinline__ void advance_cursor(Cursor &c, const int *prefix,
+                                               int batch, int h_kv) {
+  if (++c.j == (prefix[c.b + 1] - prefix[c.b]) / h_kv) {
+    c.j = 0;
+    if (++c.h == h_kv) {
+      c.h = 0;
+      do {
+        ++c.b;
+      } while (c.b < batch && prefix[c.b + 1] == prefix[c.b]);
+    }
   }
-  TileInfo ti;
-  ti.b = lo;
-  const int rem = (int)(t - prefix[lo]);
-  const int tiles_b = (prefix[lo + 1] - prefix[lo]) / h_kv;
-  ti.h = rem / tiles_b;
-  const int j = rem - ti.h * tiles_b;
-  ti.page0 = j * kTilePages;
-  ti.npg = min(kTilePages, nfull[lo] - ti.page0);
-  return ti;
+}
+
+// lane 0 starts the bulk copy of tile c into `dst`, completing on `bar`
+__device__ __forceinline__ void issue_tile(const Cursor &c, const int *nfull,
+                                           const uint8_t *summaries, int h_kv,
+                                           int max_pages, uint8_t *dst,
+                                           uint64_t *bar, int lane) {
+  if (lane == 0) {
+    const int page0 = c.j * kTilePages;
+    const int npg = min(kTilePages, nfull[c.b] - page0);
+    const uint8_t *src =
+        summaries +
+        (((size_t)c.b * h_kv + c.h) * max_pages + page0) * (size_t)kRec;
+    const uint32_t bytes = (uint32_t)npg * kRec;
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    mbar_arrive_tx(bar, bytes);
+    bulk_g2s(dst, src, bytes, bar);
+  }
 }
 
 template <bool WIDE>
@@ -123,109 +187,126 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const long long W = (long long)gridDim.x * kScoreWarps;
   const long long gw = (long long)blockIdx.x * kScoreWarps + wid;
   const long long t_begin = gw * total / W, t_end = (gw + 1) * total / W;
+  if (t_begin >= t_end) return;
   uint8_t *my_ring = ring + (size_t)wid * kStages * kTileBytes;
   uint64_t *my_bar = bars + wid * kStages;
 
-  auto issue = [&](long long t, int stage) {
-    if (lane == 0) {
-      const TileInfo ti = decode_tile(t, prefix, nfull, batch, h_kv);
-      const uint8_t *src =
-          summaries +
-          (((size_t)ti.b * h_kv + ti.h) * max_pages + ti.page0) * (size_t)kRec;
-      const uint32_t bytes = (uint32_t)ti.npg * kRec;
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      mbar_arrive_tx(&my_bar[stage], bytes);
-      bulk_g2s(my_ring + stage * kTileBytes, src, bytes, &my_bar[stage]);
+  Cursor cur;
+  {  // largest b with prefix[b] <= t_begin
+    int lo = 0, hi = batch;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= t_begin) lo = mid; else hi = mid;
     }
-  };
+    const int rem = (int)(t_begin - prefix[lo]);
+    const int tb = (prefix[lo + 1] - prefix[lo]) / h_kv;
+    cur.b = lo;
+    cur.h = rem / tb;
+    cur.j = rem - cur.h * tb;
+  }
+  Cursor nxt = cur;
+  issue_tile(nxt, nfull, summaries, h_kv, max_pages, my_ring, &my_bar[0],
+             lane);
+  advance_cursor(nxt, prefix, batch, h_kv);
+  if (t_begin + 1 < t_end) {
+    issue_tile(nxt, nfull, summaries, h_kv, max_pages, my_ring + kTileBytes,
+               &my_bar[1], lane);
+    advance_cursor(nxt, prefix, batch, h_kv);
+  }
 
-  if (t_begin < t_end) issue(t_begin, 0);
-  if (t_begin + 1 < t_end) issue(t_begin + 1, 1);
-
-  uint32_t qa[8][4];  // query A fragments (fp16), rows = heads of the group
+  uint32_t qb[8][4];  // query A fragments, bf16 (basis product)
+  uint32_t qh[8][4];  // query A fragments, fp16 (centroid product)
+  float off_v = 0.f, off_v8 = 0.f, off_m = 0.f, off_m8 = 0.f;
   int cur_b = -1, cur_h = -1;
   bool failed = false;
 
   for (long long t = t_begin, it = 0; t < t_end; ++t, ++it) {
     const int stage = (int)(it & 1);
     const uint32_t phase = (uint32_t)((it >> 1) & 1);
-    const TileInfo ti = decode_tile(t, prefix, nfull, batch, h_kv);
+    if (cur.b != cur_b || cur.h != cur_h) {
+      cur_b = cur.b;
+      cur_h = cur.h;
+      const __nv_bfloat16 *qrow =
+          q + ((size_t)cur.b * h_kv * G + (size_t)cur.h * G) * kDim;
+      float sum = 0.f, sum8 = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const int d0 = 16 * s + 2 * t4;
+        uint32_t u0 = 0, u2 = 0, u1 = 0, u3 = 0;
+        if (gq < G) {
+          u0 = __ldg(reinterpret_cast<const uint32_t *>(qrow + gq * kDim + d0));
+          u2 = __ldg(reinterpret_cast<const uint32_t *>(qrow + gq * kDim + d0 + 8));
+        }
+        if (WIDE && gq + 8 < G) {
+          u1 = __ldg(reinterpret_cast<const uint32_t *>(qrow + (gq + 8) * kDim + d0));
+          u3 = __ldg(reinterpret_cast<const uint32_t *>(qrow + (gq + 8) * kDim + d0 + 8));
+        }
+        qb[s][0] = u0;
+        qb[s][1] = u1;
+        qb[s][2] = u2;
+        qb[s][3] = u3;
+        qh[s][0] = pack_h2(bf16_lo(u0), bf16_hi(u0));
+        qh[s][1] = pack_h2(bf16_lo(u1), bf16_hi(u1));
+        qh[s][2] = pack_h2(bf16_lo(u2), bf16_hi(u2));
+        qh[s][3] = pack_h2(bf16_lo(u3), bf16_hi(u3));
+        sum += (bf16_lo(u0) + bf16_hi(u0)) + (bf16_lo(u2) + bf16_hi(u2));
+        sum8 += (bf16_lo(u1) + bf16_hi(u1)) + (bf16_lo(u3) + bf16_hi(u3));
+      }
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      sum8 += __shfl_xor_sync(0xffffffffu, sum8, 1);
+      sum8 += __shfl_xor_sync(0xffffffffu, sum8, 2);
+      off_v = -136.f * sum;     // cancels the +136 of every basis code
+      off_v8 = -136.f * sum8;
+      off_m = -1152.f * sum;    // cancels the +1152 of every centroid code
+      off_m8 = -1152.f * sum8;
+    }
+    const int page0 = cur.j * kTilePages;
+    const int npg = min(kTilePages, nfull[cur.b] - page0);
     if (!mbar_wait(&my_bar[stage], phase)) {
       failed = true;
       break;
     }
-    if (ti.b != cur_b || ti.h != cur_h) {
-      cur_b = ti.b;
-      cur_h = ti.h;
-      const __nv_bfloat16 *qb = q + ((size_t)ti.b * h_kv * G + (size_t)ti.h * G) * kDim;
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const int d0 = 16 * s + 2 * t4;
-        uint32_t r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-        if (gq < G) {
-          const uint32_t u0 = __ldg(reinterpret_cast<const uint32_t *>(qb + gq * kDim + d0));
-          const uint32_t u2 = __ldg(reinterpret_cast<const uint32_t *>(qb + gq * kDim + d0 + 8));
-          r0 = pack_h2(bf16_lo(u0), bf16_hi(u0));
-          r2 = pack_h2(bf16_lo(u2), bf16_hi(u2));
-        }
-        if (WIDE && gq + 8 < G) {
-          const uint32_t u1 = __ldg(reinterpret_cast<const uint32_t *>(qb + (gq + 8) * kDim + d0));
-          const uint32_t u3 = __ldg(reinterpret_cast<const uint32_t *>(qb + (gq + 8) * kDim + d0 + 8));
-          r1 = pack_h2(bf16_lo(u1), bf16_hi(u1));
-          r3 = pack_h2(bf16_lo(u3), bf16_hi(u3));
-        }
-        qa[s][0] = r0;
-        qa[s][1] = r1;
-        qa[s][2] = r2;
-        qa[s][3] = r3;
-      }
-    }
     const uint8_t *base = my_ring + stage * kTileBytes;
 
-    // mma3: q . mu for the tile's 8 pages (column n = page)
-    float qm[4] = {0.f, 0.f, 0.f, 0.f}, qm2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const uint32_t u =
-          gq < ti.npg ? ld_shared_u32(base + gq * kRec + kOffMu8 + 32 * t4 + 4 * s)
-                      : 0u;
-      if (s & 1)
-        mma_f16(qm2, qa[s], i8x2_to_h2(u), i8x2_to_h2(u >> 16));
-      else
-        mma_f16(qm, qa[s], i8x2_to_h2(u), i8x2_to_h2(u >> 16));
-    }
-    float qmu0 = 0.f, qmu1 = 0.f, qmu8_0 = 0.f, qmu8_1 = 0.f;
+    // q . mu for the tile's 8 pages (column n = page gq of the tile)
+    float qm[4] = {off_m, off_m, off_m8, off_m8};
+    float qm2[4] = {0.f, 0.f, 0.f, 0.f};
     {
-      const int p0 = 2 * t4, p1 = 2 * t4 + 1;
-      const float sm0 =
-          p0 < ti.npg ? __half2float(*reinterpret_cast<const __half *>(base + p0 * kRec + kOffSMu)) : 0.f;
-      const float sm1 =
-          p1 < ti.npg ? __half2float(*reinterpret_cast<const __half *>(base + p1 * kRec + kOffSMu)) : 0.f;
-      qmu0 = (qm[0] + qm2[0]) * sm0 * kLog2eRsqrtD;
-      qmu1 = (qm[1] + qm2[1]) * sm1 * kLog2eRsqrtD;
-      if (WIDE) {
-        qmu8_0 = (qm[2] + qm2[2]) * sm0 * kLog2eRsqrtD;
-        qmu8_1 = (qm[3] + qm2[3]) * sm1 * kLog2eRsqrtD;
+      const uint8_t *mrow = base + gq * kRec + kOffMu8 + 32 * t4;
+      const uint4 m0 = ld_shared_v4(mrow), m1 = ld_shared_v4(mrow + 16);
+      const uint32_t mw[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        uint32_t b01, b23;
+        i8x4_to_h2_off(mw[s], b01, b23);
+        if (s & 1)
+          mma_f16(qm2, qh[s], b01, b23);
+        else
+          mma_f16(qm, qh[s], b01, b23);
       }
     }
 
-    float lse[kTilePages], lse8[kTilePages];
+    // lane (g, t4) keeps the page LSEs of pages 2*t4 and 2*t4 + 1
+    float o0 = 0.f, o1 = 0.f, o80 = 0.f, o81 = 0.f;
 #pragma unroll
     for (int p = 0; p < kTilePages; ++p) {
-      lse[p] = 0.f;
-      lse8[p] = 0.f;
-      if (p < ti.npg) {
+      if (p < npg) {
         const uint8_t *rec = base + p * kRec;
         const uint4 vw = ld_shared_v4(rec + kOffV4 + 16 * lane);
+        const uint4 sc = ld_shared_v4(rec + kOffSV + 16 * t4);
+        const uint32_t cw = ld_shared_u32(rec + kOffC8 + 4 * lane);
         const uint32_t vwa[4] = {vw.x, vw.y, vw.z, vw.w};
-        float a1[4] = {0.f, 0.f, 0.f, 0.f}, a1b[4] = {0.f, 0.f, 0.f, 0.f};
+        float a1[4] = {off_v, off_v, off_v8, off_v8};
+        float a1b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-          const uint32_t x = vwa[w], y = x >> 8;
-          mma_f16(a1, qa[2 * w], nib_lo_to_h2(x), nib_hi_to_h2(x));
-          mma_f16(a1b, qa[2 * w + 1], nib_lo_to_h2(y), nib_hi_to_h2(y));
+          const uint32_t x = vwa[w];
+          mma_bf16(a1, qb[2 * w], nib_bf16_off(x), nib_bf16_off(x >> 4));
+          mma_bf16(a1b, qb[2 * w + 1], nib_bf16_off(x >> 8),
+                   nib_bf16_off(x >> 12));
         }
-        const __half2 sv = u32_as_h2(ld_shared_u32(rec + kOffSV + 4 * t4));
+        const __half2 sv = u32_as_h2(sc.x);
         const float sv0 = __low2float(sv) * kLog2eRsqrtD;
         const float sv1 = __high2float(sv) * kLog2eRsqrtD;
         const float P0 = (a1[0] + a1b[0]) * sv0, P1 = (a1[1] + a1b[1]) * sv1;
@@ -241,44 +322,59 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           A2[1] = h2_as_u32(h23);
           A2[3] = pack_h2(P2 - __low2float(h23), P3 - __high2float(h23));
         }
-        const uint32_t cw = ld_shared_u32(rec + kOffC8 + 4 * lane);
-        const uint32_t bt0 = i8x2_to_h2(cw), bt1 = i8x2_to_h2(cw >> 16);
-        float l0[4] = {0.f, 0.f, 0.f, 0.f}, l1[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f16(l0, A2, bt0, bt0);
-        mma_f16(l1, A2, bt1, bt1);
-        const __half2 sc0 = u32_as_h2(ld_shared_u32(rec + kOffSC + 4 * t4));
-        const __half2 sc1 = u32_as_h2(ld_shared_u32(rec + kOffSC + 16 + 4 * t4));
+        uint32_t bt0, bt1;
+        i8x4_to_h2(cw, bt0, bt1);
+        float l0[4], l1[4];
+        mma_f16_z(l0, A2, bt0, bt0);
+        mma_f16_z(l1, A2, bt1, bt1);
+        const __half2 sc0 = u32_as_h2(sc.y), sc1 = u32_as_h2(sc.z);
         const float c0 = __low2float(sc0), c1 = __high2float(sc0);
         const float c8 = __low2float(sc1), c9 = __high2float(sc1);
-        lse[p] = lse2_quad(l0[0] * c0, l0[1] * c1, l1[0] * c8, l1[1] * c9);
+        const float e = lse2_quad(l0[0] * c0, l0[1] * c1, l1[0] * c8,
+                                  l1[1] * c9);
+        float e8 = 0.f;
         if (WIDE)
-          lse8[p] = lse2_quad(l0[2] * c0, l0[3] * c1, l1[2] * c8, l1[3] * c9);
-      }
-    }
-    // lane (g, t4) owns pages 2*t4 and 2*t4 + 1 of the tile
-    float o0 = 0.f, o1 = 0.f, o80 = 0.f, o81 = 0.f;
-#pragma unroll
-    for (int p = 0; p < kTilePages; p += 2) {
-      if (p == 2 * t4) {
-        o0 = lse[p];
-        o1 = lse[p + 1];
-        o80 = lse8[p];
-        o81 = lse8[p + 1];
+          e8 = lse2_quad(l0[2] * c0, l0[3] * c1, l1[2] * c8, l1[3] * c9);
+        if ((p >> 1) == t4) {
+          if (p & 1) {
+            o1 = e;
+            o81 = e8;
+          } else {
+            o0 = e;
+            o80 = e8;
+          }
+        }
       }
     }
     const int pg0 = 2 * t4, pg1 = 2 * t4 + 1;
+    const float sm0 = __half2float(*reinterpret_cast<const __half *>(
+        base + pg0 * kRec + kOffSMu));
+    const float sm1 = __half2float(*reinterpret_cast<const __half *>(
+        base + pg1 * kRec + kOffSMu));
     if (gq < G) {
-      float *dst = s_hat + (((size_t)ti.b * h_kv + ti.h) * G + gq) * max_pages + ti.page0;
-      if (pg0 < ti.npg) dst[pg0] = (o0 + qmu0) * kLn2;
-      if (pg1 < ti.npg) dst[pg1] = (o1 + qmu1) * kLn2;
+      float *dst = s_hat +
+                   (((size_t)cur.b * h_kv + cur.h) * G + gq) * max_pages + page0;
+      if (pg0 < npg)
+        dst[pg0] = (o0 + (qm[0] + qm2[0]) * sm0 * kLog2eRsqrtD) * kLn2;
+      if (pg1 < npg)
+        dst[pg1] = (o1 + (qm[1] + qm2[1]) * sm1 * kLog2eRsqrtD) * kLn2;
     }
     if (WIDE && gq + 8 < G) {
-      float *dst = s_hat + (((size_t)ti.b * h_kv + ti.h) * G + gq + 8) * max_pages + ti.page0;
-      if (pg0 < ti.npg) dst[pg0] = (o80 + qmu8_0) * kLn2;
-      if (pg1 < ti.npg) dst[pg1] = (o81 + qmu8_1) * kLn2;
+      float *dst = s_hat +
+                   (((size_t)cur.b * h_kv + cur.h) * G + gq + 8) * max_pages +
+                   page0;
+      if (pg0 < npg)
+        dst[pg0] = (o80 + (qm[2] + qm2[2]) * sm0 * kLog2eRsqrtD) * kLn2;
+      if (pg1 < npg)
+        dst[pg1] = (o81 + (qm[3] + qm2[3]) * sm1 * kLog2eRsqrtD) * kLn2;
     }
     __syncwarp();
-    if (t + 2 < t_end) issue(t + 2, stage);
+    if (t + 2 < t_end) {
+      issue_tile(nxt, nfull, summaries, h_kv, max_pages,
+                 my_ring + stage * kTileBytes, &my_bar[stage], lane);
+      advance_cursor(nxt, prefix, batch, h_kv);
+    }
+    advance_cursor(cur, prefix, batch, h_kv);
   }
   if (failed) {
     if (lane == 0) set_status(status, LOCKS_DEV_TIMEOUT);

@@ -8,8 +8,6 @@ the sampled pairs must match the oracle's exactly as on small cases; the
 attention outputs of the sampled pairs are checked with the oracle's
 selection fed to the full-batch decode.
 """
-import math
-
 import numpy as np
 import pytest
 import torch
@@ -93,4 +91,3 @@ def test_full_size_sampled_parity():
         assert np.abs(og - o_ref).max() <= 2e-2 * np.abs(o_ref).max()
         assert np.abs(lse[b, h * G:(h + 1) * G].cpu().numpy() - lse_ref).max() \
             <= 1e-3
-    del math
