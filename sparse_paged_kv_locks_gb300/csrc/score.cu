@@ -83,7 +83,8 @@ __device__ __forceinline__ void mma_f16_z(float (&d)[4],
         "f"(0.f));
 }
 
-// log2-sum-exp2 of 16 logits spread 4 per lane over a quad
+// log2-sum-exp2 of 16 logits spread 4 per lane over a quad, with the
+// maximum subtracted first (always finite)
 __device__ __forceinline__ float lse2_quad(float a, float b, float c,
                                            float d) {
   float m = fmaxf(fmaxf(a, b), fmaxf(c, d));
@@ -94,6 +95,19 @@ __device__ __forceinline__ float lse2_quad(float a, float b, float c,
   e += __shfl_xor_sync(0xffffffffu, e, 1);
   e += __shfl_xor_sync(0xffffffffu, e, 2);
   return m + lg2_fast(e);
+}
+
+// Same value without the max pass: sums 2^x directly and falls back to the
+// max-subtracted form for the whole warp when any quad's sum overflows or
+// underflows (logits beyond about +-126 in base-2 units).
+__device__ __forceinline__ float lse2_quad_fast(float a, float b, float c,
+                                                float d) {
+  float e = (ex2_fast(a) + ex2_fast(b)) + (ex2_fast(c) + ex2_fast(d));
+  e += __shfl_xor_sync(0xffffffffu, e, 1);
+  e += __shfl_xor_sync(0xffffffffu, e, 2);
+  const bool bad = !(e > 0.f) || !(e < INFINITY);
+  if (__any_sync(0xffffffffu, bad)) return lse2_quad(a, b, c, d);
+  return lg2_fast(e);
 }
 
 // position of a warp in its contiguous range of tiles
@@ -132,7 +146,7 @@ __device__ __forceinline__ void issue_tile(const Cursor &c, const int *nfull,
   }
 }
 
-template <bool WIDE>
+template <int MODE>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_kernel(const __nv_bfloat16 *__restrict__ q,
                  const uint8_t *__restrict__ summaries,
@@ -189,6 +203,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const long long t_begin = gw * total / W, t_end = (gw + 1) * total / W;
   if (t_begin >= t_end) return;
   uint8_t *my_ring = ring + (size_t)wid * kStages * kTileBytes;
+  const uint32_t ring_s = smem_u32(my_ring);
   uint64_t *my_bar = bars + wid * kStages;
 
   Cursor cur;
@@ -214,8 +229,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     advance_cursor(nxt, prefix, batch, h_kv);
   }
 
-  uint32_t qb[8][4];  // query A fragments, bf16 (basis product)
+  constexpr bool WIDE = MODE == 3;
+  uint32_t qb[8][4];  // query A fragments, bf16 (basis product, one page)
   uint32_t qh[8][4];  // query A fragments, fp16 (centroid product)
+  uint32_t qv[8][2];  // query B fragments, bf16 (basis product, two pages)
+  float offc0 = 0.f, offc1 = 0.f;  // offsets of columns 2*t4, 2*t4 + 1
   float off_v = 0.f, off_v8 = 0.f, off_m = 0.f, off_m8 = 0.f;
   int cur_b = -1, cur_h = -1;
   bool failed = false;
@@ -256,6 +274,25 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       sum += __shfl_xor_sync(0xffffffffu, sum, 2);
       sum8 += __shfl_xor_sync(0xffffffffu, sum8, 1);
       sum8 += __shfl_xor_sync(0xffffffffu, sum8, 2);
+      if constexpr (MODE != 3) {
+        // column n of the transposed basis product is query head
+        // (n mod 4) for G <= 4 and head n for G <= 8
+        const int hc = MODE == 1 ? (gq & 3) : gq;
+        const __nv_bfloat16 *qc = qrow + hc * kDim;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const int d0 = 16 * s + 2 * t4;
+          qv[s][0] = hc < G ? __ldg(reinterpret_cast<const uint32_t *>(qc + d0)) : 0u;
+          qv[s][1] = hc < G ? __ldg(reinterpret_cast<const uint32_t *>(qc + d0 + 8)) : 0u;
+        }
+        // -136 * sum_d q[head of column][d], for columns 2*t4 and 2*t4 + 1
+        const int c0 = 2 * t4, c1 = 2 * t4 + 1;
+        const int g0 = MODE == 1 ? (c0 & 3) : c0, g1 = MODE == 1 ? (c1 & 3) : c1;
+        const float s0 = __shfl_sync(0xffffffffu, sum, 4 * g0);
+        const float s1 = __shfl_sync(0xffffffffu, sum, 4 * g1);
+        offc0 = -136.f * s0;
+        offc1 = -136.f * s1;
+      }
       off_v = -136.f * sum;     // cancels the +136 of every basis code
       off_v8 = -136.f * sum8;
       off_m = -1152.f * sum;    // cancels the +1152 of every centroid code
@@ -268,105 +305,252 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       break;
     }
     const uint8_t *base = my_ring + stage * kTileBytes;
+    const uint32_t base_s = ring_s + stage * kTileBytes;
 
-    // q . mu for the tile's 8 pages (column n = page gq of the tile)
-    float qm[4] = {off_m, off_m, off_m8, off_m8};
-    float qm2[4] = {0.f, 0.f, 0.f, 0.f};
-    {
-      const uint8_t *mrow = base + gq * kRec + kOffMu8 + 32 * t4;
-      const uint4 m0 = ld_shared_v4(mrow), m1 = ld_shared_v4(mrow + 16);
-      const uint32_t mw[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    float *srow = s_hat + ((size_t)cur.b * h_kv + cur.h) * G * (size_t)max_pages +
+                  page0;
+    if constexpr (MODE != 3) {
+      // Two pages per step.  Product 1 is transposed: rows 0..7 are page A's
+      // basis components, rows 8..15 page B's (A operand = unpacked codes,
+      // straight into the fragment registers), columns are query heads (B
+      // operand = the query, resident).  The 8x8 (component x head) blocks
+      // are turned with movmatrix into head-major operands for product 2.
+      float keepA = 0.f, keepB = 0.f;
+      const bool lowh = gq < 4;
+      const uint32_t maskA = lowh ? 0xffffffffu : 0u;
+#pragma unroll 1
+      for (int pp = 0; pp < kTilePages / 2; ++pp) {
+        if (2 * pp < npg) {
+          const uint32_t ra = base_s + (uint32_t)(2 * pp) * kRec;
+          const uint32_t rb = ra + kRec;
+          const uint4 va = lds128(ra + kOffV4 + 16 * lane);
+          const uint4 vb = lds128(rb + kOffV4 + 16 * lane);
+          const uint32_t ca = lds32(ra + kOffC8 + 4 * lane);
+          const uint32_t cb = lds32(rb + kOffC8 + 4 * lane);
+          // sV of component gq in each page
+          const uint32_t svo = kOffSV + 16 * (gq >> 1) + 2 * (gq & 1);
+          const float sva = __half2float(__ushort_as_half(
+                                (unsigned short)lds16(ra + svo))) * kLog2eRsqrtD;
+          const float svb = __half2float(__ushort_as_half(
+                                (unsigned short)lds16(rb + svo))) * kLog2eRsqrtD;
+          const uint32_t vaw[4] = {va.x, va.y, va.z, va.w};
+          const uint32_t vbw[4] = {vb.x, vb.y, vb.z, vb.w};
+          float d0[4], d1[4];
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        uint32_t b01, b23;
-        i8x4_to_h2_off(mw[s], b01, b23);
-        if (s & 1)
-          mma_f16(qm2, qh[s], b01, b23);
-        else
-          mma_f16(qm, qh[s], b01, b23);
-      }
-    }
-
-    // lane (g, t4) keeps the page LSEs of pages 2*t4 and 2*t4 + 1
-    float o0 = 0.f, o1 = 0.f, o80 = 0.f, o81 = 0.f;
-#pragma unroll
-    for (int p = 0; p < kTilePages; ++p) {
-      if (p < npg) {
-        const uint8_t *rec = base + p * kRec;
-        const uint4 vw = ld_shared_v4(rec + kOffV4 + 16 * lane);
-        const uint4 sc = ld_shared_v4(rec + kOffSV + 16 * t4);
-        const uint32_t cw = ld_shared_u32(rec + kOffC8 + 4 * lane);
-        const uint32_t vwa[4] = {vw.x, vw.y, vw.z, vw.w};
-        float a1[4] = {off_v, off_v, off_v8, off_v8};
-        float a1b[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const uint32_t x = vwa[w];
-          mma_bf16(a1, qb[2 * w], nib_bf16_off(x), nib_bf16_off(x >> 4));
-          mma_bf16(a1b, qb[2 * w + 1], nib_bf16_off(x >> 8),
-                   nib_bf16_off(x >> 12));
-        }
-        const __half2 sv = u32_as_h2(sc.x);
-        const float sv0 = __low2float(sv) * kLog2eRsqrtD;
-        const float sv1 = __high2float(sv) * kLog2eRsqrtD;
-        const float P0 = (a1[0] + a1b[0]) * sv0, P1 = (a1[1] + a1b[1]) * sv1;
-        const __half2 h01 = __floats2half2_rn(P0, P1);
-        uint32_t A2[4];
-        A2[0] = h2_as_u32(h01);
-        A2[2] = pack_h2(P0 - __low2float(h01), P1 - __high2float(h01));
-        A2[1] = 0u;
-        A2[3] = 0u;
-        if (WIDE) {
-          const float P2 = (a1[2] + a1b[2]) * sv0, P3 = (a1[3] + a1b[3]) * sv1;
-          const __half2 h23 = __floats2half2_rn(P2, P3);
-          A2[1] = h2_as_u32(h23);
-          A2[3] = pack_h2(P2 - __low2float(h23), P3 - __high2float(h23));
-        }
-        uint32_t bt0, bt1;
-        i8x4_to_h2(cw, bt0, bt1);
-        float l0[4], l1[4];
-        mma_f16_z(l0, A2, bt0, bt0);
-        mma_f16_z(l1, A2, bt1, bt1);
-        const __half2 sc0 = u32_as_h2(sc.y), sc1 = u32_as_h2(sc.z);
-        const float c0 = __low2float(sc0), c1 = __high2float(sc0);
-        const float c8 = __low2float(sc1), c9 = __high2float(sc1);
-        const float e = lse2_quad(l0[0] * c0, l0[1] * c1, l1[0] * c8,
-                                  l1[1] * c9);
-        float e8 = 0.f;
-        if (WIDE)
-          e8 = lse2_quad(l0[2] * c0, l0[3] * c1, l1[2] * c8, l1[3] * c9);
-        if ((p >> 1) == t4) {
-          if (p & 1) {
-            o1 = e;
-            o81 = e8;
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t xa = vaw[w], xb = vbw[w];
+            const uint32_t a0[4] = {nib_bf16_off(xa), nib_bf16_off(xb),
+                                    nib_bf16_off(xa >> 4),
+                                    nib_bf16_off(xb >> 4)};
+            const uint32_t a1[4] = {nib_bf16_off(xa >> 8),
+                                    nib_bf16_off(xb >> 8),
+                                    nib_bf16_off(xa >> 12),
+                                    nib_bf16_off(xb >> 12)};
+            if (w == 0) {
+              mma_bf16_c(d0, a0, qv[0][0], qv[0][1], offc0, offc1, offc0,
+                         offc1);
+              mma_bf16_c(d1, a1, qv[1][0], qv[1][1], 0.f, 0.f, 0.f, 0.f);
+            } else {
+              mma_bf16(d0, a0, qv[2 * w][0], qv[2 * w][1]);
+              mma_bf16(d1, a1, qv[2 * w + 1][0], qv[2 * w + 1][1]);
+            }
+          }
+          // proj (log2 units) = D * sV * log2(e)/sqrt(d), split hi + lo fp16
+          const float pa0 = (d0[0] + d1[0]) * sva, pa1 = (d0[1] + d1[1]) * sva;
+          const float pb0 = (d0[2] + d1[2]) * svb, pb1 = (d0[3] + d1[3]) * svb;
+          const __half2 ha = __floats2half2_rn(pa0, pa1);
+          const __half2 hb = __floats2half2_rn(pb0, pb1);
+          const uint32_t la =
+              pack_h2(pa0 - __low2float(ha), pa1 - __high2float(ha));
+          const uint32_t lb =
+              pack_h2(pb0 - __low2float(hb), pb1 - __high2float(hb));
+          const uint32_t tha = movmatrix_trans(h2_as_u32(ha));
+          const uint32_t tla = movmatrix_trans(la);
+          const uint32_t thb = movmatrix_trans(h2_as_u32(hb));
+          const uint32_t tlb = movmatrix_trans(lb);
+          uint32_t ba0, ba1, bb0, bb1;
+          i8x4_to_h2(ca, ba0, ba1);
+          i8x4_to_h2(cb, bb0, bb1);
+          float l0[4], l1[4];
+          if constexpr (MODE == 1) {
+            // rows 0-3: page A heads (high halves, k 0..7 = page A comps),
+            // rows 4-7: page B heads (high, k 8..15 = page B comps),
+            // rows 8-15: the same with the low halves
+            const uint32_t A2[4] = {tha & maskA, tla & maskA, thb & ~maskA,
+                                    tlb & ~maskA};
+            mma_f16_z(l0, A2, ba0, bb0);
+            mma_f16_z(l1, A2, ba1, bb1);
+            const uint32_t rs = lowh ? ra : rb;
+            const uint4 sc = lds128(rs + kOffSV + 16 * t4);
+            const __half2 s0 = u32_as_h2(sc.y), s1 = u32_as_h2(sc.z);
+            const float e = lse2_quad_fast((l0[0] + l0[2]) * __low2float(s0),
+                                           (l0[1] + l0[3]) * __high2float(s0),
+                                           (l1[0] + l1[2]) * __low2float(s1),
+                                           (l1[1] + l1[3]) * __high2float(s1));
+            if (pp == t4) keepA = e;
           } else {
-            o0 = e;
-            o80 = e8;
+            float m0[4], m1[4];
+            mma1688_f16_z(l0, tha, tla, ba0);
+            mma1688_f16_z(l1, tha, tla, ba1);
+            mma1688_f16_z(m0, thb, tlb, bb0);
+            mma1688_f16_z(m1, thb, tlb, bb1);
+            const uint4 sa = lds128(ra + kOffSV + 16 * t4);
+            const uint4 sb = lds128(rb + kOffSV + 16 * t4);
+            const __half2 a0 = u32_as_h2(sa.y), a1 = u32_as_h2(sa.z);
+            const __half2 b0 = u32_as_h2(sb.y), b1 = u32_as_h2(sb.z);
+            const float ea = lse2_quad_fast((l0[0] + l0[2]) * __low2float(a0),
+                                            (l0[1] + l0[3]) * __high2float(a0),
+                                            (l1[0] + l1[2]) * __low2float(a1),
+                                            (l1[1] + l1[3]) * __high2float(a1));
+            const float eb = lse2_quad_fast((m0[0] + m0[2]) * __low2float(b0),
+                                            (m0[1] + m0[3]) * __high2float(b0),
+                                            (m1[0] + m1[2]) * __low2float(b1),
+                                            (m1[1] + m1[3]) * __high2float(b1));
+            if (pp == t4) {
+              keepA = ea;
+              keepB = eb;
+            }
           }
         }
       }
-    }
-    const int pg0 = 2 * t4, pg1 = 2 * t4 + 1;
-    const float sm0 = __half2float(*reinterpret_cast<const __half *>(
-        base + pg0 * kRec + kOffSMu));
-    const float sm1 = __half2float(*reinterpret_cast<const __half *>(
-        base + pg1 * kRec + kOffSMu));
-    if (gq < G) {
-      float *dst = s_hat +
-                   (((size_t)cur.b * h_kv + cur.h) * G + gq) * max_pages + page0;
-      if (pg0 < npg)
-        dst[pg0] = (o0 + (qm[0] + qm2[0]) * sm0 * kLog2eRsqrtD) * kLn2;
-      if (pg1 < npg)
-        dst[pg1] = (o1 + (qm[1] + qm2[1]) * sm1 * kLog2eRsqrtD) * kLn2;
-    }
-    if (WIDE && gq + 8 < G) {
-      float *dst = s_hat +
-                   (((size_t)cur.b * h_kv + cur.h) * G + gq + 8) * max_pages +
-                   page0;
-      if (pg0 < npg)
-        dst[pg0] = (o80 + (qm[2] + qm2[2]) * sm0 * kLog2eRsqrtD) * kLn2;
-      if (pg1 < npg)
-        dst[pg1] = (o81 + (qm[3] + qm2[3]) * sm1 * kLog2eRsqrtD) * kLn2;
+      // q . mu for the tile's 8 pages (column n = page gq of the tile)
+      float qm[4] = {off_m, off_m, off_m8, off_m8};
+      float qm2[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const uint32_t mrow = base_s + gq * kRec + kOffMu8 + 32 * t4;
+        const uint4 m0 = lds128(mrow), m1 = lds128(mrow + 16);
+        const uint32_t mw[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          uint32_t b01, b23;
+          i8x4_to_h2_off(mw[s], b01, b23);
+          if (s & 1)
+            mma_f16(qm2, qh[s], b01, b23);
+          else
+            mma_f16(qm, qh[s], b01, b23);
+        }
+      }
+      const float qm_lo = qm[0] + qm2[0], qm_hi = qm[1] + qm2[1];
+      if constexpr (MODE == 1) {
+        // lane (g, t4) of the low half owns page 2*t4, of the high half page
+        // 2*t4 + 1, head g & 3
+        const bool up = lane >= 16;
+        const float qm_from_low = __shfl_xor_sync(0xffffffffu, qm_hi, 16);
+        const int pg = 2 * t4 + (up ? 1 : 0);
+        const int head = gq & 3;
+        const float smu = __half2float(*reinterpret_cast<const __half *>(
+            base + pg * kRec + kOffSMu));
+        const float qmu = up ? qm_from_low : qm_lo;
+        if (head < G && pg < npg)
+          srow[(size_t)head * max_pages + pg] =
+              (keepA + qmu * smu * kLog2eRsqrtD) * kLn2;
+      } else {
+        const int pg0 = 2 * t4, pg1 = pg0 + 1;
+        const float sm0 = __half2float(*reinterpret_cast<const __half *>(
+            base + pg0 * kRec + kOffSMu));
+        const float sm1 = __half2float(*reinterpret_cast<const __half *>(
+            base + pg1 * kRec + kOffSMu));
+        if (gq < G) {
+          if (pg0 < npg)
+            srow[(size_t)gq * max_pages + pg0] =
+                (keepA + qm_lo * sm0 * kLog2eRsqrtD) * kLn2;
+          if (pg1 < npg)
+            srow[(size_t)gq * max_pages + pg1] =
+                (keepB + qm_hi * sm1 * kLog2eRsqrtD) * kLn2;
+        }
+      }
+    } else {
+      // one page per mma group, heads in all 16 rows
+      float o0 = 0.f, o1 = 0.f, o80 = 0.f, o81 = 0.f;
+#pragma unroll
+      for (int p = 0; p < kTilePages; ++p) {
+        if (p < npg) {
+          const uint8_t *rec = base + p * kRec;
+          const uint4 vw = ld_shared_v4(rec + kOffV4 + 16 * lane);
+          const uint4 sc = ld_shared_v4(rec + kOffSV + 16 * t4);
+          const uint32_t cw = ld_shared_u32(rec + kOffC8 + 4 * lane);
+          const uint32_t vwa[4] = {vw.x, vw.y, vw.z, vw.w};
+          float a1[4] = {off_v, off_v, off_v8, off_v8};
+          float a1b[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t x = vwa[w];
+            mma_bf16(a1, qb[2 * w], nib_bf16_off(x), nib_bf16_off(x >> 4));
+            mma_bf16(a1b, qb[2 * w + 1], nib_bf16_off(x >> 8),
+                     nib_bf16_off(x >> 12));
+          }
+          const __half2 sv = u32_as_h2(sc.x);
+          const float sv0 = __low2float(sv) * kLog2eRsqrtD;
+          const float sv1 = __high2float(sv) * kLog2eRsqrtD;
+          const float P0 = (a1[0] + a1b[0]) * sv0, P1 = (a1[1] + a1b[1]) * sv1;
+          const float P2 = (a1[2] + a1b[2]) * sv0, P3 = (a1[3] + a1b[3]) * sv1;
+          const __half2 h01 = __floats2half2_rn(P0, P1);
+          const __half2 h23 = __floats2half2_rn(P2, P3);
+          const uint32_t A2h[4] = {h2_as_u32(h01), h2_as_u32(h23), 0u, 0u};
+          const uint32_t A2l[4] = {
+              pack_h2(P0 - __low2float(h01), P1 - __high2float(h01)),
+              pack_h2(P2 - __low2float(h23), P3 - __high2float(h23)), 0u, 0u};
+          // K 0..7 carry the high halves, K 8..15 the low halves
+          const uint32_t A2[4] = {A2h[0], A2h[1], A2l[0], A2l[1]};
+          uint32_t bt0, bt1;
+          i8x4_to_h2(cw, bt0, bt1);
+          float l0[4], l1[4];
+          mma_f16_z(l0, A2, bt0, bt0);
+          mma_f16_z(l1, A2, bt1, bt1);
+          const __half2 sc0 = u32_as_h2(sc.y), sc1 = u32_as_h2(sc.z);
+          const float c0 = __low2float(sc0), c1 = __high2float(sc0);
+          const float c8 = __low2float(sc1), c9 = __high2float(sc1);
+          const float e = lse2_quad_fast(l0[0] * c0, l0[1] * c1, l1[0] * c8,
+                                         l1[1] * c9);
+          const float e8 = lse2_quad_fast(l0[2] * c0, l0[3] * c1, l1[2] * c8,
+                                          l1[3] * c9);
+          if ((p >> 1) == t4) {
+            if (p & 1) {
+              o1 = e;
+              o81 = e8;
+            } else {
+              o0 = e;
+              o80 = e8;
+            }
+          }
+        }
+      }
+      // q . mu for the tile's 8 pages (column n = page gq of the tile)
+      float qm[4] = {off_m, off_m, off_m8, off_m8};
+      float qm2[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const uint32_t mrow = base_s + gq * kRec + kOffMu8 + 32 * t4;
+        const uint4 m0 = lds128(mrow), m1 = lds128(mrow + 16);
+        const uint32_t mw[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          uint32_t b01, b23;
+          i8x4_to_h2_off(mw[s], b01, b23);
+          if (s & 1)
+            mma_f16(qm2, qh[s], b01, b23);
+          else
+            mma_f16(qm, qh[s], b01, b23);
+        }
+      }
+      const int pg0 = 2 * t4, pg1 = 2 * t4 + 1;
+      const float sm0 = __half2float(*reinterpret_cast<const __half *>(
+          base + pg0 * kRec + kOffSMu));
+      const float sm1 = __half2float(*reinterpret_cast<const __half *>(
+          base + pg1 * kRec + kOffSMu));
+      if (gq < G) {
+        float *dst = srow + (size_t)gq * max_pages;
+        if (pg0 < npg)
+          dst[pg0] = (o0 + (qm[0] + qm2[0]) * sm0 * kLog2eRsqrtD) * kLn2;
+        if (pg1 < npg)
+          dst[pg1] = (o1 + (qm[1] + qm2[1]) * sm1 * kLog2eRsqrtD) * kLn2;
+      }
+      if (gq + 8 < G) {
+        float *dst = srow + (size_t)(gq + 8) * max_pages;
+        if (pg0 < npg)
+          dst[pg0] = (o80 + (qm[2] + qm2[2]) * sm0 * kLog2eRsqrtD) * kLn2;
+        if (pg1 < npg)
+          dst[pg1] = (o81 + (qm[3] + qm2[3]) * sm1 * kLog2eRsqrtD) * kLn2;
+      }
     }
     __syncwarp();
     if (t + 2 < t_end) {
@@ -644,26 +828,31 @@ cudaError_t launch_score(const void *q, const void *summaries,
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(
-        score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        score_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         227 * 1024);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(score_kernel<true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             227 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(score_kernel<2>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               227 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(score_kernel<3>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               227 * 1024);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int grid = sm_count();
+  auto *qq = static_cast<const __nv_bfloat16 *>(q);
+  auto *ss = static_cast<const uint8_t *>(summaries);
   if (G > 8)
-    score_kernel<true><<<grid, kScoreThreads, smem, stream>>>(
-        static_cast<const __nv_bfloat16 *>(q),
-        static_cast<const uint8_t *>(summaries), seq_lens, batch, h_kv, G,
-        max_pages, s_hat, status);
+    score_kernel<3><<<grid, kScoreThreads, smem, stream>>>(
+        qq, ss, seq_lens, batch, h_kv, G, max_pages, s_hat, status);
+  else if (G > 4)
+    score_kernel<2><<<grid, kScoreThreads, smem, stream>>>(
+        qq, ss, seq_lens, batch, h_kv, G, max_pages, s_hat, status);
   else
-    score_kernel<false><<<grid, kScoreThreads, smem, stream>>>(
-        static_cast<const __nv_bfloat16 *>(q),
-        static_cast<const uint8_t *>(summaries), seq_lens, batch, h_kv, G,
-        max_pages, s_hat, status);
+    score_kernel<1><<<grid, kScoreThreads, smem, stream>>>(
+        qq, ss, seq_lens, batch, h_kv, G, max_pages, s_hat, status);
   return cudaGetLastError();
 }
 
