@@ -78,25 +78,37 @@ __global__ void __launch_bounds__(kDecThreads)
 
   uint8_t *wbase = smem + wid * (4 * kKvTile);  // [stage][K|V]
   const uint32_t wbase_s = smem_u32(wbase);
-  int e_next = begin + wid;
-  // next valid page of this warp's share of the list
+  // resolve the whole slice (index -> page table -> physical page) at once,
+  // so the per-page loop below only issues copies
+  int *s_phys = reinterpret_cast<int *>(smem + kDecSmem);
+  int *s_ntok = s_phys + pps;
+  for (int i = threadIdx.x; i < end - begin; i += blockDim.x) {
+    const int pg = my_idx ? my_idx[begin + i] : begin + i;
+    int ph = -1, nt = 0;
+    if (pg >= n) {
+      set_status(status, LOCKS_DEV_BAD_INDEX);
+    } else if (pg >= 0) {
+      ph = my_pt[pg];
+      if (ph < 0 || ph >= num_phys) {
+        set_status(status, LOCKS_DEV_BAD_PAGE_ID);
+        ph = -1;
+      } else {
+        nt = min(kPage, L - pg * kPage);
+      }
+    }
+    s_phys[i] = ph;
+    s_ntok[i] = nt;
+  }
+  __syncthreads();
+  int e_next = wid;
+  // next valid page of this warp's share of the slice
   auto fetch_next = [&](int &phys, int &ntok) -> bool {
-    while (e_next < end) {
+    while (e_next < end - begin) {
       const int e = e_next;
       e_next += kDecWarps;
-      const int pg = my_idx ? my_idx[e] : e;
-      if (pg < 0) continue;
-      if (pg >= n) {
-        if (lane == 0) set_status(status, LOCKS_DEV_BAD_INDEX);
-        continue;
-      }
-      const int ph = my_pt[pg];
-      if (ph < 0 || ph >= num_phys) {
-        if (lane == 0) set_status(status, LOCKS_DEV_BAD_PAGE_ID);
-        continue;
-      }
-      phys = ph;
-      ntok = min(kPage, L - pg * kPage);
+      if (s_phys[e] < 0) continue;
+      phys = s_phys[e];
+      ntok = s_ntok[e];
       return true;
     }
     return false;
@@ -330,28 +342,30 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(
         decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        kDecSmem);
+        227 * 1024);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(decode_kernel<true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kDecSmem);
+                             227 * 1024);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int list_len = idx ? k : max_pages;
   const int pps = decode_pages_per_split(list_len, (long long)batch * h_kv);
   const int n_split = (list_len + pps - 1) / pps;
+  const size_t smem = kDecSmem + 2 * sizeof(int) * (size_t)pps;
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
   dim3 grid(n_split, h_kv, batch);
   auto *qq = static_cast<const __nv_bfloat16 *>(q);
   auto *kc = static_cast<const __nv_bfloat16 *>(k_cache);
   auto *vc = static_cast<const __nv_bfloat16 *>(v_cache);
   auto *oo = static_cast<__nv_bfloat16 *>(o_out);
   if (G > 8)
-    decode_kernel<true><<<grid, kDecThreads, kDecSmem, stream>>>(
+    decode_kernel<true><<<grid, kDecThreads, smem, stream>>>(
         qq, kc, vc, num_phys, pt, seq_lens, idx, k, h_kv, G, max_pages, pps,
         n_split, oo, lse_out, o_part, lse_part, status);
   else
-    decode_kernel<false><<<grid, kDecThreads, kDecSmem, stream>>>(
+    decode_kernel<false><<<grid, kDecThreads, smem, stream>>>(
         qq, kc, vc, num_phys, pt, seq_lens, idx, k, h_kv, G, max_pages, pps,
         n_split, oo, lse_out, o_part, lse_part, status);
   cudaError_t e = cudaGetLastError();

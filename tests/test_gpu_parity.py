@@ -484,3 +484,28 @@ def test_device_status_flags():
                           d.seq_lens, idx2, 4, o, lse, ws)
     torch.cuda.synchronize()
     assert B.locks_read_status(ws) == B.DEV_BAD_PAGE_ID
+
+
+@pytest.mark.parametrize("G,max_pages", [(8, 300), (16, 97), (4, 33001),
+                                         (2, 33004)])
+def test_select_group_sizes_and_long_tables(G, max_pages):
+    """Selection with other group sizes and with page tables too long for
+    the on-chip key buffer (keys then live in the workspace)."""
+    rng = np.random.default_rng(G * 1000 + max_pages)
+    batch, h_kv, k = 2, 2, 20
+    lens = [16 * max_pages - 3, 16 * (max_pages // 3)]
+    scores = rng.normal(0, 3, (batch, h_kv, G, max_pages)).astype(np.float32)
+    ws = B.new_workspace(batch, G * h_kv, h_kv, max_pages, k, DEV)
+    idx = torch.zeros(batch, h_kv, k, dtype=torch.int32, device=DEV)
+    B.locks_select_pages(torch.from_numpy(scores).to(DEV), i32(lens),
+                         G * h_kv, k, idx, ws)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == 0
+    ig = idx.cpu().numpy()
+    io = O.select_store(scores.astype(np.float64), lens, k)
+    for b in range(batch):
+        for h in range(h_kv):
+            ok, _ = selection_agrees(ig[b, h], io[b, h],
+                                     scores[b, h].astype(np.float64),
+                                     lens[b], k, 1e-4)
+            assert ok, (b, h, ig[b, h], io[b, h])
