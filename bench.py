@@ -160,6 +160,26 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def score_traffic(n_records):
+    """DRAM bytes per score launch from the committed ncu capture
+    (profiles/score_kernel_traffic.json), scaled by records; None when the
+    scoring kernel's source changed since the capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles",
+                               "score_kernel_traffic.json")) as f:
+            d = json.load(f)
+        src = os.path.join(ROOT, "sparse_paged_kv_locks_gb300", "csrc",
+                           "score.cu")
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, ValueError):
+        return None
+    if d.get("score_cu_sha256") != digest:
+        return None
+    return round(float(d["dram_bytes_per_record"]) * n_records)
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -346,7 +366,8 @@ def run_locks(args):
         "roofline": {
             "bound": "hbm", "kernel": "score (summary stream)",
             "achieved": round(score_gbs, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(score_gbs / peak, 4), "traffic": None,
+            "frac": round(score_gbs / peak, 4),
+            "traffic": score_traffic(n_records),
             "peak_source": peak_src,
             "algorithmic_bytes": score_bytes},
         "step_roofline": {

@@ -1,5 +1,4 @@
-// Summary scoring (LOCKS reading notes §4.2 Eq.(4)) and GQA-shared page
-// selection (§4.2 Eq.(5) with the sink/recent rule, §4.4 Algorithm 2).
+// Summary scoring (LOCKS reading notes §4.2 Eq.(4), §4.4 Algorithm 2).
 //
 // Scoring streams the summary store, which is the dominant read of a decode
 // step.  A persistent grid gives every warp a contiguous range of 8-record
@@ -56,19 +55,6 @@ __device__ __forceinline__ void i8x4_to_h2(uint32_t x, uint32_t &lo,
   const __half2 k = __half2half2(__ushort_as_half((unsigned short)0x6480));
   lo = h2_as_u32(__hsub2(u32_as_h2(a), k));
   hi = h2_as_u32(__hsub2(u32_as_h2(b), k));
-}
-
-// Hardware base-2 exponential and logarithm (PTX approximate forms, relative
-// error ~2^-22), used for the 16-token log-sum-exp of a page.
-__device__ __forceinline__ float ex2_fast(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float lg2_fast(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
 }
 
 // D = A * B (zero accumulator), m16n8k16 fp16
@@ -570,383 +556,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   }
 }
 
-// ---------------------------------------------------------------------------
-// selection: one CTA per (sequence, KV head)
-// ---------------------------------------------------------------------------
-constexpr int kSelThreads = 512;
-
-__device__ __forceinline__ uint32_t order_key(float x) {
-  const uint32_t u = __float_as_uint(x);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// block-wide exclusive scan of two counters (blockDim = kSelThreads)
-__device__ __forceinline__ void block_scan2(int a, int b, int &ea, int &eb,
-                                            int *sh /* [2*32] */) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  int ia = a, ib = b;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int va = __shfl_up_sync(0xffffffffu, ia, o);
-    const int vb = __shfl_up_sync(0xffffffffu, ib, o);
-    if (lane >= o) {
-      ia += va;
-      ib += vb;
-    }
-  }
-  if (lane == 31) {
-    sh[wid] = ia;
-    sh[32 + wid] = ib;
-  }
-  __syncthreads();
-  if (wid == 0) {
-    const int nw = (int)(blockDim.x >> 5);
-    int wa = lane < nw ? sh[lane] : 0, wb = lane < nw ? sh[32 + lane] : 0;
-    int sa = wa, sb = wb;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int va = __shfl_up_sync(0xffffffffu, sa, o);
-      const int vb = __shfl_up_sync(0xffffffffu, sb, o);
-      if (lane >= o) {
-        sa += va;
-        sb += vb;
-      }
-    }
-    sh[lane] = sa - wa;
-    sh[32 + lane] = sb - wb;
-  }
-  __syncthreads();
-  ea = sh[wid] + ia - a;
-  eb = sh[32 + wid] + ib - b;
-  __syncthreads();
-}
-
-// Keys live in shared memory when they fit (SMEM_KEYS), else in the
-// workspace.  Keys are indexed by page; the sink, the recent page and pages
-// past the candidates hold key 0, which is below every real key.
-constexpr int kRadixBits = 11;
-constexpr int kRadixBins = 1 << kRadixBits;
-
-template <bool SMEM_KEYS, int GT>
-__global__ void __launch_bounds__(kSelThreads, 2)
-    select_kernel(const float *__restrict__ scores,
-                  const int32_t *__restrict__ seq_lens, int h_kv, int G,
-                  int max_pages, int k, int32_t *__restrict__ idx,
-                  uint32_t *__restrict__ keybuf, int32_t *status) {
-  extern __shared__ __align__(16) uint32_t sel_keys[];
-  __shared__ float zs[kMaxGroup];
-  __shared__ float red_m[32][kMaxGroup], red_s[32][kMaxGroup];
-  __shared__ int hist[kRadixBins];
-  __shared__ int sh_wcnt[2][32];
-  __shared__ uint32_t red_u[2][32];
-  __shared__ uint32_t sh_prefix, sh_mask;
-  __shared__ int sh_remaining, sh_varying;
-
-  const int b = blockIdx.y, h = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int nwarps = blockDim.x >> 5;
-  int L = seq_lens[b];
-  if (L < 0 || L > max_pages * kPage) {
-    if (tid == 0 && h == 0) set_status(status, LOCKS_DEV_BAD_SEQ_LEN);
-    L = max(0, min(L, max_pages * kPage));
-  }
-  const int n = (L + kPage - 1) / kPage, nf = L / kPage;
-  int32_t *out = idx + ((size_t)b * h_kv + h) * k;
-  if (n <= k) {
-    for (int i = tid; i < k; i += blockDim.x) out[i] = i < n ? i : -1;
-    return;
-  }
-  if (k == 2) {  // only the sink and the recent page
-    if (tid == 0) {
-      out[0] = 0;
-      out[1] = n - 1;
-    }
-    return;
-  }
-  const float *sc = scores + ((size_t)b * h_kv + h) * G * (size_t)max_pages;
-  uint32_t *keys = SMEM_KEYS
-                       ? sel_keys
-                       : keybuf + ((size_t)b * h_kv + h) * (size_t)max_pages;
-  constexpr float kLog2e = 1.4426950408889634f;
-  // pages are read four at a time when every row starts 16-byte aligned
-  const bool vec = (max_pages & 3) == 0 &&
-                   ((reinterpret_cast<uintptr_t>(scores) & 15u) == 0);
-  const bool kvec = SMEM_KEYS || (max_pages & 3) == 0;  // 16-byte key rows
-  const int nq = (n + 3) >> 2;        // quads of pages covering [0, n)
-
-  // Z_g: log2-sum-exp2 over the summarised pages [0, nf)
-  {
-    float m[GT], s[GT];
-#pragma unroll
-    for (int g = 0; g < GT; ++g) {
-      m[g] = -INFINITY;
-      s[g] = 0.f;
-    }
-    for (int qd = tid; qd < nq; qd += blockDim.x) {
-      const int j0 = 4 * qd;
-      float x[GT][4];
-#pragma unroll
-      for (int g = 0; g < GT; ++g) {
-        if (g < G) {
-          const float *row = sc + (size_t)g * max_pages;
-          if (vec && j0 + 3 < nf) {
-            const float4 v = *reinterpret_cast<const float4 *>(row + j0);
-            x[g][0] = v.x;
-            x[g][1] = v.y;
-            x[g][2] = v.z;
-            x[g][3] = v.w;
-          } else {
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              x[g][u] = j0 + u < nf ? row[j0 + u] : -INFINITY;
-          }
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < GT; ++g) {
-        if (g >= G) continue;
-        const float cm = fmaxf(fmaxf(x[g][0], x[g][1]), fmaxf(x[g][2], x[g][3])) * kLog2e;
-        const float mm = fmaxf(m[g], cm);
-        if (mm != -INFINITY) {
-          float cs = 0.f;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) cs += ex2_fast(x[g][u] * kLog2e - mm);
-          s[g] = (m[g] == -INFINITY ? 0.f : s[g] * ex2_fast(m[g] - mm)) + cs;
-          m[g] = mm;
-        }
-      }
-    }
-#pragma unroll
-    for (int g = 0; g < GT; ++g) {
-      float mg = m[g], sg = s[g];
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, mg, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, sg, o);
-        const float mm = fmaxf(mg, m2);
-        sg = (mg == -INFINITY ? 0.f : sg * ex2_fast(mg - mm)) +
-             (m2 == -INFINITY ? 0.f : s2 * ex2_fast(m2 - mm));
-        mg = mm;
-      }
-      if (lane == 0 && g < G) {
-        red_m[wid][g] = mg;
-        red_s[wid][g] = sg;
-      }
-    }
-  }
-  __syncthreads();
-  if (tid < G) {
-    float m = -INFINITY;
-    for (int w = 0; w < nwarps; ++w) m = fmaxf(m, red_m[w][tid]);
-    float s = 0.f;
-    for (int w = 0; w < nwarps; ++w)
-      if (red_m[w][tid] != -INFINITY)
-        s += red_s[w][tid] * ex2_fast(red_m[w][tid] - m);
-    zs[tid] = m + lg2_fast(s);
-  }
-  __syncthreads();
-
-  // share-average key of page j (candidates 1..n-2):
-  // log2 sum_g 2^(s_gj - Z_g), each term <= 1 since Z_g bounds every score
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-  float zreg[GT];
-#pragma unroll
-  for (int g = 0; g < GT; ++g) zreg[g] = g < G ? zs[g] : 0.f;
-  for (int qd = tid; qd < nq; qd += blockDim.x) {
-    const int j0 = 4 * qd;
-    float x[GT][4];
-#pragma unroll
-    for (int g = 0; g < GT; ++g) {
-      if (g < G) {
-        const float *row = sc + (size_t)g * max_pages;
-        if (vec && j0 + 3 < nf) {
-          const float4 v = *reinterpret_cast<const float4 *>(row + j0);
-          x[g][0] = v.x;
-          x[g][1] = v.y;
-          x[g][2] = v.z;
-          x[g][3] = v.w;
-        } else {
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            x[g][u] = j0 + u < nf ? row[j0 + u] : 0.f;
-        }
-      }
-    }
-    uint32_t kq[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j = j0 + u;
-      kq[u] = 0u;
-      if (j < 1 || j > n - 2) continue;
-      float sum = 0.f;
-#pragma unroll
-      for (int g = 0; g < GT; ++g)
-        if (g < G) sum += ex2_fast(x[g][u] * kLog2e - zreg[g]);
-      float key;
-      if (sum > 0.f) {
-        key = lg2_fast(sum);
-      } else {  // every term underflowed: subtract the largest first
-        float m = -INFINITY;
-#pragma unroll
-        for (int g = 0; g < GT; ++g)
-          if (g < G) m = fmaxf(m, x[g][u] * kLog2e - zreg[g]);
-        float t = 0.f;
-#pragma unroll
-        for (int g = 0; g < GT; ++g)
-          if (g < G) t += ex2_fast(x[g][u] * kLog2e - zreg[g] - m);
-        key = m + lg2_fast(t);
-      }
-      kq[u] = order_key(key);
-      kmin = min(kmin, kq[u]);
-      kmax = max(kmax, kq[u]);
-    }
-    if (kvec) {
-      *reinterpret_cast<uint4 *>(keys + j0) = make_uint4(kq[0], kq[1], kq[2], kq[3]);
-    } else {
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (j0 + u < n) keys[j0 + u] = kq[u];
-    }
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-  }
-  if (lane == 0) {
-    red_u[0][wid] = kmin;
-    red_u[1][wid] = kmax;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    uint32_t a = 0xffffffffu, z = 0u;
-    for (int w = 0; w < nwarps; ++w) {
-      a = min(a, red_u[0][w]);
-      z = max(z, red_u[1][w]);
-    }
-    // bits above the highest one where min and max differ are common to
-    // every candidate key
-    const int varying = (a == z) ? 0 : 32 - __clz(a ^ z);
-    const uint32_t msk = varying == 32 ? 0u : ~((1u << varying) - 1u);
-    sh_prefix = z & msk;
-    sh_mask = msk;
-    sh_remaining = k - 2;
-    sh_varying = varying;
-  }
-  __syncthreads();
-
-  // radix select of the (k-2)-th largest key over the varying bits,
-  // 11-bit digits from the top; key 0 never matches a candidate prefix
-  const int varying = sh_varying;
-  const int nk4 = (n + 3) >> 2;
-  for (int top = varying; top > 0; top -= kRadixBits) {
-    const int width = min(kRadixBits, top), shift = top - width;
-    const uint32_t dmask = (1u << width) - 1u;
-    for (int i = tid; i < kRadixBins; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    const uint32_t pre = sh_prefix, msk = sh_mask;
-    for (int qd = tid; qd < nk4; qd += blockDim.x) {
-      uint32_t kv[4];
-      if (kvec) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(keys + 4 * qd);
-        kv[0] = v.x;
-        kv[1] = v.y;
-        kv[2] = v.z;
-        kv[3] = v.w;
-      } else {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          kv[u] = 4 * qd + u < n ? keys[4 * qd + u] : 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (kv[u] != 0u && (kv[u] & msk) == pre)
-          atomicAdd(&hist[(kv[u] >> shift) & dmask], 1);
-    }
-    __syncthreads();
-    if (wid == 0) {
-      // lane l covers digits (bins - 1 - 64l) down to (bins - 64 - 64l)
-      constexpr int per = kRadixBins / 32;
-      int tot = 0;
-      for (int i = 0; i < per; ++i) tot += hist[kRadixBins - 1 - per * lane - i];
-      int incl = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      const int before = incl - tot;
-      const int rem = sh_remaining;
-      if (before < rem && rem <= incl) {
-        int acc = before;
-        for (int i = 0; i < per; ++i) {
-          const int d = kRadixBins - 1 - per * lane - i;
-          const int cnt = hist[d];
-          if (acc < rem && rem <= acc + cnt) {
-            sh_prefix = pre | ((uint32_t)d << shift);
-            sh_mask = msk | (dmask << shift);
-            sh_remaining = rem - acc;
-            break;
-          }
-          acc += cnt;
-        }
-      }
-    }
-    __syncthreads();
-  }
-  const uint32_t T = sh_prefix;
-  const int need_eq = sh_remaining;  // keys equal to T to keep (lowest j)
-
-  // ordered compaction: warp w owns pages [w*seg, (w+1)*seg), walked 32 at a
-  // time with ballots; warps' counts are scanned once
-  const int seg = ((n + nwarps - 1) / nwarps + 31) & ~31;
-  const int w_lo = min(n, wid * seg), w_hi = min(n, w_lo + seg);
-  int gt = 0, eq = 0;
-  for (int j = w_lo + lane; j < w_hi; j += 32) {
-    const uint32_t u = keys[j];
-    gt += u > T;
-    eq += u == T;
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    gt += __shfl_xor_sync(0xffffffffu, gt, o);
-    eq += __shfl_xor_sync(0xffffffffu, eq, o);
-  }
-  if (lane == 0) {
-    sh_wcnt[0][wid] = gt;
-    sh_wcnt[1][wid] = eq;
-  }
-  __syncthreads();
-  int gt_before = 0, eq_before = 0;
-  for (int w = 0; w < wid; ++w) {
-    gt_before += sh_wcnt[0][w];
-    eq_before += sh_wcnt[1][w];
-  }
-  const uint32_t below = (1u << lane) - 1u;
-  for (int j0 = w_lo; j0 < w_hi; j0 += 32) {
-    const int j = j0 + lane;
-    const uint32_t u = j < w_hi ? keys[j] : 0u;
-    const uint32_t bgt = __ballot_sync(0xffffffffu, u > T);
-    const uint32_t beq = __ballot_sync(0xffffffffu, u == T && j < w_hi);
-    const int my_gt = gt_before + __popc(bgt & below);
-    const int my_eq = eq_before + __popc(beq & below);
-    const bool sel = (u > T) || (u == T && j < w_hi && my_eq < need_eq);
-    if (sel) {
-      const int pos = 1 + my_gt + min(my_eq, need_eq);
-      if (pos >= 1 && pos < k - 1)
-        out[pos] = j;
-      else
-        set_status(status, LOCKS_DEV_BAD_INDEX);
-    }
-    gt_before += __popc(bgt);
-    eq_before += __popc(beq);
-  }
-  if (tid == 0) {
-    out[0] = 0;
-    out[k - 1] = n - 1;
-  }
-}
-
 // --------------------------------------------------------------------------
 // launchers
 // --------------------------------------------------------------------------
@@ -1007,43 +616,6 @@ cudaError_t launch_score(const void *q, const void *summaries,
     score_kernel<1><<<grid, kScoreThreads, smem, stream>>>(
         qq, ss, seq_lens, batch, h_kv, G, max_pages, s_hat, status);
   return cudaGetLastError();
-}
-
-constexpr int kSelSmemKeys = 32 * 1024;   // candidate keys held on chip
-
-cudaError_t launch_select(const float *scores, const int32_t *seq_lens,
-                          int batch, int h_kv, int G, int max_pages, int k,
-                          int32_t *idx, uint32_t *keybuf, int32_t *status,
-                          cudaStream_t stream) {
-  dim3 grid(h_kv, batch);
-  const bool on_chip = max_pages <= kSelSmemKeys;
-  const size_t smem = on_chip ? (size_t)((max_pages + 3) & ~3) * 4 : 0;
-  auto run = [&](auto kern) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(
-        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmemKeys * 4);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kSelThreads, smem, stream>>>(scores, seq_lens, h_kv, G,
-                                              max_pages, k, idx, keybuf,
-                                              status);
-    return cudaGetLastError();
-  };
-  const int gt = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : G <= 8 ? 8 : 16;
-  if (on_chip) {
-    switch (gt) {
-      case 1: return run(select_kernel<true, 1>);
-      case 2: return run(select_kernel<true, 2>);
-      case 4: return run(select_kernel<true, 4>);
-      case 8: return run(select_kernel<true, 8>);
-      default: return run(select_kernel<true, 16>);
-    }
-  }
-  switch (gt) {
-    case 1: return run(select_kernel<false, 1>);
-    case 2: return run(select_kernel<false, 2>);
-    case 4: return run(select_kernel<false, 4>);
-    case 8: return run(select_kernel<false, 8>);
-    default: return run(select_kernel<false, 16>);
-  }
 }
 
 }  // namespace locks
