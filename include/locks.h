@@ -173,6 +173,34 @@ locks_status_t locks_score_pages(const void *q, const void *summaries,
                                  int h_kv, int max_pages, float *scores_out,
                                  int32_t *status, locks_stream_t stream);
 
+/* Score and select without any caller workspace, for callers that may not
+ * allocate device memory on the decode path (an engine whose memory plan is
+ * frozen after start-up, or a plugin handed only its input and output
+ * buffers).  The pages describe no such call; it exists for deployment.
+ * Computes exactly what locks_score_select computes, with the page scores
+ * and selection keys kept in a 16 MiB array built into the library (every
+ * GPU that loads the library holds it until the process exits).
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - Limit: 256-byte-rounded 4*batch*h_kv*G*max_pages (scores) plus
+ *     4*batch*h_kv*max_pages (keys) must fit in 16 MiB, else
+ *     LOCKS_ERR_UNSUPPORTED and nothing is launched.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero.  Calls that overlap on the GPU
+ *     (on different streams) race on it.
+ *   - status: optional int32 device status word (LOCKS_DEV_* bits).
+ *   - On LOCKS_ERR_CUDA the CUDA error is not kept for
+ *     locks_last_cuda_error.
+ * Other arguments as locks_score_select. */
+locks_status_t locks_score_select_static(const void *q, const void *summaries,
+                                         const int32_t *seq_lens, int batch,
+                                         int h_q, int h_kv, int max_pages,
+                                         int k, int32_t *idx_out,
+                                         int32_t *status,
+                                         locks_stream_t stream);
+
 /* Selection alone (Eq.(5) and the sink/recent rule of §4.2) from given
  * natural-log page scores scores[batch][h_kv][G][max_pages] (entries of
  * full pages are read; a score of exact LSE turns this into the exact-mass
