@@ -381,10 +381,8 @@ def run_locks(args):
                        "sparse_decode_gbs": round(decode_gbs, 1)},
         "gpu_launches": None, "clocks": clk,
     }
-    # launches per step: score, select, decode (+ split combine)
-    pps = _decode_pages_per_split(k, batch * h_kv)
-    launches = 3 + (1 if math.ceil(k / pps) > 1 else 0)
-    line["gpu_launches"] = launches * args.steps
+    # launches per step: score, select, decode and its merge kernel
+    line["gpu_launches"] = 4 * args.steps
     line["build"] = {"page_heads": n_records, "ms": round(build_ms, 3),
                      "page_heads_per_s": round(n_records / (build_ms / 1e3))}
 
@@ -448,20 +446,6 @@ def run_locks(args):
                           "the timed region; numpy default threading"}
     if rank == 0:
         print(json.dumps(line), flush=True)
-
-
-def _decode_pages_per_split(list_len, units):
-    """Mirror of the library's split rule, for the launch count only."""
-    import torch
-    sms = torch.cuda.get_device_properties(
-        torch.cuda.current_device()).multi_processor_count
-    pps = 16
-    while pps < list_len and math.ceil(list_len / pps) > 64:
-        pps *= 2
-    while pps > 4 and units * math.ceil(list_len / pps) < 4 * sms and \
-            math.ceil(list_len / (pps // 2)) <= 64:
-        pps //= 2
-    return pps
 
 
 # ---------------------------------------------------------------------------

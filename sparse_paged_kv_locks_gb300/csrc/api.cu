@@ -25,17 +25,30 @@ static size_t score_region(int batch, int h_q, int h_kv, int max_pages) {
          round_up((size_t)batch * h_kv * max_pages * 4, 256);
 }
 
-static int max_splits_for(int list_len) {
-  int s = (list_len + 3) / 4;
-  return s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
+// Decode partials: one slot per (unit, warp) piece, slot index unit + warp,
+// so units + (warps launched) slots suffice.  The grid never has more warps
+// than list positions nor more than kDecMaxWarps.
+constexpr long long kDecMaxWarps = 8192;
+
+static long long decode_warps_cap(int batch, int h_kv, int list_len) {
+  long long w = (long long)batch * h_kv * list_len;
+  if (w > kDecMaxWarps) w = kDecMaxWarps;
+  return w < 1 ? 1 : w;
 }
 
-// bytes of the split-K region: o_part [batch][h_q][splits][128] float and
-// lse_part [batch][h_q][splits] float
-static size_t decode_region(int batch, int h_q, int list_len) {
-  const size_t s = (size_t)max_splits_for(list_len);
-  return round_up((size_t)batch * h_q * s * kDim * 4, 256) +
-         round_up((size_t)batch * h_q * s * 4, 256);
+// bytes of the decode region: the unit layout written by the decode kernel
+// (int meta[batch + 2]), o_part [slots][G][128] float and lse_part
+// [slots][G] float
+static size_t decode_meta_bytes(int batch) {
+  return round_up(((size_t)batch + 2) * 4, 256);
+}
+static size_t decode_slots(int batch, int h_kv, int list_len) {
+  return (size_t)batch * h_kv + (size_t)decode_warps_cap(batch, h_kv, list_len);
+}
+static size_t decode_region(int batch, int h_q, int h_kv, int list_len) {
+  const size_t rows = decode_slots(batch, h_kv, list_len) * (size_t)(h_q / h_kv);
+  return decode_meta_bytes(batch) + round_up(rows * kDim * 4, 256) +
+         round_up(rows * 4, 256);
 }
 
 static bool heads_ok(int h_q, int h_kv) {
@@ -65,7 +78,7 @@ locks_status_t locks_workspace_size(int batch, int h_q, int h_kv,
     return LOCKS_ERR_INVALID_ARG;
   if (h_q / h_kv > kMaxGroup) return LOCKS_ERR_UNSUPPORTED;
   const size_t a = score_region(batch, h_q, h_kv, max_pages);
-  const size_t b = decode_region(batch, h_q, k);
+  const size_t b = decode_region(batch, h_q, h_kv, k);
   *bytes = kWsHeader + (a > b ? a : b);
   return LOCKS_OK;
 }
@@ -199,19 +212,26 @@ locks_status_t locks_sparse_decode(
       !lse_out || !workspace)
     return LOCKS_ERR_INVALID_ARG;
   const int list_len = idx ? k : max_pages;
-  if (workspace_bytes < kWsHeader + decode_region(batch, h_q, list_len))
+  // every list entry of every (sequence, KV head) is one int32 position
+  if ((long long)batch * h_kv * list_len > 0x7fffffffLL)
+    return LOCKS_ERR_UNSUPPORTED;
+  if (batch > decode_max_batch()) return LOCKS_ERR_UNSUPPORTED;
+  if (workspace_bytes < kWsHeader + decode_region(batch, h_q, h_kv, list_len))
     return LOCKS_ERR_WORKSPACE;
   const int G = h_q / h_kv;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   int32_t *status = reinterpret_cast<int32_t *>(ws);
-  const size_t s = (size_t)max_splits_for(list_len);
-  float *o_part = reinterpret_cast<float *>(ws + kWsHeader);
+  const size_t rows = decode_slots(batch, h_kv, list_len) * (size_t)G;
+  int *meta = reinterpret_cast<int *>(ws + kWsHeader);
+  float *o_part =
+      reinterpret_cast<float *>(ws + kWsHeader + decode_meta_bytes(batch));
   float *lse_part = reinterpret_cast<float *>(
-      ws + kWsHeader + round_up((size_t)batch * h_q * s * kDim * 4, 256));
-  cudaError_t e = launch_decode(q, k_cache, v_cache, num_phys_pages,
-                                page_table, seq_lens, idx, k, batch, h_kv, G,
-                                max_pages, o_out, lse_out, o_part, lse_part,
-                                status, (cudaStream_t)stream);
+      ws + kWsHeader + decode_meta_bytes(batch) + round_up(rows * kDim * 4, 256));
+  const int max_warps = (int)decode_warps_cap(batch, h_kv, list_len);
+  cudaError_t e = launch_decode(
+      q, k_cache, v_cache, num_phys_pages, page_table, seq_lens, idx, k, batch,
+      h_kv, G, max_pages, max_warps, o_out, lse_out, o_part, lse_part, meta,
+      status, (cudaStream_t)stream);
   return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
 }
 

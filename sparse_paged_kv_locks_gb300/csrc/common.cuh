@@ -18,7 +18,6 @@ constexpr int kOffV4 = 0, kOffC8 = 512, kOffMu8 = 640;
 constexpr int kOffSV = 768;   // 64-byte scale block (see include/locks.h)
 constexpr int kOffSMu = 780;
 constexpr int kMaxGroup = 16;
-constexpr int kMaxSplits = 64;     // split-K partials per (b, query head)
 constexpr size_t kWsHeader = 256;  // status word + reserved
 
 __device__ __forceinline__ void set_status(int32_t *status, int bits) {

@@ -2,14 +2,22 @@
 // Algorithm 2: fetch full K/V only for the selected pages, then standard
 // softmax attention for every query head of the group).
 //
-// Split-K flash decode.  A CTA owns one (sequence, KV head, split) and a
-// slice of that pair's selected-page list; its four warps take every fourth
-// page.  Each warp gathers its pages (one 4 KB K run and one 4 KB V run per
-// page through the page table) with 16-byte cp.async into a private, double
-// buffered, XOR-swizzled shared-memory tile, so every K/V byte is read once
-// for the whole GQA group.  Q K^T and P V run on bf16 mma.sync with the
-// query heads as the M dimension; softmax is online in base 2.  Warps merge
-// in shared memory; splits merge in a second small kernel.
+// Warp-streamed flash decode.  The page lists of all (sequence, KV head)
+// units are laid end to end (a "position" is one entry of one unit's list:
+// idx[b][h][i] for sparse decode, page i of sequence b for dense decode) and
+// every warp of a grid sized to fill the GPU takes one contiguous run of
+// `chunk` positions, so all warps stream the same number of pages whatever
+// the list lengths.  A warp resolves 32 positions at a time (index -> page
+// table -> physical page, one per lane), gathers each valid page (one 4 KB
+// K run and one 4 KB V run) with 16-byte cp.async into a private,
+// double-buffered, XOR-swizzled shared-memory tile, and runs Q K^T and P V on
+// bf16 mma.sync with the query heads as the M dimension; every K/V byte is
+// read once for the whole GQA group.  Softmax is online in base 2.
+//
+// A unit that lies inside one warp's run is finished by that warp.  A unit
+// split across warps leaves one normalised partial (o, lse) per warp in
+// slot (unit + warp) -- distinct for distinct (unit, warp) pieces because
+// both grow along the positions -- and a second small kernel merges them.
 #include "common.cuh"
 #include "launch.h"
 
@@ -17,9 +25,13 @@ namespace locks {
 
 constexpr int kDecWarps = 4;
 constexpr int kDecThreads = 32 * kDecWarps;
-constexpr int kKvTile = kPage * kDim * 2;                     // 4096 bytes
-constexpr int kDecSmem = kDecWarps * 2 * 2 * kKvTile;         // 64 KB
-constexpr float kDecScale = 0.12751743074602467f;             // log2e/sqrt(d)
+constexpr int kDecStages = 2;
+constexpr int kKvTile = kPage * kDim * 2;                          // 4096 B
+constexpr int kDecRing = kDecWarps * kDecStages * 2 * kKvTile;      // 64 KB
+// resident CTAs per SM the register budget is sized for (G > 8 keeps a
+// second row of accumulators and takes two)
+constexpr int kDecMinBlocks = 3;
+constexpr float kDecScale = 0.12751743074602467f;  // log2(e)/sqrt(d)
 constexpr float kLn2f = 0.69314718055994531f;
 
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
@@ -32,39 +44,159 @@ __device__ __forceinline__ uint32_t swz(int row, int ch) {
   return (uint32_t)(row * 256 + ((ch ^ (row & 7)) << 4));
 }
 
+// Position layout shared by the two kernels.  Sequence b's h_kv units are
+// consecutive, each len_b positions long, and start at position first(b):
+// b * h_kv * k for sparse decode (per_seq = h_kv * k), pre[b] (a prefix sum
+// over the sequences' page counts) for dense decode (per_seq = 0).
+struct Layout {
+  const int *pre;
+  int batch, h_kv, per_seq;
+
+  __device__ __forceinline__ int first(int b) const {
+    return per_seq ? b * per_seq : pre[b];
+  }
+  // sequence holding position p (p below the total)
+  __device__ __forceinline__ int seq(int p) const {
+    if (per_seq) return p / per_seq;
+    int lo = 0, hi = batch;  // largest b with pre[b] <= p
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pre[mid] <= p) lo = mid; else hi = mid;
+    }
+    return lo;
+  }
+  __device__ __forceinline__ int unit_len(int b) const {
+    return (first(b + 1) - first(b)) / h_kv;
+  }
+  __device__ __forceinline__ int unit_of(int p) const {
+    const int b = seq(p);
+    return b * h_kv + (p - first(b)) / unit_len(b);
+  }
+  // positions [begin, end) of unit u
+  __device__ __forceinline__ int2 span(int u) const {
+    const int b = u / h_kv, h = u - b * h_kv;
+    const int f = first(b), len = unit_len(b);
+    return make_int2(f + h * len, f + (h + 1) * len);
+  }
+};
+
+__device__ __forceinline__ int clamp_len(const int32_t *seq_lens, int b,
+                                         int max_pages, int32_t *status) {
+  int L = __ldg(seq_lens + b);
+  if (L < 0 || L > max_pages * kPage) {
+    set_status(status, LOCKS_DEV_BAD_SEQ_LEN);
+    L = max(0, min(L, max_pages * kPage));
+  }
+  return L;
+}
+
+// One lane's entry of a 32-position window.
+struct Entry {
+  int phys;  // physical page, -1 when the position is skipped
+  int ntok;  // tokens of the page inside the sequence
+  int u;     // unit (b * h_kv + h)
+};
+
+__device__ __forceinline__ Entry resolve(int p, int pe, const Layout &lay,
+                                         const int32_t *seq_lens,
+                                         const int32_t *idx, int k,
+                                         const int32_t *pt, int max_pages,
+                                         int64_t num_phys, int32_t *status) {
+  Entry e{-1, 0, 0};
+  if (p >= pe) return e;
+  const int b = lay.seq(p);
+  const int len = lay.unit_len(b);
+  const int r = p - lay.first(b);
+  const int h = r / len, slot = r - h * len;
+  e.u = b * lay.h_kv + h;
+  const int L = clamp_len(seq_lens, b, max_pages, status);
+  const int n = (L + kPage - 1) / kPage;
+  const int pg = idx ? __ldg(idx + (size_t)e.u * k + slot) : slot;
+  if (pg >= n) {
+    set_status(status, LOCKS_DEV_BAD_INDEX);
+  } else if (pg >= 0) {
+    const int ph = __ldg(pt + (size_t)b * max_pages + pg);
+    if (ph < 0 || ph >= num_phys) {
+      set_status(status, LOCKS_DEV_BAD_PAGE_ID);
+    } else {
+      e.phys = ph;
+      e.ntok = min(kPage, L - pg * kPage);
+    }
+  }
+  return e;
+}
+
 template <bool WIDE>
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
     decode_kernel(const __nv_bfloat16 *__restrict__ q,
                   const __nv_bfloat16 *__restrict__ k_cache,
                   const __nv_bfloat16 *__restrict__ v_cache, int64_t num_phys,
                   const int32_t *__restrict__ pt,
                   const int32_t *__restrict__ seq_lens,
-                  const int32_t *__restrict__ idx, int k, int h_kv, int G,
-                  int max_pages, int pps, int n_split,
+                  const int32_t *__restrict__ idx, int k, int batch, int h_kv,
+                  int G, int max_pages, int n_warps,
                   __nv_bfloat16 *__restrict__ o_out,
                   float *__restrict__ lse_out, float *__restrict__ o_part,
-                  float *__restrict__ lse_part, int32_t *status) {
+                  float *__restrict__ lse_part, int *__restrict__ meta,
+                  int32_t *status) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  int *s_pre = reinterpret_cast<int *>(smem + kDecRing);  // [batch + 1]
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int gq = lane >> 2, t4 = lane & 3;
   const int h_q = h_kv * G;
+  const Layout lay{s_pre, batch, h_kv, idx ? h_kv * k : 0};
 
-  int L = seq_lens[b];
-  if (L < 0 || L > max_pages * kPage) {
-    if (threadIdx.x == 0 && h == 0 && split == 0)
-      set_status(status, LOCKS_DEV_BAD_SEQ_LEN);
-    L = max(0, min(L, max_pages * kPage));
+  int total;
+  if (idx) {
+    total = batch * h_kv * k;
+  } else {
+    // dense: h_kv lists of the sequence's page count; inclusive scan into
+    // s_pre[1..batch]
+    for (int b = threadIdx.x; b < batch; b += blockDim.x) {
+      const int L = clamp_len(seq_lens, b, max_pages,
+                              blockIdx.x == 0 ? status : nullptr);
+      s_pre[b + 1] = h_kv * ((L + kPage - 1) / kPage);
+    }
+    if (threadIdx.x == 0) s_pre[0] = 0;
+    __syncthreads();
+    if (wid == 0) {
+      const int per = (batch + 31) / 32;
+      const int lo = 1 + lane * per, hi = min(batch + 1, lo + per);
+      int run = 0;
+      for (int i = lo; i < hi; ++i) {
+        run += s_pre[i];
+        s_pre[i] = run;
+      }
+      int incl = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const int excl = incl - run;
+      for (int i = lo; i < hi; ++i) s_pre[i] += excl;
+    }
+    __syncthreads();
+    total = s_pre[batch];
   }
-  const int n = (L + kPage - 1) / kPage;
-  const int list_len = idx ? k : n;
-  const int begin = split * pps, end = min(list_len, begin + pps);
-  const int32_t *my_idx = idx ? idx + ((size_t)b * h_kv + h) * k : nullptr;
-  const int32_t *my_pt = pt + (size_t)b * max_pages;
+  const int chunk = max(1, (total + n_warps - 1) / n_warps);
+  if (blockIdx.x == 0) {  // layout for the merge kernel
+    if (threadIdx.x == 0) meta[0] = chunk;
+    if (!idx)
+      for (int b = threadIdx.x; b <= batch; b += blockDim.x)
+        meta[1 + b] = s_pre[b];
+  }
+  const int gw = blockIdx.x * kDecWarps + wid;
+  if (gw >= n_warps || (long long)gw * chunk >= total) return;
+  const int pb = gw * chunk, pe = min(total, pb + chunk);
 
-  // query A fragments (bf16), rows = heads of the group
+  uint8_t *wbase = smem + wid * (kDecStages * 2 * kKvTile);
+  const uint32_t wbase_s = smem_u32(wbase);
+
+  // query A fragments (bf16) of unit u, rows = heads of the group
   uint32_t qa[8][4];
-  {
+  auto load_q = [&](int u) {
+    const int b = u / h_kv, h = u - b * h_kv;
     const __nv_bfloat16 *qb = q + ((size_t)b * h_q + (size_t)h * G) * kDim;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
@@ -74,46 +206,36 @@ __global__ void __launch_bounds__(kDecThreads)
       qa[s][1] = (WIDE && gq + 8 < G) ? __ldg(reinterpret_cast<const uint32_t *>(qb + (gq + 8) * kDim + d0)) : 0u;
       qa[s][3] = (WIDE && gq + 8 < G) ? __ldg(reinterpret_cast<const uint32_t *>(qb + (gq + 8) * kDim + d0 + 8)) : 0u;
     }
-  }
-
-  uint8_t *wbase = smem + wid * (4 * kKvTile);  // [stage][K|V]
-  const uint32_t wbase_s = smem_u32(wbase);
-  // resolve the whole slice (index -> page table -> physical page) at once,
-  // so the per-page loop below only issues copies
-  int *s_phys = reinterpret_cast<int *>(smem + kDecSmem);
-  int *s_ntok = s_phys + pps;
-  for (int i = threadIdx.x; i < end - begin; i += blockDim.x) {
-    const int pg = my_idx ? my_idx[begin + i] : begin + i;
-    int ph = -1, nt = 0;
-    if (pg >= n) {
-      set_status(status, LOCKS_DEV_BAD_INDEX);
-    } else if (pg >= 0) {
-      ph = my_pt[pg];
-      if (ph < 0 || ph >= num_phys) {
-        set_status(status, LOCKS_DEV_BAD_PAGE_ID);
-        ph = -1;
-      } else {
-        nt = min(kPage, L - pg * kPage);
-      }
-    }
-    s_phys[i] = ph;
-    s_ntok[i] = nt;
-  }
-  __syncthreads();
-  int e_next = wid;
-  // next valid page of this warp's share of the slice
-  auto fetch_next = [&](int &phys, int &ntok) -> bool {
-    while (e_next < end - begin) {
-      const int e = e_next;
-      e_next += kDecWarps;
-      if (s_phys[e] < 0) continue;
-      phys = s_phys[e];
-      ntok = s_ntok[e];
-      return true;
-    }
-    return false;
   };
-  auto issue = [&](int stage, int phys) {
+  int cur_u = lay.unit_of(pb);
+  load_q(cur_u);
+  bool q_ready = true;
+
+  // window of 32 positions: this lane's entry and the valid ones not yet
+  // handed to the copy engine
+  int win = pb - 32;
+  uint32_t wmask = 0;
+  Entry we{-1, 0, 0};
+  // next valid position in order (phys < 0: none left)
+  auto next_valid = [&](int &phys, int &ntok, int &u) {
+    while (wmask == 0) {
+      win += 32;
+      if (win >= pe) {
+        phys = -1;
+        return;
+      }
+      we = resolve(win + lane, pe, lay, seq_lens, idx, k, pt, max_pages,
+                   num_phys, status);
+      wmask = __ballot_sync(0xffffffffu, we.phys >= 0);
+    }
+    const int j = __ffs(wmask) - 1;
+    wmask &= wmask - 1;
+    phys = __shfl_sync(0xffffffffu, we.phys, j);
+    ntok = __shfl_sync(0xffffffffu, we.ntok, j);
+    u = __shfl_sync(0xffffffffu, we.u, j);
+  };
+  auto issue = [&](int stage, int phys, int u) {
+    const int h = u % h_kv;
     const uint8_t *ks = reinterpret_cast<const uint8_t *>(k_cache) +
                         ((size_t)phys * h_kv + h) * kKvTile;
     const uint8_t *vs = reinterpret_cast<const uint8_t *>(v_cache) +
@@ -132,19 +254,79 @@ __global__ void __launch_bounds__(kDecThreads)
   for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m_run = -INFINITY, m_run8 = -INFINITY, l_run = 0.f, l_run8 = 0.f;
 
-  int ph0 = 0, nt0 = 0, ph1 = 0, nt1 = 0;
-  bool have0 = fetch_next(ph0, nt0);
-  if (have0) issue(0, ph0);
+  // write unit u's result (whole unit inside this run) or partial (slot
+  // u + gw), then reset the accumulators
+  auto flush = [&](int u) {
+    float l = l_run, l8 = l_run8;
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    l8 += __shfl_xor_sync(0xffffffffu, l8, 1);
+    l8 += __shfl_xor_sync(0xffffffffu, l8, 2);
+    const int2 sp = lay.span(u);
+    const bool whole = sp.x >= pb && sp.y <= pe;
+    const int b = u / h_kv, h = u - b * h_kv;
+#pragma unroll
+    for (int half = 0; half < (WIDE ? 2 : 1); ++half) {
+      const int g = gq + 8 * half;
+      const float lh = half ? l8 : l;
+      const float mh = half ? m_run8 : m_run;
+      const float inv = lh > 0.f ? 1.f / lh : 0.f;
+      const float lse = lh > 0.f ? (mh + log2f(lh)) * kLn2f : -INFINITY;
+      if (g < G) {
+        if (whole) {
+          const size_t row = (size_t)b * h_q + (size_t)h * G + g;
+          uint32_t *dst = reinterpret_cast<uint32_t *>(o_out + row * kDim);
+#pragma unroll
+          for (int nt = 0; nt < 16; ++nt)
+            dst[(nt * 8 + 2 * t4) >> 1] =
+                pack_bf2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+          if (t4 == 0) lse_out[row] = lse;
+        } else {
+          const size_t slot = ((size_t)u + gw) * G + g;
+          float2 *dst = reinterpret_cast<float2 *>(o_part + slot * kDim);
+#pragma unroll
+          for (int nt = 0; nt < 16; ++nt)
+            dst[(nt * 8 + 2 * t4) >> 1] =
+                make_float2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+          if (t4 == 0) lse_part[slot] = lse;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    m_run = m_run8 = -INFINITY;
+    l_run = l_run8 = 0.f;
+  };
+  // close every unit before `u` (units with no positions are the merge
+  // kernel's)
+  auto advance_to = [&](int u) {
+    while (cur_u < u) {
+      const int2 sp = lay.span(cur_u);
+      if (sp.y > sp.x) flush(cur_u);
+      ++cur_u;
+      q_ready = false;
+    }
+  };
+
+  int ph0, nt0 = 0, u0 = 0, ph1, nt1 = 0, u1 = 0;
+  next_valid(ph0, nt0, u0);
+  if (ph0 >= 0) issue(0, ph0, u0);
   cp_async_commit();
-  bool have1 = fetch_next(ph1, nt1);
-  if (have1) issue(1, ph1);
+  if (ph0 >= 0) next_valid(ph1, nt1, u1); else ph1 = -1;
+  if (ph1 >= 0) issue(1, ph1, u1);
   cp_async_commit();
 
   for (int it = 0;; ++it) {
     const int st = it & 1;
-    const bool have = st ? have1 : have0;
-    if (!have) break;
+    const int phys = st ? ph1 : ph0;
+    if (phys < 0) break;
     const int ntok = st ? nt1 : nt0;
+    const int u = st ? u1 : u0;
+    if (u != cur_u) advance_to(u);
+    if (!q_ready) {
+      load_q(cur_u);
+      q_ready = true;
+    }
     cp_async_wait<1>();
     __syncwarp();
     const uint32_t kb_s = wbase_s + st * 2 * kKvTile, vb_s = kb_s + kKvTile;
@@ -220,91 +402,98 @@ __global__ void __launch_bounds__(kDecThreads)
       }
     }
     __syncwarp();
-    if (st) {
-      have1 = fetch_next(ph1, nt1);
-      if (have1) issue(1, ph1);
-    } else {
-      have0 = fetch_next(ph0, nt0);
-      if (have0) issue(0, ph0);
-    }
+    int nph, nnt = 0, nu = 0;
+    next_valid(nph, nnt, nu);
+    if (nph >= 0) issue(st, nph, nu);
     cp_async_commit();
+    if (st) {
+      ph1 = nph;
+      nt1 = nnt;
+      u1 = nu;
+    } else {
+      ph0 = nph;
+      nt0 = nnt;
+      u0 = nu;
+    }
   }
   cp_async_wait<0>();
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-  l_run8 += __shfl_xor_sync(0xffffffffu, l_run8, 1);
-  l_run8 += __shfl_xor_sync(0xffffffffu, l_run8, 2);
-  __syncthreads();
-
-  // merge the four warps: smem [warp][16 rows][128] + m, l
-  float *sO = reinterpret_cast<float *>(smem);
-  float *sM = sO + kDecWarps * 16 * kDim;
-  float *sL = sM + kDecWarps * 16;
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    const int d = nt * 8 + 2 * t4;
-    sO[(wid * 16 + gq) * kDim + d] = o[nt][0];
-    sO[(wid * 16 + gq) * kDim + d + 1] = o[nt][1];
-    sO[(wid * 16 + gq + 8) * kDim + d] = o[nt][2];
-    sO[(wid * 16 + gq + 8) * kDim + d + 1] = o[nt][3];
-  }
-  if (t4 == 0) {
-    sM[wid * 16 + gq] = m_run;
-    sL[wid * 16 + gq] = l_run;
-    sM[wid * 16 + gq + 8] = m_run8;
-    sL[wid * 16 + gq + 8] = l_run8;
-  }
-  __syncthreads();
-  const int d = threadIdx.x;  // 128 threads = head dim
-  for (int g = 0; g < G; ++g) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sM[w * 16 + g]);
-    float Lsum = 0.f, acc = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) {
-        const float mw = sM[w * 16 + g];
-        if (mw == -INFINITY) continue;
-        const float f = exp2f(mw - M);
-        Lsum += sL[w * 16 + g] * f;
-        acc += sO[(w * 16 + g) * kDim + d] * f;
-      }
-    }
-    const float ov = Lsum > 0.f ? acc / Lsum : 0.f;
-    const float lse = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2f : -INFINITY;
-    const size_t row = (size_t)b * h_q + (size_t)h * G + g;
-    if (n_split == 1) {
-      o_out[row * kDim + d] = __float2bfloat16_rn(ov);
-      if (d == 0) lse_out[row] = lse;
-    } else {
-      o_part[(row * n_split + split) * kDim + d] = ov;
-      if (d == 0) lse_part[row * n_split + split] = lse;
-    }
+  // close the units up to the one holding the run's last position
+  {
+    const int u_last = lay.unit_of(pe - 1);
+    advance_to(u_last);
+    flush(u_last);
   }
 }
 
-__global__ void __launch_bounds__(kDim)
+// Merge of the partials of units split across warps; also writes the
+// empty result of units with no positions.  One warp per (unit, head) row;
+// lane l owns head dimensions 4l..4l+3 and the pieces are visited 32 at a
+// time with their weights held one per lane.
+constexpr int kCombineWarps = 4;
+
+__global__ void __launch_bounds__(32 * kCombineWarps)
     combine_kernel(const float *__restrict__ o_part,
-                   const float *__restrict__ lse_part, int n_split,
-                   __nv_bfloat16 *__restrict__ o_out,
+                   const float *__restrict__ lse_part,
+                   const int *__restrict__ meta, int batch, int h_kv, int k,
+                   int dense, int G, __nv_bfloat16 *__restrict__ o_out,
                    float *__restrict__ lse_out) {
-  const size_t row = blockIdx.x;
-  const int d = threadIdx.x;
-  const float *lp = lse_part + row * n_split;
+  const int lane = threadIdx.x & 31;
+  const long long row =
+      (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  if (row >= (long long)batch * h_kv * G) return;
+  const int u = (int)(row / G), g = (int)(row - (long long)u * G);
+  const Layout lay{meta + 1, batch, h_kv, dense ? 0 : h_kv * k};
+  const int chunk = meta[0];
+  const int2 sp = lay.span(u);
+  uint2 *dst = reinterpret_cast<uint2 *>(o_out + row * kDim) + lane;
+  int w0 = 0, w1 = 0;
+  if (sp.y > sp.x) {
+    w0 = sp.x / chunk;
+    w1 = (sp.y - 1) / chunk;
+    if (w0 == w1) return;  // finished by its warp
+  }
   float M = -INFINITY;
-  for (int s = 0; s < n_split; ++s) M = fmaxf(M, lp[s]);
-  float wsum = 0.f, acc = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < n_split; ++s) {
-      if (lp[s] == -INFINITY) continue;
-      const float w = expf(lp[s] - M);
-      wsum += w;
-      acc += w * o_part[(row * n_split + s) * kDim + d];
+  if (sp.y > sp.x)
+    for (int w = w0 + lane; w <= w1; w += 32)
+      M = fmaxf(M, lse_part[((size_t)u + w) * G + g]);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1)
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (M == -INFINITY) {  // no tokens
+    *dst = make_uint2(0u, 0u);
+    if (lane == 0) lse_out[row] = -INFINITY;
+    return;
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  for (int wb = w0; wb <= w1; wb += 32) {
+    const int w = wb + lane;
+    float f = 0.f;
+    if (w <= w1) {
+      const float l = lse_part[((size_t)u + w) * G + g];
+      f = l == -INFINITY ? 0.f : expf(l - M);
+    }
+    wsum += f;
+    const int cnt = min(32, w1 - wb + 1);
+    const float4 *src =
+        reinterpret_cast<const float4 *>(o_part) + (((size_t)u + wb) * G + g) * 32 + lane;
+#pragma unroll 8
+    for (int j = 0; j < cnt; ++j) {
+      const float fj = __shfl_sync(0xffffffffu, f, j);
+      const float4 v = src[(size_t)j * G * 32];
+      acc.x += fj * v.x;
+      acc.y += fj * v.y;
+      acc.z += fj * v.z;
+      acc.w += fj * v.w;
     }
   }
-  o_out[row * kDim + d] = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
-  if (d == 0) lse_out[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1)
+    wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  const float inv = 1.f / wsum;
+  *dst = make_uint2(pack_bf2(acc.x * inv, acc.y * inv),
+                    pack_bf2(acc.z * inv, acc.w * inv));
+  if (lane == 0) lse_out[row] = M + logf(wsum);
 }
 
 // --------------------------------------------------------------------------
@@ -321,24 +510,23 @@ static int dec_sm_count() {
   return n;
 }
 
-int decode_pages_per_split(int list_len, long long units) {
-  const int sms = dec_sm_count();
-  int pps = 16;
-  while (pps < list_len && (list_len + pps - 1) / pps > kMaxSplits) pps *= 2;
-  while (pps > 4 && units * ((list_len + pps - 1) / pps) < 4LL * sms &&
-         (list_len + pps / 2 - 1) / (pps / 2) <= kMaxSplits)
-    pps /= 2;
-  return pps;
+size_t decode_smem_bytes(int batch) {
+  return (size_t)kDecRing + sizeof(int) * ((size_t)batch + 1);
+}
+
+int decode_max_batch() {
+  return (int)((227 * 1024 - (size_t)kDecRing - 64) / sizeof(int));
 }
 
 cudaError_t launch_decode(const void *q, const void *k_cache,
                           const void *v_cache, int64_t num_phys,
                           const int32_t *pt, const int32_t *seq_lens,
                           const int32_t *idx, int k, int batch, int h_kv,
-                          int G, int max_pages, void *o_out, float *lse_out,
-                          float *o_part, float *lse_part, int32_t *status,
-                          cudaStream_t stream) {
+                          int G, int max_pages, int max_warps, void *o_out,
+                          float *lse_out, float *o_part, float *lse_part,
+                          int *meta, int32_t *status, cudaStream_t stream) {
   static bool attr_set = false;
+  static int blocks_per_sm[2] = {0, 0};
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(
         decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -350,28 +538,42 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int list_len = idx ? k : max_pages;
-  const int pps = decode_pages_per_split(list_len, (long long)batch * h_kv);
-  const int n_split = (list_len + pps - 1) / pps;
-  const size_t smem = kDecSmem + 2 * sizeof(int) * (size_t)pps;
+  const size_t smem = decode_smem_bytes(batch);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  dim3 grid(n_split, h_kv, batch);
+  const int wide = G > 8 ? 1 : 0;
+  // resident CTAs per SM at the common (small-batch) footprint; a larger
+  // batch only lowers the count the hardware actually fits
+  if (blocks_per_sm[wide] == 0) {
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &n, wide ? decode_kernel<true> : decode_kernel<false>, kDecThreads,
+        decode_smem_bytes(64));
+    if (e != cudaSuccess) return e;
+    blocks_per_sm[wide] = n > 0 ? n : 1;
+  }
+  long long warps = (long long)blocks_per_sm[wide] * dec_sm_count() * kDecWarps;
+  if (warps > max_warps) warps = max_warps;
+  if (warps < 1) warps = 1;
+  const int n_warps = (int)warps;
+  const int grid = (n_warps + kDecWarps - 1) / kDecWarps;
   auto *qq = static_cast<const __nv_bfloat16 *>(q);
   auto *kc = static_cast<const __nv_bfloat16 *>(k_cache);
   auto *vc = static_cast<const __nv_bfloat16 *>(v_cache);
   auto *oo = static_cast<__nv_bfloat16 *>(o_out);
-  if (G > 8)
+  if (wide)
     decode_kernel<true><<<grid, kDecThreads, smem, stream>>>(
-        qq, kc, vc, num_phys, pt, seq_lens, idx, k, h_kv, G, max_pages, pps,
-        n_split, oo, lse_out, o_part, lse_part, status);
+        qq, kc, vc, num_phys, pt, seq_lens, idx, k, batch, h_kv, G, max_pages,
+        n_warps, oo, lse_out, o_part, lse_part, meta, status);
   else
     decode_kernel<false><<<grid, kDecThreads, smem, stream>>>(
-        qq, kc, vc, num_phys, pt, seq_lens, idx, k, h_kv, G, max_pages, pps,
-        n_split, oo, lse_out, o_part, lse_part, status);
+        qq, kc, vc, num_phys, pt, seq_lens, idx, k, batch, h_kv, G, max_pages,
+        n_warps, oo, lse_out, o_part, lse_part, meta, status);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || n_split == 1) return e;
-  combine_kernel<<<(unsigned)((size_t)batch * h_kv * G), kDim, 0, stream>>>(
-      o_part, lse_part, n_split, oo, lse_out);
+  if (e != cudaSuccess) return e;
+  const long long rows = (long long)batch * h_kv * G;
+  combine_kernel<<<(unsigned)((rows + kCombineWarps - 1) / kCombineWarps),
+                   32 * kCombineWarps, 0, stream>>>(
+      o_part, lse_part, meta, batch, h_kv, k, idx ? 0 : 1, G, oo, lse_out);
   return cudaGetLastError();
 }
 

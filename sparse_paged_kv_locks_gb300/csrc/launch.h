@@ -38,11 +38,11 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
                           const void *v_cache, int64_t num_phys,
                           const int32_t *pt, const int32_t *seq_lens,
                           const int32_t *idx, int k, int batch, int h_kv,
-                          int G, int max_pages, void *o_out, float *lse_out,
-                          float *o_part, float *lse_part, int32_t *status,
-                          cudaStream_t stream);
+                          int G, int max_pages, int max_warps, void *o_out,
+                          float *lse_out, float *o_part, float *lse_part,
+                          int *meta, int32_t *status, cudaStream_t stream);
 
 int score_max_batch();
-int decode_pages_per_split(int list_len, long long units);
+int decode_max_batch();
 
 }  // namespace locks

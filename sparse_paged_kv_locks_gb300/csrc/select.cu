@@ -59,11 +59,47 @@ __device__ __forceinline__ void block_scan2(int a, int b, int &ea, int &eb,
   __syncthreads();
 }
 
+// Scores of pages j0..j0+3 of every head of the group; pages at or past
+// `lim` read as `fill`.
+template <int GT>
+__device__ __forceinline__ void load_quad(const float *sc, int max_pages,
+                                          int G, bool vec, int j0, int lim,
+                                          float fill, float (&x)[GT][4]) {
+#pragma unroll
+  for (int g = 0; g < GT; ++g) {
+    const float *row = sc + (size_t)g * max_pages;
+    if (g < G && vec && j0 + 3 < lim) {
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(row + j0));
+      x[g][0] = v.x;
+      x[g][1] = v.y;
+      x[g][2] = v.z;
+      x[g][3] = v.w;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        x[g][u] = (g < G && j0 + u < lim) ? __ldg(row + j0 + u) : fill;
+    }
+  }
+}
+
+// Keys j0..j0+3 (16-byte aligned when `kvec`); keys at or past `lim` read 0.
+__device__ __forceinline__ uint4 load_keys4(const uint32_t *keys, int j0,
+                                            int lim, bool kvec) {
+  if (kvec && j0 + 3 < lim) return *reinterpret_cast<const uint4 *>(keys + j0);
+  uint4 v;
+  v.x = j0 < lim ? keys[j0] : 0u;
+  v.y = j0 + 1 < lim ? keys[j0 + 1] : 0u;
+  v.z = j0 + 2 < lim ? keys[j0 + 2] : 0u;
+  v.w = j0 + 3 < lim ? keys[j0 + 3] : 0u;
+  return v;
+}
+
 // Keys live in shared memory when they fit (SMEM_KEYS), else in the
 // workspace.  Keys are indexed by page; the sink, the recent page and pages
 // past the candidates hold key 0, which is below every real key.
 constexpr int kRadixBits = 11;
 constexpr int kRadixBins = 1 << kRadixBits;
+constexpr int kBinsPerWarp = kRadixBins / (kSelThreads / 32);  // 128
 
 template <bool SMEM_KEYS, int GT>
 __global__ void __launch_bounds__(kSelThreads, 2)
@@ -74,7 +110,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   extern __shared__ __align__(16) uint32_t sel_keys[];
   __shared__ float zs[kMaxGroup];
   __shared__ float red_m[32][kMaxGroup], red_s[32][kMaxGroup];
-  __shared__ int hist[kRadixBins];
+  __shared__ __align__(16) int hist[2][kRadixBins];
   __shared__ int sh_wcnt[2][32];
   __shared__ uint32_t red_u[2][32];
   __shared__ uint32_t sh_prefix, sh_mask;
@@ -82,7 +118,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
 
   const int b = blockIdx.y, h = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int nwarps = blockDim.x >> 5;
+  constexpr int nwarps = kSelThreads / 32;
   int L = seq_lens[b];
   if (L < 0 || L > max_pages * kPage) {
     if (tid == 0 && h == 0) set_status(status, LOCKS_DEV_BAD_SEQ_LEN);
@@ -111,6 +147,9 @@ __global__ void __launch_bounds__(kSelThreads, 2)
                    ((reinterpret_cast<uintptr_t>(scores) & 15u) == 0);
   const bool kvec = SMEM_KEYS || (max_pages & 3) == 0;  // 16-byte key rows
   const int nq = (n + 3) >> 2;        // quads of pages covering [0, n)
+  // quads a thread has in flight at once (registers allow two for G <= 4)
+  constexpr int R = GT <= 4 ? 2 : 1;
+  for (int i = tid; i < kRadixBins; i += blockDim.x) hist[0][i] = 0;
 
   // Z_g: log2-sum-exp2 over the summarised pages [0, nf)
   {
@@ -120,37 +159,27 @@ __global__ void __launch_bounds__(kSelThreads, 2)
       m[g] = -INFINITY;
       s[g] = 0.f;
     }
-    for (int qd = tid; qd < nq; qd += blockDim.x) {
-      const int j0 = 4 * qd;
-      float x[GT][4];
+    for (int qd = tid; qd < nq; qd += R * blockDim.x) {
+      float x[R][GT][4];
 #pragma unroll
-      for (int g = 0; g < GT; ++g) {
-        if (g < G) {
-          const float *row = sc + (size_t)g * max_pages;
-          if (vec && j0 + 3 < nf) {
-            const float4 v = *reinterpret_cast<const float4 *>(row + j0);
-            x[g][0] = v.x;
-            x[g][1] = v.y;
-            x[g][2] = v.z;
-            x[g][3] = v.w;
-          } else {
+      for (int r = 0; r < R; ++r)
+        load_quad<GT>(sc, max_pages, G, vec, 4 * (qd + r * blockDim.x), nf,
+                      -INFINITY, x[r]);
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              x[g][u] = j0 + u < nf ? row[j0 + u] : -INFINITY;
+      for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int g = 0; g < GT; ++g) {
+          if (g >= G) continue;
+          const float cm = fmaxf(fmaxf(x[r][g][0], x[r][g][1]),
+                                 fmaxf(x[r][g][2], x[r][g][3])) * kLog2e;
+          const float mm = fmaxf(m[g], cm);
+          if (mm != -INFINITY) {
+            float cs = 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) cs += ex2_fast(x[r][g][u] * kLog2e - mm);
+            s[g] = (m[g] == -INFINITY ? 0.f : s[g] * ex2_fast(m[g] - mm)) + cs;
+            m[g] = mm;
           }
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < GT; ++g) {
-        if (g >= G) continue;
-        const float cm = fmaxf(fmaxf(x[g][0], x[g][1]), fmaxf(x[g][2], x[g][3])) * kLog2e;
-        const float mm = fmaxf(m[g], cm);
-        if (mm != -INFINITY) {
-          float cs = 0.f;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) cs += ex2_fast(x[g][u] * kLog2e - mm);
-          s[g] = (m[g] == -INFINITY ? 0.f : s[g] * ex2_fast(m[g] - mm)) + cs;
-          m[g] = mm;
         }
       }
     }
@@ -190,60 +219,52 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   float zreg[GT];
 #pragma unroll
   for (int g = 0; g < GT; ++g) zreg[g] = g < G ? zs[g] : 0.f;
-  for (int qd = tid; qd < nq; qd += blockDim.x) {
-    const int j0 = 4 * qd;
-    float x[GT][4];
+  for (int qd = tid; qd < nq; qd += R * blockDim.x) {
+    float x[R][GT][4];
 #pragma unroll
-    for (int g = 0; g < GT; ++g) {
-      if (g < G) {
-        const float *row = sc + (size_t)g * max_pages;
-        if (vec && j0 + 3 < nf) {
-          const float4 v = *reinterpret_cast<const float4 *>(row + j0);
-          x[g][0] = v.x;
-          x[g][1] = v.y;
-          x[g][2] = v.z;
-          x[g][3] = v.w;
-        } else {
+    for (int r = 0; r < R; ++r)
+      load_quad<GT>(sc, max_pages, G, vec, 4 * (qd + r * blockDim.x), nf, 0.f,
+                    x[r]);
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            x[g][u] = j0 + u < nf ? row[j0 + u] : 0.f;
+    for (int r = 0; r < R; ++r) {
+      const int j0 = 4 * (qd + r * blockDim.x);
+      if (j0 >= 4 * nq) break;
+      uint32_t kq[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u;
+        kq[u] = 0u;
+        if (j < 1 || j > n - 2) continue;
+        float sum = 0.f;
+#pragma unroll
+        for (int g = 0; g < GT; ++g)
+          if (g < G) sum += ex2_fast(x[r][g][u] * kLog2e - zreg[g]);
+        float key;
+        if (sum > 0.f) {
+          key = lg2_fast(sum);
+        } else {  // every term underflowed: subtract the largest first
+          float m = -INFINITY;
+#pragma unroll
+          for (int g = 0; g < GT; ++g)
+            if (g < G) m = fmaxf(m, x[r][g][u] * kLog2e - zreg[g]);
+          float t = 0.f;
+#pragma unroll
+          for (int g = 0; g < GT; ++g)
+            if (g < G) t += ex2_fast(x[r][g][u] * kLog2e - zreg[g] - m);
+          key = m + lg2_fast(t);
         }
+        kq[u] = order_key(key);
+        kmin = min(kmin, kq[u]);
+        kmax = max(kmax, kq[u]);
       }
-    }
-    uint32_t kq[4];
+      if (kvec) {
+        *reinterpret_cast<uint4 *>(keys + j0) =
+            make_uint4(kq[0], kq[1], kq[2], kq[3]);
+      } else {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j = j0 + u;
-      kq[u] = 0u;
-      if (j < 1 || j > n - 2) continue;
-      float sum = 0.f;
-#pragma unroll
-      for (int g = 0; g < GT; ++g)
-        if (g < G) sum += ex2_fast(x[g][u] * kLog2e - zreg[g]);
-      float key;
-      if (sum > 0.f) {
-        key = lg2_fast(sum);
-      } else {  // every term underflowed: subtract the largest first
-        float m = -INFINITY;
-#pragma unroll
-        for (int g = 0; g < GT; ++g)
-          if (g < G) m = fmaxf(m, x[g][u] * kLog2e - zreg[g]);
-        float t = 0.f;
-#pragma unroll
-        for (int g = 0; g < GT; ++g)
-          if (g < G) t += ex2_fast(x[g][u] * kLog2e - zreg[g] - m);
-        key = m + lg2_fast(t);
+        for (int u = 0; u < 4; ++u)
+          if (j0 + u < n) keys[j0 + u] = kq[u];
       }
-      kq[u] = order_key(key);
-      kmin = min(kmin, kq[u]);
-      kmax = max(kmax, kq[u]);
-    }
-    if (kvec) {
-      *reinterpret_cast<uint4 *>(keys + j0) = make_uint4(kq[0], kq[1], kq[2], kq[3]);
-    } else {
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (j0 + u < n) keys[j0 + u] = kq[u];
     }
   }
 #pragma unroll
@@ -274,60 +295,55 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   __syncthreads();
 
   // radix select of the (k-2)-th largest key over the varying bits,
-  // 11-bit digits from the top; key 0 never matches a candidate prefix
+  // 11-bit digits from the top; key 0 never matches a candidate prefix.
+  // Histograms alternate between two buffers so the next one is cleared
+  // while the current one fills.
   const int varying = sh_varying;
   const int nk4 = (n + 3) >> 2;
-  for (int top = varying; top > 0; top -= kRadixBits) {
+  for (int top = varying, pass = 0; top > 0; top -= kRadixBits, ++pass) {
     const int width = min(kRadixBits, top), shift = top - width;
     const uint32_t dmask = (1u << width) - 1u;
-    for (int i = tid; i < kRadixBins; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
+    int *hc = hist[pass & 1];
+    int *hn = hist[(pass & 1) ^ 1];
     const uint32_t pre = sh_prefix, msk = sh_mask;
+    const int rem = sh_remaining;
+    for (int i = tid; i < kRadixBins; i += blockDim.x) hn[i] = 0;
     for (int qd = tid; qd < nk4; qd += blockDim.x) {
-      uint32_t kv[4];
-      if (kvec) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(keys + 4 * qd);
-        kv[0] = v.x;
-        kv[1] = v.y;
-        kv[2] = v.z;
-        kv[3] = v.w;
-      } else {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          kv[u] = 4 * qd + u < n ? keys[4 * qd + u] : 0u;
-      }
+      const uint4 v = load_keys4(keys, 4 * qd, n, kvec);
+      const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         if (kv[u] != 0u && (kv[u] & msk) == pre)
-          atomicAdd(&hist[(kv[u] >> shift) & dmask], 1);
+          atomicAdd(&hc[(kv[u] >> shift) & dmask], 1);
     }
     __syncthreads();
-    if (wid == 0) {
-      // lane l covers digits (bins - 1 - 64l) down to (bins - 64 - 64l)
-      constexpr int per = kRadixBins / 32;
-      int tot = 0;
-      for (int i = 0; i < per; ++i) tot += hist[kRadixBins - 1 - per * lane - i];
-      int incl = tot;
+    // warp w covers digits [bins-128(w+1), bins-128w), lane l its four
+    // digits from the top; counts are scanned from the largest digit down
+    const int hi = kRadixBins - 1 - kBinsPerWarp * wid - 4 * lane;
+    const int4 c4 = *reinterpret_cast<const int4 *>(hc + hi - 3);
+    const int cnt = c4.x + c4.y + c4.z + c4.w;
+    int incl = cnt;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      const int before = incl - tot;
-      const int rem = sh_remaining;
-      if (before < rem && rem <= incl) {
-        int acc = before;
-        for (int i = 0; i < per; ++i) {
-          const int d = kRadixBins - 1 - per * lane - i;
-          const int cnt = hist[d];
-          if (acc < rem && rem <= acc + cnt) {
-            sh_prefix = pre | ((uint32_t)d << shift);
-            sh_mask = msk | (dmask << shift);
-            sh_remaining = rem - acc;
-            break;
-          }
-          acc += cnt;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) sh_wcnt[0][wid] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < wid; ++w) before += sh_wcnt[0][w];
+    const int mine = before + incl - cnt;  // count above this lane's digits
+    if (mine < rem && rem <= mine + cnt) {
+      const int c[4] = {c4.w, c4.z, c4.y, c4.x};  // digits hi, hi-1, ...
+      int acc = mine;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (acc < rem && rem <= acc + c[i]) {
+          sh_prefix = pre | ((uint32_t)(hi - i) << shift);
+          sh_mask = msk | (dmask << shift);
+          sh_remaining = rem - acc;
         }
+        acc += c[i];
       }
     }
     __syncthreads();
@@ -335,15 +351,15 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   const uint32_t T = sh_prefix;
   const int need_eq = sh_remaining;  // keys equal to T to keep (lowest j)
 
-  // ordered compaction: warp w owns pages [w*seg, (w+1)*seg), walked 32 at a
-  // time with ballots; warps' counts are scanned once
-  const int seg = ((n + nwarps - 1) / nwarps + 31) & ~31;
+  // ordered compaction: warp w owns pages [w*seg, (w+1)*seg), walked 128 at
+  // a time (four per lane); warps' counts are scanned once
+  const int seg = ((n + nwarps - 1) / nwarps + 127) & ~127;
   const int w_lo = min(n, wid * seg), w_hi = min(n, w_lo + seg);
   int gt = 0, eq = 0;
-  for (int j = w_lo + lane; j < w_hi; j += 32) {
-    const uint32_t u = keys[j];
-    gt += u > T;
-    eq += u == T;
+  for (int j0 = w_lo + 4 * lane; j0 < w_hi; j0 += 128) {
+    const uint4 v = load_keys4(keys, j0, w_hi, kvec);
+    gt += (v.x > T) + (v.y > T) + (v.z > T) + (v.w > T);
+    eq += (v.x == T) + (v.y == T) + (v.z == T) + (v.w == T);
   }
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
@@ -360,24 +376,44 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     gt_before += sh_wcnt[0][w];
     eq_before += sh_wcnt[1][w];
   }
-  const uint32_t below = (1u << lane) - 1u;
-  for (int j0 = w_lo; j0 < w_hi; j0 += 32) {
-    const int j = j0 + lane;
-    const uint32_t u = j < w_hi ? keys[j] : 0u;
-    const uint32_t bgt = __ballot_sync(0xffffffffu, u > T);
-    const uint32_t beq = __ballot_sync(0xffffffffu, u == T && j < w_hi);
-    const int my_gt = gt_before + __popc(bgt & below);
-    const int my_eq = eq_before + __popc(beq & below);
-    const bool sel = (u > T) || (u == T && j < w_hi && my_eq < need_eq);
-    if (sel) {
-      const int pos = 1 + my_gt + min(my_eq, need_eq);
-      if (pos >= 1 && pos < k - 1)
-        out[pos] = j;
-      else
-        set_status(status, LOCKS_DEV_BAD_INDEX);
+  for (int base = w_lo; base < w_hi; base += 128) {
+    const int j0 = base + 4 * lane;
+    const uint4 v = load_keys4(keys, j0, w_hi, kvec);
+    const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
+    int ngt = 0, neq = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      ngt += kv[u] > T;
+      neq += kv[u] == T;
     }
-    gt_before += __popc(bgt);
-    eq_before += __popc(beq);
+    // most groups of 128 hold no key at or above the threshold
+    if (!__any_sync(0xffffffffu, ngt + neq > 0)) continue;
+    // exclusive scan of (eq << 16 | gt) over the lanes
+    const int packed = (neq << 16) | ngt;
+    int incl = packed;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int tot = __shfl_sync(0xffffffffu, incl, 31);
+    int my_gt = gt_before + ((incl - packed) & 0xffff);
+    int my_eq = eq_before + ((incl - packed) >> 16);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool is_gt = kv[u] > T, is_eq = kv[u] == T;
+      if (is_gt || (is_eq && my_eq < need_eq)) {
+        const int pos = 1 + my_gt + min(my_eq, need_eq);
+        if (pos >= 1 && pos < k - 1)
+          out[pos] = j0 + u;
+        else
+          set_status(status, LOCKS_DEV_BAD_INDEX);
+      }
+      my_gt += is_gt;
+      my_eq += is_eq;
+    }
+    gt_before += tot & 0xffff;
+    eq_before += tot >> 16;
   }
   if (tid == 0) {
     out[0] = 0;

@@ -351,6 +351,51 @@ def test_sparse_decode_matches_oracle(G, h_kv, k):
             assert np.abs(lg[b] - rl[b]).max() <= LSE_TOL
 
 
+@pytest.mark.parametrize("G,mode", [(4, "sparse"), (4, "dense"),
+                                    (16, "sparse"), (2, "dense")])
+def test_decode_many_short_units(G, mode):
+    """Thousands of short page lists, so that runs of consecutive list
+    entries hold several whole (sequence, KV head) lists as well as pieces
+    of lists shared with the neighbouring runs; empty sequences, partial
+    pages and -1 padding give skipped entries at every place in a run."""
+    rng = np.random.default_rng(90 + G)
+    batch, h_kv, max_pages, k = 2048, 1, 4, 2
+    h_q = G * h_kv
+    lens = rng.integers(0, 16 * max_pages + 1, batch)
+    lens[::97] = 0
+    lens[1::89] = 1
+    num_phys = batch * max_pages
+    pt = rng.permutation(num_phys).reshape(batch, max_pages).astype(np.int32)
+    gen = torch.Generator().manual_seed(int(G))
+    kc = torch.randn(num_phys, h_kv, 16, 128, generator=gen).to(torch.bfloat16)
+    vc = torch.randn(num_phys, h_kv, 16, 128, generator=gen).to(torch.bfloat16)
+    q = torch.randn(batch, h_q, 128, generator=gen).to(torch.bfloat16)
+    idx = np.full((batch, h_kv, k), -1, np.int32)
+    for b in range(batch):
+        n = -(-int(lens[b]) // 16)
+        m = min(k, n)
+        if m:
+            idx[b, :, :m] = np.sort(rng.choice(n, m, replace=False))
+    o_ref, lse_ref = O.sparse_decode(q.float().numpy(), kc.float().numpy(),
+                                     vc.float().numpy(), pt, lens,
+                                     None if mode == "dense" else idx)
+    ws = B.new_workspace(batch, h_q, h_kv, max_pages, max(k, max_pages), DEV)
+    o = torch.empty(batch, h_q, 128, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(batch, h_q, dtype=torch.float32, device=DEV)
+    B.locks_sparse_decode(q.to(DEV), kc.to(DEV), vc.to(DEV), i32(pt),
+                          i32(lens), None if mode == "dense" else i32(idx),
+                          k if mode == "sparse" else 0, o, lse, ws)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == 0
+    og, lg = o.float().cpu().numpy(), lse.cpu().numpy()
+    empty = lens == 0
+    assert (og[empty] == 0).all() and np.isneginf(lg[empty]).all()
+    scale = np.abs(o_ref[~empty]).max(axis=(1, 2))
+    err = np.abs(og[~empty] - o_ref[~empty]).max(axis=(1, 2))
+    assert (err <= O_TOL * scale).all(), float((err / scale).max())
+    assert np.abs(lg[~empty] - lse_ref[~empty]).max() <= LSE_TOL
+
+
 # ---------------------------------------------------------------------------
 # the whole step on the 4K-context workload, 8 decode steps
 # ---------------------------------------------------------------------------
