@@ -96,20 +96,39 @@ __device__ __forceinline__ float lse2_quad_fast(float a, float b, float c,
   return lg2_fast(e);
 }
 
+// Same value without the max pass and without the check: the caller folds
+// `bits(e) - bits(FLT_MIN)` into `bad` (unsigned max) and recomputes the
+// tile with lse2_quad when any quad sum was zero, subnormal, inf or NaN.
+__device__ __forceinline__ float lse2_quad_raw(float a, float b, float c,
+                                               float d, uint32_t &bad) {
+  float e = (ex2_fast(a) + ex2_fast(b)) + (ex2_fast(c) + ex2_fast(d));
+  e += __shfl_xor_sync(0xffffffffu, e, 1);
+  e += __shfl_xor_sync(0xffffffffu, e, 2);
+  bad = max(bad, __float_as_uint(e) - 0x00800000u);
+  return lg2_fast(e);
+}
+constexpr uint32_t kLseBad = 0x7F000000u;  // bad >= this: recompute
+
+__device__ __forceinline__ float lse2_quad_sel(float a, float b, float c,
+                                               float d, bool safe,
+                                               uint32_t &bad) {
+  return safe ? lse2_quad(a, b, c, d) : lse2_quad_raw(a, b, c, d, bad);
+}
+
 // position of a warp in its contiguous range of tiles
 struct Cursor {
   int b, h, j;
 };
 
-__device__ __forceinline__ void advance_cursor(Cursor &c, const int *prefix,
+__device__ __forceinline__ void advance_cursor(Cursor &c, const int *tph,
                                                int batch, int h_kv) {
-  if (++c.j == (prefix[c.b + 1] - prefix[c.b]) / h_kv) {
+  if (++c.j == tph[c.b]) {
     c.j = 0;
     if (++c.h == h_kv) {
       c.h = 0;
       do {
         ++c.b;
-      } while (c.b < batch && prefix[c.b + 1] == prefix[c.b]);
+      } while (c.b < batch && tph[c.b] == 0);
     }
   }
 }
@@ -144,6 +163,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes);
   int *prefix = reinterpret_cast<int *>(bars + kScoreWarps * kStages);
   int *nfull = prefix + batch + 1;
+  int *tph = nfull + batch;  // tiles per KV head of each sequence
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int gq = lane >> 2, t4 = lane & 3;  // mma groupID / thread-in-group
 
@@ -155,7 +175,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       L = max(0, min(L, max_pages * kPage));
     }
     nfull[b] = L / kPage;
-    prefix[b + 1] = ((L / kPage + kTilePages - 1) / kTilePages) * h_kv;
+    tph[b] = (L / kPage + kTilePages - 1) / kTilePages;
+    prefix[b + 1] = tph[b] * h_kv;
   }
   if (threadIdx.x == 0) prefix[0] = 0;
   if (lane == 0) {
@@ -200,7 +221,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (prefix[mid] <= t_begin) lo = mid; else hi = mid;
     }
     const int rem = (int)(t_begin - prefix[lo]);
-    const int tb = (prefix[lo + 1] - prefix[lo]) / h_kv;
+    const int tb = tph[lo];
     cur.b = lo;
     cur.h = rem / tb;
     cur.j = rem - cur.h * tb;
@@ -208,11 +229,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   Cursor nxt = cur;
   issue_tile(nxt, nfull, summaries, h_kv, max_pages, my_ring, &my_bar[0],
              lane);
-  advance_cursor(nxt, prefix, batch, h_kv);
+  advance_cursor(nxt, tph, batch, h_kv);
   if (t_begin + 1 < t_end) {
     issue_tile(nxt, nfull, summaries, h_kv, max_pages, my_ring + kTileBytes,
                &my_bar[1], lane);
-    advance_cursor(nxt, prefix, batch, h_kv);
+    advance_cursor(nxt, tph, batch, h_kv);
   }
 
   constexpr bool WIDE = MODE == 3;
@@ -223,13 +244,21 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   float off_v = 0.f, off_v8 = 0.f, off_m = 0.f, off_m8 = 0.f;
   int cur_b = -1, cur_h = -1;
   bool failed = false;
+  // this lane's score rows of the current unit (MODE 3: heads gq, gq + 8;
+  // MODE 1: head gq & 3; MODE 2: head gq)
+  float *lane_row = nullptr, *lane_row8 = nullptr;
+  const int n_tiles = (int)(t_end - t_begin);
 
-  for (long long t = t_begin, it = 0; t < t_end; ++t, ++it) {
-    const int stage = (int)(it & 1);
+  for (int it = 0; it < n_tiles; ++it) {
+    const int stage = it & 1;
     const uint32_t phase = (uint32_t)((it >> 1) & 1);
     if (cur.b != cur_b || cur.h != cur_h) {
       cur_b = cur.b;
       cur_h = cur.h;
+      float *unit_rows =
+          s_hat + ((size_t)cur.b * h_kv + cur.h) * G * (size_t)max_pages;
+      lane_row = unit_rows + (size_t)(MODE == 1 ? (gq & 3) : gq) * max_pages;
+      lane_row8 = unit_rows + (size_t)(gq + 8) * max_pages;
       const __nv_bfloat16 *qrow =
           q + ((size_t)cur.b * h_kv * G + (size_t)cur.h * G) * kDim;
       float sum = 0.f, sum8 = 0.f;
@@ -290,11 +319,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       failed = true;
       break;
     }
-    const uint8_t *base = my_ring + stage * kTileBytes;
     const uint32_t base_s = ring_s + stage * kTileBytes;
-
-    float *srow = s_hat + ((size_t)cur.b * h_kv + cur.h) * G * (size_t)max_pages +
-                  page0;
     if constexpr (MODE != 3) {
       // Two pages per step.  Product 1 is transposed: rows 0..7 are page A's
       // basis components, rows 8..15 page B's (A operand = unpacked codes,
@@ -304,6 +329,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       float keepA = 0.f, keepB = 0.f;
       const bool lowh = gq < 4;
       const uint32_t maskA = lowh ? 0xffffffffu : 0u;
+      // first pass without per-pair overflow checks; a second, max-
+      // subtracted pass only when some quad sum left the normal range
+      for (int attempt = 0; attempt < 2; ++attempt) {
+      const bool safe = attempt != 0;
+      uint32_t bad = 0u;
 #pragma unroll 1
       for (int pp = 0; pp < kTilePages / 2; ++pp) {
         if (2 * pp < npg) {
@@ -369,10 +399,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             const uint32_t rs = lowh ? ra : rb;
             const uint4 sc = lds128(rs + kOffSV + 16 * t4);
             const __half2 s0 = u32_as_h2(sc.y), s1 = u32_as_h2(sc.z);
-            const float e = lse2_quad_fast((l0[0] + l0[2]) * __low2float(s0),
-                                           (l0[1] + l0[3]) * __high2float(s0),
-                                           (l1[0] + l1[2]) * __low2float(s1),
-                                           (l1[1] + l1[3]) * __high2float(s1));
+            const float e = lse2_quad_sel((l0[0] + l0[2]) * __low2float(s0),
+                                          (l0[1] + l0[3]) * __high2float(s0),
+                                          (l1[0] + l1[2]) * __low2float(s1),
+                                          (l1[1] + l1[3]) * __high2float(s1),
+                                          safe, bad);
             if (pp == t4) keepA = e;
           } else {
             float m0[4], m1[4];
@@ -384,20 +415,24 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             const uint4 sb = lds128(rb + kOffSV + 16 * t4);
             const __half2 a0 = u32_as_h2(sa.y), a1 = u32_as_h2(sa.z);
             const __half2 b0 = u32_as_h2(sb.y), b1 = u32_as_h2(sb.z);
-            const float ea = lse2_quad_fast((l0[0] + l0[2]) * __low2float(a0),
-                                            (l0[1] + l0[3]) * __high2float(a0),
-                                            (l1[0] + l1[2]) * __low2float(a1),
-                                            (l1[1] + l1[3]) * __high2float(a1));
-            const float eb = lse2_quad_fast((m0[0] + m0[2]) * __low2float(b0),
-                                            (m0[1] + m0[3]) * __high2float(b0),
-                                            (m1[0] + m1[2]) * __low2float(b1),
-                                            (m1[1] + m1[3]) * __high2float(b1));
+            const float ea = lse2_quad_sel((l0[0] + l0[2]) * __low2float(a0),
+                                           (l0[1] + l0[3]) * __high2float(a0),
+                                           (l1[0] + l1[2]) * __low2float(a1),
+                                           (l1[1] + l1[3]) * __high2float(a1),
+                                           safe, bad);
+            const float eb = lse2_quad_sel((m0[0] + m0[2]) * __low2float(b0),
+                                           (m0[1] + m0[3]) * __high2float(b0),
+                                           (m1[0] + m1[2]) * __low2float(b1),
+                                           (m1[1] + m1[3]) * __high2float(b1),
+                                           safe, bad);
             if (pp == t4) {
               keepA = ea;
               keepB = eb;
             }
           }
         }
+      }
+      if (!__any_sync(0xffffffffu, bad >= kLseBad)) break;
       }
       // q . mu for the tile's 8 pages (column n = page gq of the tile)
       float qm[4] = {off_m, off_m, off_m8, off_m8};
@@ -424,25 +459,22 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const float qm_from_low = __shfl_xor_sync(0xffffffffu, qm_hi, 16);
         const int pg = 2 * t4 + (up ? 1 : 0);
         const int head = gq & 3;
-        const float smu = __half2float(*reinterpret_cast<const __half *>(
-            base + pg * kRec + kOffSMu));
+        const float smu = __half2float(__ushort_as_half(
+            (unsigned short)lds16(base_s + pg * kRec + kOffSMu)));
         const float qmu = up ? qm_from_low : qm_lo;
         if (head < G && pg < npg)
-          srow[(size_t)head * max_pages + pg] =
-              (keepA + qmu * smu * kLog2eRsqrtD) * kLn2;
+          lane_row[page0 + pg] = (keepA + qmu * smu * kLog2eRsqrtD) * kLn2;
       } else {
         const int pg0 = 2 * t4, pg1 = pg0 + 1;
-        const float sm0 = __half2float(*reinterpret_cast<const __half *>(
-            base + pg0 * kRec + kOffSMu));
-        const float sm1 = __half2float(*reinterpret_cast<const __half *>(
-            base + pg1 * kRec + kOffSMu));
+        const float sm0 = __half2float(__ushort_as_half(
+            (unsigned short)lds16(base_s + pg0 * kRec + kOffSMu)));
+        const float sm1 = __half2float(__ushort_as_half(
+            (unsigned short)lds16(base_s + pg1 * kRec + kOffSMu)));
         if (gq < G) {
           if (pg0 < npg)
-            srow[(size_t)gq * max_pages + pg0] =
-                (keepA + qm_lo * sm0 * kLog2eRsqrtD) * kLn2;
+            lane_row[page0 + pg0] = (keepA + qm_lo * sm0 * kLog2eRsqrtD) * kLn2;
           if (pg1 < npg)
-            srow[(size_t)gq * max_pages + pg1] =
-                (keepB + qm_hi * sm1 * kLog2eRsqrtD) * kLn2;
+            lane_row[page0 + pg1] = (keepB + qm_hi * sm1 * kLog2eRsqrtD) * kLn2;
         }
       }
     } else {
@@ -451,10 +483,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 #pragma unroll
       for (int p = 0; p < kTilePages; ++p) {
         if (p < npg) {
-          const uint8_t *rec = base + p * kRec;
-          const uint4 vw = ld_shared_v4(rec + kOffV4 + 16 * lane);
-          const uint4 sc = ld_shared_v4(rec + kOffSV + 16 * t4);
-          const uint32_t cw = ld_shared_u32(rec + kOffC8 + 4 * lane);
+          const uint32_t rec = base_s + p * kRec;
+          const uint4 vw = lds128(rec + kOffV4 + 16 * lane);
+          const uint4 sc = lds128(rec + kOffSV + 16 * t4);
+          const uint32_t cw = lds32(rec + kOffC8 + 4 * lane);
           const uint32_t vwa[4] = {vw.x, vw.y, vw.z, vw.w};
           float a1[4] = {off_v, off_v, off_v8, off_v8};
           float a1b[4] = {0.f, 0.f, 0.f, 0.f};
@@ -519,19 +551,19 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
       }
       const int pg0 = 2 * t4, pg1 = 2 * t4 + 1;
-      const float sm0 = __half2float(*reinterpret_cast<const __half *>(
-          base + pg0 * kRec + kOffSMu));
-      const float sm1 = __half2float(*reinterpret_cast<const __half *>(
-          base + pg1 * kRec + kOffSMu));
+      const float sm0 = __half2float(__ushort_as_half(
+          (unsigned short)lds16(base_s + pg0 * kRec + kOffSMu)));
+      const float sm1 = __half2float(__ushort_as_half(
+          (unsigned short)lds16(base_s + pg1 * kRec + kOffSMu)));
       if (gq < G) {
-        float *dst = srow + (size_t)gq * max_pages;
+        float *dst = lane_row + page0;
         if (pg0 < npg)
           dst[pg0] = (o0 + (qm[0] + qm2[0]) * sm0 * kLog2eRsqrtD) * kLn2;
         if (pg1 < npg)
           dst[pg1] = (o1 + (qm[1] + qm2[1]) * sm1 * kLog2eRsqrtD) * kLn2;
       }
       if (gq + 8 < G) {
-        float *dst = srow + (size_t)(gq + 8) * max_pages;
+        float *dst = lane_row8 + page0;
         if (pg0 < npg)
           dst[pg0] = (o80 + (qm[2] + qm2[2]) * sm0 * kLog2eRsqrtD) * kLn2;
         if (pg1 < npg)
@@ -539,12 +571,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
     }
     __syncwarp();
-    if (t + 2 < t_end) {
+    if (it + 2 < n_tiles) {
       issue_tile(nxt, nfull, summaries, h_kv, max_pages,
                  my_ring + stage * kTileBytes, &my_bar[stage], lane);
-      advance_cursor(nxt, prefix, batch, h_kv);
+      advance_cursor(nxt, tph, batch, h_kv);
     }
-    advance_cursor(cur, prefix, batch, h_kv);
+    advance_cursor(cur, tph, batch, h_kv);
   }
   if (failed) {
     if (lane == 0) set_status(status, LOCKS_DEV_TIMEOUT);
@@ -572,14 +604,14 @@ static int sm_count() {
 
 size_t score_smem_bytes(int batch) {
   return (size_t)kRingBytes + sizeof(uint64_t) * kScoreWarps * kStages +
-         sizeof(int) * (2 * (size_t)batch + 1);
+         sizeof(int) * (3 * (size_t)batch + 1);
 }
 
 int score_max_batch() {
   // the per-sequence tables must fit next to the ring in 227 KB
   return (int)((227 * 1024 - (size_t)kRingBytes -
                 sizeof(uint64_t) * kScoreWarps * kStages - 64) /
-               (2 * sizeof(int)));
+               (3 * sizeof(int)));
 }
 
 cudaError_t launch_score(const void *q, const void *summaries,
