@@ -57,6 +57,30 @@ __device__ __forceinline__ void i8x4_to_h2(uint32_t x, uint32_t &lo,
   hi = h2_as_u32(__hsub2(u32_as_h2(b), k));
 }
 
+// Two int4 codes at bits [0,4) and [16,20) -> fp16x2 holding 1032 + code;
+// at bits [4,8) and [20,24) -> fp16x2 holding 1152 + 16 code (exact).  An
+// fp16 half has room for two code positions, a bf16 half for one, so the
+// fp16 form needs one shift per four code pairs instead of three.
+__device__ __forceinline__ uint32_t nib_f16_lo(uint32_t x) {
+  return lop3_and_xor(x, 0x000F000Fu, 0x64086408u);
+}
+__device__ __forceinline__ uint32_t nib_f16_hi(uint32_t x) {
+  return lop3_and_xor(x, 0x00F000F0u, 0x64806480u);
+}
+
+// D = A * B + C, m16n8k16 fp16
+__device__ __forceinline__ void mma_f16_c(float (&d)[4],
+                                          const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1, float c0, float c1,
+                                          float c2, float c3) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1),
+        "f"(c0), "f"(c1), "f"(c2), "f"(c3));
+}
+
 // D = A * B (zero accumulator), m16n8k16 fp16
 __device__ __forceinline__ void mma_f16_z(float (&d)[4],
                                           const uint32_t (&a)[4], uint32_t b0,
@@ -113,6 +137,120 @@ __device__ __forceinline__ float lse2_quad_sel(float a, float b, float c,
                                                float d, bool safe,
                                                uint32_t &bad) {
   return safe ? lse2_quad(a, b, c, d) : lse2_quad_raw(a, b, c, d, bad);
+}
+
+// The basis and coefficient products and the per-page log-sum-exp for the
+// pages of one tile, two pages per step (G <= 8).  Product 1 is transposed:
+// rows 0..7 are page A's basis components, rows 8..15 page B's (A operand =
+// unpacked codes, straight into the fragment registers), columns are query
+// heads (B operand = the query, resident).  The 8x8 (component x head)
+// blocks are turned with movmatrix into head-major operands for product 2.
+// Lane (gq, t4) keeps the value of pair t4.  SAFE selects the max-subtracted
+// log-sum-exp; otherwise the return value folds every quad sum's distance
+// from the normal range (>= kLseBad: recompute with SAFE).
+template <int MODE, bool SAFE>
+__device__ __forceinline__ uint32_t score_pairs(
+    uint32_t base_s, int npg, int lane, const uint32_t (&qv)[8][2],
+    float offc0, float offc1, float vscale, float &keepA, float &keepB) {
+  const int gq = lane >> 2, t4 = lane & 3;
+  const bool lowh = gq < 4;
+  const uint32_t maskA = lowh ? 0xffffffffu : 0u;
+  uint32_t bad = 0u;
+#pragma unroll 1
+  for (int pp = 0; 2 * pp < npg; ++pp) {
+    const uint32_t ra = base_s + (uint32_t)(2 * pp) * kRec;
+    const uint32_t rb = ra + kRec;
+    const uint4 va = lds128(ra + kOffV4 + 16 * lane);
+    const uint4 vb = lds128(rb + kOffV4 + 16 * lane);
+    const uint32_t ca = lds32(ra + kOffC8 + 4 * lane);
+    const uint32_t cb = lds32(rb + kOffC8 + 4 * lane);
+    // sV of component gq in each page
+    const uint32_t svo = kOffSV + 16 * (gq >> 1) + 2 * (gq & 1);
+    const float sva = __half2float(__ushort_as_half(
+                          (unsigned short)lds16(ra + svo))) * vscale;
+    const float svb = __half2float(__ushort_as_half(
+                          (unsigned short)lds16(rb + svo))) * vscale;
+    const uint32_t vaw[4] = {va.x, va.y, va.z, va.w};
+    const uint32_t vbw[4] = {vb.x, vb.y, vb.z, vb.w};
+    float d0[4], d1[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t xa = vaw[w], xb = vbw[w];
+      const uint32_t za = xa >> 8, zb = xb >> 8;
+      const uint32_t a0[4] = {nib_f16_lo(xa), nib_f16_lo(xb),
+                              nib_f16_hi(xa), nib_f16_hi(xb)};
+      const uint32_t a1[4] = {nib_f16_lo(za), nib_f16_lo(zb),
+                              nib_f16_hi(za), nib_f16_hi(zb)};
+      if (w == 0) {
+        mma_f16_c(d0, a0, qv[0][0], qv[0][1], offc0, offc1, offc0,
+                  offc1);
+        mma_f16_c(d1, a1, qv[1][0], qv[1][1], 0.f, 0.f, 0.f, 0.f);
+      } else {
+        mma_f16(d0, a0, qv[2 * w][0], qv[2 * w][1]);
+        mma_f16(d1, a1, qv[2 * w + 1][0], qv[2 * w + 1][1]);
+      }
+    }
+    // proj (log2 units) = D * sV * log2(e)/sqrt(d), split hi + lo fp16
+    const float pa0 = (d0[0] + d1[0]) * sva, pa1 = (d0[1] + d1[1]) * sva;
+    const float pb0 = (d0[2] + d1[2]) * svb, pb1 = (d0[3] + d1[3]) * svb;
+    const __half2 ha = __floats2half2_rn(pa0, pa1);
+    const __half2 hb = __floats2half2_rn(pb0, pb1);
+    const uint32_t la =
+        pack_h2(pa0 - __low2float(ha), pa1 - __high2float(ha));
+    const uint32_t lb =
+        pack_h2(pb0 - __low2float(hb), pb1 - __high2float(hb));
+    const uint32_t tha = movmatrix_trans(h2_as_u32(ha));
+    const uint32_t tla = movmatrix_trans(la);
+    const uint32_t thb = movmatrix_trans(h2_as_u32(hb));
+    const uint32_t tlb = movmatrix_trans(lb);
+    uint32_t ba0, ba1, bb0, bb1;
+    i8x4_to_h2(ca, ba0, ba1);
+    i8x4_to_h2(cb, bb0, bb1);
+    float l0[4], l1[4];
+    if constexpr (MODE == 1) {
+      // rows 0-3: page A heads (high halves, k 0..7 = page A comps),
+      // rows 4-7: page B heads (high, k 8..15 = page B comps),
+      // rows 8-15: the same with the low halves
+      const uint32_t A2[4] = {tha & maskA, tla & maskA, thb & ~maskA,
+                              tlb & ~maskA};
+      mma_f16_z(l0, A2, ba0, bb0);
+      mma_f16_z(l1, A2, ba1, bb1);
+      const uint32_t rs = lowh ? ra : rb;
+      const uint4 sc = lds128(rs + kOffSV + 16 * t4);
+      const __half2 s0 = u32_as_h2(sc.y), s1 = u32_as_h2(sc.z);
+      const float e = lse2_quad_sel((l0[0] + l0[2]) * __low2float(s0),
+                                    (l0[1] + l0[3]) * __high2float(s0),
+                                    (l1[0] + l1[2]) * __low2float(s1),
+                                    (l1[1] + l1[3]) * __high2float(s1),
+                                    SAFE, bad);
+      if (pp == t4) keepA = e;
+    } else {
+      float m0[4], m1[4];
+      mma1688_f16_z(l0, tha, tla, ba0);
+      mma1688_f16_z(l1, tha, tla, ba1);
+      mma1688_f16_z(m0, thb, tlb, bb0);
+      mma1688_f16_z(m1, thb, tlb, bb1);
+      const uint4 sa = lds128(ra + kOffSV + 16 * t4);
+      const uint4 sb = lds128(rb + kOffSV + 16 * t4);
+      const __half2 a0 = u32_as_h2(sa.y), a1 = u32_as_h2(sa.z);
+      const __half2 b0 = u32_as_h2(sb.y), b1 = u32_as_h2(sb.z);
+      const float ea = lse2_quad_sel((l0[0] + l0[2]) * __low2float(a0),
+                                     (l0[1] + l0[3]) * __high2float(a0),
+                                     (l1[0] + l1[2]) * __low2float(a1),
+                                     (l1[1] + l1[3]) * __high2float(a1),
+                                     SAFE, bad);
+      const float eb = lse2_quad_sel((m0[0] + m0[2]) * __low2float(b0),
+                                     (m0[1] + m0[3]) * __high2float(b0),
+                                     (m1[0] + m1[2]) * __low2float(b1),
+                                     (m1[1] + m1[3]) * __high2float(b1),
+                                     SAFE, bad);
+      if (pp == t4) {
+        keepA = ea;
+        keepB = eb;
+      }
+    }
+  }
+  return bad;
 }
 
 // position of a warp in its contiguous range of tiles
@@ -239,9 +377,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   constexpr bool WIDE = MODE == 3;
   uint32_t qb[8][4];  // query A fragments, bf16 (basis product, one page)
   uint32_t qh[8][4];  // query A fragments, fp16 (centroid product)
-  uint32_t qv[8][2];  // query B fragments, bf16 (basis product, two pages)
+  uint32_t qv[8][2];  // query B fragments, fp16 (basis product, two pages;
+                      // k 8..15 of each step hold q / 16)
   float offc0 = 0.f, offc1 = 0.f;  // offsets of columns 2*t4, 2*t4 + 1
   float off_v = 0.f, off_v8 = 0.f, off_m = 0.f, off_m8 = 0.f;
+  // fp16 operands carry the query times 2^-e (e > 0 only when some |q| of
+  // the unit reaches 2^14); these undo it in log2 units
+  float vscale = kLog2eRsqrtD, mscale = kLog2eRsqrtD;
   int cur_b = -1, cur_h = -1;
   bool failed = false;
   // this lane's score rows of the current unit (MODE 3: heads gq, gq + 8;
@@ -261,7 +403,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       lane_row8 = unit_rows + (size_t)(gq + 8) * max_pages;
       const __nv_bfloat16 *qrow =
           q + ((size_t)cur.b * h_kv * G + (size_t)cur.h * G) * kDim;
-      float sum = 0.f, sum8 = 0.f;
+      float amax = 0.f;
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const int d0 = 16 * s + 2 * t4;
@@ -278,40 +420,83 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         qb[s][1] = u1;
         qb[s][2] = u2;
         qb[s][3] = u3;
-        qh[s][0] = pack_h2(bf16_lo(u0), bf16_hi(u0));
-        qh[s][1] = pack_h2(bf16_lo(u1), bf16_hi(u1));
-        qh[s][2] = pack_h2(bf16_lo(u2), bf16_hi(u2));
-        qh[s][3] = pack_h2(bf16_lo(u3), bf16_hi(u3));
-        sum += (bf16_lo(u0) + bf16_hi(u0)) + (bf16_lo(u2) + bf16_hi(u2));
-        sum8 += (bf16_lo(u1) + bf16_hi(u1)) + (bf16_lo(u3) + bf16_hi(u3));
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(u0)), fabsf(bf16_hi(u0))),
+                                 fmaxf(fabsf(bf16_lo(u2)), fabsf(bf16_hi(u2)))));
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(u1)), fabsf(bf16_hi(u1))),
+                                 fmaxf(fabsf(bf16_lo(u3)), fabsf(bf16_hi(u3)))));
       }
-      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-      sum8 += __shfl_xor_sync(0xffffffffu, sum8, 1);
-      sum8 += __shfl_xor_sync(0xffffffffu, sum8, 2);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      // power-of-two prescale keeping every fp16 operand below 2^14
+      const int ex =
+          amax >= 16384.f ? ((__float_as_int(amax) >> 23) & 0xff) - 140 : 0;
+      const float qsc = __int_as_float((127 - ex) << 23);  // 2^-ex
+      const float qun = __int_as_float((127 + ex) << 23);  // 2^ex
+      mscale = kLog2eRsqrtD * qun;
+      vscale = MODE == 3 ? kLog2eRsqrtD : kLog2eRsqrtD * qun;
+      float sum = 0.f, sum8 = 0.f, sumh = 0.f, sumh8 = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t u = qb[s][i];
+          const __half2 hq =
+              __floats2half2_rn(bf16_lo(u) * qsc, bf16_hi(u) * qsc);
+          qh[s][i] = h2_as_u32(hq);
+          const float bs = bf16_lo(u) + bf16_hi(u);
+          const float hs = __low2float(hq) + __high2float(hq);
+          if (i & 1) {
+            sum8 += bs;
+            sumh8 += hs;
+          } else {
+            sum += bs;
+            sumh += hs;
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        sum8 += __shfl_xor_sync(0xffffffffu, sum8, o);
+        sumh += __shfl_xor_sync(0xffffffffu, sumh, o);
+        sumh8 += __shfl_xor_sync(0xffffffffu, sumh8, o);
+      }
       if constexpr (MODE != 3) {
         // column n of the transposed basis product is query head
         // (n mod 4) for G <= 4 and head n for G <= 8
         const int hc = MODE == 1 ? (gq & 3) : gq;
         const __nv_bfloat16 *qc = qrow + hc * kDim;
+        float clo = 0.f, chi = 0.f;
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
           const int d0 = 16 * s + 2 * t4;
-          qv[s][0] = hc < G ? __ldg(reinterpret_cast<const uint32_t *>(qc + d0)) : 0u;
-          qv[s][1] = hc < G ? __ldg(reinterpret_cast<const uint32_t *>(qc + d0 + 8)) : 0u;
+          const uint32_t u =
+              hc < G ? __ldg(reinterpret_cast<const uint32_t *>(qc + d0)) : 0u;
+          const uint32_t u8 =
+              hc < G ? __ldg(reinterpret_cast<const uint32_t *>(qc + d0 + 8))
+                     : 0u;
+          const __half2 lo =
+              __floats2half2_rn(bf16_lo(u) * qsc, bf16_hi(u) * qsc);
+          const __half2 hi = __floats2half2_rn(bf16_lo(u8) * qsc * 0.0625f,
+                                               bf16_hi(u8) * qsc * 0.0625f);
+          qv[s][0] = h2_as_u32(lo);
+          qv[s][1] = h2_as_u32(hi);
+          clo += __low2float(lo) + __high2float(lo);
+          chi += __low2float(hi) + __high2float(hi);
         }
-        // -136 * sum_d q[head of column][d], for columns 2*t4 and 2*t4 + 1
-        const int c0 = 2 * t4, c1 = 2 * t4 + 1;
-        const int g0 = MODE == 1 ? (c0 & 3) : c0, g1 = MODE == 1 ? (c1 & 3) : c1;
-        const float s0 = __shfl_sync(0xffffffffu, sum, 4 * g0);
-        const float s1 = __shfl_sync(0xffffffffu, sum, 4 * g1);
-        offc0 = -136.f * s0;
-        offc1 = -136.f * s1;
+        // cancels the 1032 (k 0..7) and 1152 (k 8..15) of every basis code
+        float cs = -1032.f * clo - 1152.f * chi;
+        cs += __shfl_xor_sync(0xffffffffu, cs, 1);
+        cs += __shfl_xor_sync(0xffffffffu, cs, 2);
+        // offsets of columns 2*t4 and 2*t4 + 1
+        offc0 = __shfl_sync(0xffffffffu, cs, 4 * (2 * t4));
+        offc1 = __shfl_sync(0xffffffffu, cs, 4 * (2 * t4 + 1));
       }
-      off_v = -136.f * sum;     // cancels the +136 of every basis code
+      off_v = -136.f * sum;     // cancels the +136 of every bf16 basis code
       off_v8 = -136.f * sum8;
-      off_m = -1152.f * sum;    // cancels the +1152 of every centroid code
-      off_m8 = -1152.f * sum8;
+      off_m = -1152.f * sumh;   // cancels the +1152 of every centroid code
+      off_m8 = -1152.f * sumh8;
     }
     const int page0 = cur.j * kTilePages;
     const int npg = min(kTilePages, nfull[cur.b] - page0);
@@ -321,119 +506,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
     const uint32_t base_s = ring_s + stage * kTileBytes;
     if constexpr (MODE != 3) {
-      // Two pages per step.  Product 1 is transposed: rows 0..7 are page A's
-      // basis components, rows 8..15 page B's (A operand = unpacked codes,
-      // straight into the fragment registers), columns are query heads (B
-      // operand = the query, resident).  The 8x8 (component x head) blocks
-      // are turned with movmatrix into head-major operands for product 2.
       float keepA = 0.f, keepB = 0.f;
-      const bool lowh = gq < 4;
-      const uint32_t maskA = lowh ? 0xffffffffu : 0u;
       // first pass without per-pair overflow checks; a second, max-
       // subtracted pass only when some quad sum left the normal range
-      for (int attempt = 0; attempt < 2; ++attempt) {
-      const bool safe = attempt != 0;
-      uint32_t bad = 0u;
-#pragma unroll 1
-      for (int pp = 0; pp < kTilePages / 2; ++pp) {
-        if (2 * pp < npg) {
-          const uint32_t ra = base_s + (uint32_t)(2 * pp) * kRec;
-          const uint32_t rb = ra + kRec;
-          const uint4 va = lds128(ra + kOffV4 + 16 * lane);
-          const uint4 vb = lds128(rb + kOffV4 + 16 * lane);
-          const uint32_t ca = lds32(ra + kOffC8 + 4 * lane);
-          const uint32_t cb = lds32(rb + kOffC8 + 4 * lane);
-          // sV of component gq in each page
-          const uint32_t svo = kOffSV + 16 * (gq >> 1) + 2 * (gq & 1);
-          const float sva = __half2float(__ushort_as_half(
-                                (unsigned short)lds16(ra + svo))) * kLog2eRsqrtD;
-          const float svb = __half2float(__ushort_as_half(
-                                (unsigned short)lds16(rb + svo))) * kLog2eRsqrtD;
-          const uint32_t vaw[4] = {va.x, va.y, va.z, va.w};
-          const uint32_t vbw[4] = {vb.x, vb.y, vb.z, vb.w};
-          float d0[4], d1[4];
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const uint32_t xa = vaw[w], xb = vbw[w];
-            const uint32_t a0[4] = {nib_bf16_off(xa), nib_bf16_off(xb),
-                                    nib_bf16_off(xa >> 4),
-                                    nib_bf16_off(xb >> 4)};
-            const uint32_t a1[4] = {nib_bf16_off(xa >> 8),
-                                    nib_bf16_off(xb >> 8),
-                                    nib_bf16_off(xa >> 12),
-                                    nib_bf16_off(xb >> 12)};
-            if (w == 0) {
-              mma_bf16_c(d0, a0, qv[0][0], qv[0][1], offc0, offc1, offc0,
-                         offc1);
-              mma_bf16_c(d1, a1, qv[1][0], qv[1][1], 0.f, 0.f, 0.f, 0.f);
-            } else {
-              mma_bf16(d0, a0, qv[2 * w][0], qv[2 * w][1]);
-              mma_bf16(d1, a1, qv[2 * w + 1][0], qv[2 * w + 1][1]);
-            }
-          }
-          // proj (log2 units) = D * sV * log2(e)/sqrt(d), split hi + lo fp16
-          const float pa0 = (d0[0] + d1[0]) * sva, pa1 = (d0[1] + d1[1]) * sva;
-          const float pb0 = (d0[2] + d1[2]) * svb, pb1 = (d0[3] + d1[3]) * svb;
-          const __half2 ha = __floats2half2_rn(pa0, pa1);
-          const __half2 hb = __floats2half2_rn(pb0, pb1);
-          const uint32_t la =
-              pack_h2(pa0 - __low2float(ha), pa1 - __high2float(ha));
-          const uint32_t lb =
-              pack_h2(pb0 - __low2float(hb), pb1 - __high2float(hb));
-          const uint32_t tha = movmatrix_trans(h2_as_u32(ha));
-          const uint32_t tla = movmatrix_trans(la);
-          const uint32_t thb = movmatrix_trans(h2_as_u32(hb));
-          const uint32_t tlb = movmatrix_trans(lb);
-          uint32_t ba0, ba1, bb0, bb1;
-          i8x4_to_h2(ca, ba0, ba1);
-          i8x4_to_h2(cb, bb0, bb1);
-          float l0[4], l1[4];
-          if constexpr (MODE == 1) {
-            // rows 0-3: page A heads (high halves, k 0..7 = page A comps),
-            // rows 4-7: page B heads (high, k 8..15 = page B comps),
-            // rows 8-15: the same with the low halves
-            const uint32_t A2[4] = {tha & maskA, tla & maskA, thb & ~maskA,
-                                    tlb & ~maskA};
-            mma_f16_z(l0, A2, ba0, bb0);
-            mma_f16_z(l1, A2, ba1, bb1);
-            const uint32_t rs = lowh ? ra : rb;
-            const uint4 sc = lds128(rs + kOffSV + 16 * t4);
-            const __half2 s0 = u32_as_h2(sc.y), s1 = u32_as_h2(sc.z);
-            const float e = lse2_quad_sel((l0[0] + l0[2]) * __low2float(s0),
-                                          (l0[1] + l0[3]) * __high2float(s0),
-                                          (l1[0] + l1[2]) * __low2float(s1),
-                                          (l1[1] + l1[3]) * __high2float(s1),
-                                          safe, bad);
-            if (pp == t4) keepA = e;
-          } else {
-            float m0[4], m1[4];
-            mma1688_f16_z(l0, tha, tla, ba0);
-            mma1688_f16_z(l1, tha, tla, ba1);
-            mma1688_f16_z(m0, thb, tlb, bb0);
-            mma1688_f16_z(m1, thb, tlb, bb1);
-            const uint4 sa = lds128(ra + kOffSV + 16 * t4);
-            const uint4 sb = lds128(rb + kOffSV + 16 * t4);
-            const __half2 a0 = u32_as_h2(sa.y), a1 = u32_as_h2(sa.z);
-            const __half2 b0 = u32_as_h2(sb.y), b1 = u32_as_h2(sb.z);
-            const float ea = lse2_quad_sel((l0[0] + l0[2]) * __low2float(a0),
-                                           (l0[1] + l0[3]) * __high2float(a0),
-                                           (l1[0] + l1[2]) * __low2float(a1),
-                                           (l1[1] + l1[3]) * __high2float(a1),
-                                           safe, bad);
-            const float eb = lse2_quad_sel((m0[0] + m0[2]) * __low2float(b0),
-                                           (m0[1] + m0[3]) * __high2float(b0),
-                                           (m1[0] + m1[2]) * __low2float(b1),
-                                           (m1[1] + m1[3]) * __high2float(b1),
-                                           safe, bad);
-            if (pp == t4) {
-              keepA = ea;
-              keepB = eb;
-            }
-          }
-        }
-      }
-      if (!__any_sync(0xffffffffu, bad >= kLseBad)) break;
-      }
+      const uint32_t bad = score_pairs<MODE, false>(
+          base_s, npg, lane, qv, offc0, offc1, vscale, keepA, keepB);
+      if (__any_sync(0xffffffffu, bad >= kLseBad))
+        score_pairs<MODE, true>(base_s, npg, lane, qv, offc0, offc1, vscale,
+                                keepA, keepB);
       // q . mu for the tile's 8 pages (column n = page gq of the tile)
       float qm[4] = {off_m, off_m, off_m8, off_m8};
       float qm2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -463,7 +543,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             (unsigned short)lds16(base_s + pg * kRec + kOffSMu)));
         const float qmu = up ? qm_from_low : qm_lo;
         if (head < G && pg < npg)
-          lane_row[page0 + pg] = (keepA + qmu * smu * kLog2eRsqrtD) * kLn2;
+          lane_row[page0 + pg] = (keepA + qmu * smu * mscale) * kLn2;
       } else {
         const int pg0 = 2 * t4, pg1 = pg0 + 1;
         const float sm0 = __half2float(__ushort_as_half(
@@ -472,9 +552,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             (unsigned short)lds16(base_s + pg1 * kRec + kOffSMu)));
         if (gq < G) {
           if (pg0 < npg)
-            lane_row[page0 + pg0] = (keepA + qm_lo * sm0 * kLog2eRsqrtD) * kLn2;
+            lane_row[page0 + pg0] = (keepA + qm_lo * sm0 * mscale) * kLn2;
           if (pg1 < npg)
-            lane_row[page0 + pg1] = (keepB + qm_hi * sm1 * kLog2eRsqrtD) * kLn2;
+            lane_row[page0 + pg1] = (keepB + qm_hi * sm1 * mscale) * kLn2;
         }
       }
     } else {
@@ -558,16 +638,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (gq < G) {
         float *dst = lane_row + page0;
         if (pg0 < npg)
-          dst[pg0] = (o0 + (qm[0] + qm2[0]) * sm0 * kLog2eRsqrtD) * kLn2;
+          dst[pg0] = (o0 + (qm[0] + qm2[0]) * sm0 * mscale) * kLn2;
         if (pg1 < npg)
-          dst[pg1] = (o1 + (qm[1] + qm2[1]) * sm1 * kLog2eRsqrtD) * kLn2;
+          dst[pg1] = (o1 + (qm[1] + qm2[1]) * sm1 * mscale) * kLn2;
       }
       if (gq + 8 < G) {
         float *dst = lane_row8 + page0;
         if (pg0 < npg)
-          dst[pg0] = (o80 + (qm[2] + qm2[2]) * sm0 * kLog2eRsqrtD) * kLn2;
+          dst[pg0] = (o80 + (qm[2] + qm2[2]) * sm0 * mscale) * kLn2;
         if (pg1 < npg)
-          dst[pg1] = (o81 + (qm[3] + qm2[3]) * sm1 * kLog2eRsqrtD) * kLn2;
+          dst[pg1] = (o81 + (qm[3] + qm2[3]) * sm1 * mscale) * kLn2;
       }
     }
     __syncwarp();

@@ -274,6 +274,37 @@ def test_score_matches_oracle_on_same_records(G, h_kv):
             assert ok, (b, h, ig[b, h], idx_o[b, h])
 
 
+@pytest.mark.parametrize("G,h_kv", [(4, 2), (16, 1)])
+def test_score_extreme_query_magnitude(G, h_kv):
+    """Queries far beyond the fp16 range (|q| up to ~6e4): the kernels carry
+    fp16 tensor-core operands, so each (sequence, KV head) prescales its
+    query by a power of two.  Scores must stay finite and keep fp32-level
+    relative accuracy (1e-4 of the largest score; the absolute 1e-3 bound
+    of the specification does not apply to scores of this size)."""
+    spec = W.custom_spec(batch=2, h_q=G * h_kv, h_kv=h_kv, ctx=16 * 24,
+                         k=6, needles=0, seed=60 + G)
+    wl = W.generate(spec, "cpu")
+    kc, vc, pt, _ = host(wl)
+    lens = [16 * 24, 16 * 9 + 3]
+    batch, max_pages = pt.shape
+    seq, pg = full_pairs(lens)
+    store, _ = O.build_summaries(kc, pt, seq, pg, batch, max_pages)
+    qb = (wl.queries[0].float() * 16384.0).to(torch.bfloat16)
+    s_orc = O.score_store(qb.float().numpy(), store, lens)
+    sc = torch.zeros(batch, h_kv, G, max_pages, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.locks_score_pages(qb.to(DEV), torch.from_numpy(store).to(DEV),
+                        i32(lens), sc, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    s = sc.cpu().numpy()
+    for b in range(batch):
+        nf = lens[b] // 16
+        got, ref = s[b, :, :, :nf], s_orc[b, :, :, :nf]
+        assert np.isfinite(got).all()
+        assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max()
+
+
 # ---------------------------------------------------------------------------
 # select (Eq.(5) + sink/recent) from identical scores
 # ---------------------------------------------------------------------------
