@@ -25,6 +25,38 @@ __device__ __forceinline__ void set_status(int32_t *status, int bits) {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel of the decode step lets the next
+// one launch while it runs (pdl_trigger), and the next one waits for the
+// previous grid to finish, with its memory visible, before it touches that
+// grid's outputs or any buffer the previous grid reads (pdl_wait).  A kernel
+// launched without a programmatic predecessor returns from pdl_wait at once.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// Launch with programmatic stream serialisation allowed (host side).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block,
+                              size_t smem, cudaStream_t stream,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// ---------------------------------------------------------------------------
 // quantiser (storage paragraph of §4.1): symmetric, fp16 scale
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ __half quant_scale(float absmax, float qmax) {

@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
   const int gq = lane >> 2, t4 = lane & 3;
   const int h_q = h_kv * G;
   const Layout lay{s_pre, batch, h_kv, idx ? h_kv * k : 0};
+  pdl_trigger();
 
   int total;
   if (idx) {
@@ -179,6 +180,9 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
     __syncthreads();
     total = s_pre[batch];
   }
+  // the page lists come from the selection kernel, and the workspace may
+  // still be read by it
+  pdl_wait();
   const int chunk = max(1, (total + n_warps - 1) / n_warps);
   if (blockIdx.x == 0) {  // layout for the merge kernel
     if (threadIdx.x == 0) meta[0] = chunk;
@@ -438,6 +442,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
                    int dense, int G, __nv_bfloat16 *__restrict__ o_out,
                    float *__restrict__ lse_out) {
   const int lane = threadIdx.x & 31;
+  pdl_wait();  // partials and layout of the decode kernel
   const long long row =
       (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
   if (row >= (long long)batch * h_kv * G) return;
@@ -560,21 +565,18 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
   auto *kc = static_cast<const __nv_bfloat16 *>(k_cache);
   auto *vc = static_cast<const __nv_bfloat16 *>(v_cache);
   auto *oo = static_cast<__nv_bfloat16 *>(o_out);
-  if (wide)
-    decode_kernel<true><<<grid, kDecThreads, smem, stream>>>(
-        qq, kc, vc, num_phys, pt, seq_lens, idx, k, batch, h_kv, G, max_pages,
-        n_warps, oo, lse_out, o_part, lse_part, meta, status);
-  else
-    decode_kernel<false><<<grid, kDecThreads, smem, stream>>>(
-        qq, kc, vc, num_phys, pt, seq_lens, idx, k, batch, h_kv, G, max_pages,
-        n_warps, oo, lse_out, o_part, lse_part, meta, status);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(
+      wide ? decode_kernel<true> : decode_kernel<false>, dim3(grid),
+      dim3(kDecThreads), smem, stream, qq, kc, vc, num_phys, pt, seq_lens,
+      idx, k, batch, h_kv, G, max_pages, n_warps, oo, lse_out, o_part,
+      lse_part, meta, status);
   if (e != cudaSuccess) return e;
   const long long rows = (long long)batch * h_kv * G;
-  combine_kernel<<<(unsigned)((rows + kCombineWarps - 1) / kCombineWarps),
-                   32 * kCombineWarps, 0, stream>>>(
-      o_part, lse_part, meta, batch, h_kv, k, idx ? 0 : 1, G, oo, lse_out);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel,
+                    dim3((unsigned)((rows + kCombineWarps - 1) / kCombineWarps)),
+                    dim3(32 * kCombineWarps), 0, stream, o_part, lse_part,
+                    (const int *)meta, batch, h_kv, k, idx ? 0 : 1, G, oo,
+                    lse_out);
 }
 
 }  // namespace locks

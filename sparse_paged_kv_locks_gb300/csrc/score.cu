@@ -304,6 +304,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   int *tph = nfull + batch;  // tiles per KV head of each sequence
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int gq = lane >> 2, t4 = lane & 3;  // mma groupID / thread-in-group
+  // selection may launch now; it waits for these scores before reading them
+  pdl_trigger();
 
   // per-sequence full pages and tile counts
   for (int b = threadIdx.x; b < batch; b += blockDim.x) {

@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   const int b = blockIdx.y, h = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   constexpr int nwarps = kSelThreads / 32;
+  pdl_trigger();
   int L = seq_lens[b];
   if (L < 0 || L > max_pages * kPage) {
     if (tid == 0 && h == 0) set_status(status, LOCKS_DEV_BAD_SEQ_LEN);
@@ -126,6 +127,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   }
   const int n = (L + kPage - 1) / kPage, nf = L / kPage;
   int32_t *out = idx + ((size_t)b * h_kv + h) * k;
+  pdl_wait();  // scores of the scoring kernel; idx may still be read before
   if (n <= k) {
     for (int i = tid; i < k; i += blockDim.x) out[i] = i < n ? i : -1;
     return;
@@ -437,10 +439,8 @@ cudaError_t launch_select(const float *scores, const int32_t *seq_lens,
     cudaError_t e = cudaFuncSetAttribute(
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmemKeys * 4);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kSelThreads, smem, stream>>>(scores, seq_lens, h_kv, G,
-                                              max_pages, k, idx, keybuf,
-                                              status);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kSelThreads), smem, stream, scores,
+                      seq_lens, h_kv, G, max_pages, k, idx, keybuf, status);
   };
   const int gt = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : G <= 8 ? 8 : 16;
   if (on_chip) {
