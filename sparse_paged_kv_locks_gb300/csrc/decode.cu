@@ -180,19 +180,10 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
     __syncthreads();
     total = s_pre[batch];
   }
-  // the page lists come from the selection kernel, and the workspace may
-  // still be read by it
-  pdl_wait();
   const int chunk = max(1, (total + n_warps - 1) / n_warps);
-  if (blockIdx.x == 0) {  // layout for the merge kernel
-    if (threadIdx.x == 0) meta[0] = chunk;
-    if (!idx)
-      for (int b = threadIdx.x; b <= batch; b += blockDim.x)
-        meta[1 + b] = s_pre[b];
-  }
   const int gw = blockIdx.x * kDecWarps + wid;
-  if (gw >= n_warps || (long long)gw * chunk >= total) return;
-  const int pb = gw * chunk, pe = min(total, pb + chunk);
+  const bool active = gw < n_warps && (long long)gw * chunk < total;
+  const int pb = active ? gw * chunk : 0, pe = min(total, pb + chunk);
 
   uint8_t *wbase = smem + wid * (kDecStages * 2 * kKvTile);
   const uint32_t wbase_s = smem_u32(wbase);
@@ -211,8 +202,20 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
       qa[s][3] = (WIDE && gq + 8 < G) ? __ldg(reinterpret_cast<const uint32_t *>(qb + (gq + 8) * kDim + d0 + 8)) : 0u;
     }
   };
-  int cur_u = lay.unit_of(pb);
-  load_q(cur_u);
+  // the query is an input of the step: fetch it while the selection kernel
+  // may still run
+  int cur_u = active ? lay.unit_of(pb) : 0;
+  if (active) load_q(cur_u);
+  // the page lists come from the selection kernel, and the workspace may
+  // still be read by it
+  pdl_wait();
+  if (blockIdx.x == 0) {  // layout for the merge kernel
+    if (threadIdx.x == 0) meta[0] = chunk;
+    if (!idx)
+      for (int b = threadIdx.x; b <= batch; b += blockDim.x)
+        meta[1 + b] = s_pre[b];
+  }
+  if (!active) return;
   bool q_ready = true;
 
   // window of 32 positions: this lane's entry and the valid ones not yet
@@ -431,9 +434,11 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
 
 // Merge of the partials of units split across warps; also writes the
 // empty result of units with no positions.  One warp per (unit, head) row;
-// lane l owns head dimensions 4l..4l+3 and the pieces are visited 32 at a
-// time with their weights held one per lane.
+// lane l owns head dimensions 4l..4l+3.  Pieces are merged eight at a time
+// with an online rescale, all loads of a group issued together, so a unit
+// split across at most eight warps costs one round trip.
 constexpr int kCombineWarps = 4;
+constexpr int kCombineGroup = 8;
 
 __global__ void __launch_bounds__(32 * kCombineWarps)
     combine_kernel(const float *__restrict__ o_part,
@@ -451,50 +456,50 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
   const int chunk = meta[0];
   const int2 sp = lay.span(u);
   uint2 *dst = reinterpret_cast<uint2 *>(o_out + row * kDim) + lane;
-  int w0 = 0, w1 = 0;
+  float M = -INFINITY, wsum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (sp.y > sp.x) {
-    w0 = sp.x / chunk;
-    w1 = (sp.y - 1) / chunk;
+    const int w0 = sp.x / chunk, w1 = (sp.y - 1) / chunk;
     if (w0 == w1) return;  // finished by its warp
-  }
-  float M = -INFINITY;
-  if (sp.y > sp.x)
-    for (int w = w0 + lane; w <= w1; w += 32)
-      M = fmaxf(M, lse_part[((size_t)u + w) * G + g]);
+    const float4 *o4 = reinterpret_cast<const float4 *>(o_part);
+    for (int wb = w0; wb <= w1; wb += kCombineGroup) {
+      float l[kCombineGroup];
+      float4 v[kCombineGroup];
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1)
-    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      for (int j = 0; j < kCombineGroup; ++j) {
+        const size_t slot = ((size_t)u + wb + j) * G + g;
+        const bool in = wb + j <= w1;
+        l[j] = in ? lse_part[slot] : -INFINITY;
+        v[j] = in ? o4[slot * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float gm = l[0];
+#pragma unroll
+      for (int j = 1; j < kCombineGroup; ++j) gm = fmaxf(gm, l[j]);
+      const float Mn = fmaxf(M, gm);
+      if (Mn == -INFINITY) continue;
+      const float cf = M == -INFINITY ? 0.f : expf(M - Mn);
+      wsum *= cf;
+      acc.x *= cf;
+      acc.y *= cf;
+      acc.z *= cf;
+      acc.w *= cf;
+#pragma unroll
+      for (int j = 0; j < kCombineGroup; ++j) {
+        const float f = l[j] == -INFINITY ? 0.f : expf(l[j] - Mn);
+        wsum += f;
+        acc.x += f * v[j].x;
+        acc.y += f * v[j].y;
+        acc.z += f * v[j].z;
+        acc.w += f * v[j].w;
+      }
+      M = Mn;
+    }
+  }
   if (M == -INFINITY) {  // no tokens
     *dst = make_uint2(0u, 0u);
     if (lane == 0) lse_out[row] = -INFINITY;
     return;
   }
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  for (int wb = w0; wb <= w1; wb += 32) {
-    const int w = wb + lane;
-    float f = 0.f;
-    if (w <= w1) {
-      const float l = lse_part[((size_t)u + w) * G + g];
-      f = l == -INFINITY ? 0.f : expf(l - M);
-    }
-    wsum += f;
-    const int cnt = min(32, w1 - wb + 1);
-    const float4 *src =
-        reinterpret_cast<const float4 *>(o_part) + (((size_t)u + wb) * G + g) * 32 + lane;
-#pragma unroll 8
-    for (int j = 0; j < cnt; ++j) {
-      const float fj = __shfl_sync(0xffffffffu, f, j);
-      const float4 v = src[(size_t)j * G * 32];
-      acc.x += fj * v.x;
-      acc.y += fj * v.y;
-      acc.z += fj * v.z;
-      acc.w += fj * v.w;
-    }
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1)
-    wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
   const float inv = 1.f / wsum;
   *dst = make_uint2(pack_bf2(acc.x * inv, acc.y * inv),
                     pack_bf2(acc.z * inv, acc.w * inv));

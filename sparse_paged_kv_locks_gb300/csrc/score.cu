@@ -253,6 +253,20 @@ __device__ __forceinline__ uint32_t score_pairs(
   return bad;
 }
 
+// L2 policy for the scores: kept in L2 ahead of the summary stream, so the
+// selection kernel that follows reads them from L2
+__device__ __forceinline__ uint64_t l2_keep_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n"
+               : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void st_keep(float *p, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;\n" ::"l"(p),
+               "f"(v), "l"(pol)
+               : "memory");
+}
+
 // position of a warp in its contiguous range of tiles
 struct Cursor {
   int b, h, j;
@@ -306,6 +320,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int gq = lane >> 2, t4 = lane & 3;  // mma groupID / thread-in-group
   // selection may launch now; it waits for these scores before reading them
   pdl_trigger();
+  const uint64_t keep = l2_keep_policy();
 
   // per-sequence full pages and tile counts
   for (int b = threadIdx.x; b < batch; b += blockDim.x) {
@@ -545,7 +560,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             (unsigned short)lds16(base_s + pg * kRec + kOffSMu)));
         const float qmu = up ? qm_from_low : qm_lo;
         if (head < G && pg < npg)
-          lane_row[page0 + pg] = (keepA + qmu * smu * mscale) * kLn2;
+          st_keep(lane_row + page0 + pg, (keepA + qmu * smu * mscale) * kLn2,
+                  keep);
       } else {
         const int pg0 = 2 * t4, pg1 = pg0 + 1;
         const float sm0 = __half2float(__ushort_as_half(
@@ -554,9 +570,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             (unsigned short)lds16(base_s + pg1 * kRec + kOffSMu)));
         if (gq < G) {
           if (pg0 < npg)
-            lane_row[page0 + pg0] = (keepA + qm_lo * sm0 * mscale) * kLn2;
+            st_keep(lane_row + page0 + pg0,
+                    (keepA + qm_lo * sm0 * mscale) * kLn2, keep);
           if (pg1 < npg)
-            lane_row[page0 + pg1] = (keepB + qm_hi * sm1 * mscale) * kLn2;
+            st_keep(lane_row + page0 + pg1,
+                    (keepB + qm_hi * sm1 * mscale) * kLn2, keep);
         }
       }
     } else {
