@@ -31,6 +31,20 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   return h2_as_u32(__floats2half2_rn(lo, hi));
 }
 
+// fp16x2 of (p0 - h.x, p1 - h.y) for h = fp16x2(p0, p1): the low halves of a
+// two-term fp16 split (both differences are exact in fp32; mixed-precision
+// fma takes h's halves without converting them first)
+__device__ __forceinline__ uint32_t split_lo(uint32_t h, float p0, float p1) {
+  float l0, l1;
+  asm("{\n .reg .b16 a, b, m1;\n mov.b32 {a, b}, %2;\n"
+      " mov.b16 m1, 0xBC00;\n"
+      " fma.rn.f32.f16 %0, a, m1, %3;\n"
+      " fma.rn.f32.f16 %1, b, m1, %4;\n}\n"
+      : "=f"(l0), "=f"(l1)
+      : "r"(h), "f"(p0), "f"(p1));
+  return pack_h2(l0, l1);
+}
+
 // Two int4 codes at bits [0,4) and [16,20) -> bf16x2 holding 136 + code
 // (exact); the constant 136 is cancelled through the accumulator's initial
 // value, so no subtraction is spent per element.
@@ -195,10 +209,8 @@ __device__ __forceinline__ uint32_t score_pairs(
     const float pb0 = (d0[2] + d1[2]) * svb, pb1 = (d0[3] + d1[3]) * svb;
     const __half2 ha = __floats2half2_rn(pa0, pa1);
     const __half2 hb = __floats2half2_rn(pb0, pb1);
-    const uint32_t la =
-        pack_h2(pa0 - __low2float(ha), pa1 - __high2float(ha));
-    const uint32_t lb =
-        pack_h2(pb0 - __low2float(hb), pb1 - __high2float(hb));
+    const uint32_t la = split_lo(h2_as_u32(ha), pa0, pa1);
+    const uint32_t lb = split_lo(h2_as_u32(hb), pb0, pb1);
     const uint32_t tha = movmatrix_trans(h2_as_u32(ha));
     const uint32_t tla = movmatrix_trans(la);
     const uint32_t thb = movmatrix_trans(h2_as_u32(hb));
@@ -605,9 +617,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           const __half2 h01 = __floats2half2_rn(P0, P1);
           const __half2 h23 = __floats2half2_rn(P2, P3);
           const uint32_t A2h[4] = {h2_as_u32(h01), h2_as_u32(h23), 0u, 0u};
-          const uint32_t A2l[4] = {
-              pack_h2(P0 - __low2float(h01), P1 - __high2float(h01)),
-              pack_h2(P2 - __low2float(h23), P3 - __high2float(h23)), 0u, 0u};
+          const uint32_t A2l[4] = {split_lo(h2_as_u32(h01), P0, P1),
+                                   split_lo(h2_as_u32(h23), P2, P3), 0u, 0u};
           // K 0..7 carry the high halves, K 8..15 the low halves
           const uint32_t A2[4] = {A2h[0], A2h[1], A2l[0], A2l[1]};
           uint32_t bt0, bt1;
