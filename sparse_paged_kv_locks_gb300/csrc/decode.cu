@@ -315,26 +315,29 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
     }
   };
 
-  int ph0, nt0 = 0, u0 = 0, ph1, nt1 = 0, u1 = 0;
-  next_valid(ph0, nt0, u0);
-  if (ph0 >= 0) issue(0, ph0, u0);
-  cp_async_commit();
-  if (ph0 >= 0) next_valid(ph1, nt1, u1); else ph1 = -1;
-  if (ph1 >= 0) issue(1, ph1, u1);
-  cp_async_commit();
+  // pages in flight, oldest first (qp < 0: none); the oldest sits in shared
+  // memory stage `st`, the next ones in the stages after it
+  int qp[kDecStages], qn[kDecStages], qu[kDecStages];
+#pragma unroll
+  for (int i = 0; i < kDecStages; ++i) {
+    qn[i] = 0;
+    qu[i] = 0;
+    next_valid(qp[i], qn[i], qu[i]);
+    if (qp[i] >= 0) issue(i, qp[i], qu[i]);
+    cp_async_commit();
+  }
 
-  for (int it = 0;; ++it) {
-    const int st = it & 1;
-    const int phys = st ? ph1 : ph0;
+  for (int st = 0;; st = st + 1 == kDecStages ? 0 : st + 1) {
+    const int phys = qp[0];
     if (phys < 0) break;
-    const int ntok = st ? nt1 : nt0;
-    const int u = st ? u1 : u0;
+    const int ntok = qn[0];
+    const int u = qu[0];
     if (u != cur_u) advance_to(u);
     if (!q_ready) {
       load_q(cur_u);
       q_ready = true;
     }
-    cp_async_wait<1>();
+    cp_async_wait<kDecStages - 1>();
     __syncwarp();
     const uint32_t kb_s = wbase_s + st * 2 * kKvTile, vb_s = kb_s + kKvTile;
 
@@ -409,19 +412,17 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
       }
     }
     __syncwarp();
-    int nph, nnt = 0, nu = 0;
-    next_valid(nph, nnt, nu);
-    if (nph >= 0) issue(st, nph, nu);
-    cp_async_commit();
-    if (st) {
-      ph1 = nph;
-      nt1 = nnt;
-      u1 = nu;
-    } else {
-      ph0 = nph;
-      nt0 = nnt;
-      u0 = nu;
+#pragma unroll
+    for (int i = 0; i + 1 < kDecStages; ++i) {
+      qp[i] = qp[i + 1];
+      qn[i] = qn[i + 1];
+      qu[i] = qu[i + 1];
     }
+    qn[kDecStages - 1] = 0;
+    qu[kDecStages - 1] = 0;
+    next_valid(qp[kDecStages - 1], qn[kDecStages - 1], qu[kDecStages - 1]);
+    if (qp[kDecStages - 1] >= 0) issue(st, qp[kDecStages - 1], qu[kDecStages - 1]);
+    cp_async_commit();
   }
   cp_async_wait<0>();
   // close the units up to the one holding the run's last position
