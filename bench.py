@@ -387,9 +387,10 @@ def run_locks(args):
                      "page_heads_per_s": round(n_records / (build_ms / 1e3))}
 
     if not args.quick:
-        # e2e: pinned host query in, pinned host (o, lse) out, every step
+        # e2e: pinned host query in, pinned host (o, lse) out, every step;
+        # the decoder replays the step as one captured CUDA graph
         dec = B.LocksDecoder(wl.k_cache, wl.v_cache, wl.page_table, store,
-                             spec.h_q, k)
+                             spec.h_q, k, graph=True)
         q_host = qs.cpu().pin_memory()
         o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         lse_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
@@ -404,7 +405,8 @@ def run_locks(args):
         line["e2e"] = {"value": world * batch * n_e2e / dt, "unit": "tokens/s",
                        "steps": n_e2e,
                        "h2d_bytes_per_step": q_bytes,
-                       "d2h_bytes_per_step": q_bytes + batch * spec.h_q * 4}
+                       "d2h_bytes_per_step": q_bytes + batch * spec.h_q * 4,
+                       "api": "LocksDecoder.step_host, CUDA graph replay"}
         # dense full-cache decode of the same shape, as context
         for _ in range(2):
             B.locks_sparse_decode(qs[0], wl.k_cache, wl.v_cache,

@@ -321,9 +321,16 @@ def locks_read_status(status_word, stream=None) -> int:
 # a decode step for one layer: score + select + sparse attention
 # ---------------------------------------------------------------------------
 class LocksDecoder:
-    """Owns the per-step buffers of one layer's decode step."""
+    """Owns the per-step buffers of one layer's decode step.
 
-    def __init__(self, k_cache, v_cache, page_table, summaries, h_q, k):
+    With graph=True the step (score + select + sparse attention, five
+    kernels) is captured once into a CUDA graph on the first call and
+    replayed afterwards; the query and the lengths are then copied into
+    static device buffers first.  The library allocates nothing and never
+    synchronises, so the captured step is the eager one."""
+
+    def __init__(self, k_cache, v_cache, page_table, summaries, h_q, k,
+                 graph=False):
         self.k_cache, self.v_cache = k_cache, v_cache
         self.page_table, self.summaries = page_table, summaries
         self.batch, self.h_kv, self.max_pages = summaries.shape[:3]
@@ -339,14 +346,44 @@ class LocksDecoder:
                                device=dev)
         self.q_dev = torch.empty(self.batch, h_q, HEAD_DIM,
                                  dtype=torch.bfloat16, device=dev)
+        self.seq_lens_dev = torch.empty(self.batch, dtype=torch.int32,
+                                        device=dev)
+        self.use_graph = graph
+        self._graph = None
 
-    def step(self, q, seq_lens, stream=None):
-        """Device-resident query -> (o, lse) on the device."""
+    def _eager(self, q, seq_lens, stream=None):
         locks_score_select(q, self.summaries, seq_lens, self.k, self.idx,
                            self.workspace, stream)
         locks_sparse_decode(q, self.k_cache, self.v_cache, self.page_table,
                             seq_lens, self.idx, self.k, self.o, self.lse,
                             self.workspace, stream)
+
+    def _capture(self):
+        cur = torch.cuda.current_stream()
+        side = torch.cuda.Stream()
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):   # one-time setup outside the capture
+            self._eager(self.q_dev, self.seq_lens_dev)
+        cur.wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self._eager(self.q_dev, self.seq_lens_dev)
+        self._graph = g
+
+    def step(self, q, seq_lens, stream=None):
+        """Device-resident query -> (o, lse) on the device."""
+        if not self.use_graph:
+            self._eager(q, seq_lens, stream)
+            return self.o, self.lse
+        if stream is not None:
+            raise ValueError("graph replay runs on the current stream")
+        if q is not self.q_dev:
+            self.q_dev.copy_(q, non_blocking=True)
+        if seq_lens is not self.seq_lens_dev:
+            self.seq_lens_dev.copy_(seq_lens, non_blocking=True)
+        if self._graph is None:
+            self._capture()
+        self._graph.replay()
         return self.o, self.lse
 
     def step_host(self, q_host, seq_lens, o_host, lse_host, stream=None):
