@@ -376,6 +376,80 @@ def share_average(s_hat_g, n_full):
     return mass_fractions(s_hat_g, n_full).mean(axis=0)
 
 
+def exact_store(q, k_cache, page_table, seq_lens, h_kv):
+    """Exact page LSE s_j(q_g) of every full page (the quantity Eq.(4)
+    estimates; ranking by it is the exact-mass selector the notes compare
+    against in §6 Fig. 1(b) and Fig. 2): [batch][h_kv][G][max_pages], NaN
+    where a page is not full.  q [batch][h_q][d]; caches as the C ABI."""
+    q = np.asarray(q, np.float64)
+    batch, max_pages = page_table.shape
+    G = q.shape[1] // h_kv
+    out = np.full((batch, h_kv, G, max_pages), np.nan)
+    for b in range(batch):
+        nf = int(seq_lens[b]) // PAGE
+        if nf == 0:
+            continue
+        phys = np.asarray(page_table[b, :nf], np.int64)
+        for h in range(h_kv):
+            keys = np.asarray(k_cache[phys, h], np.float64)
+            out[b, h, :, :nf] = exact_page_lse(q[b, h * G:(h + 1) * G], keys)
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Theorem 1 (notes §5): coverage retention and the output-error bound
+# ----------------------------------------------------------------------------
+def group_coverage(s_exact_g, pages, n_full):
+    """gamma_bar(S) = (1/G) sum_g sum_{j in S} m_g(j): the group-average
+    attention mass that the page set S keeps, m_g the exact mass fractions
+    over the n_full full pages (§5 Theorem 1 (ii))."""
+    m = mass_fractions(s_exact_g, n_full).mean(axis=0)
+    return float(sum(m[j] for j in pages if j < n_full))
+
+
+def theorem1_terms(s_hat_g, s_exact_g, seq_len, k):
+    """For one (sequence, KV head) of full pages: eta of Eq.(6), the
+    coverage of the share-average selection from the summaries (S_hat) and
+    of the exact-mass selection (S_star), and the Eq.(8) guarantee
+    exp(-4 eta) * gamma_bar(S_star)."""
+    nf = int(seq_len) // PAGE
+    eta = float(np.abs(np.asarray(s_hat_g)[:, :nf] -
+                       np.asarray(s_exact_g)[:, :nf]).max())
+    s_hat_sel = select_one(s_hat_g, seq_len, k)
+    s_star = select_one(s_exact_g, seq_len, k)
+    g_hat = group_coverage(s_exact_g, s_hat_sel, nf)
+    g_star = group_coverage(s_exact_g, s_star, nf)
+    return {"eta": eta, "S_hat": s_hat_sel, "S_star": s_star,
+            "gamma_hat": g_hat, "gamma_star": g_star,
+            "eq8": math.exp(-4.0 * eta) * g_star}
+
+
+def eq9_bound(R, eta, gamma_star):
+    """Output-error bound of §5 Theorem 1 (iii).  The printed form
+    2R(1 - e^{-4 eta}) gamma_bar* vanishes at eta = 0, where the exact
+    selection itself still drops mass; the bound that Eq.(1) and Eq.(8)
+    give, and the reading taken here, is 2R(1 - e^{-4 eta} gamma_bar*)."""
+    return 2.0 * R * (1.0 - math.exp(-4.0 * eta) * gamma_star)
+
+
+def carrier_retention(idx, carriers):
+    """Fraction of carrier (needle) pages present in the selections:
+    idx [batch][h_kv][k], carriers [batch][h_kv][c] logical pages (<0
+    ignored) — the key-page retention the notes measure in §6 Fig. 1(b)."""
+    idx = np.asarray(idx)
+    carriers = np.asarray(carriers)
+    hit = tot = 0
+    for b in range(carriers.shape[0]):
+        for h in range(carriers.shape[1]):
+            sel = set(int(x) for x in idx[b, h] if x >= 0)
+            for p in carriers[b, h]:
+                if p < 0:
+                    continue
+                tot += 1
+                hit += int(p) in sel
+    return hit / tot if tot else float("nan")
+
+
 # ----------------------------------------------------------------------------
 # Attention over selected pages: notes §2, Algorithm 2
 # ----------------------------------------------------------------------------

@@ -162,6 +162,76 @@ def test_eq7_bound_unquantised():
             assert abs(s_hat[g, j] - s_ex[g, j]) <= b + 1e-12
 
 
+@pytest.mark.parametrize("r,G,k", [(1, 4, 5), (2, 1, 4), (4, 4, 8),
+                                   (8, 3, 6)])
+def test_theorem1_coverage_and_output_bounds(r, G, k):
+    """§5 Theorem 1 on unquantised summaries, by brute force: with eta the
+    largest page-score error (Eq.(6)), the share-average selection from the
+    summaries keeps at least exp(-4 eta) of the exact-mass selection's group
+    coverage (Eq.(8)) and never more than it (the exact-mass selection
+    maximises group coverage); the group-average output error, measured by
+    attending over all tokens and over the selected pages, stays within
+    2R(1 - gamma_bar(S_hat)) (Eq.(1) per head) and so within
+    2R(1 - e^{-4 eta} gamma_bar*) (Eq.(9), reading in eq9_bound)."""
+    rng = _rng(40 + r + G + k)
+    n = 12
+    for _ in range(6):
+        keys = _pages(rng, n)
+        vals = rng.normal(size=(n, 16, 128))
+        s = O.page_summary(keys, r=r)
+        q = rng.normal(size=(G, 128)) * rng.uniform(0.5, 3.0)
+        s_hat = O.score_from_summaries(q, s["mu"], s["V"], s["C"])
+        s_ex = O.exact_page_lse(q, keys)
+        t = O.theorem1_terms(s_hat, s_ex, 16 * n, k)
+        assert t["eta"] > 0
+        assert t["gamma_hat"] >= t["eq8"] - 1e-12
+        assert t["gamma_star"] >= t["gamma_hat"] - 1e-12
+        R = np.linalg.norm(vals.reshape(-1, 128), axis=1).max()
+        o_full, _ = O.attend(q, keys.reshape(-1, 128), vals.reshape(-1, 128))
+        sel = t["S_hat"]
+        o_sel, _ = O.attend(q, keys[sel].reshape(-1, 128),
+                            vals[sel].reshape(-1, 128))
+        err = np.linalg.norm(o_sel - o_full, axis=1).mean()
+        assert err <= 2 * R * (1 - t["gamma_hat"]) + 1e-12
+        assert err <= O.eq9_bound(R, t["eta"], t["gamma_star"]) + 1e-12
+    # at r = rank the summaries are exact: eta = 0 and the two selections
+    # coincide
+    keys = _pages(rng, n)
+    s = O.page_summary(keys, r=15)
+    q = rng.normal(size=(G, 128))
+    t = O.theorem1_terms(O.score_from_summaries(q, s["mu"], s["V"], s["C"]),
+                         O.exact_page_lse(q, keys), 16 * n, k)
+    assert t["eta"] < 1e-9 and t["S_hat"] == t["S_star"]
+
+
+def test_exact_store_brute_force():
+    """Exact page LSE over the page table, by a direct double loop."""
+    rng = _rng(51)
+    h_kv, G = 2, 2
+    kc = rng.normal(size=(7, h_kv, 16, 128))
+    pt = np.array([[3, 0, 5, -1], [6, 1, 2, 4]])
+    lens = [16 * 3 + 5, 16 * 4]
+    q = rng.normal(size=(2, h_kv * G, 128))
+    ex = O.exact_store(q, kc, pt, lens, h_kv)
+    for b in range(2):
+        for h in range(h_kv):
+            for g in range(G):
+                for j in range(4):
+                    if j < lens[b] // 16:
+                        z = [float(q[b, h * G + g] @ kc[pt[b, j], h, i])
+                             / math.sqrt(128) for i in range(16)]
+                        ref = math.log(sum(math.exp(x) for x in z))
+                        assert abs(ex[b, h, g, j] - ref) < 1e-9
+                    else:
+                        assert np.isnan(ex[b, h, g, j])
+
+
+def test_carrier_retention_counts():
+    idx = np.array([[[0, 3, 9, -1]], [[0, 1, 2, 7]]])
+    car = np.array([[[3, 5]], [[7, -1]]])
+    assert O.carrier_retention(idx, car) == pytest.approx(2 / 3)
+
+
 # --------------------------------------------------------------------------
 # Selection: brute force, ties, degenerate cases (Eq.(5) and sink/recent)
 # --------------------------------------------------------------------------
