@@ -180,6 +180,71 @@ def score_traffic(n_records):
     return round(float(d["dram_bytes_per_record"]) * n_records)
 
 
+def selection_quality(B, wl, store, scores, ws, lens, k, h_q, n_records,
+                      n_steps=4):
+    """Selection quality on the planted needles, GPU only.  The pages
+    holding a needle token (carrier pages) kept by the LOCKS selection and
+    by the exact-mass selection (exact page LSE from every key, the
+    selector the LOCKS notes compare against in §6 Fig. 1(b)), over a budget
+    sweep; the page-score error of the quantised summaries against the
+    exact page LSE (the measured counterpart of eta, Eq.(6)); and the exact
+    scorer's time and bandwidth (it reads every full page's keys)."""
+    import torch
+    dev = scores.device
+    batch, h_kv, G, max_pages = scores.shape
+    ex = torch.empty_like(scores)
+    status = ws[:4].view(torch.int32)
+    sweep = [kk for kk in (16, 32, 64, 128) if kk <= k] or [k]
+    needles = wl.needle_pages.to(dev)                     # [b][h_kv][nn]
+    hit_l = {kk: 0 for kk in sweep}
+    hit_e = {kk: 0 for kk in sweep}
+    n_car = 0
+    err_max, err_sum, err_cnt, p99 = 0.0, 0.0, 0, []
+    times = []
+    e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+    n_steps = min(n_steps, wl.queries.shape[0])
+    for i in range(n_steps):
+        q = wl.queries[i]
+        B.locks_score_pages(q, store, wl.seq_lens, scores, status)
+        e0.record()
+        B.locks_exact_page_scores(q, wl.k_cache, wl.page_table, wl.seq_lens,
+                                  ex, status)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+        for b in range(batch):
+            nf = lens[b] // 16
+            d = (scores[b, :, :, :nf] - ex[b, :, :, :nf]).abs().flatten()
+            err_max = max(err_max, float(d.max()))
+            err_sum += float(d.double().sum())
+            err_cnt += d.numel()
+            p99.append(float(torch.kthvalue(
+                d.cpu(), max(1, int(0.99 * d.numel()))).values))
+        n_car += int((needles >= 0).sum())
+        for kk in sweep:
+            for src, hits in ((scores, hit_l), (ex, hit_e)):
+                idx = torch.empty(batch, h_kv, kk, dtype=torch.int32,
+                                  device=dev)
+                B.locks_select_pages(src, wl.seq_lens, h_q, kk, idx, ws)
+                kept = (idx[:, :, None, :] == needles[:, :, :, None]).any(-1)
+                hits[kk] += int((kept & (needles >= 0)).sum())
+    assert B.locks_read_status(ws) == 0, "quality pass reported an error"
+    ms = statistics.mean(times)
+    return {
+        "budget_pages": sweep,
+        "carrier_retention": {
+            "locks": [round(hit_l[kk] / max(1, n_car), 4) for kk in sweep],
+            "exact_mass": [round(hit_e[kk] / max(1, n_car), 4)
+                           for kk in sweep]},
+        "carrier_pages": n_car // n_steps, "steps": n_steps,
+        "score_error_vs_exact": {"max": round(err_max, 4),
+                                 "mean": round(err_sum / max(1, err_cnt), 5),
+                                 "p99_per_sequence_max": round(max(p99), 4)},
+        "exact_scorer": {"ms": round(ms, 4),
+                         "gbs": round(n_records * 4096 / (ms / 1e3) / 1e9,
+                                      1)}}
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -427,6 +492,8 @@ def run_locks(args):
             "value": batch / (dms / 1e3), "unit": "tokens/s",
             "ms_per_step": round(dms, 4),
             "gbs": round(dense_bytes / (dms / 1e3) / 1e9, 1)}
+        line["quality"] = selection_quality(B, wl, store, scores, ws, lens,
+                                            k, spec.h_q, n_records)
         if rank == 0 and world == 1:
             from oracle import locks_oracle as O
             b0 = 0

@@ -173,6 +173,29 @@ locks_status_t locks_score_pages(const void *q, const void *summaries,
                                  int h_kv, int max_pages, float *scores_out,
                                  int32_t *status, locks_stream_t stream);
 
+/* Exact page scores (LOCKS reading notes §4.2 Eq.(4), the quantity the
+ * summaries estimate; ranking by it is the exact-mass selector of §6
+ * Fig. 1(b) and Fig. 2, which reads every key): for every full page j of
+ * every (b, KV head) and query head g,
+ *   scores_out[b][h][g][j] = ln sum_{i < 16} exp(q_g . k_i / sqrt(128))
+ * in the layout of locks_score_pages (entries of pages that are not full
+ * are left untouched; a page whose physical id is out of range gets -inf
+ * and sets LOCKS_DEV_BAD_PAGE_ID).  Feeding these scores to
+ * locks_select_pages gives the exact-mass selection.
+ *   q           bf16 [batch][h_q][128]
+ *   k_cache     bf16 [num_phys_pages][h_kv][16][128]
+ *   page_table  int32 [batch][max_pages];  seq_lens int32 [batch]
+ *   scores_out  float [batch][h_kv][h_q/h_kv][max_pages] (device)
+ *   status      optional int32 device status word
+ * Returns LOCKS_ERR_UNSUPPORTED when batch * h_kv * max_pages exceeds
+ * 2^31 - 1 or the per-sequence table does not fit in shared memory
+ * (batch above about 48,000). */
+locks_status_t locks_exact_page_scores(
+    const void *q, const void *k_cache, int64_t num_phys_pages,
+    const int32_t *page_table, const int32_t *seq_lens, int batch, int h_q,
+    int h_kv, int max_pages, float *scores_out, int32_t *status,
+    locks_stream_t stream);
+
 /* Score and select without any caller workspace, for callers that may not
  * allocate device memory on the decode path (an engine whose memory plan is
  * frozen after start-up, or a plugin handed only its input and output

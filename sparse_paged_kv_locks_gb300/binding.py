@@ -56,6 +56,8 @@ _SIGS = {
     "locks_score_pages": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "locks_select_pages": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ,
                                 _P]),
+    "locks_exact_page_scores": (_I, [_P, _P, _I64, _P, _P, _I, _I, _I, _I,
+                                     _P, _P, _P]),
     "locks_sparse_decode": (_I, [_P, _P, _P, _I64, _P, _P, _P, _I, _I, _I, _I,
                                  _I, _P, _P, _P, _SZ, _P]),
     "locks_append_kv": (_I, [_P, _P, _P, _P, _I64, _I, _P, _I, _I, _P, _P, _P,
@@ -238,6 +240,26 @@ def locks_score_pages(q, summaries, seq_lens, scores_out, status=None,
     _check("locks_score_pages", lib().locks_score_pages(
         _ptr(q), _ptr(summaries), _ptr(seq_lens), batch, h_q, h_kv,
         max_pages, _ptr(scores_out), _ptr(status), _stream(stream)))
+
+
+def locks_exact_page_scores(q, k_cache, page_table, seq_lens, scores_out,
+                            status=None, stream=None):
+    """Exact page LSE of every full page (the exact-mass selector's scores),
+    same layout as locks_score_pages."""
+    _req(q, "q", torch.bfloat16, 3)
+    _req(k_cache, "k_cache", torch.bfloat16, 4)
+    _req(page_table, "page_table", torch.int32, 2)
+    _req(seq_lens, "seq_lens", torch.int32, 1)
+    _req(scores_out, "scores_out", torch.float32, 4)
+    batch, h_q, _ = q.shape
+    P, h_kv = k_cache.shape[:2]
+    max_pages = page_table.shape[1]
+    if tuple(scores_out.shape) != (batch, h_kv, h_q // h_kv, max_pages):
+        raise ValueError("scores_out must be [batch][h_kv][G][max_pages]")
+    _check("locks_exact_page_scores", lib().locks_exact_page_scores(
+        _ptr(q), _ptr(k_cache), P, _ptr(page_table), _ptr(seq_lens), batch,
+        h_q, h_kv, max_pages, _ptr(scores_out), _ptr(status),
+        _stream(stream)))
 
 
 def locks_select_pages(scores, seq_lens, h_q, k, idx_out, workspace,

@@ -22,7 +22,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIB = os.path.join(LIBDIR, "liblocks.so")
-SOURCES = ["api.cu", "build.cu", "score.cu", "select.cu", "decode.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "build.cu", "score.cu", "select.cu", "decode.cu",
+           "exact.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

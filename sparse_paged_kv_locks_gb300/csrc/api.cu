@@ -173,6 +173,27 @@ locks_status_t locks_score_pages(const void *q, const void *summaries,
   return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
 }
 
+locks_status_t locks_exact_page_scores(
+    const void *q, const void *k_cache, int64_t num_phys_pages,
+    const int32_t *page_table, const int32_t *seq_lens, int batch, int h_q,
+    int h_kv, int max_pages, float *scores_out, int32_t *status,
+    locks_stream_t stream) {
+  if (batch < 0 || max_pages < 1 || num_phys_pages < 1 || !heads_ok(h_q, h_kv))
+    return LOCKS_ERR_INVALID_ARG;
+  if (h_q / h_kv > kMaxGroup) return LOCKS_ERR_UNSUPPORTED;
+  if ((long long)max_pages * kPage > 0x7fffffffLL ||
+      (long long)batch * h_kv * max_pages > 0x7fffffffLL)
+    return LOCKS_ERR_UNSUPPORTED;
+  if (batch == 0) return LOCKS_OK;
+  if (!q || !k_cache || !page_table || !seq_lens || !scores_out)
+    return LOCKS_ERR_INVALID_ARG;
+  if (batch > exact_max_batch()) return LOCKS_ERR_UNSUPPORTED;
+  cudaError_t e = launch_exact(q, k_cache, num_phys_pages, page_table,
+                               seq_lens, batch, h_kv, h_q / h_kv, max_pages,
+                               scores_out, status, (cudaStream_t)stream);
+  return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
+}
+
 locks_status_t locks_select_pages(const float *scores, const int32_t *seq_lens,
                                   int batch, int h_q, int h_kv, int max_pages,
                                   int k, int32_t *idx_out, void *workspace,

@@ -42,7 +42,13 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
                           float *lse_out, float *o_part, float *lse_part,
                           int *meta, int32_t *status, cudaStream_t stream);
 
+cudaError_t launch_exact(const void *q, const void *k_cache, int64_t num_phys,
+                         const int32_t *pt, const int32_t *seq_lens,
+                         int batch, int h_kv, int G, int max_pages,
+                         float *scores, int32_t *status, cudaStream_t stream);
+
 int score_max_batch();
+int exact_max_batch();
 int decode_max_batch();
 
 }  // namespace locks

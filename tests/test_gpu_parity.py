@@ -305,6 +305,44 @@ def test_score_extreme_query_magnitude(G, h_kv):
         assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max()
 
 
+@pytest.mark.parametrize("G,h_kv", [(4, 2), (1, 3), (8, 1), (16, 1)])
+def test_exact_page_scores_match_oracle(G, h_kv):
+    """Exact page LSE (what Eq.(4) estimates) of every full page, and the
+    exact-mass selection obtained by feeding it to the selection kernel."""
+    spec = W.custom_spec(batch=3, h_q=G * h_kv, h_kv=h_kv, ctx=16 * 70 + 9,
+                         k=10, needles=0, seed=80 + G)
+    wl = W.generate(spec, "cpu")
+    d = Dev(wl)
+    kc, _, pt, _ = host(wl)
+    lens = [16 * 70 + 9, 16 * 3, 0]
+    batch, max_pages = pt.shape
+    q = wl.queries[0]
+    ex_o = O.exact_store(q.float().numpy(), kc, pt, lens, h_kv)
+    sc = torch.full((batch, h_kv, G, max_pages), 7.0, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.locks_exact_page_scores(q.to(DEV), d.k_cache, d.page_table, i32(lens),
+                              sc, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    s = sc.cpu().numpy()
+    for b in range(batch):
+        nf = lens[b] // 16
+        assert np.abs(s[b, :, :, :nf] - ex_o[b, :, :, :nf]).max(initial=0) \
+            <= S_TOL
+        assert (s[b, :, :, nf:] == 7.0).all()
+    ws = B.new_workspace(batch, spec.h_q, h_kv, max_pages, spec.k, DEV)
+    idx = torch.zeros(batch, h_kv, spec.k, dtype=torch.int32, device=DEV)
+    B.locks_select_pages(sc, i32(lens), spec.h_q, spec.k, idx, ws)
+    torch.cuda.synchronize()
+    ig = idx.cpu().numpy()
+    io = O.select_store(ex_o, lens, spec.k)
+    for b in range(batch):
+        for h in range(h_kv):
+            ok, _ = selection_agrees(ig[b, h], io[b, h], ex_o[b, h], lens[b],
+                                     spec.k, 1e-3)
+            assert ok, (b, h)
+
+
 # ---------------------------------------------------------------------------
 # select (Eq.(5) + sink/recent) from identical scores
 # ---------------------------------------------------------------------------
