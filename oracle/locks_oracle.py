@@ -361,6 +361,51 @@ def select_one(s_hat_g, seq_len, k):
     return sorted([0, n - 1] + top.tolist())
 
 
+# GQA merge rules of the notes' §4.2 design discussion and §6 ablation:
+# share-average (the shipped rule, Eq.(5)), group-max (pages any head of the
+# group gives a large mass fraction: the largest of the heads' fractions)
+# and group-mass (the group's pooled page mass: the sum over heads of
+# exp(s_hat), without per-head normalisation).  Per-head selection (each
+# query head its own set) is select_one on that head alone.
+MERGE_RULES = ("share_average", "group_max", "group_mass")
+
+
+def merge_key(s_hat_g, n_full, rule):
+    """Per-page ranking value of a merge rule, [n_full] (monotone in the
+    rule's pooled quantity)."""
+    s = np.asarray(s_hat_g, np.float64)[:, :n_full]
+    if rule == "share_average":
+        return mass_fractions(s, n_full).mean(axis=0)
+    if rule == "group_max":
+        return mass_fractions(s, n_full).max(axis=0)
+    if rule == "group_mass":
+        return logsumexp(s, axis=0)
+    raise ValueError(rule)
+
+
+def select_one_rule(s_hat_g, seq_len, k, rule):
+    """select_one with the candidates ranked by a merge rule's key (ties to
+    the lower page)."""
+    n = -(-int(seq_len) // PAGE)
+    if n == 0:
+        return []
+    if n <= k:
+        return list(range(n))
+    nf = int(seq_len) // PAGE
+    key = merge_key(s_hat_g, nf, rule)
+    cand = np.arange(1, n - 1)
+    order = np.lexsort((cand, -key[cand]))
+    return sorted([0, n - 1] + cand[order[:k - 2]].tolist())
+
+
+def head_coverage(s_exact_g, pages, n_full):
+    """gamma_g(S) = sum_{j in S} m_g(j) for every head g of the group: the
+    exact attention mass over full pages that S keeps, [G]."""
+    m = mass_fractions(s_exact_g, n_full)
+    sel = [j for j in pages if j < n_full]
+    return m[:, sel].sum(axis=1)
+
+
 def select_store(s_hat, seq_lens, k):
     """idx [batch][h_kv][k] int32, ascending, -1 padded."""
     batch, h_kv = s_hat.shape[:2]

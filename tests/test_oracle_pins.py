@@ -226,6 +226,69 @@ def test_exact_store_brute_force():
                         assert np.isnan(ex[b, h, g, j])
 
 
+def _brute_rule_select(s, L, k, rule):
+    """Top-(k-2) subset by brute force with the rule's per-page value
+    computed by plain loops (ties: lexicographically smallest pages)."""
+    n, nf, G = -(-L // 16), L // 16, len(s)
+    if n <= k:
+        return list(range(n))
+    z = [sum(math.exp(s[g][jj]) for jj in range(nf)) for g in range(G)]
+    val = []
+    for j in range(nf):
+        fr = [math.exp(s[g][j]) / z[g] for g in range(G)]
+        if rule == "share_average":
+            val.append(sum(fr) / G)
+        elif rule == "group_max":
+            val.append(max(fr))
+        else:
+            val.append(math.log(sum(math.exp(s[g][j]) for g in range(G))))
+    best, best_key = None, None
+    for sub in itertools.combinations(range(1, n - 1), k - 2):
+        vals = sorted((val[j] for j in sub), reverse=True)
+        key = (tuple(vals), tuple(-j for j in sub))
+        if best_key is None or key > best_key:
+            best, best_key = sub, key
+    return sorted([0, n - 1] + list(best))
+
+
+@pytest.mark.parametrize("rule", O.MERGE_RULES)
+def test_merge_rules_match_brute_force(rule):
+    rng = _rng(61)
+    for trial in range(20):
+        G = int(rng.integers(1, 5))
+        n = int(rng.integers(3, 10))
+        L = 16 * n - int(rng.integers(0, 2)) * int(rng.integers(1, 15))
+        k = int(rng.integers(2, n + 1))
+        s = rng.normal(0, 2, (G, n))
+        assert O.select_one_rule(s, L, k, rule) == \
+            _brute_rule_select(s.tolist(), L, k, rule), (trial, rule)
+
+
+def test_share_average_maximises_group_coverage():
+    """The notes' Corollary 3 (§4.2 design discussion): among selections
+    shared by the group, ranking by the share-average of the exact masses
+    maximises the group-average coverage; per-head selection bounds every
+    head's coverage from above; with G = 1 the rules coincide."""
+    rng = _rng(62)
+    for trial in range(40):
+        G = int(rng.integers(2, 6))
+        n = int(rng.integers(6, 30))
+        k = int(rng.integers(3, n))
+        s = rng.normal(0, 2.5, (G, n)) + rng.normal(0, 1, (1, n))
+        cov = {r: O.head_coverage(s, O.select_one_rule(s, 16 * n, k, r), n)
+               for r in O.MERGE_RULES}
+        for r in O.MERGE_RULES:
+            assert cov["share_average"].mean() >= cov[r].mean() - 1e-12
+        for g in range(G):
+            own = O.head_coverage(s[g:g + 1],
+                                  O.select_one(s[g:g + 1], 16 * n, k), n)[0]
+            for r in O.MERGE_RULES:
+                assert own >= cov[r][g] - 1e-12
+    s1 = rng.normal(size=(1, 25))
+    sels = {tuple(O.select_one_rule(s1, 16 * 25, 7, r)) for r in O.MERGE_RULES}
+    assert len(sels) == 1
+
+
 def test_carrier_retention_counts():
     idx = np.array([[[0, 3, 9, -1]], [[0, 1, 2, 7]]])
     car = np.array([[[3, 5]], [[7, -1]]])
