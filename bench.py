@@ -201,6 +201,10 @@ def selection_quality(B, wl, store, scores, ws, lens, k, h_q, n_records,
     n_car = 0
     err_max, err_sum, err_cnt, p99 = 0.0, 0.0, 0, []
     times = []
+    rules = ("share_average", "group_max", "group_mass", "per_head")
+    # per-head selection treats every query head as its own group
+    ws_ph = B.new_workspace(batch, h_q, h_q, max_pages, k, dev)
+    coverage = {r: [] for r in rules}
     e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
     n_steps = min(n_steps, wl.queries.shape[0])
     for i in range(n_steps):
@@ -221,6 +225,28 @@ def selection_quality(B, wl, store, scores, ws, lens, k, h_q, n_records,
             p99.append(float(torch.kthvalue(
                 d.cpu(), max(1, int(0.99 * d.numel()))).values))
         n_car += int((needles >= 0).sum())
+        # exact mass fractions of every full page, per head
+        mass = torch.zeros_like(ex)
+        for b in range(batch):
+            nf = lens[b] // 16
+            if nf:
+                mass[b, :, :, :nf] = torch.softmax(ex[b, :, :, :nf].double(),
+                                                   -1).float()
+        for rule in rules:
+            idx = torch.empty(batch, h_kv, k, dtype=torch.int32, device=dev)
+            if rule == "per_head":
+                idx = torch.empty(batch, h_q, k, dtype=torch.int32,
+                                  device=dev)
+                B.locks_select_pages(scores.view(batch, h_q, 1, max_pages),
+                                     wl.seq_lens, h_q, k, idx, ws_ph)
+                idx = idx.view(batch, h_kv, G, k)
+            else:
+                B.locks_select_pages_merge(scores, wl.seq_lens, h_q, k, rule,
+                                           idx, ws)
+                idx = idx[:, :, None, :].expand(batch, h_kv, G, k)
+            valid = idx >= 0
+            cov = torch.gather(mass, 3, idx.clamp(min=0).long())
+            coverage[rule].append((cov * valid).sum(-1))     # [b][h][G]
         for kk in sweep:
             for src, hits in ((scores, hit_l), (ex, hit_e)):
                 idx = torch.empty(batch, h_kv, kk, dtype=torch.int32,
@@ -229,7 +255,15 @@ def selection_quality(B, wl, store, scores, ws, lens, k, h_q, n_records,
                 kept = (idx[:, :, None, :] == needles[:, :, :, None]).any(-1)
                 hits[kk] += int((kept & (needles >= 0)).sum())
     assert B.locks_read_status(ws) == 0, "quality pass reported an error"
+    assert B.locks_read_status(ws_ph) == 0, "quality pass reported an error"
     ms = statistics.mean(times)
+    merge = {}
+    for r in rules:
+        c = torch.stack(coverage[r])                        # [steps][b][h][G]
+        flat = c.flatten().double()
+        merge[r] = {"mean": round(float(flat.mean()), 4),
+                    "worst_head": round(float(c.min(-1).values.mean()), 4),
+                    "p5": round(float(torch.quantile(flat, 0.05)), 4)}
     return {
         "budget_pages": sweep,
         "carrier_retention": {
@@ -237,6 +271,10 @@ def selection_quality(B, wl, store, scores, ws, lens, k, h_q, n_records,
             "exact_mass": [round(hit_e[kk] / max(1, n_car), 4)
                            for kk in sweep]},
         "carrier_pages": n_car // n_steps, "steps": n_steps,
+        "gqa_merge_coverage": {"budget_pages": k, "rules": merge,
+                               "note": "exact attention mass kept per "
+                                       "query head, selections from the "
+                                       "summaries' scores"},
         "score_error_vs_exact": {"max": round(err_max, 4),
                                  "mean": round(err_sum / max(1, err_cnt), 5),
                                  "p99_per_sequence_max": round(max(p99), 4)},

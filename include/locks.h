@@ -79,6 +79,16 @@ typedef enum {
 #define LOCKS_DEV_BAD_PAIR 0x8    /* build pair outside batch/max_pages   */
 #define LOCKS_DEV_TIMEOUT 0x10    /* an on-chip copy wait gave up         */
 
+/* GQA merge rules of the selection (LOCKS reading notes §4.2 design
+ * discussion and the §6 ablation).  The shipped rule is the share-average
+ * of Eq.(5); group-max ranks pages by the largest mass fraction any head of
+ * the group gives them; group-mass by the group's pooled unnormalised page
+ * mass sum_g exp(s_hat[g][j]).  Per-head selection (each query head its own
+ * page set) needs no rule: call locks_select_pages with h_kv = h_q. */
+#define LOCKS_MERGE_SHARE_AVERAGE 0
+#define LOCKS_MERGE_GROUP_MAX 1
+#define LOCKS_MERGE_GROUP_MASS 2
+
 #define LOCKS_PAGE_TOKENS 16
 #define LOCKS_HEAD_DIM 128
 #define LOCKS_RANK 8
@@ -233,6 +243,19 @@ locks_status_t locks_select_pages(const float *scores, const int32_t *seq_lens,
                                   int k, int32_t *idx_out, void *workspace,
                                   size_t workspace_bytes,
                                   locks_stream_t stream);
+
+/* locks_select_pages with the candidates ranked by another GQA merge rule
+ * (LOCKS_MERGE_*; LOCKS_MERGE_SHARE_AVERAGE is locks_select_pages itself).
+ * Same arguments, layouts and workspace; the sink and recent pages and the
+ * tie rule are unchanged.  Returns LOCKS_ERR_INVALID_ARG for an unknown
+ * rule. */
+locks_status_t locks_select_pages_merge(const float *scores,
+                                        const int32_t *seq_lens, int batch,
+                                        int h_q, int h_kv, int max_pages,
+                                        int k, int rule, int32_t *idx_out,
+                                        void *workspace,
+                                        size_t workspace_bytes,
+                                        locks_stream_t stream);
 
 /* Attention over the selected pages, LOCKS reading notes §2 (fetch full
  * K/V only for the selected pages, then standard softmax attention for all

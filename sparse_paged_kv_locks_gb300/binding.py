@@ -56,6 +56,8 @@ _SIGS = {
     "locks_score_pages": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "locks_select_pages": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ,
                                 _P]),
+    "locks_select_pages_merge": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
+                                      _SZ, _P]),
     "locks_exact_page_scores": (_I, [_P, _P, _I64, _P, _P, _I, _I, _I, _I,
                                      _P, _P, _P]),
     "locks_sparse_decode": (_I, [_P, _P, _P, _I64, _P, _P, _P, _I, _I, _I, _I,
@@ -276,6 +278,30 @@ def locks_select_pages(scores, seq_lens, h_q, k, idx_out, workspace,
     _check("locks_select_pages", lib().locks_select_pages(
         _ptr(scores), _ptr(seq_lens), batch, h_q, h_kv, max_pages, k,
         _ptr(idx_out), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+MERGE_SHARE_AVERAGE, MERGE_GROUP_MAX, MERGE_GROUP_MASS = 0, 1, 2
+MERGE_RULES = {"share_average": MERGE_SHARE_AVERAGE,
+               "group_max": MERGE_GROUP_MAX, "group_mass": MERGE_GROUP_MASS}
+
+
+def locks_select_pages_merge(scores, seq_lens, h_q, k, rule, idx_out,
+                             workspace, stream=None):
+    """locks_select_pages with another GQA merge rule (name or code)."""
+    rule = MERGE_RULES.get(rule, rule)
+    _req(scores, "scores", torch.float32, 4)
+    _req(seq_lens, "seq_lens", torch.int32, 1)
+    _req(idx_out, "idx_out", torch.int32, 3)
+    _req(workspace, "workspace", torch.uint8, 1)
+    batch, h_kv, G, max_pages = scores.shape
+    if G * h_kv != h_q:
+        raise ValueError("scores must be [batch][h_kv][h_q/h_kv][max_pages]")
+    if tuple(idx_out.shape) != (batch, h_kv, k) or seq_lens.numel() != batch:
+        raise ValueError("idx_out must be [batch][h_kv][k]")
+    _check("locks_select_pages_merge", lib().locks_select_pages_merge(
+        _ptr(scores), _ptr(seq_lens), batch, h_q, h_kv, max_pages, k,
+        int(rule), _ptr(idx_out), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
 
 
 def locks_sparse_decode(q, k_cache, v_cache, page_table, seq_lens, idx, k,

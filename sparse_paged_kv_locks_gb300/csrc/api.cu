@@ -150,8 +150,9 @@ locks_status_t locks_score_select(const void *q, const void *summaries,
   cudaError_t e = launch_score(q, summaries, seq_lens, batch, h_kv, G,
                                max_pages, s_hat, status, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail_cuda(e);
-  e = launch_select(s_hat, seq_lens, batch, h_kv, G, max_pages, k, idx_out,
-                    keys, status, (cudaStream_t)stream);
+  e = launch_select(s_hat, seq_lens, batch, h_kv, G, max_pages, k,
+                    LOCKS_MERGE_SHARE_AVERAGE, idx_out, keys, status,
+                    (cudaStream_t)stream);
   return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
 }
 
@@ -194,11 +195,16 @@ locks_status_t locks_exact_page_scores(
   return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
 }
 
-locks_status_t locks_select_pages(const float *scores, const int32_t *seq_lens,
-                                  int batch, int h_q, int h_kv, int max_pages,
-                                  int k, int32_t *idx_out, void *workspace,
-                                  size_t workspace_bytes,
-                                  locks_stream_t stream) {
+locks_status_t locks_select_pages_merge(const float *scores,
+                                        const int32_t *seq_lens, int batch,
+                                        int h_q, int h_kv, int max_pages,
+                                        int k, int rule, int32_t *idx_out,
+                                        void *workspace,
+                                        size_t workspace_bytes,
+                                        locks_stream_t stream) {
+  if (rule != LOCKS_MERGE_SHARE_AVERAGE && rule != LOCKS_MERGE_GROUP_MAX &&
+      rule != LOCKS_MERGE_GROUP_MASS)
+    return LOCKS_ERR_INVALID_ARG;
   locks_status_t st = check_select_args(batch, h_q, h_kv, max_pages, k,
                                         seq_lens, idx_out, workspace);
   if (st != LOCKS_OK) return st;
@@ -211,9 +217,20 @@ locks_status_t locks_select_pages(const float *scores, const int32_t *seq_lens,
   int32_t *status = reinterpret_cast<int32_t *>(ws);
   uint32_t *keys = reinterpret_cast<uint32_t *>(
       ws + kWsHeader + round_up((size_t)batch * h_kv * G * max_pages * 4, 256));
-  cudaError_t e = launch_select(scores, seq_lens, batch, h_kv, G, max_pages, k,
-                                idx_out, keys, status, (cudaStream_t)stream);
+  cudaError_t e =
+      launch_select(scores, seq_lens, batch, h_kv, G, max_pages, k, rule,
+                    idx_out, keys, status, (cudaStream_t)stream);
   return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
+}
+
+locks_status_t locks_select_pages(const float *scores, const int32_t *seq_lens,
+                                  int batch, int h_q, int h_kv, int max_pages,
+                                  int k, int32_t *idx_out, void *workspace,
+                                  size_t workspace_bytes,
+                                  locks_stream_t stream) {
+  return locks_select_pages_merge(scores, seq_lens, batch, h_q, h_kv,
+                                  max_pages, k, LOCKS_MERGE_SHARE_AVERAGE,
+                                  idx_out, workspace, workspace_bytes, stream);
 }
 
 locks_status_t locks_sparse_decode(

@@ -31,8 +31,8 @@ cudaError_t launch_score(const void *q, const void *summaries,
 
 cudaError_t launch_select(const float *scores, const int32_t *seq_lens,
                           int batch, int h_kv, int G, int max_pages, int k,
-                          int32_t *idx, uint32_t *keybuf, int32_t *status,
-                          cudaStream_t stream);
+                          int rule, int32_t *idx, uint32_t *keybuf,
+                          int32_t *status, cudaStream_t stream);
 
 cudaError_t launch_decode(const void *q, const void *k_cache,
                           const void *v_cache, int64_t num_phys,

@@ -105,8 +105,9 @@ template <bool SMEM_KEYS, int GT>
 __global__ void __launch_bounds__(kSelThreads, 2)
     select_kernel(const float *__restrict__ scores,
                   const int32_t *__restrict__ seq_lens, int h_kv, int G,
-                  int max_pages, int k, int32_t *__restrict__ idx,
-                  uint32_t *__restrict__ keybuf, int32_t *status) {
+                  int max_pages, int k, int rule,
+                  int32_t *__restrict__ idx, uint32_t *__restrict__ keybuf,
+                  int32_t *status) {
   extern __shared__ __align__(16) uint32_t sel_keys[];
   __shared__ float zs[kMaxGroup];
   __shared__ float red_m[32][kMaxGroup], red_s[32][kMaxGroup];
@@ -153,7 +154,9 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   constexpr int R = GT <= 4 ? 2 : 1;
   for (int i = tid; i < kRadixBins; i += blockDim.x) hist[0][i] = 0;
 
-  // Z_g: log2-sum-exp2 over the summarised pages [0, nf)
+  // Z_g: log2-sum-exp2 over the summarised pages [0, nf) (group-mass
+  // pooling does not normalise per head and skips it)
+  if (rule != LOCKS_MERGE_GROUP_MASS) {
   {
     float m[GT], s[GT];
 #pragma unroll
@@ -214,9 +217,15 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     zs[tid] = m + lg2_fast(s);
   }
   __syncthreads();
+  } else {
+    if (tid < G) zs[tid] = 0.f;
+    __syncthreads();
+  }
 
-  // share-average key of page j (candidates 1..n-2):
-  // log2 sum_g 2^(s_gj - Z_g), each term <= 1 since Z_g bounds every score
+  // key of page j (candidates 1..n-2), in base 2: share-average
+  // log2 sum_g 2^(s_gj - Z_g) (each term <= 1 since Z_g bounds every
+  // score), group-mass log2 sum_g 2^(s_gj) (Z_g = 0 above), group-max
+  // max_g (s_gj - Z_g)
   uint32_t kmin = 0xffffffffu, kmax = 0u;
   float zreg[GT];
 #pragma unroll
@@ -237,14 +246,23 @@ __global__ void __launch_bounds__(kSelThreads, 2)
         const int j = j0 + u;
         kq[u] = 0u;
         if (j < 1 || j > n - 2) continue;
-        float sum = 0.f;
-#pragma unroll
-        for (int g = 0; g < GT; ++g)
-          if (g < G) sum += ex2_fast(x[r][g][u] * kLog2e - zreg[g]);
         float key;
-        if (sum > 0.f) {
+        float sum = 0.f;
+        if (rule == LOCKS_MERGE_GROUP_MAX) {
+          key = -INFINITY;
+#pragma unroll
+          for (int g = 0; g < GT; ++g)
+            if (g < G) key = fmaxf(key, x[r][g][u] * kLog2e - zreg[g]);
+        } else {
+#pragma unroll
+          for (int g = 0; g < GT; ++g)
+            if (g < G) sum += ex2_fast(x[r][g][u] * kLog2e - zreg[g]);
+        }
+        if (rule == LOCKS_MERGE_GROUP_MAX) {
+        } else if (sum > 0.f && sum < INFINITY) {
           key = lg2_fast(sum);
-        } else {  // every term underflowed: subtract the largest first
+        } else {  // every term underflowed (or, pooling raw masses,
+                  // overflowed): subtract the largest first
           float m = -INFINITY;
 #pragma unroll
           for (int g = 0; g < GT; ++g)
@@ -430,8 +448,8 @@ constexpr int kSelSmemKeys = 32 * 1024;   // candidate keys held on chip
 
 cudaError_t launch_select(const float *scores, const int32_t *seq_lens,
                           int batch, int h_kv, int G, int max_pages, int k,
-                          int32_t *idx, uint32_t *keybuf, int32_t *status,
-                          cudaStream_t stream) {
+                          int rule, int32_t *idx, uint32_t *keybuf,
+                          int32_t *status, cudaStream_t stream) {
   dim3 grid(h_kv, batch);
   const bool on_chip = max_pages <= kSelSmemKeys;
   const size_t smem = on_chip ? (size_t)((max_pages + 3) & ~3) * 4 : 0;
@@ -440,7 +458,8 @@ cudaError_t launch_select(const float *scores, const int32_t *seq_lens,
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmemKeys * 4);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, grid, dim3(kSelThreads), smem, stream, scores,
-                      seq_lens, h_kv, G, max_pages, k, idx, keybuf, status);
+                      seq_lens, h_kv, G, max_pages, k, rule, idx, keybuf,
+                      status);
   };
   const int gt = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : G <= 8 ? 8 : 16;
   if (on_chip) {

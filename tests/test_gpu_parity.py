@@ -629,6 +629,58 @@ def test_device_status_flags():
     assert B.locks_read_status(ws) == B.DEV_BAD_PAGE_ID
 
 
+@pytest.mark.parametrize("rule", ["share_average", "group_max",
+                                  "group_mass", "per_head"])
+@pytest.mark.parametrize("G", [4, 8])
+def test_merge_rules_match_oracle(rule, G):
+    """GQA merge rules of the selection on identical scores; per-head
+    selection is the selection kernel with every query head as its own
+    group."""
+    rng = np.random.default_rng(100 + G)
+    batch, h_kv, max_pages, k = 5, 2, 400, 14
+    lens = [16 * 400, 16 * 123 + 7, 16 * 9, 16 * 250, 16 * 16]
+    scores = (rng.normal(0, 3, (batch, h_kv, G, max_pages)) +
+              rng.normal(0, 4, (batch, h_kv, 1, max_pages))).astype(np.float32)
+    sd = torch.from_numpy(scores).to(DEV)
+    if rule == "per_head":
+        hq = h_kv * G
+        ws = B.new_workspace(batch, hq, hq, max_pages, k, DEV)
+        idx = torch.zeros(batch, hq, k, dtype=torch.int32, device=DEV)
+        B.locks_select_pages(sd.view(batch, hq, 1, max_pages), i32(lens), hq,
+                             k, idx, ws)
+        s_rows = scores.reshape(batch, hq, 1, max_pages).astype(np.float64)
+        orc = lambda b, h: O.select_one(s_rows[b, h], lens[b], k)   # noqa
+        key = lambda b, h, nf: np.log(O.share_average(s_rows[b, h], nf))  # noqa
+        n_rows = hq
+    else:
+        ws = B.new_workspace(batch, h_kv * G, h_kv, max_pages, k, DEV)
+        idx = torch.zeros(batch, h_kv, k, dtype=torch.int32, device=DEV)
+        B.locks_select_pages_merge(sd, i32(lens), h_kv * G, k, rule, idx, ws)
+        s64 = scores.astype(np.float64)
+        orc = lambda b, h: O.select_one_rule(s64[b, h], lens[b], k, rule)  # noqa
+        key = lambda b, h, nf: (O.merge_key(s64[b, h], nf, rule)   # noqa
+                                if rule == "group_mass" else
+                                np.log(O.merge_key(s64[b, h], nf, rule)))
+        n_rows = h_kv
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == 0
+    ig = idx.cpu().numpy()
+    for b in range(batch):
+        n = -(-lens[b] // 16)
+        for h in range(n_rows):
+            got = set(int(x) for x in ig[b, h] if x >= 0)
+            want = set(orc(b, h))
+            if got == want:
+                continue
+            lk = key(b, h, lens[b] // 16)
+            cand = np.arange(1, n - 1)
+            order = cand[np.lexsort((cand, -lk[cand]))]
+            edge = lk[order[k - 3]]
+            for p in got ^ want:
+                assert p not in (0, n - 1) and abs(lk[p] - edge) <= 1e-4, \
+                    (rule, b, h, p)
+
+
 @pytest.mark.parametrize("G,max_pages", [(8, 300), (16, 97), (4, 33001),
                                          (2, 33004)])
 def test_select_group_sizes_and_long_tables(G, max_pages):
