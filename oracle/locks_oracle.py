@@ -155,7 +155,8 @@ def quantize_summary(mu32, V32, C32):
 def dequantize(q):
     """(mu_hat [..., d], V_hat [..., d, r], C_hat [..., B, r]) in float64."""
     mu = q["smu"].astype(np.float64)[..., None] * q["mu8"].astype(np.float64)
-    V = q["sV"].astype(np.float64)[..., None, :] * q["V4"].astype(np.float64)
+    Vc = q["V4"] if "V4" in q else q["Vq"]
+    V = q["sV"].astype(np.float64)[..., None, :] * Vc.astype(np.float64)
     C = q["sC"].astype(np.float64)[..., :, None] * q["C8"].astype(np.float64)
     return mu, V, C
 
@@ -168,6 +169,95 @@ def build_page(keys_bf16_as_f32: np.ndarray):
     q = quantize_summary(centroid_f32(keys_bf16_as_f32),
                          s["V"].astype(np.float32), s["C"].astype(np.float32))
     return q, s
+
+
+# ----------------------------------------------------------------------------
+# Rank / precision variants (notes §6 ablation: "秩与量化精度" -- int8, int4
+# and int2 bases at several ranks).  Same quantiser readings as the shipped
+# int4 basis, with qmax = 2^(bits-1) - 1 for the basis codes (1 for int2, 7
+# for int4, 127 for int8); coefficients and centroid stay int8.
+# ----------------------------------------------------------------------------
+VARIANT_RANKS = (4, 8, 12, 15)
+VARIANT_BITS = (2, 4, 8)
+
+
+def quantize_variant(mu32, V32, C32, vbits):
+    q = quantize_summary(mu32, np.zeros(np.shape(V32)[:-2] + (1, 1),
+                                        np.float32), C32)
+    qv = (1 << (vbits - 1)) - 1
+    V32 = np.asarray(V32, np.float32)
+    sV = _scale(np.abs(V32).max(axis=-2), qv)
+    return dict(Vq=_codes(V32, sV[..., None, :], qv), C8=q["C8"],
+                mu8=q["mu8"], sV=sV, sC=q["sC"], smu=q["smu"], vbits=vbits)
+
+
+def build_page_variant(keys_bf16_as_f32, r, vbits):
+    """Algorithm 1 at rank r with a `vbits`-bit basis (full pages)."""
+    s = page_summary(keys_bf16_as_f32, r)
+    return quantize_variant(centroid_f32(keys_bf16_as_f32),
+                            s["V"].astype(np.float32),
+                            s["C"].astype(np.float32), vbits), s
+
+
+def variant_layout(r, vbits):
+    """Byte offsets of a variant record (include/locks.h, variant records):
+    basis codes [128][r] d-major, bit-packed little-endian; int8 C [16][r];
+    int8 mu [128]; fp16 sV [r], sC [16], smu; 16-byte stride."""
+    off = {"V": 0}
+    off["C"] = 16 * r * vbits
+    off["MU"] = off["C"] + 16 * r
+    off["SV"] = off["MU"] + HEAD_DIM
+    off["SC"] = off["SV"] + 2 * r
+    off["SMU"] = off["SC"] + 2 * PAGE
+    off["payload"] = off["SMU"] + 2
+    off["stride"] = -(-off["payload"] // 16) * 16
+    return off
+
+
+def encode_variant(q, r, vbits):
+    off = variant_layout(r, vbits)
+    Vq = np.asarray(q["Vq"], np.int64)
+    lead = Vq.shape[:-2]
+    out = np.zeros(lead + (off["stride"],), np.uint8)
+    codes = (Vq.reshape(lead + (-1,)) & ((1 << vbits) - 1)).astype(np.uint64)
+    per = 8 // vbits
+    codes = codes.reshape(lead + (-1, per))
+    byte = np.zeros(lead + (codes.shape[-2],), np.uint64)
+    for t in range(per):
+        byte |= codes[..., t] << np.uint64(t * vbits)
+    out[..., off["V"]:off["C"]] = byte.astype(np.uint8)
+    out[..., off["C"]:off["MU"]] = np.asarray(q["C8"], np.int8).reshape(
+        lead + (-1,)).view(np.uint8)
+    out[..., off["MU"]:off["SV"]] = np.asarray(q["mu8"], np.int8).view(
+        np.uint8)
+    out[..., off["SV"]:off["SC"]] = np.ascontiguousarray(
+        np.asarray(q["sV"], np.float16)).view(np.uint8)
+    out[..., off["SC"]:off["SMU"]] = np.ascontiguousarray(
+        np.asarray(q["sC"], np.float16)).view(np.uint8)
+    out[..., off["SMU"]:off["payload"]] = np.ascontiguousarray(
+        np.asarray(q["smu"], np.float16)[..., None]).view(np.uint8)
+    return out
+
+
+def decode_variant(rec, r, vbits):
+    off = variant_layout(r, vbits)
+    rec = np.ascontiguousarray(np.asarray(rec, np.uint8))
+    lead = rec.shape[:-1]
+    byte = rec[..., off["V"]:off["C"]].astype(np.int64)
+    per = 8 // vbits
+    mask = (1 << vbits) - 1
+    codes = np.stack([(byte >> (t * vbits)) & mask for t in range(per)], -1)
+    codes = codes.reshape(lead + (HEAD_DIM, r))
+    codes = np.where(codes >= (1 << (vbits - 1)), codes - (1 << vbits), codes)
+    return dict(
+        Vq=codes.astype(np.int8),
+        C8=rec[..., off["C"]:off["MU"]].copy().view(np.int8).reshape(
+            lead + (PAGE, r)),
+        mu8=rec[..., off["MU"]:off["SV"]].copy().view(np.int8),
+        sV=rec[..., off["SV"]:off["SC"]].copy().view(np.float16),
+        sC=rec[..., off["SC"]:off["SMU"]].copy().view(np.float16),
+        smu=rec[..., off["SMU"]:off["payload"]].copy().view(np.float16)[..., 0],
+        vbits=vbits)
 
 
 # ----------------------------------------------------------------------------

@@ -289,6 +289,57 @@ def test_share_average_maximises_group_coverage():
     assert len(sels) == 1
 
 
+def test_variant_record_bytes_by_hand():
+    """Variant record codec against bytes written out by hand: rank 4 with
+    a 2-bit basis packs the codes of dimension 0 (components 0..3) into byte
+    0, two bits each from the low end, two's complement."""
+    r, vb = 4, 2
+    off = O.variant_layout(r, vb)
+    assert (off["C"], off["MU"], off["SV"], off["SC"], off["SMU"],
+            off["payload"], off["stride"]) == (128, 192, 320, 328, 360, 362,
+                                               368)
+    Vq = np.zeros((128, r), np.int8)
+    Vq[0] = [1, -1, 0, 1]          # 0b01, 0b11, 0b00, 0b01
+    Vq[1] = [-1, -1, -1, -1]       # all 0b11
+    q = dict(Vq=Vq, C8=np.arange(-32, 32, dtype=np.int8).reshape(16, r),
+             mu8=np.full(128, -3, np.int8),
+             sV=np.array([1, 2, 0.5, 0.25], np.float16),
+             sC=np.full(16, 0.125, np.float16), smu=np.float16(3.0))
+    rec = O.encode_variant(q, r, vb)
+    assert rec[0] == 0b01001101 and rec[1] == 0xFF and rec[2] == 0
+    assert rec[128] == 256 - 32 and rec[129] == 256 - 31     # C8 row 0
+    assert rec[192] == 253                                    # mu8[0] = -3
+    assert rec[320:322].tobytes() == np.float16(1).tobytes()  # sV[0]
+    assert rec[360:362].tobytes() == np.float16(3).tobytes()  # smu
+    d = O.decode_variant(rec, r, vb)
+    assert (d["Vq"] == Vq).all() and (d["C8"] == q["C8"]).all()
+
+
+def test_variant_r8_int4_is_the_shipped_summary():
+    """Rank 8 with a 4-bit basis quantises exactly as the shipped record
+    (same codes and scales, same page scores); finer basis bits reconstruct
+    the unquantised basis more closely."""
+    rng = _rng(71)
+    keys = _pages(rng, 20).astype(np.float32)
+    q8, _ = O.build_page(keys)
+    qv, _ = O.build_page_variant(keys, 8, 4)
+    for a, b in (("V4", "Vq"), ("C8", "C8"), ("mu8", "mu8")):
+        assert (q8[a] == qv[b]).all()
+    for a in ("sV", "sC", "smu"):
+        assert (np.asarray(q8[a]).view(np.uint16) ==
+                np.asarray(qv[a]).view(np.uint16)).all()
+    qh = rng.normal(size=(4, 128))
+    rec = O.decode_variant(O.encode_variant(qv, 8, 4), 8, 4)
+    assert np.array_equal(O.score_from_summaries(qh, *O.dequantize(q8)),
+                          O.score_from_summaries(qh, *O.dequantize(rec)))
+    err = {}
+    for vb in O.VARIANT_BITS:
+        q, s = O.build_page_variant(keys, 8, vb)
+        _, V, _ = O.dequantize(q)
+        err[vb] = np.abs(V - s["V"]).mean()
+    assert err[8] < err[4] < err[2]
+
+
 def test_carrier_retention_counts():
     idx = np.array([[[0, 3, 9, -1]], [[0, 1, 2, 7]]])
     car = np.array([[[3, 5]], [[7, -1]]])
