@@ -141,6 +141,49 @@ locks_status_t locks_build_summaries(
     void *summaries, float *tau_out, float *unquantised_out, int32_t *status,
     locks_stream_t stream);
 
+/* Rank / precision variants of the page summary (LOCKS reading notes §6
+ * ablation "rank and quantisation precision": int8, int4 and int2 bases at
+ * several ranks).  A variant record of rank r in {4, 8, 12, 15} with a
+ * basis of vbits in {2, 4, 8} bits holds, at byte offsets
+ *   0                basis codes [128][r], element (d, k) at index d*r + k,
+ *                    vbits bits each, packed little-endian from bit 0,
+ *                    two's complement (qmax = 2^(vbits-1) - 1)
+ *   16 r vbits       int8 C [16][r] row-major (c_i = row i)
+ *   + 16 r           int8 mu [128]
+ *   + 128            fp16 sV [r] (one scale per basis column)
+ *   + 2 r            fp16 sC [16] (one scale per coefficient row)
+ *   + 32             fp16 smu
+ * and zero padding to a 16-byte stride.  Quantiser as the shipped record
+ * (symmetric, fp16 scale = fp16_rn(absmax / qmax), codes rint(x / s)
+ * clamped).  The shipped 832-byte record carries the same values as the
+ * (r = 8, 4-bit) variant in a tensor-core layout; variants are for the
+ * ablation, scored on CUDA cores.
+ * locks_variant_record_bytes: the stride (0 for an unsupported pair). */
+size_t locks_variant_record_bytes(int rank, int vbits);
+
+/* Algorithm 1 at rank `rank` with a `vbits`-bit basis for the listed
+ * (seq_ids[i], page_ids[i]) pairs and every KV head, written to
+ *   records  [batch][h_kv][max_pages] variant records of
+ *            locks_variant_record_bytes(rank, vbits) bytes.
+ * Other arguments, status bits and errors as locks_build_summaries. */
+locks_status_t locks_build_variant(
+    const void *k_cache, int64_t num_phys_pages, int h_kv,
+    const int32_t *page_table, int batch, int max_pages,
+    const int32_t *seq_ids, const int32_t *page_ids, int n_pairs, int rank,
+    int vbits, void *records, float *tau_out, int32_t *status,
+    locks_stream_t stream);
+
+/* Eq.(4) page scores of every full page from variant records, in the
+ * layout of locks_score_pages (scores_out float [batch][h_kv][G][max_pages];
+ * entries of pages that are not full are left untouched).  Feed them to
+ * locks_select_pages for the variant's selection. */
+locks_status_t locks_score_variant(const void *q, const void *records,
+                                   int rank, int vbits,
+                                   const int32_t *seq_lens, int batch,
+                                   int h_q, int h_kv, int max_pages,
+                                   float *scores_out, int32_t *status,
+                                   locks_stream_t stream);
+
 /* Quantise and pack n given fp32 summaries into records with the same rule
  * as locks_build_summaries (the storage paragraph of §4.1).
  *   mu [n][128], basis [n][128][8] (V), coeffs [n][16][8] (C): float32

@@ -58,6 +58,11 @@ _SIGS = {
                                 _P]),
     "locks_select_pages_merge": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
                                       _SZ, _P]),
+    "locks_variant_record_bytes": (_SZ, [_I, _I]),
+    "locks_build_variant": (_I, [_P, _I64, _I, _P, _I, _I, _P, _P, _I, _I, _I,
+                                 _P, _P, _P, _P]),
+    "locks_score_variant": (_I, [_P, _P, _I, _I, _P, _I, _I, _I, _I, _P, _P,
+                                 _P]),
     "locks_exact_page_scores": (_I, [_P, _P, _I64, _P, _P, _I, _I, _I, _I,
                                      _P, _P, _P]),
     "locks_sparse_decode": (_I, [_P, _P, _P, _I64, _P, _P, _P, _I, _I, _I, _I,
@@ -262,6 +267,51 @@ def locks_exact_page_scores(q, k_cache, page_table, seq_lens, scores_out,
         _ptr(q), _ptr(k_cache), P, _ptr(page_table), _ptr(seq_lens), batch,
         h_q, h_kv, max_pages, _ptr(scores_out), _ptr(status),
         _stream(stream)))
+
+
+def locks_variant_record_bytes(rank, vbits) -> int:
+    return int(lib().locks_variant_record_bytes(rank, vbits))
+
+
+def new_variant_store(batch, h_kv, max_pages, rank, vbits, device="cuda"):
+    """Zeroed variant-record store [batch][h_kv][max_pages][stride] uint8."""
+    stride = locks_variant_record_bytes(rank, vbits)
+    if stride == 0:
+        raise ValueError(f"unsupported variant rank={rank} vbits={vbits}")
+    return torch.zeros(batch, h_kv, max_pages, stride, dtype=torch.uint8,
+                       device=device)
+
+
+def locks_build_variant(k_cache, page_table, seq_ids, page_ids, records,
+                        rank, vbits, tau_out=None, status=None, stream=None):
+    _req(k_cache, "k_cache", torch.bfloat16, 4)
+    _req(page_table, "page_table", torch.int32, 2)
+    _req(seq_ids, "seq_ids", torch.int32, 1)
+    _req(page_ids, "page_ids", torch.int32, 1)
+    _req(records, "records", torch.uint8, 4)
+    P, h_kv = k_cache.shape[:2]
+    batch, max_pages = page_table.shape
+    if records.shape[3] != locks_variant_record_bytes(rank, vbits):
+        raise ValueError("records stride does not match the variant")
+    _check("locks_build_variant", lib().locks_build_variant(
+        _ptr(k_cache), P, h_kv, _ptr(page_table), batch, max_pages,
+        _ptr(seq_ids), _ptr(page_ids), seq_ids.numel(), rank, vbits,
+        _ptr(records), _ptr(tau_out), _ptr(status), _stream(stream)))
+
+
+def locks_score_variant(q, records, rank, vbits, seq_lens, scores_out,
+                        status=None, stream=None):
+    _req(q, "q", torch.bfloat16, 3)
+    _req(records, "records", torch.uint8, 4)
+    _req(seq_lens, "seq_lens", torch.int32, 1)
+    _req(scores_out, "scores_out", torch.float32, 4)
+    batch, h_q, _ = q.shape
+    _, h_kv, max_pages, stride = records.shape
+    if stride != locks_variant_record_bytes(rank, vbits):
+        raise ValueError("records stride does not match the variant")
+    _check("locks_score_variant", lib().locks_score_variant(
+        _ptr(q), _ptr(records), rank, vbits, _ptr(seq_lens), batch, h_q,
+        h_kv, max_pages, _ptr(scores_out), _ptr(status), _stream(stream)))
 
 
 def locks_select_pages(scores, seq_lens, h_q, k, idx_out, workspace,

@@ -102,6 +102,57 @@ locks_status_t locks_build_summaries(
   return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
 }
 
+static bool variant_ok(int rank, int vbits) {
+  return (rank == 4 || rank == 8 || rank == 12 || rank == 15) &&
+         (vbits == 2 || vbits == 4 || vbits == 8);
+}
+
+size_t locks_variant_record_bytes(int rank, int vbits) {
+  return variant_ok(rank, vbits) ? variant_record_bytes(rank, vbits) : 0;
+}
+
+locks_status_t locks_build_variant(
+    const void *k_cache, int64_t num_phys_pages, int h_kv,
+    const int32_t *page_table, int batch, int max_pages,
+    const int32_t *seq_ids, const int32_t *page_ids, int n_pairs, int rank,
+    int vbits, void *records, float *tau_out, int32_t *status,
+    locks_stream_t stream) {
+  if (!variant_ok(rank, vbits)) return LOCKS_ERR_INVALID_ARG;
+  if (n_pairs < 0 || h_kv < 1 || batch < 1 || max_pages < 1 ||
+      num_phys_pages < 1)
+    return LOCKS_ERR_INVALID_ARG;
+  if (n_pairs == 0) return LOCKS_OK;
+  if (!k_cache || !page_table || !seq_ids || !page_ids || !records)
+    return LOCKS_ERR_INVALID_ARG;
+  cudaError_t e = launch_build_variant(
+      k_cache, num_phys_pages, h_kv, page_table, batch, max_pages, seq_ids,
+      page_ids, n_pairs, rank, vbits, records, tau_out, status,
+      (cudaStream_t)stream);
+  return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
+}
+
+locks_status_t locks_score_variant(const void *q, const void *records,
+                                   int rank, int vbits,
+                                   const int32_t *seq_lens, int batch,
+                                   int h_q, int h_kv, int max_pages,
+                                   float *scores_out, int32_t *status,
+                                   locks_stream_t stream) {
+  if (!variant_ok(rank, vbits)) return LOCKS_ERR_INVALID_ARG;
+  if (batch < 0 || max_pages < 1 || !heads_ok(h_q, h_kv))
+    return LOCKS_ERR_INVALID_ARG;
+  if (h_q / h_kv > kMaxGroup) return LOCKS_ERR_UNSUPPORTED;
+  if (batch > 65535 || h_kv > 65535 ||
+      (long long)max_pages * kPage > 0x7fffffffLL)
+    return LOCKS_ERR_UNSUPPORTED;
+  if (batch == 0) return LOCKS_OK;
+  if (!q || !records || !seq_lens || !scores_out) return LOCKS_ERR_INVALID_ARG;
+  cudaError_t e = launch_score_variant(q, records, rank, vbits, seq_lens,
+                                       batch, h_kv, h_q / h_kv, max_pages,
+                                       scores_out, status,
+                                       (cudaStream_t)stream);
+  return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
+}
+
 locks_status_t locks_pack_summaries(const float *mu, const float *basis,
                                     const float *coeffs, int n, void *records,
                                     locks_stream_t stream) {

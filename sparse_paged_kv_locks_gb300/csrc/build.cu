@@ -199,14 +199,14 @@ __device__ void write_record(const float (&V)[4][8], const float (&mu)[4],
   __syncwarp();
 }
 
-// Algorithm 1 on one page-head held as kx[token][4 dims of this lane]
-// (bf16 values widened to fp32).  Writes the record and returns tau (valid
-// on every lane).
-__device__ float summarize_page(float (&kx)[16][4], BuildSmem &sm,
-                                uint8_t *rec, int lane,
-                                float *unq = nullptr) {
+// Algorithm 1 up to the eigendecomposition, on one page-head held as
+// kx[token][4 dims of this lane] (bf16 values widened to fp32): centres kx
+// on the fp32 centroid mu (lane-owned entries), and leaves in sm the
+// eigenvectors U (columns), the eigenvalues lam (descending, clipped at
+// zero) and perm (column of U of the k-th eigenvalue).
+__device__ void page_eigen(float (&kx)[16][4], float (&mu)[4], BuildSmem &sm,
+                           int lane) {
   // Eq.(2): centroid (fp32, tokens summed in order, then /16) and deviations
-  float mu[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     float acc = 0.f;
@@ -320,8 +320,16 @@ __device__ float summarize_page(float (&kx)[16][4], BuildSmem &sm,
     sm.lam[rank] = fmaxf(li, 0.f);
   }
   __syncwarp();
-  // sign rule and per-component factors
-  if (lane < 8) {
+}
+
+// Sign rule and per-component factors of the first r components (lanes
+// < r): U column perm[k] is signed so its largest-magnitude entry is
+// positive (lowest index on exact ties); components with lam <= 1e-6 lam_1
+// are zeroed.  cv = sign / sigma (basis), cc = sign * sigma (coefficients).
+__device__ __forceinline__ void component_factors(const BuildSmem &sm, int r,
+                                                  int lane, float *cv,
+                                                  float *cc) {
+  if (lane < r) {
     const int col = sm.perm[lane];
     float best = -1.f;
     int bi = 0;
@@ -336,10 +344,22 @@ __device__ float summarize_page(float (&kx)[16][4], BuildSmem &sm,
     const float lam = sm.lam[lane], lam1 = sm.lam[0];
     const bool keep = lam1 > 0.f && lam > 1e-6f * lam1;
     const float sig = sqrtf(lam);
-    sm.cv[lane] = keep ? sg / sig : 0.f;
-    sm.cc[lane] = keep ? sg * sig : 0.f;
+    cv[lane] = keep ? sg / sig : 0.f;
+    cc[lane] = keep ? sg * sig : 0.f;
   }
   __syncwarp();
+}
+
+// Algorithm 1 on one page-head held as kx[token][4 dims of this lane]
+// (bf16 values widened to fp32).  Writes the record and returns tau (valid
+// on every lane).
+__device__ float summarize_page(float (&kx)[16][4], BuildSmem &sm,
+                                uint8_t *rec, int lane,
+                                float *unq = nullptr) {
+  float mu[4];
+  page_eigen(kx, mu, sm, lane);
+  // sign rule and per-component factors
+  component_factors(sm, kRank, lane, sm.cv, sm.cc);
   float tau = 0.f;
 #pragma unroll
   for (int k = kRank; k < 16; ++k) tau += sm.lam[k];
@@ -529,6 +549,153 @@ __global__ void append_kernel(const __nv_bfloat16 *__restrict__ k_new,
 }
 
 // --------------------------------------------------------------------------
+// rank / precision variants (notes §6 ablation): Algorithm 1 at rank R with
+// a `vbits`-bit basis, written as a variant record (include/locks.h):
+// basis codes [128][R] d-major, bit-packed little-endian; int8 C [16][R];
+// int8 mu; fp16 sV [R], sC [16], smu; zero padding to the 16-byte stride.
+// --------------------------------------------------------------------------
+struct VariantSmem {
+  float cv[16], cc[16];
+  float Cf[16][16];
+};
+
+__device__ __forceinline__ int variant_payload(int r, int vbits) {
+  return 16 * r * vbits + 16 * r + kDim + 2 * r + 2 * kPage + 2;
+}
+__device__ __forceinline__ int variant_stride(int r, int vbits) {
+  return (variant_payload(r, vbits) + 15) / 16 * 16;
+}
+
+template <int R>
+__device__ float summarize_variant(float (&kx)[16][4], BuildSmem &sm,
+                                   VariantSmem &vs, uint8_t *rec, int vbits,
+                                   int lane) {
+  float mu[4];
+  page_eigen(kx, mu, sm, lane);
+  component_factors(sm, R, lane, vs.cv, vs.cc);
+  float tau = 0.f;
+  for (int k = R; k < 16; ++k) tau += sm.lam[k];
+  // V = D^T U_R Sigma_R^{-1} (lane rows), C = U_R Sigma_R (shared)
+  float V[4][R];
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    const int col = sm.perm[k];
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float u = sm.U[i][col];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[j] = fmaf(kx[i][j], u, acc[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) V[j][k] = acc[j] * vs.cv[k];
+  }
+  for (int e = lane; e < 16 * R; e += 32) {
+    const int i = e / R, k = e - i * R;
+    vs.Cf[i][k] = sm.U[i][sm.perm[k]] * vs.cc[k];
+  }
+  __syncwarp();
+  const int off_c = 16 * R * vbits, off_mu = off_c + 16 * R;
+  const int off_sv = off_mu + kDim, off_sc = off_sv + 2 * R;
+  const int off_smu = off_sc + 2 * kPage;
+  const float qv = (float)((1 << (vbits - 1)) - 1);
+  const uint32_t cmask = (1u << vbits) - 1u;
+  // basis: one scale per column; this lane's 4 dims x R codes are bits
+  // [4R vbits lane, 4R vbits (lane + 1)) of the code array
+  uint32_t acc = 0;
+  int nbits = 0, pos = lane * R * vbits / 2;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      float a = 0.f;
+      if (j == 0) {  // scale of column k (same for every j)
+        a = fmaxf(fmaxf(fabsf(V[0][k]), fabsf(V[1][k])),
+                  fmaxf(fabsf(V[2][k]), fabsf(V[3][k])));
+        a = warp_max(a);
+        const __half h = quant_scale(a, qv);
+        if (lane == k) *reinterpret_cast<__half *>(rec + off_sv + 2 * k) = h;
+        vs.cv[k] = __half2float(h);  // reuse: per-column float scale
+      }
+      __syncwarp();
+      const int c = quant_code(V[j][k], vs.cv[k], (int)qv);
+      acc |= ((uint32_t)c & cmask) << nbits;
+      nbits += vbits;
+      if (nbits >= 8) {
+        rec[pos++] = (uint8_t)(acc & 0xFFu);
+        acc >>= 8;
+        nbits -= 8;
+      }
+    }
+  }
+  // centroid: one scale, int8 codes
+  {
+    float a = fmaxf(fmaxf(fabsf(mu[0]), fabsf(mu[1])),
+                    fmaxf(fabsf(mu[2]), fabsf(mu[3])));
+    a = warp_max(a);
+    const __half h = quant_scale(a, 127.f);
+    const float sc = __half2float(h);
+    if (lane == 0) *reinterpret_cast<__half *>(rec + off_smu) = h;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      rec[off_mu + 4 * lane + j] = (uint8_t)(int8_t)quant_code(mu[j], sc, 127);
+  }
+  // coefficients: one scale per row (token), int8 codes
+  if (lane < 16) {
+    float a = 0.f;
+    for (int k = 0; k < R; ++k) a = fmaxf(a, fabsf(vs.Cf[lane][k]));
+    const __half h = quant_scale(a, 127.f);
+    const float sc = __half2float(h);
+    *reinterpret_cast<__half *>(rec + off_sc + 2 * lane) = h;
+    for (int k = 0; k < R; ++k)
+      rec[off_c + lane * R + k] =
+          (uint8_t)(int8_t)quant_code(vs.Cf[lane][k], sc, 127);
+  }
+  const int pay = off_smu + 2, stride = variant_stride(R, vbits);
+  for (int b = pay + lane; b < stride; b += 32) rec[b] = 0;
+  __syncwarp();
+  return tau;
+}
+
+template <int R>
+__global__ void __launch_bounds__(32 * kBuildWarps)
+    build_variant_kernel(const __nv_bfloat16 *__restrict__ k_cache,
+                         int64_t num_phys, int h_kv,
+                         const int32_t *__restrict__ pt, int batch,
+                         int max_pages, const int32_t *__restrict__ seq_ids,
+                         const int32_t *__restrict__ page_ids, int n_pairs,
+                         int vbits, uint8_t *__restrict__ records,
+                         float *__restrict__ tau_out, int32_t *status) {
+  __shared__ BuildSmem smem[kBuildWarps];
+  __shared__ VariantSmem vsm[kBuildWarps];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const size_t stride = (size_t)variant_stride(R, vbits);
+  const long long total = (long long)n_pairs * h_kv;
+  for (long long w = (long long)blockIdx.x * kBuildWarps + wid; w < total;
+       w += (long long)gridDim.x * kBuildWarps) {
+    const int pair = (int)(w / h_kv), h = (int)(w % h_kv);
+    const int b = seq_ids[pair], pg = page_ids[pair];
+    if (b < 0 || b >= batch || pg < 0 || pg >= max_pages) {
+      if (lane == 0) set_status(status, LOCKS_DEV_BAD_PAIR);
+      continue;
+    }
+    const int phys = pt[(size_t)b * max_pages + pg];
+    if (phys < 0 || phys >= num_phys) {
+      if (lane == 0) set_status(status, LOCKS_DEV_BAD_PAGE_ID);
+      continue;
+    }
+    float kx[16][4];
+    load_page_keys(k_cache + ((size_t)phys * h_kv + h) * kPage * kDim, kx,
+                   lane);
+    uint8_t *rec =
+        records + (((size_t)b * h_kv + h) * max_pages + pg) * stride;
+    const float tau =
+        summarize_variant<R>(kx, smem[wid], vsm[wid], rec, vbits, lane);
+    if (tau_out && lane == 0) tau_out[w] = tau;
+  }
+}
+
+// --------------------------------------------------------------------------
 // launchers
 // --------------------------------------------------------------------------
 static int grid_for(long long warps, int warps_per_cta) {
@@ -549,6 +716,33 @@ cudaError_t launch_build(const void *k_cache, int64_t num_phys, int h_kv,
       static_cast<const __nv_bfloat16 *>(k_cache), num_phys, h_kv, pt, batch,
       max_pages, seq_ids, page_ids, n_pairs,
       static_cast<uint8_t *>(summaries), tau_out, unq_out, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_build_variant(const void *k_cache, int64_t num_phys,
+                                 int h_kv, const int32_t *pt, int batch,
+                                 int max_pages, const int32_t *seq_ids,
+                                 const int32_t *page_ids, int n_pairs,
+                                 int rank, int vbits, void *records,
+                                 float *tau_out, int32_t *status,
+                                 cudaStream_t stream) {
+  const long long warps = (long long)n_pairs * h_kv;
+  if (warps == 0) return cudaSuccess;
+  const int grid = grid_for(warps, kBuildWarps);
+  auto *kc = static_cast<const __nv_bfloat16 *>(k_cache);
+  auto *rec = static_cast<uint8_t *>(records);
+#define LOCKS_BUILD_VARIANT(R)                                              \
+  build_variant_kernel<R><<<grid, 32 * kBuildWarps, 0, stream>>>(           \
+      kc, num_phys, h_kv, pt, batch, max_pages, seq_ids, page_ids, n_pairs, \
+      vbits, rec, tau_out, status)
+  switch (rank) {
+    case 4: LOCKS_BUILD_VARIANT(4); break;
+    case 8: LOCKS_BUILD_VARIANT(8); break;
+    case 12: LOCKS_BUILD_VARIANT(12); break;
+    case 15: LOCKS_BUILD_VARIANT(15); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef LOCKS_BUILD_VARIANT
   return cudaGetLastError();
 }
 

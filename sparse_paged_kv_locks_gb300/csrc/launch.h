@@ -47,6 +47,22 @@ cudaError_t launch_exact(const void *q, const void *k_cache, int64_t num_phys,
                          int batch, int h_kv, int G, int max_pages,
                          float *scores, int32_t *status, cudaStream_t stream);
 
+cudaError_t launch_build_variant(const void *k_cache, int64_t num_phys,
+                                 int h_kv, const int32_t *pt, int batch,
+                                 int max_pages, const int32_t *seq_ids,
+                                 const int32_t *page_ids, int n_pairs,
+                                 int rank, int vbits, void *records,
+                                 float *tau_out, int32_t *status,
+                                 cudaStream_t stream);
+
+cudaError_t launch_score_variant(const void *q, const void *records,
+                                 int rank, int vbits,
+                                 const int32_t *seq_lens, int batch, int h_kv,
+                                 int G, int max_pages, float *scores,
+                                 int32_t *status, cudaStream_t stream);
+
+size_t variant_record_bytes(int rank, int vbits);
+
 int score_max_batch();
 int exact_max_batch();
 int decode_max_batch();

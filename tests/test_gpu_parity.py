@@ -344,6 +344,87 @@ def test_exact_page_scores_match_oracle(G, h_kv):
 
 
 # ---------------------------------------------------------------------------
+# rank / precision variants (notes §6 ablation)
+# ---------------------------------------------------------------------------
+def test_variant_r8_int4_build_equals_shipped_build():
+    """On the GPU, the (r = 8, 4-bit) variant record carries exactly the
+    shipped record's codes and scales (one eigensolver, one quantiser)."""
+    wl = W.generate(W.SPECS["tiny_4k"], "cpu")
+    d = Dev(wl)
+    _, _, pt, lens = host(wl)
+    store, _, _, seq, pg = gpu_build(d, lens)
+    batch, max_pages = pt.shape
+    h_kv = d.k_cache.shape[1]
+    var = B.new_variant_store(batch, h_kv, max_pages, 8, 4, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.locks_build_variant(d.k_cache, d.page_table, i32(seq), i32(pg), var, 8,
+                          4, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    a = O.decode_records(store.cpu().numpy()[seq, :, pg])
+    v = O.decode_variant(var.cpu().numpy()[seq, :, pg], 8, 4)
+    assert (a["V4"] == v["Vq"]).all() and (a["C8"] == v["C8"]).all()
+    assert (a["mu8"] == v["mu8"]).all()
+    for key in ("sV", "sC", "smu"):
+        assert (np.asarray(a[key]).view(np.uint16) ==
+                np.asarray(v[key]).view(np.uint16)).all()
+
+
+@pytest.mark.parametrize("rank,vbits", [(4, 2), (4, 8), (8, 2), (8, 8),
+                                        (12, 4), (15, 2), (15, 4), (15, 8)])
+def test_variant_build_and_score_match_oracle(rank, vbits):
+    wl = W.generate(W.SPECS["tiny_4k"], "cpu", steps=1)
+    d = Dev(wl)
+    kc, _, pt, lens = host(wl)
+    lens = [lens[0] - 5]                       # partial last page
+    seq, pg = full_pairs(lens)
+    batch, max_pages = pt.shape
+    h_kv, G = kc.shape[1], W.SPECS["tiny_4k"].group
+    var = B.new_variant_store(batch, h_kv, max_pages, rank, vbits, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.locks_build_variant(d.k_cache, d.page_table, i32(seq), i32(pg), var,
+                          rank, vbits, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    keys = kc[pt[seq, pg]]                                 # [n][h_kv][16][128]
+    qo, s = O.build_page_variant(keys, rank, vbits)
+    got = O.decode_variant(var.cpu().numpy()[seq, :, pg], rank, vbits)
+    # centroid bytes exact; basis codes equal up to eigenvector sign and a
+    # one-step rounding difference on well separated components
+    assert (got["mu8"] == qo["mu8"]).all() and (got["smu"] == qo["smu"]).all()
+    _, Vg, _ = O.dequantize(got)
+    sgn = np.sign(np.einsum("nhdk,nhdk->nhk", Vg, s["V"]))
+    sgn[sgn == 0] = 1
+    lam = s["lam"]
+    gap = np.minimum(np.concatenate([np.full(lam[..., :1].shape, np.inf),
+                                     lam[..., :rank - 1]], -1) - lam[..., :rank],
+                     lam[..., :rank] - lam[..., 1:rank + 1]) / lam[..., :1]
+    ok = gap > 1e-3
+    dv = np.abs(got["Vq"].astype(int) * sgn[..., None, :].astype(int) -
+                qo["Vq"].astype(int))
+    m = ok[..., None, :] & np.ones_like(dv, bool)
+    assert dv[m].max(initial=0) <= 1 and (dv[m] > 0).mean() < 0.02
+    # scores from the oracle's own records (encoded as variant records)
+    recs = torch.zeros_like(var)
+    recs[seq, :, pg] = torch.from_numpy(O.encode_variant(qo, rank, vbits)).to(
+        DEV)
+    q = wl.queries[0]
+    sc = torch.full((batch, h_kv, G, max_pages), 5.0, device=DEV)
+    B.locks_score_variant(q.to(DEV), recs, rank, vbits, i32(lens), sc, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    mu, V, C = O.dequantize(qo)                            # [n][h_kv] ...
+    qn = q.float().numpy()
+    nf = lens[0] // 16
+    s_gpu = sc.cpu().numpy()
+    for h in range(h_kv):
+        ref = O.score_from_summaries(qn[0, h * G:(h + 1) * G], mu[:, h],
+                                     V[:, h], C[:, h])
+        assert np.abs(s_gpu[0, h, :, :nf] - ref).max() <= S_TOL
+        assert (s_gpu[0, h, :, nf:] == 5.0).all()
+
+
+# ---------------------------------------------------------------------------
 # select (Eq.(5) + sink/recent) from identical scores
 # ---------------------------------------------------------------------------
 def test_select_matches_oracle_on_same_scores():
