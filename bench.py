@@ -283,6 +283,87 @@ def selection_quality(B, wl, store, scores, ws, lens, k, h_q, n_records,
                                       1)}}
 
 
+def rank_precision_ablation(B, wl, lens, k, h_q, n_seqs=4, n_steps=2):
+    """The notes' rank / basis-precision ablation (§6) on the first n_seqs
+    sequences of the workload: for every variant, carrier retention on the
+    planted needles, exact coverage and page-score error against the exact
+    LSE at budget k, with the variant's record bytes (the scoring stream's
+    bytes per page-head) and its build and scoring times."""
+    import torch
+    dev = wl.k_cache.device
+    batch = min(n_seqs, wl.page_table.shape[0])
+    pt = wl.page_table[:batch].contiguous()
+    sl = wl.seq_lens[:batch].contiguous()
+    max_pages = pt.shape[1]
+    h_kv = wl.k_cache.shape[1]
+    G = h_q // h_kv
+    seq = torch.tensor([b for b in range(batch) for _ in range(lens[b] // 16)],
+                       dtype=torch.int32, device=dev)
+    pgs = torch.tensor([p for b in range(batch) for p in range(lens[b] // 16)],
+                       dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = B.new_workspace(batch, h_q, h_kv, max_pages, k, dev)
+    sc = torch.zeros(batch, h_kv, G, max_pages, device=dev)
+    ex = torch.zeros_like(sc)
+    idx = torch.empty(batch, h_kv, k, dtype=torch.int32, device=dev)
+    needles = wl.needle_pages[:batch].to(dev)
+    e0, e1, e2 = (torch.cuda.Event(True) for _ in range(3))
+    out = []
+    for rank in (4, 8, 12, 15):
+        for vbits in (2, 4, 8):
+            rec = B.new_variant_store(batch, h_kv, max_pages, rank, vbits, dev)
+            e0.record()
+            B.locks_build_variant(wl.k_cache, pt, seq, pgs, rec, rank, vbits,
+                                  status=status)
+            e1.record()
+            torch.cuda.synchronize()
+            build_ms = e0.elapsed_time(e1)
+            hit = tot = 0
+            cov, err = [], []
+            score_ms = []
+            for i in range(n_steps):
+                q = wl.queries[i, :batch].contiguous()
+                B.locks_exact_page_scores(q, wl.k_cache, pt, sl, ex, status)
+                e1.record()
+                B.locks_score_variant(q, rec, rank, vbits, sl, sc, status)
+                e2.record()
+                torch.cuda.synchronize()
+                score_ms.append(e1.elapsed_time(e2))
+                B.locks_select_pages(sc, sl, h_q, k, idx, ws)
+                kept = (idx[:, :, None, :] == needles[:, :, :, None]).any(-1)
+                hit += int((kept & (needles >= 0)).sum())
+                tot += int((needles >= 0).sum())
+                for b in range(batch):
+                    nf = lens[b] // 16
+                    mass = torch.softmax(ex[b, :, :, :nf].double(), -1)
+                    sel = idx[b][:, None, :].expand(h_kv, G, k)
+                    valid = (sel >= 0) & (sel < nf)
+                    c = torch.gather(mass, 2, sel.clamp(0, nf - 1).long())
+                    cov.append(float((c * valid).sum(-1).mean()))
+                    err.append((sc[b, :, :, :nf] - ex[b, :, :, :nf]).abs()
+                               .flatten())
+            assert int(status.item()) == 0 and B.locks_read_status(ws) == 0
+            e = torch.cat(err).double()
+            n_rec = int(seq.numel()) * h_kv
+            out.append({
+                "rank": rank, "basis_bits": vbits,
+                "record_bytes": B.locks_variant_record_bytes(rank, vbits),
+                "carrier_retention": round(hit / max(1, tot), 4),
+                "coverage_mean": round(statistics.mean(cov), 5),
+                "score_error_mean": round(float(e.mean()), 5),
+                "score_error_p99": round(float(torch.quantile(
+                    e[torch.randperm(e.numel(), device=e.device)[:1 << 20]],
+                    0.99)), 5),
+                "build_ms": round(build_ms, 3),
+                "score_ms": round(statistics.mean(score_ms), 4),
+                "page_heads": n_rec})
+            del rec
+    return {"sequences": batch, "budget_pages": k, "steps": n_steps,
+            "variants": out,
+            "note": "variant records scored on CUDA cores (ablation path); "
+                    "the shipped (8, 4-bit) record is the tensor-core path"}
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -532,6 +613,8 @@ def run_locks(args):
             "gbs": round(dense_bytes / (dms / 1e3) / 1e9, 1)}
         line["quality"] = selection_quality(B, wl, store, scores, ws, lens,
                                             k, spec.h_q, n_records)
+        line["quality"]["rank_precision_ablation"] = rank_precision_ablation(
+            B, wl, lens, k, spec.h_q)
         if rank == 0 and world == 1:
             from oracle import locks_oracle as O
             b0 = 0
