@@ -25,9 +25,10 @@
  *    a LOCKS_DEV_* bit into a device status word (first int32 of the
  *    workspace, or the explicit `status` pointer), which the caller reads
  *    with locks_read_status and clears with locks_clear_status.
- *  - Numerics: the fast paths feed the tensor cores fp16 operands (query
- *    converted from bf16, summary codes exact) with fp32 accumulation, so
- *    query entries must satisfy |q| < 65504.
+ *  - Numerics: scoring feeds the tensor cores fp16 operands (summary codes
+ *    exact; the query converted from bf16 after a power-of-two prescale per
+ *    (sequence, KV head) that keeps it below 2^14, undone in fp32) with
+ *    fp32 accumulation; any finite query is accepted.
  *
  * Summary record (one per (sequence, KV head, logical page)), 832 bytes,
  * 16-byte aligned, laid out so that the scoring kernel's tensor-core
@@ -37,9 +38,10 @@
  *               component n < 8) sits in word (4n + c)*4 + w at bit
  *               16e + 8sp + 4h, where c = (d%8)/2, e = d%2, h = (d%16)/8,
  *               s = d/16, w = s/2, sp = s%2.
- *   [512, 640)  C8  int8 coefficient codes C[i][n] (token i < 16), byte
- *               512 + 4*(4*(i%8) + n/2) + 2*(i/8) + n%2, in [-127, 127].
- *   [640, 768)  MU8 int8 centroid codes mu[d], byte
+ *   [512, 640)  C8  int8 coefficient codes C[i][n] (token i < 16), in
+ *               [-127, 127], stored excess-128 (byte value = code + 128),
+ *               at byte 512 + 4*(4*(i%8) + n/2) + 2*(i/8) + n%2.
+ *   [640, 768)  MU8 int8 centroid codes mu[d], stored excess-128, at byte
  *               640 + 32*((d%8)/2) + 4*(d/16) + (d%2) + 2*((d%16)/8).
  *   [768, 832)  fp16 scales, four 16-byte groups: group t (0..3) at
  *               768 + 16t holds sV[2t], sV[2t+1] (per-column basis

@@ -320,9 +320,12 @@ def encode_records(q) -> np.ndarray:
     rec = np.zeros((n, RECORD_BYTES), dtype=np.uint8)
     rec[:, OFF_V4:OFF_V4 + 512] = np.ascontiguousarray(
         words.astype("<u4")).view(np.uint8).reshape(n, 512)
-    C8 = np.ascontiguousarray(q["C8"].reshape(n, PAGE, RANK)).view(np.uint8)
+    # int8 codes of C and mu are stored excess-128 (byte = code + 128)
+    C8 = (q["C8"].reshape(n, PAGE, RANK).astype(np.int16) + 128).astype(
+        np.uint8)
     rec[:, C8_OFF.reshape(-1)] = C8.reshape(n, -1)
-    mu8 = np.ascontiguousarray(q["mu8"].reshape(n, HEAD_DIM)).view(np.uint8)
+    mu8 = (q["mu8"].reshape(n, HEAD_DIM).astype(np.int16) + 128).astype(
+        np.uint8)
     rec[:, MU8_OFF] = mu8
     for offs, key, cnt in ((SV_OFF, "sV", RANK), (SC_OFF, "sC", PAGE),
                            (np.array([SMU_OFF]), "smu", 1)):
@@ -342,8 +345,10 @@ def decode_records(rec: np.ndarray):
     words = r[:, :512].copy().view("<u4").astype(np.int64)     # [n][128]
     nib = (words[:, V4_WORD] >> V4_SHIFT) & 0xF                 # [n][128][8]
     V4 = np.where(nib >= 8, nib - 16, nib).astype(np.int8)
-    C8 = r[:, C8_OFF.reshape(-1)].view(np.int8).reshape(n, PAGE, RANK)
-    mu8 = r[:, MU8_OFF].view(np.int8).reshape(n, HEAD_DIM)
+    C8 = (r[:, C8_OFF.reshape(-1)].astype(np.int16) - 128).astype(
+        np.int8).reshape(n, PAGE, RANK)
+    mu8 = (r[:, MU8_OFF].astype(np.int16) - 128).astype(np.int8).reshape(
+        n, HEAD_DIM)
     def halves(offs):
         lo = r[:, offs].astype(np.uint16)
         hi = r[:, offs + 1].astype(np.uint16)

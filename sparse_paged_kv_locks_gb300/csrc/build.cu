@@ -159,14 +159,15 @@ __device__ void write_record(const float (&V)[4][8], const float (&mu)[4],
     *reinterpret_cast<uint4 *>(rec + kOffV4 + 16 * lane) =
         make_uint4(wv[0], wv[1], wv[2], wv[3]);
   }
-  // C8: lane t = 4*gi + c
+  // C8: lane t = 4*gi + c; int8 codes stored excess-128 (byte = code + 128,
+  // i.e. the sign bit flipped)
   {
     const int gi = lane >> 2, c = lane & 3;
     uint32_t b0 = (uint8_t)sm.c8[gi][2 * c], b1 = (uint8_t)sm.c8[gi][2 * c + 1];
     uint32_t b2 = (uint8_t)sm.c8[gi + 8][2 * c];
     uint32_t b3 = (uint8_t)sm.c8[gi + 8][2 * c + 1];
     *reinterpret_cast<uint32_t *>(rec + kOffC8 + 4 * lane) =
-        b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        (b0 | (b1 << 8) | (b2 << 16) | (b3 << 24)) ^ 0x80808080u;
   }
   // MU8: lane l = 8c + s holds bytes d = 16s + 2c + {0, 1, 8, 9}
   {
@@ -175,7 +176,7 @@ __device__ void write_record(const float (&V)[4][8], const float (&mu)[4],
     uint32_t b0 = (uint8_t)sm.m8[d0], b1 = (uint8_t)sm.m8[d0 + 1];
     uint32_t b2 = (uint8_t)sm.m8[d0 + 8], b3 = (uint8_t)sm.m8[d0 + 9];
     *reinterpret_cast<uint32_t *>(rec + kOffMu8 + 4 * lane) =
-        b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        (b0 | (b1 << 8) | (b2 << 16) | (b3 << 24)) ^ 0x80808080u;
   }
   // scale block: 16 bytes per t = 0..3 at 768 + 16t holding sV[2t..2t+1],
   // sC[2t..2t+1], sC[8+2t..9+2t], then sMU (t = 0) or zero

@@ -52,13 +52,13 @@ __device__ __forceinline__ uint32_t nib_bf16_off(uint32_t x) {
   return lop3_and_xor(x, 0x000F000Fu, 0x43084308u);
 }
 
-// Four int8 codes -> two fp16x2 holding 1152 + code (exact); the constant is
-// cancelled through the accumulator's initial value.
+// Four int8 codes stored excess-128 (byte = code + 128) -> two fp16x2
+// holding 1024 + byte = 1152 + code (exact); the constant is cancelled
+// through the accumulator's initial value.
 __device__ __forceinline__ void i8x4_to_h2_off(uint32_t x, uint32_t &lo,
                                                uint32_t &hi) {
-  const uint32_t f = x ^ 0x80808080u;
-  asm("prmt.b32 %0, %1, %2, 0x7170;\n" : "=r"(lo) : "r"(f), "r"(0x64646464u));
-  asm("prmt.b32 %0, %1, %2, 0x7372;\n" : "=r"(hi) : "r"(f), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x7170;\n" : "=r"(lo) : "r"(x), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x7372;\n" : "=r"(hi) : "r"(x), "r"(0x64646464u));
 }
 
 // Four int8 codes -> two fp16x2 holding the codes exactly.

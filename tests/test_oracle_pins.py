@@ -500,6 +500,8 @@ def test_record_fixture(golden_dir):
     q["smu"] = np.array(q["smu"], np.float16)
     rec = O.encode_records(q)
     expect = np.zeros(O.RECORD_BYTES, np.uint8)
+    for lo, hi, val in g["defaults"]:
+        expect[lo:hi] = val
     for off, val in g["expected_bytes"]:
         expect[off] = val
     assert (rec == expect).all(), np.nonzero(rec != expect)
