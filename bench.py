@@ -571,10 +571,11 @@ def run_locks(args):
                      "page_heads_per_s": round(n_records / (build_ms / 1e3))}
 
     if not args.quick:
-        # e2e: pinned host query in, pinned host (o, lse) out, every step;
-        # the decoder replays the step as one captured CUDA graph
+        # e2e: pinned host query in, pinned host (o, lse) out, every step,
+        # through the C ABI decoder object: the query copy, the kernels and
+        # the result copies replay as one CUDA graph per step
         dec = B.LocksDecoder(wl.k_cache, wl.v_cache, wl.page_table, store,
-                             spec.h_q, k, graph=True)
+                             spec.h_q, k, graph=True, seq_lens=wl.seq_lens)
         q_host = qs.cpu().pin_memory()
         o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         lse_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
@@ -589,8 +590,12 @@ def run_locks(args):
         line["e2e"] = {"value": world * batch * n_e2e / dt, "unit": "tokens/s",
                        "steps": n_e2e,
                        "h2d_bytes_per_step": q_bytes,
-                       "d2h_bytes_per_step": q_bytes + batch * spec.h_q * 4,
-                       "api": "LocksDecoder.step_host, CUDA graph replay"}
+                       "d2h_bytes_per_step": q_bytes + batch * spec.h_q * 4 + 4,
+                       "api": "locks_decoder_step_host (C ABI): one CUDA "
+                              "graph per step: a kernel reading q from pinned "
+                              "host memory, the 4 step kernels, a kernel "
+                              "writing o, lse and the status word to pinned "
+                              "host memory"}
         # dense full-cache decode of the same shape, as context
         for _ in range(2):
             B.locks_sparse_decode(qs[0], wl.k_cache, wl.v_cache,

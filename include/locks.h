@@ -9,9 +9,10 @@
  *
  * Conventions for every call
  *  - All array pointers are CUDA device pointers owned by the caller unless a
- *    comment says "host".  The library allocates no memory, never
- *    synchronises the stream (except locks_read_status, which says so) and
- *    launches its kernels on `stream` (NULL = the legacy default stream).
+ *    comment says "host".  The library allocates no device memory, never
+ *    synchronises the stream (except locks_read_status and
+ *    locks_decoder_step_host, which say so) and launches its kernels on
+ *    `stream` (NULL = the legacy default stream).
  *  - Shapes: page size B = 16 tokens, head dim d = 128, summary rank r = 8.
  *    K/V caches are bf16, laid out [num_phys_pages][h_kv][16][128] so that
  *    each (page, KV head) is one contiguous 4 KB run.
@@ -333,6 +334,71 @@ locks_status_t locks_append_kv(const void *k_new, const void *v_new,
                                int max_pages, int32_t *seq_lens,
                                void *summaries, float *tau_out,
                                int32_t *status, locks_stream_t stream);
+
+/* Decoder object: one layer's decode step driven from host buffers (the
+ * decode path of LOCKS reading notes §2 Fig. 1: score every page summary,
+ * select k pages, attend over them; the same computation as
+ * locks_score_select followed by locks_sparse_decode).  The pages describe
+ * the computation only; this object is the deployment form of it.
+ *
+ * locks_decoder_create binds the caller's device buffers and sizes:
+ *   k_cache, v_cache, num_phys_pages, page_table, summaries, seq_lens,
+ *   batch, h_q, h_kv, max_pages, k   as in locks_score_select /
+ *                  locks_sparse_decode (seq_lens is read on the device at
+ *                  every step, so appends between steps take effect)
+ *   q_dev         bf16 [batch][h_q][128] device staging buffer for the query
+ *   idx           int32 [batch][h_kv][k] device buffer for the selection
+ *   o_dev, lse_dev  bf16 [batch][h_q][128] and float [batch][h_q] device
+ *   workspace     >= locks_workspace_size(batch, h_q, h_kv, max_pages, k)
+ * It checks the arguments, creates a private non-blocking capture stream
+ * and a 4-byte mapped page-locked host word, and allocates no device
+ * memory.  All
+ * bound buffers stay owned by the caller and must outlive the decoder.
+ * Errors: LOCKS_ERR_INVALID_ARG / _UNSUPPORTED / _WORKSPACE as the step
+ * calls would return them; LOCKS_ERR_CUDA if the stream or the host word
+ * cannot be created.  *out is NULL on any error. */
+typedef struct locks_decoder locks_decoder_t;
+locks_status_t locks_decoder_create(
+    const void *k_cache, const void *v_cache, int64_t num_phys_pages,
+    const int32_t *page_table, const void *summaries, const int32_t *seq_lens,
+    int batch, int h_q, int h_kv, int max_pages, int k, void *q_dev,
+    int32_t *idx, void *o_dev, float *lse_dev, void *workspace,
+    size_t workspace_bytes, locks_decoder_t **out);
+
+/* One decode step from host buffers, synchronous:
+ *   q_host    host bf16 [batch][h_q][128] query (page-locked)
+ *   o_host    host bf16 [batch][h_q][128] attention output (page-locked)
+ *   lse_host  host float [batch][h_q] natural-log LSE (page-locked)
+ *   status_out  optional plain host int32: the device status word
+ *             (LOCKS_DEV_* bits, sticky until locks_clear_status) as read
+ *             back at the end of this step
+ *   stream    the step is ordered after earlier work on `stream` (NULL =
+ *             the legacy default stream) and the call returns when it is
+ *             done (the stream is synchronised).
+ * The first call records the whole step (a kernel that reads the query
+ * from host memory into q_dev, the four kernels, a kernel that writes o,
+ * lse and the status word to host memory) as one CUDA graph on the
+ * decoder's capture stream, after one plain run of the same step that
+ * completes first; every call then launches that graph once.  The host
+ * buffers are accessed by those two kernels through their mapped device
+ * addresses, so they must be page-locked (cudaHostAlloc, or
+ * cudaHostRegister with mapping) with a 16-byte aligned device address;
+ * anything else returns LOCKS_ERR_INVALID_ARG before anything runs.  Other
+ * host buffers than the previous call's are patched into the two copy
+ * kernels' graph nodes.
+ * On LOCKS_ERR_CUDA, locks_decoder_last_cuda_error gives the cudaError_t.
+ * Calls on one decoder must not overlap (one host thread at a time). */
+locks_status_t locks_decoder_step_host(locks_decoder_t *decoder,
+                                       const void *q_host, void *o_host,
+                                       float *lse_host, int32_t *status_out,
+                                       locks_stream_t stream);
+
+/* cudaError_t of the decoder's last failing CUDA call (0 if none). */
+int locks_decoder_last_cuda_error(const locks_decoder_t *decoder);
+
+/* Release the decoder's graph, stream and host word (NULL is a no-op).
+ * The caller's buffers are untouched. */
+void locks_decoder_destroy(locks_decoder_t *decoder);
 
 /* Zero the device status word (the first int32 of `status_word`). */
 locks_status_t locks_clear_status(void *status_word, locks_stream_t stream);

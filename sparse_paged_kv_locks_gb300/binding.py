@@ -69,6 +69,13 @@ _SIGS = {
                                  _I, _P, _P, _P, _SZ, _P]),
     "locks_append_kv": (_I, [_P, _P, _P, _P, _I64, _I, _P, _I, _I, _P, _P, _P,
                              _P, _P]),
+    "locks_decoder_create": (_I, [_P, _P, _I64, _P, _P, _P, _I, _I, _I, _I,
+                                  _I, _P, _P, _P, _P, _P, _SZ,
+                                  ctypes.POINTER(_P)]),
+    "locks_decoder_step_host": (_I, [_P, _P, _P, _P,
+                                     ctypes.POINTER(ctypes.c_int32), _P]),
+    "locks_decoder_last_cuda_error": (_I, [_P]),
+    "locks_decoder_destroy": (None, [_P]),
     "locks_clear_status": (_I, [_P, _P]),
     "locks_read_status": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
 }
@@ -421,14 +428,19 @@ def locks_read_status(status_word, stream=None) -> int:
 class LocksDecoder:
     """Owns the per-step buffers of one layer's decode step.
 
-    With graph=True the step (score + select + sparse attention, five
-    kernels) is captured once into a CUDA graph on the first call and
-    replayed afterwards; the query and the lengths are then copied into
-    static device buffers first.  The library allocates nothing and never
-    synchronises, so the captured step is the eager one."""
+    With graph=True, `step` captures the device-resident step (score +
+    select + sparse attention, five kernels) once into a CUDA graph and
+    replays it, and `step_host` runs the C ABI decoder object
+    (locks_decoder_step_host): the query copy in, the kernels and the
+    copies of (o, lse) out replay as one CUDA graph per step.  With
+    graph=False both run the kernels eagerly.  `seq_lens`, when given, is
+    the device length buffer the step reads (it is bound, so appends that
+    update it in place take effect); otherwise the decoder keeps its own
+    and copies the lengths passed to each step into it.  The library
+    allocates no device memory and the eager step never synchronises."""
 
     def __init__(self, k_cache, v_cache, page_table, summaries, h_q, k,
-                 graph=False):
+                 graph=False, seq_lens=None):
         self.k_cache, self.v_cache = k_cache, v_cache
         self.page_table, self.summaries = page_table, summaries
         self.batch, self.h_kv, self.max_pages = summaries.shape[:3]
@@ -444,10 +456,17 @@ class LocksDecoder:
                                device=dev)
         self.q_dev = torch.empty(self.batch, h_q, HEAD_DIM,
                                  dtype=torch.bfloat16, device=dev)
-        self.seq_lens_dev = torch.empty(self.batch, dtype=torch.int32,
-                                        device=dev)
+        if seq_lens is None:
+            self.seq_lens_dev = torch.empty(self.batch, dtype=torch.int32,
+                                            device=dev)
+        else:
+            _req(seq_lens, "seq_lens", torch.int32, 1)
+            if seq_lens.numel() != self.batch:
+                raise ValueError("seq_lens must have one entry per sequence")
+            self.seq_lens_dev = seq_lens
         self.use_graph = graph
         self._graph = None
+        self._native = None
 
     def _eager(self, q, seq_lens, stream=None):
         locks_score_select(q, self.summaries, seq_lens, self.k, self.idx,
@@ -468,30 +487,90 @@ class LocksDecoder:
             self._eager(self.q_dev, self.seq_lens_dev)
         self._graph = g
 
-    def step(self, q, seq_lens, stream=None):
+    def _bind_lens(self, seq_lens, stream=None):
+        if seq_lens is not None and seq_lens is not self.seq_lens_dev:
+            _req(seq_lens, "seq_lens", torch.int32, 1)
+            s = torch.cuda.current_stream() if stream is None else stream
+            with torch.cuda.stream(s):
+                self.seq_lens_dev.copy_(seq_lens, non_blocking=True)
+
+    def step(self, q, seq_lens=None, stream=None):
         """Device-resident query -> (o, lse) on the device."""
         if not self.use_graph:
-            self._eager(q, seq_lens, stream)
+            self._eager(q, self.seq_lens_dev if seq_lens is None else seq_lens,
+                        stream)
             return self.o, self.lse
         if stream is not None:
             raise ValueError("graph replay runs on the current stream")
         if q is not self.q_dev:
             self.q_dev.copy_(q, non_blocking=True)
-        if seq_lens is not self.seq_lens_dev:
-            self.seq_lens_dev.copy_(seq_lens, non_blocking=True)
+        self._bind_lens(seq_lens)
         if self._graph is None:
             self._capture()
         self._graph.replay()
         return self.o, self.lse
 
+    def _native_decoder(self):
+        if self._native is None:
+            h = ctypes.c_void_p(None)
+            L = lib()
+            _check("locks_decoder_create", L.locks_decoder_create(
+                _ptr(self.k_cache), _ptr(self.v_cache), self.k_cache.shape[0],
+                _ptr(self.page_table), _ptr(self.summaries),
+                _ptr(self.seq_lens_dev), self.batch, self.h_q, self.h_kv,
+                self.max_pages, self.k, _ptr(self.q_dev), _ptr(self.idx),
+                _ptr(self.o), _ptr(self.lse), _ptr(self.workspace),
+                self.workspace.numel(), ctypes.byref(h)))
+            self._native = h
+        return self._native
+
     def step_host(self, q_host, seq_lens, o_host, lse_host, stream=None):
-        """Pinned host query in, pinned host (o, lse) out (synchronises)."""
-        self.q_dev.copy_(q_host, non_blocking=True)
-        self.step(self.q_dev, seq_lens, stream)
-        o_host.copy_(self.o, non_blocking=True)
-        lse_host.copy_(self.lse, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        return o_host, lse_host
+        """Pinned host query in, pinned host (o, lse) out (synchronises).
+        Returns (o_host, lse_host, device status word)."""
+        for t, name, dt in ((q_host, "q_host", torch.bfloat16),
+                            (o_host, "o_host", torch.bfloat16),
+                            (lse_host, "lse_host", torch.float32)):
+            _req(t, name, dt, device="host")
+            if t.is_cuda:
+                raise ValueError(f"{name} must be a (pinned) host tensor")
+        if tuple(q_host.shape) != (self.batch, self.h_q, HEAD_DIM) or \
+                tuple(o_host.shape) != tuple(q_host.shape) or \
+                tuple(lse_host.shape) != (self.batch, self.h_q):
+            raise ValueError("host buffers must be [batch][h_q][128] and "
+                             "[batch][h_q]")
+        if not self.use_graph:
+            s = torch.cuda.current_stream() if stream is None else stream
+            with torch.cuda.stream(s):
+                self.q_dev.copy_(q_host, non_blocking=True)
+                self._bind_lens(seq_lens, s)
+                self._eager(self.q_dev, self.seq_lens_dev, s)
+                o_host.copy_(self.o, non_blocking=True)
+                lse_host.copy_(self.lse, non_blocking=True)
+            s.synchronize()
+            return o_host, lse_host, self.status()
+        self._bind_lens(seq_lens, stream)
+        st = ctypes.c_int32(0)
+        L = lib()
+        rc = L.locks_decoder_step_host(self._native_decoder(), _ptr(q_host),
+                                       _ptr(o_host), _ptr(lse_host),
+                                       ctypes.byref(st), _stream(stream))
+        if rc != 0:
+            raise LocksError(
+                f"locks_decoder_step_host: "
+                f"{L.locks_status_string(rc).decode()} (status {rc}, cuda "
+                f"error {L.locks_decoder_last_cuda_error(self._native)})")
+        return o_host, lse_host, int(st.value)
+
+    def close(self):
+        if self._native is not None:
+            lib().locks_decoder_destroy(self._native)
+            self._native = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
     def status(self) -> int:
         return locks_read_status(self.workspace)

@@ -55,6 +55,88 @@ static bool heads_ok(int h_q, int h_kv) {
   return h_kv >= 1 && h_q >= h_kv && h_q % h_kv == 0;
 }
 
+static locks_status_t check_select_args(int batch, int h_q, int h_kv,
+                                        int max_pages, int k,
+                                        const int32_t *seq_lens,
+                                        int32_t *idx_out, void *workspace) {
+  if (batch < 0 || max_pages < 1 || k < 2 || !heads_ok(h_q, h_kv))
+    return LOCKS_ERR_INVALID_ARG;
+  if (h_q / h_kv > kMaxGroup) return LOCKS_ERR_UNSUPPORTED;
+  if (batch > 65535 || h_kv > 65535) return LOCKS_ERR_UNSUPPORTED;
+  if ((long long)max_pages * kPage > 0x7fffffffLL) return LOCKS_ERR_UNSUPPORTED;
+  if (batch > 0 && (!seq_lens || !idx_out || !workspace))
+    return LOCKS_ERR_INVALID_ARG;
+  return LOCKS_OK;
+}
+
+locks_status_t locks::score_select(const void *q, const void *summaries,
+                                   const int32_t *seq_lens, int batch, int h_q,
+                                   int h_kv, int max_pages, int k,
+                                   int32_t *idx_out, void *workspace,
+                                   size_t workspace_bytes, cudaStream_t stream,
+                                   bool after_query) {
+  locks_status_t st = check_select_args(batch, h_q, h_kv, max_pages, k,
+                                        seq_lens, idx_out, workspace);
+  if (st != LOCKS_OK) return st;
+  if (batch == 0) return LOCKS_OK;
+  if (!q || !summaries) return LOCKS_ERR_INVALID_ARG;
+  if (batch > score_max_batch()) return LOCKS_ERR_UNSUPPORTED;
+  if (workspace_bytes < kWsHeader + score_region(batch, h_q, h_kv, max_pages))
+    return LOCKS_ERR_WORKSPACE;
+  const int G = h_q / h_kv;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  int32_t *status = reinterpret_cast<int32_t *>(ws);
+  float *s_hat = reinterpret_cast<float *>(ws + kWsHeader);
+  uint32_t *keys = reinterpret_cast<uint32_t *>(
+      ws + kWsHeader + round_up((size_t)batch * h_kv * G * max_pages * 4, 256));
+  cudaError_t e = launch_score(q, summaries, seq_lens, batch, h_kv, G,
+                               max_pages, s_hat, status, stream, after_query);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = launch_select(s_hat, seq_lens, batch, h_kv, G, max_pages, k,
+                    LOCKS_MERGE_SHARE_AVERAGE, idx_out, keys, status, stream);
+  return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
+}
+
+locks_status_t locks::sparse_decode(
+    const void *q, const void *k_cache, const void *v_cache,
+    int64_t num_phys_pages, const int32_t *page_table,
+    const int32_t *seq_lens, const int32_t *idx, int k, int batch, int h_q,
+    int h_kv, int max_pages, void *o_out, float *lse_out, void *workspace,
+    size_t workspace_bytes, cudaStream_t stream, bool out_dependent) {
+  if (batch < 0 || max_pages < 1 || num_phys_pages < 1 || !heads_ok(h_q, h_kv))
+    return LOCKS_ERR_INVALID_ARG;
+  if (idx && k < 1) return LOCKS_ERR_INVALID_ARG;
+  if (h_q / h_kv > kMaxGroup) return LOCKS_ERR_UNSUPPORTED;
+  if (batch > 65535 || h_kv > 65535) return LOCKS_ERR_UNSUPPORTED;
+  if ((long long)max_pages * kPage > 0x7fffffffLL) return LOCKS_ERR_UNSUPPORTED;
+  if (batch == 0) return LOCKS_OK;
+  if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !o_out ||
+      !lse_out || !workspace)
+    return LOCKS_ERR_INVALID_ARG;
+  const int list_len = idx ? k : max_pages;
+  // every list entry of every (sequence, KV head) is one int32 position
+  if ((long long)batch * h_kv * list_len > 0x7fffffffLL)
+    return LOCKS_ERR_UNSUPPORTED;
+  if (batch > decode_max_batch()) return LOCKS_ERR_UNSUPPORTED;
+  if (workspace_bytes < kWsHeader + decode_region(batch, h_q, h_kv, list_len))
+    return LOCKS_ERR_WORKSPACE;
+  const int G = h_q / h_kv;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  int32_t *status = reinterpret_cast<int32_t *>(ws);
+  const size_t rows = decode_slots(batch, h_kv, list_len) * (size_t)G;
+  int *meta = reinterpret_cast<int *>(ws + kWsHeader);
+  float *o_part =
+      reinterpret_cast<float *>(ws + kWsHeader + decode_meta_bytes(batch));
+  float *lse_part = reinterpret_cast<float *>(
+      ws + kWsHeader + decode_meta_bytes(batch) + round_up(rows * kDim * 4, 256));
+  const int max_warps = (int)decode_warps_cap(batch, h_kv, list_len);
+  cudaError_t e = launch_decode(
+      q, k_cache, v_cache, num_phys_pages, page_table, seq_lens, idx, k, batch,
+      h_kv, G, max_pages, max_warps, o_out, lse_out, o_part, lse_part, meta,
+      status, stream, out_dependent);
+  return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
+}
+
 extern "C" {
 
 const char *locks_status_string(locks_status_t s) {
@@ -164,47 +246,15 @@ locks_status_t locks_pack_summaries(const float *mu, const float *basis,
   return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
 }
 
-static locks_status_t check_select_args(int batch, int h_q, int h_kv,
-                                        int max_pages, int k,
-                                        const int32_t *seq_lens,
-                                        int32_t *idx_out, void *workspace) {
-  if (batch < 0 || max_pages < 1 || k < 2 || !heads_ok(h_q, h_kv))
-    return LOCKS_ERR_INVALID_ARG;
-  if (h_q / h_kv > kMaxGroup) return LOCKS_ERR_UNSUPPORTED;
-  if (batch > 65535 || h_kv > 65535) return LOCKS_ERR_UNSUPPORTED;
-  if ((long long)max_pages * kPage > 0x7fffffffLL) return LOCKS_ERR_UNSUPPORTED;
-  if (batch > 0 && (!seq_lens || !idx_out || !workspace))
-    return LOCKS_ERR_INVALID_ARG;
-  return LOCKS_OK;
-}
-
 locks_status_t locks_score_select(const void *q, const void *summaries,
                                   const int32_t *seq_lens, int batch, int h_q,
                                   int h_kv, int max_pages, int k,
                                   int32_t *idx_out, void *workspace,
                                   size_t workspace_bytes,
                                   locks_stream_t stream) {
-  locks_status_t st = check_select_args(batch, h_q, h_kv, max_pages, k,
-                                        seq_lens, idx_out, workspace);
-  if (st != LOCKS_OK) return st;
-  if (batch == 0) return LOCKS_OK;
-  if (!q || !summaries) return LOCKS_ERR_INVALID_ARG;
-  if (batch > score_max_batch()) return LOCKS_ERR_UNSUPPORTED;
-  if (workspace_bytes < kWsHeader + score_region(batch, h_q, h_kv, max_pages))
-    return LOCKS_ERR_WORKSPACE;
-  const int G = h_q / h_kv;
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
-  int32_t *status = reinterpret_cast<int32_t *>(ws);
-  float *s_hat = reinterpret_cast<float *>(ws + kWsHeader);
-  uint32_t *keys = reinterpret_cast<uint32_t *>(
-      ws + kWsHeader + round_up((size_t)batch * h_kv * G * max_pages * 4, 256));
-  cudaError_t e = launch_score(q, summaries, seq_lens, batch, h_kv, G,
-                               max_pages, s_hat, status, (cudaStream_t)stream);
-  if (e != cudaSuccess) return fail_cuda(e);
-  e = launch_select(s_hat, seq_lens, batch, h_kv, G, max_pages, k,
-                    LOCKS_MERGE_SHARE_AVERAGE, idx_out, keys, status,
-                    (cudaStream_t)stream);
-  return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
+  return locks::score_select(q, summaries, seq_lens, batch, h_q, h_kv,
+                             max_pages, k, idx_out, workspace, workspace_bytes,
+                             (cudaStream_t)stream, false);
 }
 
 locks_status_t locks_score_pages(const void *q, const void *summaries,
@@ -290,38 +340,10 @@ locks_status_t locks_sparse_decode(
     const int32_t *seq_lens, const int32_t *idx, int k, int batch, int h_q,
     int h_kv, int max_pages, void *o_out, float *lse_out, void *workspace,
     size_t workspace_bytes, locks_stream_t stream) {
-  if (batch < 0 || max_pages < 1 || num_phys_pages < 1 || !heads_ok(h_q, h_kv))
-    return LOCKS_ERR_INVALID_ARG;
-  if (idx && k < 1) return LOCKS_ERR_INVALID_ARG;
-  if (h_q / h_kv > kMaxGroup) return LOCKS_ERR_UNSUPPORTED;
-  if (batch > 65535 || h_kv > 65535) return LOCKS_ERR_UNSUPPORTED;
-  if ((long long)max_pages * kPage > 0x7fffffffLL) return LOCKS_ERR_UNSUPPORTED;
-  if (batch == 0) return LOCKS_OK;
-  if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !o_out ||
-      !lse_out || !workspace)
-    return LOCKS_ERR_INVALID_ARG;
-  const int list_len = idx ? k : max_pages;
-  // every list entry of every (sequence, KV head) is one int32 position
-  if ((long long)batch * h_kv * list_len > 0x7fffffffLL)
-    return LOCKS_ERR_UNSUPPORTED;
-  if (batch > decode_max_batch()) return LOCKS_ERR_UNSUPPORTED;
-  if (workspace_bytes < kWsHeader + decode_region(batch, h_q, h_kv, list_len))
-    return LOCKS_ERR_WORKSPACE;
-  const int G = h_q / h_kv;
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
-  int32_t *status = reinterpret_cast<int32_t *>(ws);
-  const size_t rows = decode_slots(batch, h_kv, list_len) * (size_t)G;
-  int *meta = reinterpret_cast<int *>(ws + kWsHeader);
-  float *o_part =
-      reinterpret_cast<float *>(ws + kWsHeader + decode_meta_bytes(batch));
-  float *lse_part = reinterpret_cast<float *>(
-      ws + kWsHeader + decode_meta_bytes(batch) + round_up(rows * kDim * 4, 256));
-  const int max_warps = (int)decode_warps_cap(batch, h_kv, list_len);
-  cudaError_t e = launch_decode(
-      q, k_cache, v_cache, num_phys_pages, page_table, seq_lens, idx, k, batch,
-      h_kv, G, max_pages, max_warps, o_out, lse_out, o_part, lse_part, meta,
-      status, (cudaStream_t)stream);
-  return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
+  return locks::sparse_decode(q, k_cache, v_cache, num_phys_pages, page_table,
+                              seq_lens, idx, k, batch, h_q, h_kv, max_pages,
+                              o_out, lse_out, workspace, workspace_bytes,
+                              (cudaStream_t)stream, false);
 }
 
 locks_status_t locks_append_kv(const void *k_new, const void *v_new,

@@ -446,8 +446,12 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
                    const float *__restrict__ lse_part,
                    const int *__restrict__ meta, int batch, int h_kv, int k,
                    int dense, int G, __nv_bfloat16 *__restrict__ o_out,
-                   float *__restrict__ lse_out) {
+                   float *__restrict__ lse_out, int trigger) {
   const int lane = threadIdx.x & 31;
+  // A dependent that only reads o and lse after its own wait (a copy of
+  // them to the host) may launch now.  Off for plain calls: a following
+  // decode launched early would hold its SM slots idle meanwhile.
+  if (trigger) pdl_trigger();
   pdl_wait();  // partials and layout of the decode kernel
   const long long row =
       (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
@@ -535,7 +539,8 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
                           const int32_t *idx, int k, int batch, int h_kv,
                           int G, int max_pages, int max_warps, void *o_out,
                           float *lse_out, float *o_part, float *lse_part,
-                          int *meta, int32_t *status, cudaStream_t stream) {
+                          int *meta, int32_t *status, cudaStream_t stream,
+                          bool out_dependent) {
   static bool attr_set = false;
   static int blocks_per_sm[2] = {0, 0};
   if (!attr_set) {
@@ -582,7 +587,7 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
                     dim3((unsigned)((rows + kCombineWarps - 1) / kCombineWarps)),
                     dim3(32 * kCombineWarps), 0, stream, o_part, lse_part,
                     (const int *)meta, batch, h_kv, k, idx ? 0 : 1, G, oo,
-                    lse_out);
+                    lse_out, out_dependent ? 1 : 0);
 }
 
 }  // namespace locks

@@ -5,7 +5,17 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "locks.h"
+
 namespace locks {
+
+// locks_score_select on a cudaStream_t, with the scoring kernel optionally
+// launched after_query (see launch_score).
+locks_status_t score_select(const void *q, const void *summaries,
+                            const int32_t *seq_lens, int batch, int h_q,
+                            int h_kv, int max_pages, int k, int32_t *idx_out,
+                            void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream, bool after_query);
 
 cudaError_t launch_build(const void *k_cache, int64_t num_phys, int h_kv,
                          const int32_t *pt, int batch, int max_pages,
@@ -24,10 +34,13 @@ cudaError_t launch_append(const void *k_new, const void *v_new, void *k_cache,
                           int32_t *seq_lens, void *summaries, float *tau_out,
                           int32_t *status, cudaStream_t stream);
 
+// after_query: launch as a programmatic dependent of the preceding kernel,
+// which may write only the query (the kernel reads seq_lens and the
+// summaries and starts its first copies before waiting on it).
 cudaError_t launch_score(const void *q, const void *summaries,
                          const int32_t *seq_lens, int batch, int h_kv, int G,
                          int max_pages, float *s_hat, int32_t *status,
-                         cudaStream_t stream);
+                         cudaStream_t stream, bool after_query = false);
 
 cudaError_t launch_select(const float *scores, const int32_t *seq_lens,
                           int batch, int h_kv, int G, int max_pages, int k,
@@ -40,7 +53,19 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
                           const int32_t *idx, int k, int batch, int h_kv,
                           int G, int max_pages, int max_warps, void *o_out,
                           float *lse_out, float *o_part, float *lse_part,
-                          int *meta, int32_t *status, cudaStream_t stream);
+                          int *meta, int32_t *status, cudaStream_t stream,
+                          bool out_dependent = false);
+
+// locks_sparse_decode on a cudaStream_t; out_dependent: the merge kernel
+// lets a programmatic dependent that reads only o and lse launch early.
+locks_status_t sparse_decode(const void *q, const void *k_cache,
+                             const void *v_cache, int64_t num_phys_pages,
+                             const int32_t *page_table,
+                             const int32_t *seq_lens, const int32_t *idx,
+                             int k, int batch, int h_q, int h_kv,
+                             int max_pages, void *o_out, float *lse_out,
+                             void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream, bool out_dependent);
 
 cudaError_t launch_exact(const void *q, const void *k_cache, int64_t num_phys,
                          const int32_t *pt, const int32_t *seq_lens,

@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                  const uint8_t *__restrict__ summaries,
                  const int32_t *__restrict__ seq_lens, int batch, int h_kv,
                  int G, int max_pages, float *__restrict__ s_hat,
-                 int32_t *status) {
+                 int32_t *status, int wait_query) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *ring = smem;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes);
@@ -375,7 +375,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const long long W = (long long)gridDim.x * kScoreWarps;
   const long long gw = (long long)blockIdx.x * kScoreWarps + wid;
   const long long t_begin = gw * total / W, t_end = (gw + 1) * total / W;
-  if (t_begin >= t_end) return;
+  // wait_query: the query comes from the preceding kernel (this one is its
+  // programmatic dependent), so every thread waits for it before reading q
+  // or exiting.
+  if (t_begin >= t_end) {
+    if (wait_query) pdl_wait();
+    return;
+  }
   uint8_t *my_ring = ring + (size_t)wid * kStages * kTileBytes;
   const uint32_t ring_s = smem_u32(my_ring);
   uint64_t *my_bar = bars + wid * kStages;
@@ -402,6 +408,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                &my_bar[1], lane);
     advance_cursor(nxt, tph, batch, h_kv);
   }
+  if (wait_query) pdl_wait();  // first two tiles in flight; q is read next
 
   constexpr bool WIDE = MODE == 3;
   uint32_t qb[8][4];  // query A fragments, bf16 (basis product, one page)
@@ -728,7 +735,7 @@ int score_max_batch() {
 cudaError_t launch_score(const void *q, const void *summaries,
                          const int32_t *seq_lens, int batch, int h_kv, int G,
                          int max_pages, float *s_hat, int32_t *status,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, bool after_query) {
   const size_t smem = score_smem_bytes(batch);
   static bool attr_set = false;
   if (!attr_set) {
@@ -749,15 +756,14 @@ cudaError_t launch_score(const void *q, const void *summaries,
   const int grid = sm_count();
   auto *qq = static_cast<const __nv_bfloat16 *>(q);
   auto *ss = static_cast<const uint8_t *>(summaries);
-  if (G > 8)
-    score_kernel<3><<<grid, kScoreThreads, smem, stream>>>(
-        qq, ss, seq_lens, batch, h_kv, G, max_pages, s_hat, status);
-  else if (G > 4)
-    score_kernel<2><<<grid, kScoreThreads, smem, stream>>>(
-        qq, ss, seq_lens, batch, h_kv, G, max_pages, s_hat, status);
-  else
-    score_kernel<1><<<grid, kScoreThreads, smem, stream>>>(
-        qq, ss, seq_lens, batch, h_kv, G, max_pages, s_hat, status);
+  auto *kern = G > 8 ? score_kernel<3> : G > 4 ? score_kernel<2>
+                                               : score_kernel<1>;
+  if (after_query)
+    return launch_pdl(kern, dim3(grid), dim3(kScoreThreads), smem, stream, qq,
+                      ss, seq_lens, batch, h_kv, G, max_pages, s_hat, status,
+                      1);
+  kern<<<grid, kScoreThreads, smem, stream>>>(qq, ss, seq_lens, batch, h_kv, G,
+                                              max_pages, s_hat, status, 0);
   return cudaGetLastError();
 }
 

@@ -73,6 +73,22 @@ def test_host_validation_before_launch(L):
     assert L.locks_pack_summaries(None, None, None, -1, None, s) == 1
     assert L.locks_clear_status(None, s) == 1
     assert L.locks_read_status(None, None, s) == 1
+    # decoder object: argument and workspace checks before any CUDA call
+    out = ctypes.c_void_p(123)
+    args = [fake, fake, 10, fake, fake, fake, 2, 8, 2, 16, 4, fake, fake,
+            fake, fake, fake]
+    assert L.locks_decoder_create(*args, 1 << 30, None) == 1
+    assert L.locks_decoder_create(*args, 64, ctypes.byref(out)) == 3
+    assert out.value is None
+    bad = list(args)
+    bad[10] = 1                      # k < 2
+    assert L.locks_decoder_create(*bad, 1 << 30, ctypes.byref(out)) == 1
+    bad = list(args)
+    bad[7] = 7                       # h_q not a multiple of h_kv
+    assert L.locks_decoder_create(*bad, 1 << 30, ctypes.byref(out)) == 1
+    assert L.locks_decoder_step_host(None, fake, fake, fake, None, s) == 1
+    assert L.locks_decoder_last_cuda_error(None) == 0
+    L.locks_decoder_destroy(None)
     # empty batches launch nothing and succeed
     assert L.locks_score_select(None, None, None, 0, 8, 2, 16, 4, None, None,
                                 0, s) == 0

@@ -617,6 +617,52 @@ def test_decoder_graph_replay_matches_eager(name):
     assert graph._graph is not None
 
 
+def test_native_host_decoder_matches_eager():
+    """locks_decoder_step_host (query copy in, five kernels, copies of o,
+    lse and the status word out, replayed as one CUDA graph) returns the
+    eager step's bytes, with the host buffers changed between steps (the
+    graph's copy nodes retargeted) and the bound lengths grown in place by
+    appends between steps."""
+    spec = W.custom_spec(batch=5, h_q=16, h_kv=4, ctx=16 * 70 + 5, k=10,
+                         needles=1, seed=83, ragged_min=16 * 2 + 1,
+                         append_steps=12)
+    wl = W.generate(spec, "cpu", steps=6)
+    d = Dev(wl)
+    _, _, _, lens = host(wl)
+    store, _, _, _, _ = gpu_build(d, lens)
+    lens_dev = d.seq_lens.clone()
+    eager = B.LocksDecoder(d.k_cache, d.v_cache, d.page_table, store,
+                           spec.h_q, spec.k)
+    native = B.LocksDecoder(d.k_cache, d.v_cache, d.page_table, store,
+                            spec.h_q, spec.k, graph=True, seq_lens=lens_dev)
+    shape = (spec.batch, spec.h_q, 128)
+    q_bufs = [torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+              for _ in range(2)]
+    o_bufs = [torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+              for _ in range(2)]
+    lse_buf = torch.empty(spec.batch, spec.h_q).pin_memory()
+    for step in range(6):
+        if step in (2, 4):   # one token per sequence, lengths grow on device
+            for a in range(step // 2 * 3):
+                B.locks_append_kv(wl.k_append[a % 12].to(DEV),
+                                  wl.v_append[a % 12].to(DEV), d.k_cache,
+                                  d.v_cache, d.page_table, lens_dev, store)
+        qh = q_bufs[step % 2]
+        qh.copy_(wl.queries[step])
+        oe, le = eager.step(qh.to(DEV), lens_dev.clone())
+        torch.cuda.synchronize()
+        oh, lh, st = native.step_host(qh, lens_dev, o_bufs[step % 3 % 2],
+                                      lse_buf)
+        assert st == 0 and eager.status() == 0
+        assert torch.equal(eager.idx, native.idx)
+        assert torch.equal(oe.cpu(), oh) and torch.equal(le.cpu(), lh)
+    assert native._native is not None
+    pageable = torch.empty(shape, dtype=torch.bfloat16)
+    with pytest.raises(B.LocksError):
+        native.step_host(pageable, lens_dev, o_bufs[0], lse_buf)
+    native.close()
+
+
 # ---------------------------------------------------------------------------
 # append + incremental build
 # ---------------------------------------------------------------------------
