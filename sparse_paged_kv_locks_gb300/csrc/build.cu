@@ -6,8 +6,13 @@
 // quantisation of the centroid are lane-local.  The 16x16 Gram matrix is
 // accumulated as per-lane partials and reduce-scattered across the warp; the
 // symmetric eigenproblem runs as a cyclic two-sided Jacobi iteration with the
-// round-robin (circle) ordering, eight disjoint rotations per step, on a
-// per-warp shared-memory copy of the matrix.
+// round-robin (circle) ordering, eight disjoint rotations per round.  The
+// matrix and the eigenvector accumulator live in shared memory in "slot"
+// order: slots 2m and 2m+1 always hold the two indices that round's pair m
+// rotates, and each round writes its result to the other buffer with the
+// slots moved for the next round (a fixed permutation, so every address a
+// lane touches is a constant).  A lane rotates two 2x2 blocks of the matrix
+// and its own pair's eigenvector columns; one warp barrier per round.
 #include <utility>
 
 #include "common.cuh"
@@ -18,22 +23,48 @@ namespace locks {
 constexpr int kBuildWarps = 4;
 constexpr int kMaxSweeps = 15;
 constexpr float kJacobiRelTol = 1e-7f;
+constexpr int kAS = 24;  // row stride (floats) of the Jacobi matrix copy
+constexpr int kUS = 20;  // row stride (floats) of the Jacobi vector copy
 
-struct BuildSmem {
-  float A[16][17];
-  float U[16][17];
-  float rc[8], rs[8];
-  int rp[8], rq[8];
+// 16-byte aligned so that every warp's copy keeps the float2 accesses of
+// the eigensolve aligned
+struct alignas(16) BuildSmem {
+  union {
+    struct {  // the eigensolve: slot order, double-buffered
+      float Ab[2][16][kAS];
+      float Ub[2][16][kUS];
+    } jac;
+    struct {  // after it
+      float U[16][17];  // eigenvectors (columns), index order
+      float Cf[16][8];
+      int8_t v8[128][8];
+      int8_t c8[16][8];
+      int8_t m8[128];
+    } post;
+  };
+  float ev[16];  // eigenvalues, index order
   float lam[16];
   int perm[16];
   float cv[8], cc[8];
-  float Cf[16][8];
-  int8_t v8[128][8];
-  int8_t c8[16][8];
-  int8_t m8[128];
   __half sv[8], sc[16], smu;
 };
+// the append kernel keeps one per KV head (up to 32) in one CTA
+static_assert(32 * sizeof(BuildSmem) <= 227 * 1024, "append smem");
+static_assert(sizeof(BuildSmem) % 16 == 0, "per-warp copies stay aligned");
 
+// Round-robin slots.  At round 0 of every sweep slot 2m holds index p_m and
+// slot 2m+1 index q_m of pair m (p_0 = 0, p_m = m, q_m = 15 - m); after a
+// round the index in slot a moves to slot slot_next(a).  Fifteen rounds
+// bring every index back, so sweeps start and end in this arrangement.
+__host__ __device__ constexpr int slot_index(int a) {
+  return a == 0 ? 0 : (a & 1) ? 15 - (a - 1) / 2 : a / 2;
+}
+__host__ __device__ constexpr int index_slot(int i) {
+  return i == 0 ? 0 : i <= 7 ? 2 * i : 2 * (15 - i) + 1;
+}
+__host__ __device__ constexpr int slot_next(int a) {
+  return a == 0 ? 0 : a == 2 ? 1 : a == 15 ? 14 : (a & 1) ? a + 2 : a - 2;
+}
 // Upper-triangle pair (i <= j) enumeration of the 16x16 Gram matrix.
 __host__ __device__ constexpr int pair_i(int p) {
   int i = 0;
@@ -109,7 +140,7 @@ __device__ void write_record(const float (&V)[4][8], const float (&mu)[4],
     if (lane == 0) sm.sv[k] = h;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      sm.v8[4 * lane + j][k] = (int8_t)quant_code(V[j][k], s, 7);
+      sm.post.v8[4 * lane + j][k] = (int8_t)quant_code(V[j][k], s, 7);
   }
   // centroid: one scale, int8 codes
   {
@@ -121,20 +152,20 @@ __device__ void write_record(const float (&V)[4][8], const float (&mu)[4],
     if (lane == 0) sm.smu = h;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      sm.m8[4 * lane + j] = (int8_t)quant_code(mu[j], s, 127);
+      sm.post.m8[4 * lane + j] = (int8_t)quant_code(mu[j], s, 127);
   }
   __syncwarp();
   // coefficients: one scale per row (token), int8 codes
   if (lane < 16) {
     float a = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) a = fmaxf(a, fabsf(sm.Cf[lane][k]));
+    for (int k = 0; k < 8; ++k) a = fmaxf(a, fabsf(sm.post.Cf[lane][k]));
     __half h = quant_scale(a, 127.f);
     float s = __half2float(h);
     sm.sc[lane] = h;
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-      sm.c8[lane][k] = (int8_t)quant_code(sm.Cf[lane][k], s, 127);
+      sm.post.c8[lane][k] = (int8_t)quant_code(sm.post.Cf[lane][k], s, 127);
   }
   __syncwarp();
   // V4: lane t = 4n + c owns words (4n + c)*4 + w, w = 0..3
@@ -151,7 +182,7 @@ __device__ void write_record(const float (&V)[4][8], const float (&mu)[4],
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int d = 32 * w + 16 * sp + 8 * h + 2 * c + e;
-            const uint32_t nib = (uint32_t)(sm.v8[d][n]) & 0xFu;
+            const uint32_t nib = (uint32_t)(sm.post.v8[d][n]) & 0xFu;
             word |= nib << (16 * e + 8 * sp + 4 * h);
           }
       wv[w] = word;
@@ -163,9 +194,9 @@ __device__ void write_record(const float (&V)[4][8], const float (&mu)[4],
   // i.e. the sign bit flipped)
   {
     const int gi = lane >> 2, c = lane & 3;
-    uint32_t b0 = (uint8_t)sm.c8[gi][2 * c], b1 = (uint8_t)sm.c8[gi][2 * c + 1];
-    uint32_t b2 = (uint8_t)sm.c8[gi + 8][2 * c];
-    uint32_t b3 = (uint8_t)sm.c8[gi + 8][2 * c + 1];
+    uint32_t b0 = (uint8_t)sm.post.c8[gi][2 * c], b1 = (uint8_t)sm.post.c8[gi][2 * c + 1];
+    uint32_t b2 = (uint8_t)sm.post.c8[gi + 8][2 * c];
+    uint32_t b3 = (uint8_t)sm.post.c8[gi + 8][2 * c + 1];
     *reinterpret_cast<uint32_t *>(rec + kOffC8 + 4 * lane) =
         (b0 | (b1 << 8) | (b2 << 16) | (b3 << 24)) ^ 0x80808080u;
   }
@@ -173,8 +204,8 @@ __device__ void write_record(const float (&V)[4][8], const float (&mu)[4],
   {
     const int c = lane >> 3, s = lane & 7;
     const int d0 = 16 * s + 2 * c;
-    uint32_t b0 = (uint8_t)sm.m8[d0], b1 = (uint8_t)sm.m8[d0 + 1];
-    uint32_t b2 = (uint8_t)sm.m8[d0 + 8], b3 = (uint8_t)sm.m8[d0 + 9];
+    uint32_t b0 = (uint8_t)sm.post.m8[d0], b1 = (uint8_t)sm.post.m8[d0 + 1];
+    uint32_t b2 = (uint8_t)sm.post.m8[d0 + 8], b3 = (uint8_t)sm.post.m8[d0 + 9];
     *reinterpret_cast<uint32_t *>(rec + kOffMu8 + 4 * lane) =
         (b0 | (b1 << 8) | (b2 << 16) | (b3 << 24)) ^ 0x80808080u;
   }
@@ -200,6 +231,136 @@ __device__ void write_record(const float (&V)[4][8], const float (&mu)[4],
   __syncwarp();
 }
 
+__device__ __forceinline__ void load_page_keys(const __nv_bfloat16 *page,
+                                               float (&kx)[16][4], int lane) {
+  const uint2 *src = reinterpret_cast<const uint2 *>(page);
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    const uint2 raw = src[t * 32 + lane];
+    kx[t][0] = bf16_lo(raw.x);
+    kx[t][1] = bf16_hi(raw.x);
+    kx[t][2] = bf16_lo(raw.y);
+    kx[t][3] = bf16_hi(raw.y);
+  }
+}
+
+__device__ __forceinline__ void center_keys(float (&kx)[16][4],
+                                            const float (&mu)[4]) {
+#pragma unroll
+  for (int t = 0; t < 16; ++t)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) kx[t][j] = __fsub_rn(kx[t][j], mu[j]);
+}
+
+// Rotation of the pair (p, q) that zeroes A[p][q]: t = tan(phi) is the
+// smaller root of t^2 + 2 theta t - 1 = 0 with theta = (a_qq - a_pp) /
+// (2 a_pq), c = 1 / sqrt(1 + t^2), s = t c.  Skipped (c = 1, s = 0) when
+// |a_pq| <= 1e-7 sqrt(|a_pp a_qq|) or |a_pq| <= 1e-30.
+__device__ __forceinline__ bool jacobi_rotation(float app, float aqq,
+                                                float apq, float &c,
+                                                float &s) {
+  c = 1.f;
+  s = 0.f;
+  if (!(apq * apq > kJacobiRelTol * kJacobiRelTol * fabsf(app * aqq)) ||
+      !(fabsf(apq) > 1e-30f))
+    return false;
+  const float theta = __fdividef(aqq - app, 2.f * apq);
+  float t;
+  if (fabsf(theta) > 1e15f) {
+    t = __fdividef(0.5f, theta);
+  } else {
+    const float r = fmaf(theta, theta, 1.f);
+    t = __fdividef(copysignf(1.f, theta), fabsf(theta) + r * rsqrtf(r));
+  }
+  c = rsqrtf(fmaf(t, t, 1.f));
+  s = t * c;
+  return true;
+}
+
+// A lane's fixed share of a Jacobi round: the rotation of pair pm = lane % 8
+// (from the diagonal block (pm, pm)), the matrix blocks (grp + 4j, pm) for
+// j = 0, 1 with grp = lane / 8, and rows 4 grp .. 4 grp + 3 of the vector
+// columns of pair pm.  Offsets are in floats within one buffer.
+struct JacobiLane {
+  int grp, pm;
+  int o_d;           // A[2pm][2pm]
+  int o_blk;         // A[2 grp][2 pm] (block j adds 8 kAS rows)
+  int st[2][2][2];   // destination of block element (j, x, y)
+  int o_u;           // U[4 grp][2 pm]
+  int su0, su1;      // destinations of U[4 grp][2 pm], U[4 grp][2 pm + 1]
+};
+
+__device__ __forceinline__ JacobiLane jacobi_lane(int lane) {
+  JacobiLane L;
+  L.grp = lane >> 3;
+  L.pm = lane & 7;
+  L.o_d = 2 * L.pm * kAS + 2 * L.pm;
+  L.o_blk = 2 * L.grp * kAS + 2 * L.pm;
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+#pragma unroll
+      for (int y = 0; y < 2; ++y)
+        L.st[j][x][y] = slot_next(2 * (L.grp + 4 * j) + x) * kAS +
+                        slot_next(2 * L.pm + y);
+  L.o_u = 4 * L.grp * kUS + 2 * L.pm;
+  L.su0 = 4 * L.grp * kUS + slot_next(2 * L.pm);
+  L.su1 = 4 * L.grp * kUS + slot_next(2 * L.pm + 1);
+  return L;
+}
+
+// One round: reads buffer `in`, writes buffer `in ^ 1` in the next round's
+// slot order.  Returns whether this lane's pair rotated.
+__device__ __forceinline__ int jacobi_round(const float *__restrict__ A,
+                                            float *__restrict__ An,
+                                            const float *__restrict__ U,
+                                            float *__restrict__ Un,
+                                            const JacobiLane &L) {
+  float c, s;
+  const int rot = jacobi_rotation(A[L.o_d], A[L.o_d + kAS + 1], A[L.o_d + 1],
+                                  c, s);
+  // the row pair of block j is pair grp + 4j, whose rotation lane grp + 4j
+  // computed
+  float cr[2], sr[2];
+  cr[0] = __shfl_sync(0xffffffffu, c, L.grp);
+  sr[0] = __shfl_sync(0xffffffffu, s, L.grp);
+  cr[1] = __shfl_sync(0xffffffffu, c, L.grp + 4);
+  sr[1] = __shfl_sync(0xffffffffu, s, L.grp + 4);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float2 x0 = *reinterpret_cast<const float2 *>(A + L.o_blk + 8 * j * kAS);
+    const float2 x1 =
+        *reinterpret_cast<const float2 *>(A + L.o_blk + 8 * j * kAS + kAS);
+    // rows: J^T X
+    const float r00 = cr[j] * x0.x - sr[j] * x1.x;
+    const float r10 = sr[j] * x0.x + cr[j] * x1.x;
+    const float r01 = cr[j] * x0.y - sr[j] * x1.y;
+    const float r11 = sr[j] * x0.y + cr[j] * x1.y;
+    // columns: (J^T X) J
+    float y00 = c * r00 - s * r01;
+    float y01 = s * r00 + c * r01;
+    float y10 = c * r10 - s * r11;
+    float y11 = s * r10 + c * r11;
+    if (L.grp + 4 * j == L.pm && s != 0.f) {  // the pair's own 2x2 block
+      y01 = 0.f;
+      y10 = 0.f;
+    }
+    An[L.st[j][0][0]] = y00;
+    An[L.st[j][0][1]] = y01;
+    An[L.st[j][1][0]] = y10;
+    An[L.st[j][1][1]] = y11;
+  }
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {  // U <- U J
+    const float2 u = *reinterpret_cast<const float2 *>(U + L.o_u + t * kUS);
+    Un[L.su0 + t * kUS] = c * u.x - s * u.y;
+    Un[L.su1 + t * kUS] = s * u.x + c * u.y;
+  }
+  __syncwarp();
+  return rot;
+}
+
 // Algorithm 1 up to the eigendecomposition, on one page-head held as
 // kx[token][4 dims of this lane] (bf16 values widened to fp32): centres kx
 // on the fp32 centroid mu (lane-owned entries), and leaves in sm the
@@ -215,10 +376,7 @@ __device__ void page_eigen(float (&kx)[16][4], float (&mu)[4], BuildSmem &sm,
     for (int t = 0; t < 16; ++t) acc = __fadd_rn(acc, kx[t][j]);
     mu[j] = __fmul_rn(acc, 0.0625f);
   }
-#pragma unroll
-  for (int t = 0; t < 16; ++t)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) kx[t][j] = __fsub_rn(kx[t][j], mu[j]);
+  center_keys(kx, mu);
 
   // Eq.(3): Gram matrix D D^T, 136 unique entries in 5 blocks of 32
   float g[5];
@@ -239,82 +397,66 @@ __device__ void page_eigen(float (&kx)[16][4], float (&mu)[4], BuildSmem &sm,
   for (int blk = 0; blk < 5; ++blk) {
     const int p = 32 * blk + lane;
     if (p < 136) {
-      const int i = pair_i(p), j = pair_j(p);
-      sm.A[i][j] = g[blk];
-      sm.A[j][i] = g[blk];
+      const int i = index_slot(pair_i(p)), j = index_slot(pair_j(p));
+      sm.jac.Ab[0][i][j] = g[blk];
+      sm.jac.Ab[0][j][i] = g[blk];
     }
   }
   for (int e = lane; e < 256; e += 32)
-    sm.U[e >> 4][e & 15] = ((e >> 4) == (e & 15)) ? 1.f : 0.f;
+    sm.jac.Ub[0][e >> 4][e & 15] = ((e >> 4) == (e & 15)) ? 1.f : 0.f;
   __syncwarp();
 
-  // cyclic Jacobi, round-robin pairs: round r pairs position m with 15-m
-  for (int sweep = 0; sweep < kMaxSweeps; ++sweep) {
-    int rotated = 0;
-    for (int r = 0; r < 15; ++r) {
-      if (lane < 8) {
-        const int m = lane;
-        const int p = (m == 0) ? 0 : 1 + (m - 1 + r) % 15;
-        const int q = 1 + (14 - m + r) % 15;
-        const float app = sm.A[p][p], aqq = sm.A[q][q], apq = sm.A[p][q];
-        float c = 1.f, s = 0.f;
-        if (fabsf(apq) > kJacobiRelTol * sqrtf(fabsf(app) * fabsf(aqq)) &&
-            fabsf(apq) > 1e-30f) {
-          const float theta = (aqq - app) / (2.f * apq);
-          float t;
-          if (fabsf(theta) > 1e15f)
-            t = 0.5f / theta;
-          else
-            t = copysignf(1.f, theta) /
-                (fabsf(theta) + sqrtf(1.f + theta * theta));
-          c = 1.f / sqrtf(1.f + t * t);
-          s = t * c;
-          rotated = 1;
-        }
-        sm.rc[m] = c;
-        sm.rs[m] = s;
-        sm.rp[m] = p;
-        sm.rq[m] = q;
+  // cyclic Jacobi in slot order (see slot_next): rounds alternate between
+  // the two buffers, a sweep is 15 rounds, and the iteration stops after a
+  // sweep in which no pair rotated (or after kMaxSweeps sweeps)
+  const JacobiLane L = jacobi_lane(lane);
+  float *A0 = &sm.jac.Ab[0][0][0], *A1 = &sm.jac.Ab[1][0][0];
+  float *U0 = &sm.jac.Ub[0][0][0], *U1 = &sm.jac.Ub[1][0][0];
+  int fin = 0, rotated = 0, left = 15, sweeps = 0;
+  for (;;) {
+    rotated |= jacobi_round(A0, A1, U0, U1, L);
+    if (--left == 0) {
+      if (!__any_sync(0xffffffffu, rotated) || ++sweeps >= kMaxSweeps) {
+        fin = 1;
+        break;
       }
-      __syncwarp();
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {  // rows: A <- J^T A
-        const int task = lane + 32 * u, m = task >> 4, j = task & 15;
-        const int p = sm.rp[m], q = sm.rq[m];
-        const float c = sm.rc[m], s = sm.rs[m];
-        const float ap = sm.A[p][j], aq = sm.A[q][j];
-        sm.A[p][j] = c * ap - s * aq;
-        sm.A[q][j] = s * ap + c * aq;
-      }
-      __syncwarp();
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {  // columns: A <- A J, U <- U J
-        const int task = lane + 32 * u, m = task >> 4, i = task & 15;
-        const int p = sm.rp[m], q = sm.rq[m];
-        const float c = sm.rc[m], s = sm.rs[m];
-        const float ap = sm.A[i][p], aq = sm.A[i][q];
-        sm.A[i][p] = c * ap - s * aq;
-        sm.A[i][q] = s * ap + c * aq;
-        const float up = sm.U[i][p], uq = sm.U[i][q];
-        sm.U[i][p] = c * up - s * uq;
-        sm.U[i][q] = s * up + c * uq;
-      }
-      __syncwarp();
-      if (lane < 8 && sm.rs[lane] != 0.f) {
-        sm.A[sm.rp[lane]][sm.rq[lane]] = 0.f;
-        sm.A[sm.rq[lane]][sm.rp[lane]] = 0.f;
-      }
-      __syncwarp();
+      rotated = 0;
+      left = 15;
     }
-    if (!__any_sync(0xffffffffu, rotated)) break;
+    rotated |= jacobi_round(A1, A0, U1, U0, L);
+    if (--left == 0) {
+      if (!__any_sync(0xffffffffu, rotated) || ++sweeps >= kMaxSweeps) {
+        fin = 0;
+        break;
+      }
+      rotated = 0;
+      left = 15;
+    }
   }
+
+  // back to index order: eigenvalue and eigenvector of slot a belong to
+  // index slot_index(a); the vectors' rows are in slot order as well
+  if (lane < 16) sm.ev[slot_index(lane)] = sm.jac.Ab[fin][lane][lane];
+  float uv[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int e = lane + 32 * k;
+    uv[k] = sm.jac.Ub[fin][e >> 4][e & 15];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int e = lane + 32 * k;
+    sm.post.U[slot_index(e >> 4)][slot_index(e & 15)] = uv[k];
+  }
+  __syncwarp();
 
   // eigenvalues descending (ties: lower index first), clipped at zero
   if (lane < 16) {
-    const float li = sm.A[lane][lane];
+    const float li = sm.ev[lane];
     int rank = 0;
     for (int j = 0; j < 16; ++j) {
-      const float lj = sm.A[j][j];
+      const float lj = sm.ev[j];
       rank += (lj > li) || (lj == li && j < lane);
     }
     sm.perm[rank] = lane;
@@ -335,13 +477,13 @@ __device__ __forceinline__ void component_factors(const BuildSmem &sm, int r,
     float best = -1.f;
     int bi = 0;
     for (int i = 0; i < 16; ++i) {
-      const float a = fabsf(sm.U[i][col]);
+      const float a = fabsf(sm.post.U[i][col]);
       if (a > best) {
         best = a;
         bi = i;
       }
     }
-    const float sg = sm.U[bi][col] < 0.f ? -1.f : 1.f;
+    const float sg = sm.post.U[bi][col] < 0.f ? -1.f : 1.f;
     const float lam = sm.lam[lane], lam1 = sm.lam[0];
     const bool keep = lam1 > 0.f && lam > 1e-6f * lam1;
     const float sig = sqrtf(lam);
@@ -351,14 +493,19 @@ __device__ __forceinline__ void component_factors(const BuildSmem &sm, int r,
   __syncwarp();
 }
 
-// Algorithm 1 on one page-head held as kx[token][4 dims of this lane]
-// (bf16 values widened to fp32).  Writes the record and returns tau (valid
-// on every lane).
-__device__ float summarize_page(float (&kx)[16][4], BuildSmem &sm,
+// Algorithm 1 on the page-head at `page` (bf16 [16][128]; lane l handles
+// dims 4l..4l+3).  Writes the record and returns tau (valid on every lane).
+__device__ float summarize_page(const __nv_bfloat16 *page, BuildSmem &sm,
                                 uint8_t *rec, int lane,
                                 float *unq = nullptr) {
   float mu[4];
+  float kx[16][4];
+  load_page_keys(page, kx, lane);
   page_eigen(kx, mu, sm, lane);
+  // the keys again (L2-resident), centred as before: not held in registers
+  // through the eigensolve
+  load_page_keys(page, kx, lane);
+  center_keys(kx, mu);
   // sign rule and per-component factors
   component_factors(sm, kRank, lane, sm.cv, sm.cc);
   float tau = 0.f;
@@ -373,7 +520,7 @@ __device__ float summarize_page(float (&kx)[16][4], BuildSmem &sm,
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float u = sm.U[i][col];
+      const float u = sm.post.U[i][col];
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[j] = fmaf(kx[i][j], u, acc[j]);
     }
@@ -386,7 +533,7 @@ __device__ float summarize_page(float (&kx)[16][4], BuildSmem &sm,
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const int k = k0 + kk;
-      sm.Cf[i][k] = sm.U[i][sm.perm[k]] * sm.cc[k];
+      sm.post.Cf[i][k] = sm.post.U[i][sm.perm[k]] * sm.cc[k];
     }
   }
   __syncwarp();
@@ -402,27 +549,15 @@ __device__ float summarize_page(float (&kx)[16][4], BuildSmem &sm,
     }
     const int i = lane >> 1, k0 = (lane & 1) * 4;
     reinterpret_cast<float4 *>(unq + 16 + kDim + kDim * kRank)[lane] =
-        make_float4(sm.Cf[i][k0], sm.Cf[i][k0 + 1], sm.Cf[i][k0 + 2],
-                    sm.Cf[i][k0 + 3]);
+        make_float4(sm.post.Cf[i][k0], sm.post.Cf[i][k0 + 1], sm.post.Cf[i][k0 + 2],
+                    sm.post.Cf[i][k0 + 3]);
   }
   write_record(V, mu, sm, rec, lane);
   return tau;
 }
 
-__device__ __forceinline__ void load_page_keys(const __nv_bfloat16 *page,
-                                               float (&kx)[16][4], int lane) {
-  const uint2 *src = reinterpret_cast<const uint2 *>(page);
-#pragma unroll
-  for (int t = 0; t < 16; ++t) {
-    const uint2 raw = src[t * 32 + lane];
-    kx[t][0] = bf16_lo(raw.x);
-    kx[t][1] = bf16_hi(raw.x);
-    kx[t][2] = bf16_lo(raw.y);
-    kx[t][3] = bf16_hi(raw.y);
-  }
-}
 
-__global__ void __launch_bounds__(32 * kBuildWarps)
+__global__ void __launch_bounds__(32 * kBuildWarps, 4)
     build_kernel(const __nv_bfloat16 *__restrict__ k_cache,
                  int64_t num_phys, int h_kv, const int32_t *__restrict__ pt,
                  int batch, int max_pages, const int32_t *__restrict__ seq_ids,
@@ -446,13 +581,10 @@ __global__ void __launch_bounds__(32 * kBuildWarps)
       if (lane == 0) set_status(status, LOCKS_DEV_BAD_PAGE_ID);
       continue;
     }
-    float kx[16][4];
-    load_page_keys(k_cache + ((size_t)phys * h_kv + h) * kPage * kDim, kx,
-                   lane);
     uint8_t *rec =
         summaries + (((size_t)b * h_kv + h) * max_pages + pg) * (size_t)kRec;
     const float tau = summarize_page(
-        kx, sm, rec, lane,
+        k_cache + ((size_t)phys * h_kv + h) * kPage * kDim, sm, rec, lane,
         unq_out ? unq_out + (size_t)w * LOCKS_UNQUANTISED_FLOATS : nullptr);
     if (tau_out && lane == 0) tau_out[w] = tau;
   }
@@ -490,10 +622,10 @@ __global__ void __launch_bounds__(32 * kBuildWarps)
     const float4 cv =
         reinterpret_cast<const float4 *>(coeffs + w * kPage * kRank)[lane];
     const int i = lane >> 1, k0 = (lane & 1) * 4;
-    sm.Cf[i][k0] = cv.x;
-    sm.Cf[i][k0 + 1] = cv.y;
-    sm.Cf[i][k0 + 2] = cv.z;
-    sm.Cf[i][k0 + 3] = cv.w;
+    sm.post.Cf[i][k0] = cv.x;
+    sm.post.Cf[i][k0 + 1] = cv.y;
+    sm.post.Cf[i][k0 + 2] = cv.z;
+    sm.post.Cf[i][k0 + 3] = cv.w;
     __syncwarp();
     write_record(V, m, sm, records + w * (size_t)kRec, lane);
   }
@@ -536,12 +668,10 @@ __global__ void append_kernel(const __nv_bfloat16 *__restrict__ k_new,
     if ((pos + 1) % kPage == 0) {
       // each lane re-reads exactly the bytes it wrote, so program order
       // makes the new token visible to this warp's build
-      float kx[16][4];
-      load_page_keys(k_cache + page_off, kx, lane);
       uint8_t *rec = summaries +
                      (((size_t)b * h_kv + h) * max_pages + pos / kPage) *
                          (size_t)kRec;
-      const float tau = summarize_page(kx, smem[h], rec, lane);
+      const float tau = summarize_page(k_cache + page_off, smem[h], rec, lane);
       if (tau_out && lane == 0) tau_out[(size_t)b * h_kv + h] = tau;
     }
   }
@@ -568,11 +698,15 @@ __device__ __forceinline__ int variant_stride(int r, int vbits) {
 }
 
 template <int R>
-__device__ float summarize_variant(float (&kx)[16][4], BuildSmem &sm,
+__device__ float summarize_variant(const __nv_bfloat16 *page, BuildSmem &sm,
                                    VariantSmem &vs, uint8_t *rec, int vbits,
                                    int lane) {
   float mu[4];
+  float kx[16][4];
+  load_page_keys(page, kx, lane);
   page_eigen(kx, mu, sm, lane);
+  load_page_keys(page, kx, lane);
+  center_keys(kx, mu);
   component_factors(sm, R, lane, vs.cv, vs.cc);
   float tau = 0.f;
   for (int k = R; k < 16; ++k) tau += sm.lam[k];
@@ -584,7 +718,7 @@ __device__ float summarize_variant(float (&kx)[16][4], BuildSmem &sm,
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float u = sm.U[i][col];
+      const float u = sm.post.U[i][col];
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[j] = fmaf(kx[i][j], u, acc[j]);
     }
@@ -593,7 +727,7 @@ __device__ float summarize_variant(float (&kx)[16][4], BuildSmem &sm,
   }
   for (int e = lane; e < 16 * R; e += 32) {
     const int i = e / R, k = e - i * R;
-    vs.Cf[i][k] = sm.U[i][sm.perm[k]] * vs.cc[k];
+    vs.Cf[i][k] = sm.post.U[i][sm.perm[k]] * vs.cc[k];
   }
   __syncwarp();
   const int off_c = 16 * R * vbits, off_mu = off_c + 16 * R;
@@ -659,7 +793,7 @@ __device__ float summarize_variant(float (&kx)[16][4], BuildSmem &sm,
 }
 
 template <int R>
-__global__ void __launch_bounds__(32 * kBuildWarps)
+__global__ void __launch_bounds__(32 * kBuildWarps, 4)
     build_variant_kernel(const __nv_bfloat16 *__restrict__ k_cache,
                          int64_t num_phys, int h_kv,
                          const int32_t *__restrict__ pt, int batch,
@@ -685,13 +819,11 @@ __global__ void __launch_bounds__(32 * kBuildWarps)
       if (lane == 0) set_status(status, LOCKS_DEV_BAD_PAGE_ID);
       continue;
     }
-    float kx[16][4];
-    load_page_keys(k_cache + ((size_t)phys * h_kv + h) * kPage * kDim, kx,
-                   lane);
     uint8_t *rec =
         records + (((size_t)b * h_kv + h) * max_pages + pg) * stride;
-    const float tau =
-        summarize_variant<R>(kx, smem[wid], vsm[wid], rec, vbits, lane);
+    const float tau = summarize_variant<R>(
+        k_cache + ((size_t)phys * h_kv + h) * kPage * kDim, smem[wid],
+        vsm[wid], rec, vbits, lane);
     if (tau_out && lane == 0) tau_out[w] = tau;
   }
 }
