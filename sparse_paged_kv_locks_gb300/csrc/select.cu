@@ -97,9 +97,9 @@ __device__ __forceinline__ uint4 load_keys4(const uint32_t *keys, int j0,
 // Keys live in shared memory when they fit (SMEM_KEYS), else in the
 // workspace.  Keys are indexed by page; the sink, the recent page and pages
 // past the candidates hold key 0, which is below every real key.
-constexpr int kRadixBits = 11;
+constexpr int kRadixBits = 12;
 constexpr int kRadixBins = 1 << kRadixBits;
-constexpr int kBinsPerWarp = kRadixBins / (kSelThreads / 32);  // 128
+constexpr int kBinsPerWarp = kRadixBins / (kSelThreads / 32);  // 256
 
 template <bool SMEM_KEYS, int GT>
 __global__ void __launch_bounds__(kSelThreads, 2)
@@ -164,6 +164,10 @@ __global__ void __launch_bounds__(kSelThreads, 2)
       m[g] = -INFINITY;
       s[g] = 0.f;
     }
+    // Each thread sums 2^(x - m_g) against its own reference m_g, raised
+    // (and the sum rescaled) only when a quad's maximum passes it by more
+    // than 2^6, so the common step is one exponential per score; terms stay
+    // below 2^64 and the sum below 2^77.
     for (int qd = tid; qd < nq; qd += R * blockDim.x) {
       float x[R][GT][4];
 #pragma unroll
@@ -177,14 +181,14 @@ __global__ void __launch_bounds__(kSelThreads, 2)
           if (g >= G) continue;
           const float cm = fmaxf(fmaxf(x[r][g][0], x[r][g][1]),
                                  fmaxf(x[r][g][2], x[r][g][3])) * kLog2e;
-          const float mm = fmaxf(m[g], cm);
-          if (mm != -INFINITY) {
-            float cs = 0.f;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) cs += ex2_fast(x[r][g][u] * kLog2e - mm);
-            s[g] = (m[g] == -INFINITY ? 0.f : s[g] * ex2_fast(m[g] - mm)) + cs;
-            m[g] = mm;
+          if (cm > m[g] + 64.f) {  // also the first finite score
+            s[g] = m[g] == -INFINITY ? 0.f : s[g] * ex2_fast(m[g] - cm);
+            m[g] = cm;
           }
+          const float ref = m[g] == -INFINITY ? 0.f : m[g];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            s[g] += ex2_fast(fmaf(x[r][g][u], kLog2e, -ref));
         }
       }
     }
@@ -315,7 +319,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   __syncthreads();
 
   // radix select of the (k-2)-th largest key over the varying bits,
-  // 11-bit digits from the top; key 0 never matches a candidate prefix.
+  // 12-bit digits from the top; key 0 never matches a candidate prefix.
   // Histograms alternate between two buffers so the next one is cleared
   // while the current one fills.
   const int varying = sh_varying;
@@ -337,11 +341,12 @@ __global__ void __launch_bounds__(kSelThreads, 2)
           atomicAdd(&hc[(kv[u] >> shift) & dmask], 1);
     }
     __syncthreads();
-    // warp w covers digits [bins-128(w+1), bins-128w), lane l its four
+    // warp w covers digits [bins-256(w+1), bins-256w), lane l its eight
     // digits from the top; counts are scanned from the largest digit down
-    const int hi = kRadixBins - 1 - kBinsPerWarp * wid - 4 * lane;
+    const int hi = kRadixBins - 1 - kBinsPerWarp * wid - 8 * lane;
     const int4 c4 = *reinterpret_cast<const int4 *>(hc + hi - 3);
-    const int cnt = c4.x + c4.y + c4.z + c4.w;
+    const int4 d4 = *reinterpret_cast<const int4 *>(hc + hi - 7);
+    const int cnt = c4.x + c4.y + c4.z + c4.w + d4.x + d4.y + d4.z + d4.w;
     int incl = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -354,10 +359,11 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     for (int w = 0; w < wid; ++w) before += sh_wcnt[0][w];
     const int mine = before + incl - cnt;  // count above this lane's digits
     if (mine < rem && rem <= mine + cnt) {
-      const int c[4] = {c4.w, c4.z, c4.y, c4.x};  // digits hi, hi-1, ...
+      const int c[8] = {c4.w, c4.z, c4.y, c4.x,
+                        d4.w, d4.z, d4.y, d4.x};  // digits hi, hi-1, ...
       int acc = mine;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 8; ++i) {
         if (acc < rem && rem <= acc + c[i]) {
           sh_prefix = pre | ((uint32_t)(hi - i) << shift);
           sh_mask = msk | (dmask << shift);
