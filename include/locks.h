@@ -88,6 +88,15 @@ typedef enum {
  * the group gives them; group-mass by the group's pooled unnormalised page
  * mass sum_g exp(s_hat[g][j]).  Per-head selection (each query head its own
  * page set) needs no rule: call locks_select_pages with h_kv = h_q. */
+/* Build flags (locks_build_summaries_ex, locks_append_kv_ex,
+ * locks_pack_summaries_ex).  0 = one basis scale per column, as the reading
+ * notes' Algorithm 1 stores it (the default).  LOCKS_BUILD_VSCALE_PER_PAGE
+ * is the alternative reading of the basis scale: one fp16 scale
+ * sV = fp16(max over all 128 x 8 entries of |V| / 7) for the whole page,
+ * written into all eight column slots, so the record layout and every
+ * scoring call are unchanged. */
+#define LOCKS_BUILD_VSCALE_PER_PAGE 0x1
+
 #define LOCKS_MERGE_SHARE_AVERAGE 0
 #define LOCKS_MERGE_GROUP_MAX 1
 #define LOCKS_MERGE_GROUP_MASS 2
@@ -144,6 +153,15 @@ locks_status_t locks_build_summaries(
     void *summaries, float *tau_out, float *unquantised_out, int32_t *status,
     locks_stream_t stream);
 
+/* locks_build_summaries with build flags (LOCKS_BUILD_*); flags = 0 is
+ * locks_build_summaries.  Unknown flag bits return LOCKS_ERR_INVALID_ARG. */
+locks_status_t locks_build_summaries_ex(
+    const void *k_cache, int64_t num_phys_pages, int h_kv,
+    const int32_t *page_table, int batch, int max_pages,
+    const int32_t *seq_ids, const int32_t *page_ids, int n_pairs,
+    void *summaries, float *tau_out, float *unquantised_out, int flags,
+    int32_t *status, locks_stream_t stream);
+
 /* Rank / precision variants of the page summary (LOCKS reading notes §6
  * ablation "rank and quantisation precision": int8, int4 and int2 bases at
  * several ranks).  A variant record of rank r in {4, 8, 12, 15} with a
@@ -194,6 +212,12 @@ locks_status_t locks_score_variant(const void *q, const void *records,
 locks_status_t locks_pack_summaries(const float *mu, const float *basis,
                                     const float *coeffs, int n,
                                     void *records, locks_stream_t stream);
+
+/* locks_pack_summaries with build flags (LOCKS_BUILD_*). */
+locks_status_t locks_pack_summaries_ex(const float *mu, const float *basis,
+                                       const float *coeffs, int n,
+                                       void *records, int flags,
+                                       locks_stream_t stream);
 
 /* Score and select, LOCKS reading notes §4.2 Eq.(4)-(5) and §4.4
  * Algorithm 2, one decode step: for every full page j of every (sequence b,
@@ -334,6 +358,16 @@ locks_status_t locks_append_kv(const void *k_new, const void *v_new,
                                int max_pages, int32_t *seq_lens,
                                void *summaries, float *tau_out,
                                int32_t *status, locks_stream_t stream);
+
+/* locks_append_kv with build flags (LOCKS_BUILD_*) for the pages it
+ * builds; use the flags the store was built with. */
+locks_status_t locks_append_kv_ex(const void *k_new, const void *v_new,
+                                  void *k_cache, void *v_cache,
+                                  int64_t num_phys_pages, int h_kv,
+                                  const int32_t *page_table, int batch,
+                                  int max_pages, int32_t *seq_lens,
+                                  void *summaries, float *tau_out, int flags,
+                                  int32_t *status, locks_stream_t stream);
 
 /* Decoder object: one layer's decode step driven from host buffers (the
  * decode path of LOCKS reading notes §2 Fig. 1: score every page summary,

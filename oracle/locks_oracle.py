@@ -137,15 +137,27 @@ def _codes(x_f32: np.ndarray, s16: np.ndarray, qmax: int) -> np.ndarray:
     return np.clip(c, -qmax, qmax).astype(np.int8)
 
 
-def quantize_summary(mu32, V32, C32):
+VSCALE_MODES = ("column", "page")
+
+
+def quantize_summary(mu32, V32, C32, vscale="column"):
     """Storage paragraph of §4.1 / Algorithm 1: int4 basis with a per-column
-    scale, int8 coefficients with a per-row scale, int8 centroid."""
+    scale, int8 coefficients with a per-row scale, int8 centroid.
+
+    vscale="page" is the other reading of the basis scale (one fp16 scale
+    for the whole page's basis, the absolute maximum over every column; the
+    record still stores it once per column, eight equal values)."""
+    if vscale not in VSCALE_MODES:
+        raise ValueError(f"vscale must be one of {VSCALE_MODES}")
     mu32 = np.asarray(mu32, np.float32)
     V32 = np.asarray(V32, np.float32)
     C32 = np.asarray(C32, np.float32)
     smu = _scale(np.abs(mu32).max(axis=-1), 127)
     mu8 = _codes(mu32, smu[..., None], 127)
-    sV = _scale(np.abs(V32).max(axis=-2), 7)
+    absV = np.abs(V32).max(axis=-2)                                # [..., r]
+    if vscale == "page":
+        absV = np.broadcast_to(absV.max(axis=-1, keepdims=True), absV.shape)
+    sV = _scale(absV, 7)
     V4 = _codes(V32, sV[..., None, :], 7)
     sC = _scale(np.abs(C32).max(axis=-1), 127)
     C8 = _codes(C32, sC[..., :, None], 127)
@@ -161,13 +173,14 @@ def dequantize(q):
     return mu, V, C
 
 
-def build_page(keys_bf16_as_f32: np.ndarray):
+def build_page(keys_bf16_as_f32: np.ndarray, vscale="column"):
     """Algorithm 1 for full pages, keys [..., 16, 128] holding bf16 values.
 
     Returns (quantised summary dict, unquantised summary dict)."""
     s = page_summary(keys_bf16_as_f32, RANK)
     q = quantize_summary(centroid_f32(keys_bf16_as_f32),
-                         s["V"].astype(np.float32), s["C"].astype(np.float32))
+                         s["V"].astype(np.float32), s["C"].astype(np.float32),
+                         vscale)
     return q, s
 
 
@@ -365,7 +378,7 @@ def decode_records(rec: np.ndarray):
 
 
 def build_summaries(k_cache, page_table, seq_ids, page_ids, batch, max_pages,
-                    store=None):
+                    store=None, vscale="column"):
     """Algorithm 1 over listed (sequence, logical page) pairs, every KV head.
 
     k_cache [P][h_kv][16][128] (float32 holding bf16 values), page_table
@@ -379,7 +392,7 @@ def build_summaries(k_cache, page_table, seq_ids, page_ids, batch, max_pages,
     page_ids = np.asarray(page_ids, dtype=np.int64)
     phys = np.asarray(page_table)[seq_ids, page_ids].astype(np.int64)
     keys = k_cache[phys]                                 # [n][h_kv][16][128]
-    q, s = build_page(keys)
+    q, s = build_page(keys, vscale)
     rec = encode_records(q)                              # [n][h_kv][832]
     for h in range(h_kv):
         store[seq_ids, h, page_ids] = rec[:, h]

@@ -31,6 +31,8 @@ DEV_BAD_SEQ_LEN = 0x4
 DEV_BAD_PAIR = 0x8
 DEV_TIMEOUT = 0x10
 
+BUILD_VSCALE_PER_PAGE = 0x1   # one basis scale per page (see locks.h)
+
 
 class LocksError(RuntimeError):
     pass
@@ -51,6 +53,11 @@ _SIGS = {
     "locks_build_summaries": (_I, [_P, _I64, _I, _P, _I, _I, _P, _P, _I, _P,
                                    _P, _P, _P, _P]),
     "locks_pack_summaries": (_I, [_P, _P, _P, _I, _P, _P]),
+    "locks_pack_summaries_ex": (_I, [_P, _P, _P, _I, _P, _I, _P]),
+    "locks_build_summaries_ex": (_I, [_P, _I64, _I, _P, _I, _I, _P, _P, _I,
+                                      _P, _P, _P, _I, _P, _P]),
+    "locks_append_kv_ex": (_I, [_P, _P, _P, _P, _I64, _I, _P, _I, _I, _P, _P,
+                                _P, _I, _P, _P]),
     "locks_score_select": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ,
                                 _P]),
     "locks_score_pages": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
@@ -170,7 +177,7 @@ UNQUANTISED_FLOATS = 1296
 
 def locks_build_summaries(k_cache, page_table, seq_ids, page_ids, summaries,
                           tau_out=None, unquantised_out=None, status=None,
-                          stream=None):
+                          stream=None, flags=0):
     _req(k_cache, "k_cache", torch.bfloat16, 4)
     _req(page_table, "page_table", torch.int32, 2)
     _req(seq_ids, "seq_ids", torch.int32, 1)
@@ -196,13 +203,13 @@ def locks_build_summaries(k_cache, page_table, seq_ids, page_ids, summaries,
                              "floats")
     if status is not None:
         _req(status, "status", torch.int32)
-    _check("locks_build_summaries", lib().locks_build_summaries(
+    _check("locks_build_summaries_ex", lib().locks_build_summaries_ex(
         _ptr(k_cache), P, h_kv, _ptr(page_table), batch, max_pages,
         _ptr(seq_ids), _ptr(page_ids), n, _ptr(summaries), _ptr(tau_out),
-        _ptr(unquantised_out), _ptr(status), _stream(stream)))
+        _ptr(unquantised_out), flags, _ptr(status), _stream(stream)))
 
 
-def locks_pack_summaries(mu, basis, coeffs, records, stream=None):
+def locks_pack_summaries(mu, basis, coeffs, records, stream=None, flags=0):
     _req(mu, "mu", torch.float32, 2)
     _req(basis, "basis", torch.float32, 3)
     _req(coeffs, "coeffs", torch.float32, 3)
@@ -213,8 +220,8 @@ def locks_pack_summaries(mu, basis, coeffs, records, stream=None):
         raise ValueError("mu [n][128], basis [n][128][8], coeffs [n][16][8]")
     if records.numel() < n * RECORD_BYTES:
         raise ValueError("records must hold n*832 bytes")
-    _check("locks_pack_summaries", lib().locks_pack_summaries(
-        _ptr(mu), _ptr(basis), _ptr(coeffs), n, _ptr(records),
+    _check("locks_pack_summaries_ex", lib().locks_pack_summaries_ex(
+        _ptr(mu), _ptr(basis), _ptr(coeffs), n, _ptr(records), flags,
         _stream(stream)))
 
 
@@ -388,7 +395,8 @@ def locks_sparse_decode(q, k_cache, v_cache, page_table, seq_lens, idx, k,
 
 
 def locks_append_kv(k_new, v_new, k_cache, v_cache, page_table, seq_lens,
-                    summaries, tau_out=None, status=None, stream=None):
+                    summaries, tau_out=None, status=None, stream=None,
+                    flags=0):
     _req(k_new, "k_new", torch.bfloat16, 3)
     _req(v_new, "v_new", torch.bfloat16, 3)
     _req(k_cache, "k_cache", torch.bfloat16, 4)
@@ -404,10 +412,10 @@ def locks_append_kv(k_new, v_new, k_cache, v_cache, page_table, seq_lens,
         _req(tau_out, "tau_out", torch.float32)
     if status is not None:
         _req(status, "status", torch.int32)
-    _check("locks_append_kv", lib().locks_append_kv(
+    _check("locks_append_kv_ex", lib().locks_append_kv_ex(
         _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), P, h_kv,
         _ptr(page_table), batch, max_pages, _ptr(seq_lens), _ptr(summaries),
-        _ptr(tau_out), _ptr(status), _stream(stream)))
+        _ptr(tau_out), flags, _ptr(status), _stream(stream)))
 
 
 def locks_clear_status(status_word, stream=None):

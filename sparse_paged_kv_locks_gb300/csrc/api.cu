@@ -165,22 +165,38 @@ locks_status_t locks_workspace_size(int batch, int h_q, int h_kv,
   return LOCKS_OK;
 }
 
+static bool build_flags_ok(int flags) {
+  return (flags & ~LOCKS_BUILD_VSCALE_PER_PAGE) == 0;
+}
+
 locks_status_t locks_build_summaries(
     const void *k_cache, int64_t num_phys_pages, int h_kv,
     const int32_t *page_table, int batch, int max_pages,
     const int32_t *seq_ids, const int32_t *page_ids, int n_pairs,
     void *summaries, float *tau_out, float *unquantised_out, int32_t *status,
     locks_stream_t stream) {
+  return locks_build_summaries_ex(k_cache, num_phys_pages, h_kv, page_table,
+                                  batch, max_pages, seq_ids, page_ids, n_pairs,
+                                  summaries, tau_out, unquantised_out, 0,
+                                  status, stream);
+}
+
+locks_status_t locks_build_summaries_ex(
+    const void *k_cache, int64_t num_phys_pages, int h_kv,
+    const int32_t *page_table, int batch, int max_pages,
+    const int32_t *seq_ids, const int32_t *page_ids, int n_pairs,
+    void *summaries, float *tau_out, float *unquantised_out, int flags,
+    int32_t *status, locks_stream_t stream) {
   if (n_pairs < 0 || h_kv < 1 || batch < 1 || max_pages < 1 ||
-      num_phys_pages < 1)
+      num_phys_pages < 1 || !build_flags_ok(flags))
     return LOCKS_ERR_INVALID_ARG;
   if (n_pairs == 0) return LOCKS_OK;
   if (!k_cache || !page_table || !seq_ids || !page_ids || !summaries)
     return LOCKS_ERR_INVALID_ARG;
   cudaError_t e = launch_build(k_cache, num_phys_pages, h_kv, page_table,
                                batch, max_pages, seq_ids, page_ids, n_pairs,
-                               summaries, tau_out, unquantised_out, status,
-                               (cudaStream_t)stream);
+                               summaries, tau_out, unquantised_out, flags,
+                               status, (cudaStream_t)stream);
   return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
 }
 
@@ -238,11 +254,18 @@ locks_status_t locks_score_variant(const void *q, const void *records,
 locks_status_t locks_pack_summaries(const float *mu, const float *basis,
                                     const float *coeffs, int n, void *records,
                                     locks_stream_t stream) {
-  if (n < 0) return LOCKS_ERR_INVALID_ARG;
+  return locks_pack_summaries_ex(mu, basis, coeffs, n, records, 0, stream);
+}
+
+locks_status_t locks_pack_summaries_ex(const float *mu, const float *basis,
+                                       const float *coeffs, int n,
+                                       void *records, int flags,
+                                       locks_stream_t stream) {
+  if (n < 0 || !build_flags_ok(flags)) return LOCKS_ERR_INVALID_ARG;
   if (n == 0) return LOCKS_OK;
   if (!mu || !basis || !coeffs || !records) return LOCKS_ERR_INVALID_ARG;
-  cudaError_t e =
-      launch_pack(mu, basis, coeffs, n, records, (cudaStream_t)stream);
+  cudaError_t e = launch_pack(mu, basis, coeffs, n, records, flags,
+                              (cudaStream_t)stream);
   return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
 }
 
@@ -353,7 +376,20 @@ locks_status_t locks_append_kv(const void *k_new, const void *v_new,
                                int max_pages, int32_t *seq_lens,
                                void *summaries, float *tau_out,
                                int32_t *status, locks_stream_t stream) {
-  if (batch < 0 || h_kv < 1 || max_pages < 1 || num_phys_pages < 1)
+  return locks_append_kv_ex(k_new, v_new, k_cache, v_cache, num_phys_pages,
+                            h_kv, page_table, batch, max_pages, seq_lens,
+                            summaries, tau_out, 0, status, stream);
+}
+
+locks_status_t locks_append_kv_ex(const void *k_new, const void *v_new,
+                                  void *k_cache, void *v_cache,
+                                  int64_t num_phys_pages, int h_kv,
+                                  const int32_t *page_table, int batch,
+                                  int max_pages, int32_t *seq_lens,
+                                  void *summaries, float *tau_out, int flags,
+                                  int32_t *status, locks_stream_t stream) {
+  if (batch < 0 || h_kv < 1 || max_pages < 1 || num_phys_pages < 1 ||
+      !build_flags_ok(flags))
     return LOCKS_ERR_INVALID_ARG;
   if (h_kv > 32) return LOCKS_ERR_UNSUPPORTED;
   if (batch == 0) return LOCKS_OK;
@@ -362,7 +398,7 @@ locks_status_t locks_append_kv(const void *k_new, const void *v_new,
     return LOCKS_ERR_INVALID_ARG;
   cudaError_t e = launch_append(k_new, v_new, k_cache, v_cache, num_phys_pages,
                                 h_kv, page_table, batch, max_pages, seq_lens,
-                                summaries, tau_out, status,
+                                summaries, tau_out, flags, status,
                                 (cudaStream_t)stream);
   return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
 }

@@ -126,15 +126,26 @@ __device__ __forceinline__ float warp_max(float x) {
 
 // Quantise (storage paragraph of §4.1) and write one 832-byte record.
 // V: lane-owned rows 4l..4l+3 of the fp32 basis; mu: lane-owned centroid
-// entries; sm.Cf: fp32 coefficients [16][8].
+// entries; sm.post.Cf: fp32 coefficients [16][8].  vpage: one basis scale
+// for the whole page (absolute maximum over every column), stored in all
+// eight column slots; otherwise one per column.
 __device__ void write_record(const float (&V)[4][8], const float (&mu)[4],
-                             BuildSmem &sm, uint8_t *rec, int lane) {
-  // basis: one scale per column, int4 codes
+                             BuildSmem &sm, uint8_t *rec, int lane,
+                             bool vpage) {
+  float apage = 0.f;
+  if (vpage) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) apage = fmaxf(apage, fabsf(V[j][k]));
+    apage = warp_max(apage);
+  }
+  // basis: int4 codes
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     float a = fmaxf(fmaxf(fabsf(V[0][k]), fabsf(V[1][k])),
                     fmaxf(fabsf(V[2][k]), fabsf(V[3][k])));
-    a = warp_max(a);
+    a = vpage ? apage : warp_max(a);
     __half h = quant_scale(a, 7.f);
     float s = __half2float(h);
     if (lane == 0) sm.sv[k] = h;
@@ -496,7 +507,7 @@ __device__ __forceinline__ void component_factors(const BuildSmem &sm, int r,
 // Algorithm 1 on the page-head at `page` (bf16 [16][128]; lane l handles
 // dims 4l..4l+3).  Writes the record and returns tau (valid on every lane).
 __device__ float summarize_page(const __nv_bfloat16 *page, BuildSmem &sm,
-                                uint8_t *rec, int lane,
+                                uint8_t *rec, int lane, bool vpage,
                                 float *unq = nullptr) {
   float mu[4];
   float kx[16][4];
@@ -552,7 +563,7 @@ __device__ float summarize_page(const __nv_bfloat16 *page, BuildSmem &sm,
         make_float4(sm.post.Cf[i][k0], sm.post.Cf[i][k0 + 1], sm.post.Cf[i][k0 + 2],
                     sm.post.Cf[i][k0 + 3]);
   }
-  write_record(V, mu, sm, rec, lane);
+  write_record(V, mu, sm, rec, lane, vpage);
   return tau;
 }
 
@@ -563,8 +574,9 @@ __global__ void __launch_bounds__(32 * kBuildWarps, 4)
                  int batch, int max_pages, const int32_t *__restrict__ seq_ids,
                  const int32_t *__restrict__ page_ids, int n_pairs,
                  uint8_t *__restrict__ summaries, float *__restrict__ tau_out,
-                 float *__restrict__ unq_out, int32_t *status) {
+                 float *__restrict__ unq_out, int flags, int32_t *status) {
   __shared__ BuildSmem smem[kBuildWarps];
+  const bool vpage = (flags & LOCKS_BUILD_VSCALE_PER_PAGE) != 0;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   BuildSmem &sm = smem[wid];
   const long long total = (long long)n_pairs * h_kv;
@@ -585,6 +597,7 @@ __global__ void __launch_bounds__(32 * kBuildWarps, 4)
         summaries + (((size_t)b * h_kv + h) * max_pages + pg) * (size_t)kRec;
     const float tau = summarize_page(
         k_cache + ((size_t)phys * h_kv + h) * kPage * kDim, sm, rec, lane,
+        vpage,
         unq_out ? unq_out + (size_t)w * LOCKS_UNQUANTISED_FLOATS : nullptr);
     if (tau_out && lane == 0) tau_out[w] = tau;
   }
@@ -593,7 +606,7 @@ __global__ void __launch_bounds__(32 * kBuildWarps, 4)
 __global__ void __launch_bounds__(32 * kBuildWarps)
     pack_kernel(const float *__restrict__ mu, const float *__restrict__ basis,
                 const float *__restrict__ coeffs, int n,
-                uint8_t *__restrict__ records) {
+                uint8_t *__restrict__ records, int flags) {
   __shared__ BuildSmem smem[kBuildWarps];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   BuildSmem &sm = smem[wid];
@@ -627,7 +640,8 @@ __global__ void __launch_bounds__(32 * kBuildWarps)
     sm.post.Cf[i][k0 + 2] = cv.z;
     sm.post.Cf[i][k0 + 3] = cv.w;
     __syncwarp();
-    write_record(V, m, sm, records + w * (size_t)kRec, lane);
+    write_record(V, m, sm, records + w * (size_t)kRec, lane,
+                 (flags & LOCKS_BUILD_VSCALE_PER_PAGE) != 0);
   }
 }
 
@@ -638,7 +652,7 @@ __global__ void append_kernel(const __nv_bfloat16 *__restrict__ k_new,
                               int64_t num_phys, int h_kv,
                               const int32_t *__restrict__ pt, int max_pages,
                               int32_t *seq_lens, uint8_t *summaries,
-                              float *tau_out, int32_t *status) {
+                              float *tau_out, int flags, int32_t *status) {
   extern __shared__ __align__(16) unsigned char append_smem[];
   BuildSmem *smem = reinterpret_cast<BuildSmem *>(append_smem);
   const int b = blockIdx.x;
@@ -671,7 +685,9 @@ __global__ void append_kernel(const __nv_bfloat16 *__restrict__ k_new,
       uint8_t *rec = summaries +
                      (((size_t)b * h_kv + h) * max_pages + pos / kPage) *
                          (size_t)kRec;
-      const float tau = summarize_page(k_cache + page_off, smem[h], rec, lane);
+      const float tau =
+          summarize_page(k_cache + page_off, smem[h], rec, lane,
+                         (flags & LOCKS_BUILD_VSCALE_PER_PAGE) != 0);
       if (tau_out && lane == 0) tau_out[(size_t)b * h_kv + h] = tau;
     }
   }
@@ -841,14 +857,14 @@ cudaError_t launch_build(const void *k_cache, int64_t num_phys, int h_kv,
                          const int32_t *pt, int batch, int max_pages,
                          const int32_t *seq_ids, const int32_t *page_ids,
                          int n_pairs, void *summaries, float *tau_out,
-                         float *unq_out, int32_t *status,
+                         float *unq_out, int flags, int32_t *status,
                          cudaStream_t stream) {
   const long long warps = (long long)n_pairs * h_kv;
   if (warps == 0) return cudaSuccess;
   build_kernel<<<grid_for(warps, kBuildWarps), 32 * kBuildWarps, 0, stream>>>(
       static_cast<const __nv_bfloat16 *>(k_cache), num_phys, h_kv, pt, batch,
       max_pages, seq_ids, page_ids, n_pairs,
-      static_cast<uint8_t *>(summaries), tau_out, unq_out, status);
+      static_cast<uint8_t *>(summaries), tau_out, unq_out, flags, status);
   return cudaGetLastError();
 }
 
@@ -880,11 +896,11 @@ cudaError_t launch_build_variant(const void *k_cache, int64_t num_phys,
 }
 
 cudaError_t launch_pack(const float *mu, const float *basis,
-                        const float *coeffs, int n, void *records,
+                        const float *coeffs, int n, void *records, int flags,
                         cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
   pack_kernel<<<grid_for(n, kBuildWarps), 32 * kBuildWarps, 0, stream>>>(
-      mu, basis, coeffs, n, static_cast<uint8_t *>(records));
+      mu, basis, coeffs, n, static_cast<uint8_t *>(records), flags);
   return cudaGetLastError();
 }
 
@@ -892,7 +908,7 @@ cudaError_t launch_append(const void *k_new, const void *v_new, void *k_cache,
                           void *v_cache, int64_t num_phys, int h_kv,
                           const int32_t *pt, int batch, int max_pages,
                           int32_t *seq_lens, void *summaries, float *tau_out,
-                          int32_t *status, cudaStream_t stream) {
+                          int flags, int32_t *status, cudaStream_t stream) {
   if (batch == 0) return cudaSuccess;
   const size_t smem = sizeof(BuildSmem) * (size_t)h_kv;
   static bool attr_set = false;
@@ -908,7 +924,7 @@ cudaError_t launch_append(const void *k_new, const void *v_new, void *k_cache,
       static_cast<const __nv_bfloat16 *>(v_new),
       static_cast<__nv_bfloat16 *>(k_cache),
       static_cast<__nv_bfloat16 *>(v_cache), num_phys, h_kv, pt, max_pages,
-      seq_lens, static_cast<uint8_t *>(summaries), tau_out, status);
+      seq_lens, static_cast<uint8_t *>(summaries), tau_out, flags, status);
   return cudaGetLastError();
 }
 

@@ -21,18 +21,18 @@ cudaError_t launch_build(const void *k_cache, int64_t num_phys, int h_kv,
                          const int32_t *pt, int batch, int max_pages,
                          const int32_t *seq_ids, const int32_t *page_ids,
                          int n_pairs, void *summaries, float *tau_out,
-                         float *unq_out, int32_t *status,
+                         float *unq_out, int flags, int32_t *status,
                          cudaStream_t stream);
 
 cudaError_t launch_pack(const float *mu, const float *basis,
-                        const float *coeffs, int n, void *records,
+                        const float *coeffs, int n, void *records, int flags,
                         cudaStream_t stream);
 
 cudaError_t launch_append(const void *k_new, const void *v_new, void *k_cache,
                           void *v_cache, int64_t num_phys, int h_kv,
                           const int32_t *pt, int batch, int max_pages,
                           int32_t *seq_lens, void *summaries, float *tau_out,
-                          int32_t *status, cudaStream_t stream);
+                          int flags, int32_t *status, cudaStream_t stream);
 
 // after_query: launch as a programmatic dependent of the preceding kernel,
 // which may write only the query (the kernel reads seq_lens and the

@@ -51,7 +51,7 @@ def i32(x):
     return torch.as_tensor(np.asarray(x), dtype=torch.int32, device=DEV)
 
 
-def gpu_build(wl_dev, lens, want_unq=False):
+def gpu_build(wl_dev, lens, want_unq=False, flags=0):
     seq, pg = full_pairs(lens)
     batch, max_pages = wl_dev.page_table.shape
     h_kv = wl_dev.k_cache.shape[1]
@@ -61,7 +61,7 @@ def gpu_build(wl_dev, lens, want_unq=False):
                       dtype=torch.float32, device=DEV) if want_unq else None
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     B.locks_build_summaries(wl_dev.k_cache, wl_dev.page_table, i32(seq),
-                            i32(pg), store, tau, unq, status)
+                            i32(pg), store, tau, unq, status, flags=flags)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     return store, tau, unq, seq, pg
@@ -115,7 +115,8 @@ def selection_agrees(idx_gpu, idx_orc, s_hat_bh, L, k, window):
 # ---------------------------------------------------------------------------
 # quantiser and record layout: bit-exact
 # ---------------------------------------------------------------------------
-def test_pack_is_bit_exact():
+@pytest.mark.parametrize("vscale", ["column", "page"])
+def test_pack_is_bit_exact(vscale):
     rng = np.random.default_rng(0)
     n = 300
     mu = rng.normal(0, 0.5, (n, 128)).astype(np.float32)
@@ -131,12 +132,14 @@ def test_pack_is_bit_exact():
     V[5, :, 0] = 0.0
     V[5, 0, 0] = 7 * 0.0625
     V[5, 1:8, 0] = np.array([3.5, 2.5, -2.5, -3.5, 0.5, -0.5, 1.5]) * 0.0625
-    q = O.quantize_summary(mu, V, C)
+    q = O.quantize_summary(mu, V, C, vscale)
     expect = O.encode_records(q)
     rec = torch.zeros(n * 832, dtype=torch.uint8, device=DEV)
     B.locks_pack_summaries(torch.from_numpy(mu).to(DEV),
                            torch.from_numpy(V).to(DEV),
-                           torch.from_numpy(C).to(DEV), rec)
+                           torch.from_numpy(C).to(DEV), rec,
+                           flags=B.BUILD_VSCALE_PER_PAGE if vscale == "page"
+                           else 0)
     got = rec.view(n, 832).cpu().numpy()
     bad = np.nonzero((got != expect).any(axis=1))[0]
     assert bad.size == 0, f"records differ: {bad[:10]}"
@@ -237,6 +240,31 @@ def test_build_matches_oracle(which):
     C8g = gq["C8"].astype(np.int64) * sgn[..., None, :].astype(np.int64)
     dc = np.abs(C8g - q8["C8"])[full]
     assert dc.max(initial=0) <= 1 and (dc > 0).mean() < 0.01
+
+
+def test_build_per_page_basis_scale():
+    """LOCKS_BUILD_VSCALE_PER_PAGE: the records are the oracle's per-page
+    quantiser applied to the build's own fp32 values (bit for bit), and the
+    eigensolve, coefficients and centroid are those of the default build."""
+    wl = W.generate(W.SPECS["tiny_4k"], "cpu")
+    d = Dev(wl)
+    _, _, _, lens = host(wl)
+    col, _, unq_c, seq, pg = gpu_build(d, lens, want_unq=True)
+    page, _, unq_p, _, _ = gpu_build(d, lens, want_unq=True,
+                                     flags=B.BUILD_VSCALE_PER_PAGE)
+    assert torch.equal(unq_c, unq_p)
+    h_kv = d.k_cache.shape[1]
+    u = unq_p.view(len(seq), h_kv, -1).cpu().numpy()
+    q = O.quantize_summary(u[..., 16:144], u[..., 144:1168].reshape(
+        len(seq), h_kv, 128, 8), u[..., 1168:].reshape(len(seq), h_kv, 16, 8),
+        vscale="page")
+    got = page.cpu().numpy()[seq, :, pg]
+    assert np.array_equal(got, O.encode_records(q))
+    gq = O.decode_records(got)
+    assert (gq["sV"] == gq["sV"][..., :1]).all()
+    cq = O.decode_records(col.cpu().numpy()[seq, :, pg])
+    assert (cq["C8"] == gq["C8"]).all() and (cq["mu8"] == gq["mu8"]).all()
+    assert (gq["sV"][..., 0] == cq["sV"].max(axis=-1)).all()
 
 
 # ---------------------------------------------------------------------------
@@ -666,6 +694,39 @@ def test_native_host_decoder_matches_eager():
 # ---------------------------------------------------------------------------
 # append + incremental build
 # ---------------------------------------------------------------------------
+def test_append_per_page_scale_matches_build():
+    """Pages filled by appends with LOCKS_BUILD_VSCALE_PER_PAGE carry the
+    record a per-page build of the final cache gives, byte for byte."""
+    spec = W.custom_spec(batch=2, h_q=8, h_kv=2, ctx=16 * 5 + 9, k=4,
+                         steps=20, needles=0, seed=19, append_steps=20)
+    wl = W.generate(spec, "cpu")
+    d = Dev(wl)
+    batch, max_pages = wl.page_table.shape
+    flags = B.BUILD_VSCALE_PER_PAGE
+    lens0 = [int(x) for x in wl.seq_lens]
+    seq, pg = full_pairs(lens0)
+    store = B.new_summary_store(batch, spec.h_kv, max_pages, DEV)
+    B.locks_build_summaries(d.k_cache, d.page_table, i32(seq), i32(pg), store,
+                            flags=flags)
+    seq_lens = d.seq_lens.clone()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for s in range(spec.append_steps):
+        B.locks_append_kv(wl.k_append[s].to(DEV), wl.v_append[s].to(DEV),
+                          d.k_cache, d.v_cache, d.page_table, seq_lens, store,
+                          status=status, flags=flags)
+    lens1 = [L + spec.append_steps for L in lens0]
+    seq1, pg1 = full_pairs(lens1)
+    fresh = B.new_summary_store(batch, spec.h_kv, max_pages, DEV)
+    B.locks_build_summaries(d.k_cache, d.page_table, i32(seq1), i32(pg1),
+                            fresh, flags=flags)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for b, p in zip(seq1, pg1):
+        assert torch.equal(store[b, :, p], fresh[b, :, p]), (b, p)
+    rec = O.decode_records(fresh.cpu().numpy()[seq1, :, pg1])
+    assert (rec["sV"] == rec["sV"][..., :1]).all()
+
+
 def test_append_builds_filled_pages():
     spec = W.custom_spec(batch=3, h_q=8, h_kv=2, ctx=16 * 6 + 13, k=4,
                          steps=20, needles=0, seed=9, append_steps=20)

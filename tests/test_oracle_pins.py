@@ -467,6 +467,47 @@ def test_quantiser_invariants():
     assert big[0] == np.float16(65504)
 
 
+def test_per_page_basis_scale():
+    """The per-page reading of the basis scale: one fp16 scale for the page,
+    fp16(max over every column of |V| / 7), stored once per column."""
+    # hand example: column k holds one non-zero entry; page scale
+    # fp16(14 / 7) = 2, codes rint(V / 2), halves to even
+    V = np.zeros((1, 128, 8), np.float32)
+    for k, (d, v) in enumerate([(0, 14.0), (1, 3.5), (2, -7.0), (3, 5.0),
+                                (4, 1.0), (5, 3.0), (6, -2.9), (7, 0.0)]):
+        V[0, d, k] = v
+    mu = np.ones((1, 128), np.float32)
+    C = np.ones((1, 16, 8), np.float32)
+    q = O.quantize_summary(mu, V, C, vscale="page")
+    assert (q["sV"] == np.float16(2.0)).all()
+    assert [int(q["V4"][0, k, k]) for k in range(8)] == [7, 2, -4, 2, 0, 2,
+                                                         -1, 0]
+    col = O.quantize_summary(mu, V, C)
+    assert col["sV"][0].tolist() == [2.0, 0.5, 1.0, np.float16(5 / 7),
+                                     np.float16(1 / 7), np.float16(3 / 7),
+                                     np.float16(np.float32(2.9) / 7), 0.0]
+    # random pages: the page scale is the largest column scale (fp16
+    # rounding is monotone), the page's largest entry codes to +-7, and
+    # every entry is within half a step
+    rng = _rng(31)
+    V = (rng.normal(size=(30, 128, 8)) * rng.uniform(0.01, 3, (30, 1, 8))
+         ).astype(np.float32)
+    qp = O.quantize_summary(np.ones((30, 128), np.float32), V,
+                            np.ones((30, 16, 8), np.float32), vscale="page")
+    qc = O.quantize_summary(np.ones((30, 128), np.float32), V,
+                            np.ones((30, 16, 8), np.float32))
+    assert (qp["sV"] == qc["sV"].max(axis=-1, keepdims=True)).all()
+    s = qp["sV"][:, :1].astype(np.float32)[..., None]
+    assert qp["V4"].min() >= -7 and qp["V4"].max() <= 7
+    flat = np.abs(V).reshape(30, -1).argmax(axis=1)
+    assert (np.abs(qp["V4"].reshape(30, -1)[np.arange(30), flat]) == 7).all()
+    assert (np.abs(V - s * qp["V4"]) <= 0.5 * s * (1 + 1e-3)).all()
+    # coefficients and centroid do not depend on the basis reading
+    assert (qp["C8"] == qc["C8"]).all() and (qp["mu8"] == qc["mu8"]).all()
+    with pytest.raises(ValueError):
+        O.quantize_summary(mu, V[:1], C, vscale="row")
+
+
 def test_centroid_fp32_sequential():
     rng = _rng(14)
     k = (rng.integers(-64, 64, (5, 16, 128)) / 8.0).astype(np.float32)
