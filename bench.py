@@ -47,6 +47,10 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="llama8b_128k")
     p.add_argument("--batch", type=int, default=0,
                    help="override the workload's batch (profiling cases)")
+    p.add_argument("--ctx", type=int, default=0,
+                   help="override the workload's context length in tokens "
+                        "(profiling cases: the decode work is batch x h_kv x "
+                        "k pages whatever the context)")
     p.add_argument("--quick", action="store_true",
                    help="skip e2e, dense context, build timing and CPU "
                         "baseline (profiling runs)")
@@ -85,11 +89,13 @@ def reduce_max(x: float) -> float:
     return float(t.item())
 
 
-def rank_spec(spec, rank: int, batch: int = 0):
+def rank_spec(spec, rank: int, batch: int = 0, ctx: int = 0):
     """Each rank runs its own replica: same shape, its own seed."""
     kw = {"seed": spec.seed + 7919 * rank}
     if batch:
         kw["batch"] = batch
+    if ctx:
+        kw["ctx"] = ctx
     return dataclasses.replace(spec, **kw)
 
 
@@ -429,7 +435,7 @@ def run_locks(args):
         dist_init(world, "nccl")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    spec = rank_spec(W.SPECS[args.workload], rank, args.batch)
+    spec = rank_spec(W.SPECS[args.workload], rank, args.batch, args.ctx)
     B.lib()
 
     wl = W.generate(spec, dev)
@@ -655,7 +661,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    spec = rank_spec(W.SPECS[args.workload], 0, args.batch)
+    spec = rank_spec(W.SPECS[args.workload], 0, args.batch, args.ctx)
     one = W.generate_sequence(spec, 0, "cpu", steps=min(spec.steps, 8))
     keys = one["keys"].float().numpy()
     vals = one["values"].float().numpy()
