@@ -186,6 +186,36 @@ def score_traffic(n_records):
     return round(float(d["dram_bytes_per_record"]) * n_records)
 
 
+def build_issue(n_page_heads, build_ms, sm_mhz):
+    """Fraction of the instruction-issue floor the summary build reaches:
+    warp instructions per page-head from the committed ncu capture
+    (profiles/build_kernel_instructions.json), one warp instruction per
+    scheduler per cycle on every SM (4 schedulers per SM) at the sampled SM
+    clock.  None when csrc/build.cu changed since the capture."""
+    import hashlib
+
+    import torch
+    try:
+        with open(os.path.join(ROOT, "profiles",
+                               "build_kernel_instructions.json")) as f:
+            d = json.load(f)
+        src = os.path.join(ROOT, "sparse_paged_kv_locks_gb300", "csrc",
+                           "build.cu")
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, ValueError):
+        return None
+    if d.get("build_cu_sha256") != digest or not sm_mhz:
+        return None
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    per = float(d["warp_instructions_per_page_head"])
+    floor_ms = n_page_heads * per / (n_sm * 4 * sm_mhz * 1e6) * 1e3
+    return {"bound": "issue", "warp_instructions_per_page_head": per,
+            "floor_ms": round(floor_ms, 3),
+            "frac": round(floor_ms / build_ms, 4),
+            "peak": f"{n_sm} SMs x 4 schedulers x {sm_mhz:.0f} MHz"}
+
+
 def selection_quality(B, wl, store, scores, ws, lens, k, h_q, n_records,
                       n_steps=4):
     """Selection quality on the planted needles, GPU only.  The pages
@@ -574,7 +604,10 @@ def run_locks(args):
     # launches per step: score, select, decode and its merge kernel
     line["gpu_launches"] = 4 * args.steps
     line["build"] = {"page_heads": n_records, "ms": round(build_ms, 3),
-                     "page_heads_per_s": round(n_records / (build_ms / 1e3))}
+                     "page_heads_per_s": round(n_records / (build_ms / 1e3)),
+                     "roofline": build_issue(n_records, build_ms,
+                                             clk.get("sm_mhz") or
+                                             clk.get("sm_max_mhz"))}
 
     if not args.quick:
         # e2e: pinned host query in, pinned host (o, lse) out, every step,
