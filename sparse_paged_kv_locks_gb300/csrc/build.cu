@@ -12,7 +12,9 @@
 // rotates, and each round writes its result to the other buffer with the
 // slots moved for the next round (a fixed permutation, so every address a
 // lane touches is a constant).  A lane rotates two 2x2 blocks of the matrix
-// and its own pair's eigenvector columns; one warp barrier per round.
+// and, in registers, its own pair's two eigenvector columns over four rows,
+// which then move to the next round's slots by two neighbour shuffles; one
+// warp barrier per round.
 #include <utility>
 
 #include "common.cuh"
@@ -24,7 +26,6 @@ constexpr int kBuildWarps = 4;
 constexpr int kMaxSweeps = 15;
 constexpr float kJacobiRelTol = 1e-7f;
 constexpr int kAS = 24;  // row stride (floats) of the Jacobi matrix copy
-constexpr int kUS = 20;  // row stride (floats) of the Jacobi vector copy
 
 // 16-byte aligned so that every warp's copy keeps the float2 accesses of
 // the eigensolve aligned
@@ -32,7 +33,6 @@ struct alignas(16) BuildSmem {
   union {
     struct {  // the eigensolve: slot order, double-buffered
       float Ab[2][16][kAS];
-      float Ub[2][16][kUS];
     } jac;
     struct {  // after it
       float U[16][17];  // eigenvectors (columns), index order
@@ -95,17 +95,18 @@ __device__ __forceinline__ float gram_partial(const float (&D)[16][4]) {
 }
 
 template <int BLK, int... L>
-__device__ __forceinline__ void gram_block(float (&v)[32],
+__device__ __forceinline__ void gram_block(float (&v)[16],
                                            const float (&D)[16][4],
                                            std::integer_sequence<int, L...>) {
-  ((v[L] = gram_partial<32 * BLK + L>(D)), ...);
+  ((v[L] = gram_partial<16 * BLK + L>(D)), ...);
 }
 
-// Reduce-scatter of 32 per-lane partials: lane l ends with the warp sum of
-// element l in v[0].
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+// Reduce-scatter of 16 per-lane partials: within each half-warp lane l ends
+// with the half's sum of element l % 16, and one exchange across the halves
+// completes the warp sum (held by lanes l and l + 16).
+__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
+  for (int o = 8; o >= 1; o >>= 1) {
     const bool hi = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < o; ++i) {
@@ -114,7 +115,23 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
       v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
   }
-  return v[0];
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+
+// Gram block BLK (entries 16 BLK .. 16 BLK + 15 of the upper triangle) into
+// both triangles of the slot-ordered matrix.
+template <int BLK>
+__device__ __forceinline__ void gram_store(const float (&D)[16][4],
+                                           float (&A)[16][kAS], int lane) {
+  float v[16];
+  gram_block<BLK>(v, D, std::make_integer_sequence<int, 16>{});
+  const float g = reduce_scatter16(v, lane);
+  const int p = 16 * BLK + (lane & 15);
+  if (lane < 16 && p < 136) {
+    const int i = index_slot(pair_i(p)), j = index_slot(pair_j(p));
+    A[i][j] = g;
+    A[j][i] = g;
+  }
 }
 
 __device__ __forceinline__ float warp_max(float x) {
@@ -129,30 +146,51 @@ __device__ __forceinline__ float warp_max(float x) {
 // entries; sm.post.Cf: fp32 coefficients [16][8].  vpage: one basis scale
 // for the whole page (absolute maximum over every column), stored in all
 // eight column slots; otherwise one per column.
+// int4 codes and scale of basis column k (this lane's rows 4l..4l+3 in v);
+// `apage` >= 0 is the page-wide absolute maximum (one scale per page),
+// otherwise the column's own maximum is taken.
+__device__ __forceinline__ void quantize_basis_column(int k, const float (&v)[4],
+                                                      float apage,
+                                                      BuildSmem &sm,
+                                                      int lane) {
+  float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])),
+                  fmaxf(fabsf(v[2]), fabsf(v[3])));
+  a = apage >= 0.f ? apage : warp_max(a);
+  __half h = quant_scale(a, 7.f);
+  float s = __half2float(h);
+  if (lane == 0) sm.sv[k] = h;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    sm.post.v8[4 * lane + j][k] = (int8_t)quant_code(v[j], s, 7);
+}
+
+__device__ void write_record_tail(const float (&mu)[4], BuildSmem &sm,
+                                  uint8_t *rec, int lane);
+
 __device__ void write_record(const float (&V)[4][8], const float (&mu)[4],
                              BuildSmem &sm, uint8_t *rec, int lane,
                              bool vpage) {
-  float apage = 0.f;
+  float apage = -1.f;
   if (vpage) {
+    apage = 0.f;
 #pragma unroll
     for (int k = 0; k < 8; ++k)
 #pragma unroll
       for (int j = 0; j < 4; ++j) apage = fmaxf(apage, fabsf(V[j][k]));
     apage = warp_max(apage);
   }
-  // basis: int4 codes
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    float a = fmaxf(fmaxf(fabsf(V[0][k]), fabsf(V[1][k])),
-                    fmaxf(fabsf(V[2][k]), fabsf(V[3][k])));
-    a = vpage ? apage : warp_max(a);
-    __half h = quant_scale(a, 7.f);
-    float s = __half2float(h);
-    if (lane == 0) sm.sv[k] = h;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      sm.post.v8[4 * lane + j][k] = (int8_t)quant_code(V[j][k], s, 7);
+    const float v[4] = {V[0][k], V[1][k], V[2][k], V[3][k]};
+    quantize_basis_column(k, v, apage, sm, lane);
   }
+  write_record_tail(mu, sm, rec, lane);
+}
+
+// Everything of the record after the basis codes and scales (already in
+// sm.post.v8 and sm.sv): the centroid, the coefficients and the packing.
+__device__ void write_record_tail(const float (&mu)[4], BuildSmem &sm,
+                                  uint8_t *rec, int lane) {
   // centroid: one scale, int8 codes
   {
     float a = fmaxf(fmaxf(fabsf(mu[0]), fabsf(mu[1])),
@@ -291,14 +329,13 @@ __device__ __forceinline__ bool jacobi_rotation(float app, float aqq,
 // A lane's fixed share of a Jacobi round: the rotation of pair pm = lane % 8
 // (from the diagonal block (pm, pm)), the matrix blocks (grp + 4j, pm) for
 // j = 0, 1 with grp = lane / 8, and rows 4 grp .. 4 grp + 3 of the vector
-// columns of pair pm.  Offsets are in floats within one buffer.
+// columns 2 pm, 2 pm + 1 (held in registers).  Offsets are in floats within
+// one buffer.
 struct JacobiLane {
   int grp, pm;
   int o_d;           // A[2pm][2pm]
   int o_blk;         // A[2 grp][2 pm] (block j adds 8 kAS rows)
   int st[2][2][2];   // destination of block element (j, x, y)
-  int o_u;           // U[4 grp][2 pm]
-  int su0, su1;      // destinations of U[4 grp][2 pm], U[4 grp][2 pm + 1]
 };
 
 __device__ __forceinline__ JacobiLane jacobi_lane(int lane) {
@@ -315,18 +352,16 @@ __device__ __forceinline__ JacobiLane jacobi_lane(int lane) {
       for (int y = 0; y < 2; ++y)
         L.st[j][x][y] = slot_next(2 * (L.grp + 4 * j) + x) * kAS +
                         slot_next(2 * L.pm + y);
-  L.o_u = 4 * L.grp * kUS + 2 * L.pm;
-  L.su0 = 4 * L.grp * kUS + slot_next(2 * L.pm);
-  L.su1 = 4 * L.grp * kUS + slot_next(2 * L.pm + 1);
   return L;
 }
 
-// One round: reads buffer `in`, writes buffer `in ^ 1` in the next round's
-// slot order.  Returns whether this lane's pair rotated.
+// One round: reads matrix buffer A, writes An in the next round's slot
+// order, and updates this lane's vector entries u0 (column 2 pm) and u1
+// (column 2 pm + 1), rows 4 grp + t, moving them to the next round's slots.
+// Returns whether this lane's pair rotated.
 __device__ __forceinline__ int jacobi_round(const float *__restrict__ A,
                                             float *__restrict__ An,
-                                            const float *__restrict__ U,
-                                            float *__restrict__ Un,
+                                            float (&u0)[4], float (&u1)[4],
                                             const JacobiLane &L) {
   float c, s;
   const int rot = jacobi_rotation(A[L.o_d], A[L.o_d + kAS + 1], A[L.o_d + 1],
@@ -362,11 +397,18 @@ __device__ __forceinline__ int jacobi_round(const float *__restrict__ A,
     An[L.st[j][1][0]] = y10;
     An[L.st[j][1][1]] = y11;
   }
+  // U <- U J, then the columns move with the slots: the next even slot 2m
+  // takes pair m+1's even column (pair 0 keeps its own, pair 7 takes its
+  // own odd one), the next odd slot 2m+1 takes pair m-1's odd column (pair
+  // 0 takes pair 1's even one)
 #pragma unroll
-  for (int t = 0; t < 4; ++t) {  // U <- U J
-    const float2 u = *reinterpret_cast<const float2 *>(U + L.o_u + t * kUS);
-    Un[L.su0 + t * kUS] = c * u.x - s * u.y;
-    Un[L.su1 + t * kUS] = s * u.x + c * u.y;
+  for (int t = 0; t < 4; ++t) {
+    const float a = u0[t], b = u1[t];
+    const float r0 = c * a - s * b, r1 = s * a + c * b;
+    const float dn = __shfl_down_sync(0xffffffffu, r0, 1);
+    const float up = __shfl_up_sync(0xffffffffu, r1, 1);
+    u0[t] = L.pm == 7 ? r1 : (L.pm == 0 ? r0 : dn);
+    u1[t] = L.pm == 0 ? dn : up;
   }
   __syncwarp();
   return rot;
@@ -389,32 +431,16 @@ __device__ void page_eigen(float (&kx)[16][4], float (&mu)[4], BuildSmem &sm,
   }
   center_keys(kx, mu);
 
-  // Eq.(3): Gram matrix D D^T, 136 unique entries in 5 blocks of 32
-  float g[5];
-  {
-    float v[32];
-    gram_block<0>(v, kx, std::make_integer_sequence<int, 32>{});
-    g[0] = reduce_scatter32(v, lane);
-    gram_block<1>(v, kx, std::make_integer_sequence<int, 32>{});
-    g[1] = reduce_scatter32(v, lane);
-    gram_block<2>(v, kx, std::make_integer_sequence<int, 32>{});
-    g[2] = reduce_scatter32(v, lane);
-    gram_block<3>(v, kx, std::make_integer_sequence<int, 32>{});
-    g[3] = reduce_scatter32(v, lane);
-    gram_block<4>(v, kx, std::make_integer_sequence<int, 32>{});
-    g[4] = reduce_scatter32(v, lane);
-  }
-#pragma unroll
-  for (int blk = 0; blk < 5; ++blk) {
-    const int p = 32 * blk + lane;
-    if (p < 136) {
-      const int i = index_slot(pair_i(p)), j = index_slot(pair_j(p));
-      sm.jac.Ab[0][i][j] = g[blk];
-      sm.jac.Ab[0][j][i] = g[blk];
-    }
-  }
-  for (int e = lane; e < 256; e += 32)
-    sm.jac.Ub[0][e >> 4][e & 15] = ((e >> 4) == (e & 15)) ? 1.f : 0.f;
+  // Eq.(3): Gram matrix D D^T, 136 unique entries in 9 blocks of 16
+  gram_store<0>(kx, sm.jac.Ab[0], lane);
+  gram_store<1>(kx, sm.jac.Ab[0], lane);
+  gram_store<2>(kx, sm.jac.Ab[0], lane);
+  gram_store<3>(kx, sm.jac.Ab[0], lane);
+  gram_store<4>(kx, sm.jac.Ab[0], lane);
+  gram_store<5>(kx, sm.jac.Ab[0], lane);
+  gram_store<6>(kx, sm.jac.Ab[0], lane);
+  gram_store<7>(kx, sm.jac.Ab[0], lane);
+  gram_store<8>(kx, sm.jac.Ab[0], lane);
   __syncwarp();
 
   // cyclic Jacobi in slot order (see slot_next): rounds alternate between
@@ -422,10 +448,17 @@ __device__ void page_eigen(float (&kx)[16][4], float (&mu)[4], BuildSmem &sm,
   // sweep in which no pair rotated (or after kMaxSweeps sweeps)
   const JacobiLane L = jacobi_lane(lane);
   float *A0 = &sm.jac.Ab[0][0][0], *A1 = &sm.jac.Ab[1][0][0];
-  float *U0 = &sm.jac.Ub[0][0][0], *U1 = &sm.jac.Ub[1][0][0];
+  // eigenvector accumulator U, identity in slot order: this lane's entries
+  // at rows 4 grp + t of columns 2 pm (u0) and 2 pm + 1 (u1)
+  float u0[4], u1[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    u0[t] = 4 * L.grp + t == 2 * L.pm ? 1.f : 0.f;
+    u1[t] = 4 * L.grp + t == 2 * L.pm + 1 ? 1.f : 0.f;
+  }
   int fin = 0, rotated = 0, left = 15, sweeps = 0;
   for (;;) {
-    rotated |= jacobi_round(A0, A1, U0, U1, L);
+    rotated |= jacobi_round(A0, A1, u0, u1, L);
     if (--left == 0) {
       if (!__any_sync(0xffffffffu, rotated) || ++sweeps >= kMaxSweeps) {
         fin = 1;
@@ -434,7 +467,7 @@ __device__ void page_eigen(float (&kx)[16][4], float (&mu)[4], BuildSmem &sm,
       rotated = 0;
       left = 15;
     }
-    rotated |= jacobi_round(A1, A0, U1, U0, L);
+    rotated |= jacobi_round(A1, A0, u0, u1, L);
     if (--left == 0) {
       if (!__any_sync(0xffffffffu, rotated) || ++sweeps >= kMaxSweeps) {
         fin = 0;
@@ -448,17 +481,12 @@ __device__ void page_eigen(float (&kx)[16][4], float (&mu)[4], BuildSmem &sm,
   // back to index order: eigenvalue and eigenvector of slot a belong to
   // index slot_index(a); the vectors' rows are in slot order as well
   if (lane < 16) sm.ev[slot_index(lane)] = sm.jac.Ab[fin][lane][lane];
-  float uv[8];
+  __syncwarp();  // post.U overlays the matrix buffers
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int e = lane + 32 * k;
-    uv[k] = sm.jac.Ub[fin][e >> 4][e & 15];
-  }
-  __syncwarp();
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int e = lane + 32 * k;
-    sm.post.U[slot_index(e >> 4)][slot_index(e & 15)] = uv[k];
+  for (int t = 0; t < 4; ++t) {
+    const int r = slot_index(4 * L.grp + t);
+    sm.post.U[r][slot_index(2 * L.pm)] = u0[t];
+    sm.post.U[r][slot_index(2 * L.pm + 1)] = u1[t];
   }
   __syncwarp();
 
@@ -523,10 +551,10 @@ __device__ float summarize_page(const __nv_bfloat16 *page, BuildSmem &sm,
 #pragma unroll
   for (int k = kRank; k < 16; ++k) tau += sm.lam[k];
 
-  // V = D^T U_r Sigma_r^{-1} (lane rows) and C = U_r Sigma_r (shared)
-  float V[4][8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  // V = D^T U_r Sigma_r^{-1}, one column at a time (this lane's rows),
+  // quantised as soon as it is formed; with one scale per page the columns
+  // are formed twice, the first time for the page maximum
+  auto basis_column = [&](int k, float (&v)[4]) {
     const int col = sm.perm[k];
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -537,8 +565,32 @@ __device__ float summarize_page(const __nv_bfloat16 *page, BuildSmem &sm,
     }
     const float f = sm.cv[k];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) V[j][k] = acc[j] * f;
+    for (int j = 0; j < 4; ++j) v[j] = acc[j] * f;
+  };
+  float apage = -1.f;
+  if (vpage) {
+    apage = 0.f;
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) {
+      float v[4];
+      basis_column(k, v);
+      apage = fmaxf(apage, fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])),
+                                 fmaxf(fabsf(v[2]), fabsf(v[3]))));
+    }
+    apage = warp_max(apage);
   }
+#pragma unroll 1
+  for (int k = 0; k < 8; ++k) {
+    float v[4];
+    basis_column(k, v);
+    quantize_basis_column(k, v, apage, sm, lane);
+    if (unq) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        unq[16 + kDim + (4 * lane + j) * kRank + k] = v[j];
+    }
+  }
+  // C = U_r Sigma_r (shared)
   {
     const int i = lane >> 1, k0 = (lane & 1) * 4;
 #pragma unroll
@@ -548,27 +600,24 @@ __device__ float summarize_page(const __nv_bfloat16 *page, BuildSmem &sm,
     }
   }
   __syncwarp();
-  if (unq) {  // fp32 values before quantisation: lam, mu, V, C
+  if (unq) {  // fp32 values before quantisation: lam, mu, (V above), C
     if (lane < 16) unq[lane] = sm.lam[lane];
     reinterpret_cast<float4 *>(unq + 16)[lane] =
         make_float4(mu[0], mu[1], mu[2], mu[3]);
-    float4 *vo = reinterpret_cast<float4 *>(unq + 16 + kDim) + lane * 8;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      vo[2 * j] = make_float4(V[j][0], V[j][1], V[j][2], V[j][3]);
-      vo[2 * j + 1] = make_float4(V[j][4], V[j][5], V[j][6], V[j][7]);
-    }
     const int i = lane >> 1, k0 = (lane & 1) * 4;
     reinterpret_cast<float4 *>(unq + 16 + kDim + kDim * kRank)[lane] =
         make_float4(sm.post.Cf[i][k0], sm.post.Cf[i][k0 + 1], sm.post.Cf[i][k0 + 2],
                     sm.post.Cf[i][k0 + 3]);
   }
-  write_record(V, mu, sm, rec, lane, vpage);
+  write_record_tail(mu, sm, rec, lane);
   return tau;
 }
 
 
-__global__ void __launch_bounds__(32 * kBuildWarps, 4)
+// six CTAs (24 warps) per SM: the build is bound by the shared-memory data
+// pipe and by latency, and 80 registers (a few bytes of spills outside the
+// eigensolve) measured faster than 128 without spills
+__global__ void __launch_bounds__(32 * kBuildWarps, 6)
     build_kernel(const __nv_bfloat16 *__restrict__ k_cache,
                  int64_t num_phys, int h_kv, const int32_t *__restrict__ pt,
                  int batch, int max_pages, const int32_t *__restrict__ seq_ids,
