@@ -270,8 +270,9 @@ def test_build_per_page_basis_scale():
 # ---------------------------------------------------------------------------
 # score (Eq.(4)) from identical records
 # ---------------------------------------------------------------------------
+@pytest.mark.parametrize("vscale", ["column", "page"])
 @pytest.mark.parametrize("G,h_kv", [(4, 2), (1, 4), (8, 1), (16, 1), (5, 2)])
-def test_score_matches_oracle_on_same_records(G, h_kv):
+def test_score_matches_oracle_on_same_records(G, h_kv, vscale):
     spec = W.custom_spec(batch=3, h_q=G * h_kv, h_kv=h_kv, ctx=16 * 70 + 9,
                          k=10, needles=0, seed=20 + G)
     wl = W.generate(spec, "cpu")
@@ -279,7 +280,8 @@ def test_score_matches_oracle_on_same_records(G, h_kv):
     lens = [16 * 70 + 9, 16 * 3, 16 * 45 + 1]
     batch, max_pages = pt.shape
     seq, pg = full_pairs(lens)
-    store, _ = O.build_summaries(kc, pt, seq, pg, batch, max_pages)
+    store, _ = O.build_summaries(kc, pt, seq, pg, batch, max_pages,
+                                 vscale=vscale)
     q = wl.queries[0].float().numpy()
     s_orc = O.score_store(q, store, lens)
     ws = B.new_workspace(batch, spec.h_q, h_kv, max_pages, spec.k, DEV)
@@ -815,6 +817,46 @@ def test_device_status_flags():
                           d.seq_lens, idx2, 4, o, lse, ws)
     torch.cuda.synchronize()
     assert B.locks_read_status(ws) == B.DEV_BAD_PAGE_ID
+
+
+def test_native_decoder_status_wide_group_and_empty_sequence():
+    """The host-buffer decoder with a group of 16 query heads: an empty
+    sequence gives o = 0 and lse = -inf, a page table entry outside the
+    cache comes back as LOCKS_DEV_BAD_PAGE_ID in the step's status (sticky
+    until cleared), and o / lse equal the eager step's bytes throughout."""
+    spec = W.custom_spec(batch=3, h_q=16, h_kv=1, ctx=16 * 40 + 3, k=8,
+                         needles=0, seed=47)
+    wl = W.generate(spec, "cpu", steps=3)
+    d = Dev(wl)
+    batch, max_pages = wl.page_table.shape
+    lens = [16 * 40 + 3, 0, 16 * 7]
+    lens_dev = i32(lens)
+    store, _, _, _, _ = gpu_build(d, lens)
+    pt = d.page_table.clone()
+    good = int(pt[2, 3])
+    pt[2, 3] = d.k_cache.shape[0] + 7          # outside the cache
+    native = B.LocksDecoder(d.k_cache, d.v_cache, pt, store, spec.h_q,
+                            spec.k, graph=True, seq_lens=lens_dev)
+    eager = B.LocksDecoder(d.k_cache, d.v_cache, pt, store, spec.h_q, spec.k)
+    shape = (batch, spec.h_q, 128)
+    qh = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+    oh = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty(batch, spec.h_q).pin_memory()
+    for step in range(3):
+        if step == 2:                           # repair the table, clear
+            pt[2, 3] = good
+            B.locks_clear_status(native.workspace)
+            B.locks_clear_status(eager.workspace)
+        qh.copy_(wl.queries[step])
+        oe, le = eager.step(qh.to(DEV), lens_dev)
+        torch.cuda.synchronize()
+        _, _, st = native.step_host(qh, lens_dev, oh, lh)
+        assert st == (0 if step == 2 else B.DEV_BAD_PAGE_ID), (step, st)
+        assert st == eager.status()
+        assert torch.equal(oe.cpu(), oh) and torch.equal(le.cpu(), lh)
+        assert (oh[1] == 0).all() and torch.isinf(lh[1]).all()
+        assert (lh[1] < 0).all()
+    native.close()
 
 
 @pytest.mark.parametrize("rule", ["share_average", "group_max",
