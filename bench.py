@@ -216,6 +216,97 @@ def build_issue(n_page_heads, build_ms, sm_mhz):
             "peak": f"{n_sm} SMs x 4 schedulers x {sm_mhz:.0f} MHz"}
 
 
+def small_configs(B, W, dev, n_steps=200):
+    """The two small workloads (tiny_4k: 1 x 4K, 8q/2kv, k = 16;
+    llama8b_32k: 8 x 32K, 32q/8kv, k = 64), which fit largely in the
+    129 MB L2: the same decode step (score + select + sparse attention),
+    timed warm (steps launched back to back from the host), with the L2
+    flushed before every step (a 2 x L2 buffer written between steps,
+    outside the timed events), and warm as one CUDA graph replay per step
+    (these steps are launch-bound without it)."""
+    import torch
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    out = {}
+    for name in ("tiny_4k", "llama8b_32k"):
+        spec = W.SPECS[name]
+        wl = W.generate(spec, dev)
+        lens = [int(x) for x in wl.seq_lens]
+        batch, max_pages = wl.page_table.shape
+        seq = torch.tensor([b for b in range(batch)
+                            for _ in range(lens[b] // 16)],
+                           dtype=torch.int32, device=dev)
+        pgs = torch.tensor([p for b in range(batch)
+                            for p in range(lens[b] // 16)],
+                           dtype=torch.int32, device=dev)
+        store = B.new_summary_store(batch, spec.h_kv, max_pages, dev)
+        B.locks_build_summaries(wl.k_cache, wl.page_table, seq, pgs, store)
+        ws = B.new_workspace(batch, spec.h_q, spec.h_kv, max_pages, spec.k,
+                             dev)
+        idx = torch.empty(batch, spec.h_kv, spec.k, dtype=torch.int32,
+                          device=dev)
+        o = torch.empty(batch, spec.h_q, 128, dtype=torch.bfloat16,
+                        device=dev)
+        lse = torch.empty(batch, spec.h_q, dtype=torch.float32, device=dev)
+        qs = wl.queries
+
+        def step(i):
+            q = qs[i % qs.shape[0]]
+            B.locks_score_select(q, store, wl.seq_lens, spec.k, idx, ws)
+            B.locks_sparse_decode(q, wl.k_cache, wl.v_cache, wl.page_table,
+                                  wl.seq_lens, idx, spec.k, o, lse, ws)
+
+        for i in range(5):
+            step(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
+            enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for i in range(n_steps):
+            step(i)
+        e1.record()
+        torch.cuda.synchronize()
+        warm = e0.elapsed_time(e1) / n_steps
+        cold = []
+        for i in range(min(n_steps, 50)):
+            flush.fill_(float(i))
+            e0.record()
+            step(i)
+            e1.record()
+            torch.cuda.synchronize()
+            cold.append(e0.elapsed_time(e1))
+        assert B.locks_read_status(ws) == 0
+        cold_ms = statistics.mean(cold)
+        # the same step replayed as one CUDA graph (no host launch per
+        # kernel), query already on the device
+        dec = B.LocksDecoder(wl.k_cache, wl.v_cache, wl.page_table, store,
+                             spec.h_q, spec.k, graph=True,
+                             seq_lens=wl.seq_lens)
+        dec.q_dev.copy_(qs[0])
+        for _ in range(5):
+            dec.step(dec.q_dev)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n_steps):
+            dec.step(dec.q_dev)
+        e1.record()
+        torch.cuda.synchronize()
+        graph_ms = e0.elapsed_time(e1) / n_steps
+        assert dec.status() == 0
+        out[name] = {"batch": batch, "context": spec.ctx, "k": spec.k,
+                     "warm": {"ms_per_step": round(warm, 4),
+                              "tokens_per_s": round(batch / (warm / 1e3))},
+                     "l2_flushed": {"ms_per_step": round(cold_ms, 4),
+                                    "tokens_per_s":
+                                        round(batch / (cold_ms / 1e3))},
+                     "graph_warm": {"ms_per_step": round(graph_ms, 4),
+                                    "tokens_per_s":
+                                        round(batch / (graph_ms / 1e3))}}
+        del wl, store, ws, dec
+        torch.cuda.empty_cache()
+    return out
+
+
 def selection_quality(B, wl, store, scores, ws, lens, k, h_q, n_records,
                       n_steps=4):
     """Selection quality on the planted needles, GPU only.  The pages
@@ -662,6 +753,7 @@ def run_locks(args):
             "value": batch / (dms / 1e3), "unit": "tokens/s",
             "ms_per_step": round(dms, 4),
             "gbs": round(dense_bytes / (dms / 1e3) / 1e9, 1)}
+        line["small_configs"] = small_configs(B, W, dev)
         line["quality"] = selection_quality(B, wl, store, scores, ws, lens,
                                             k, spec.h_q, n_records)
         line["quality"]["rank_precision_ablation"] = rank_precision_ablation(
