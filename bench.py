@@ -307,6 +307,65 @@ def small_configs(B, W, dev, n_steps=200):
     return out
 
 
+def append_config(B, W, dev, n_steps=64):
+    """The append workload (llama70b_128k_append: 8 x 131072 tokens,
+    64q/8kv, k = 128): every step appends one token per sequence (writing K
+    and V and building the summary of a page the append fills, once every
+    16 steps here) and then runs the decode step; the incremental build is
+    part of the step.  CUDA events around the append and around the whole
+    step."""
+    import torch
+    spec = W.SPECS["llama70b_128k_append"]
+    wl = W.generate(spec, dev)
+    lens0 = [int(x) for x in wl.seq_lens]
+    batch, max_pages = wl.page_table.shape
+    seq = torch.tensor([b for b in range(batch)
+                        for _ in range(lens0[b] // 16)],
+                       dtype=torch.int32, device=dev)
+    pgs = torch.tensor([p for b in range(batch)
+                        for p in range(lens0[b] // 16)],
+                       dtype=torch.int32, device=dev)
+    store = B.new_summary_store(batch, spec.h_kv, max_pages, dev)
+    B.locks_build_summaries(wl.k_cache, wl.page_table, seq, pgs, store)
+    ws = B.new_workspace(batch, spec.h_q, spec.h_kv, max_pages, spec.k, dev)
+    idx = torch.empty(batch, spec.h_kv, spec.k, dtype=torch.int32,
+                      device=dev)
+    o = torch.empty(batch, spec.h_q, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(batch, spec.h_q, dtype=torch.float32, device=dev)
+    lens = wl.seq_lens.clone()
+    n_steps = min(n_steps, spec.append_steps)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+          for _ in range(n_steps)]
+    torch.cuda.synchronize()
+    for s in range(n_steps):
+        q = wl.queries[s % wl.queries.shape[0]]
+        ev[s][0].record()
+        B.locks_append_kv(wl.k_append[s], wl.v_append[s], wl.k_cache,
+                          wl.v_cache, wl.page_table, lens, store)
+        ev[s][1].record()
+        B.locks_score_select(q, store, lens, spec.k, idx, ws)
+        B.locks_sparse_decode(q, wl.k_cache, wl.v_cache, wl.page_table, lens,
+                              idx, spec.k, o, lse, ws)
+        ev[s][2].record()
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == 0
+    fills = [s for s in range(n_steps) if (lens0[0] + s + 1) % 16 == 0]
+    plain = [s for s in range(n_steps) if s not in fills and s >= 2]
+    app = [ev[s][0].elapsed_time(ev[s][1]) for s in range(n_steps)]
+    step = [ev[s][0].elapsed_time(ev[s][2]) for s in range(2, n_steps)]
+    res = {"batch": batch, "context": spec.ctx, "h_q": spec.h_q,
+           "h_kv": spec.h_kv, "k": spec.k, "steps": n_steps,
+           "append_us": round(1e3 * statistics.median(
+               [app[s] for s in plain]), 2),
+           "append_filling_a_page_us": round(1e3 * statistics.median(
+               [app[s] for s in fills]), 2) if fills else None,
+           "step_ms": round(statistics.mean(step), 4),
+           "tokens_per_s": round(batch / (statistics.mean(step) / 1e3))}
+    del wl, store, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 def selection_quality(B, wl, store, scores, ws, lens, k, h_q, n_records,
                       n_steps=4):
     """Selection quality on the planted needles, GPU only.  The pages
@@ -754,6 +813,7 @@ def run_locks(args):
             "ms_per_step": round(dms, 4),
             "gbs": round(dense_bytes / (dms / 1e3) / 1e9, 1)}
         line["small_configs"] = small_configs(B, W, dev)
+        line["append_config"] = append_config(B, W, dev)
         line["quality"] = selection_quality(B, wl, store, scores, ws, lens,
                                             k, spec.h_q, n_records)
         line["quality"]["rank_precision_ablation"] = rank_precision_ablation(
