@@ -101,8 +101,11 @@ constexpr int kRadixBits = 12;
 constexpr int kRadixBins = 1 << kRadixBits;
 constexpr int kBinsPerWarp = kRadixBins / (kSelThreads / 32);  // 256
 
-template <bool SMEM_KEYS, int GT>
-__global__ void __launch_bounds__(kSelThreads, 2)
+// MINB: resident CTAs per SM the registers are sized for.  2 when there are
+// more (sequence, KV head) units than SMs; 1 when every unit has an SM of
+// its own, which leaves registers for more pages in flight per thread.
+template <bool SMEM_KEYS, int GT, int MINB>
+__global__ void __launch_bounds__(kSelThreads, MINB)
     select_kernel(const float *__restrict__ scores,
                   const int32_t *__restrict__ seq_lens, int h_kv, int G,
                   int max_pages, int k, int rule,
@@ -150,8 +153,8 @@ __global__ void __launch_bounds__(kSelThreads, 2)
                    ((reinterpret_cast<uintptr_t>(scores) & 15u) == 0);
   const bool kvec = SMEM_KEYS || (max_pages & 3) == 0;  // 16-byte key rows
   const int nq = (n + 3) >> 2;        // quads of pages covering [0, n)
-  // quads a thread has in flight at once (registers allow two for G <= 4)
-  constexpr int R = GT <= 4 ? 2 : 1;
+  // quads a thread has in flight at once (what the registers allow)
+  constexpr int R = MINB == 1 ? (GT <= 8 ? 2 : 1) : (GT <= 4 ? 2 : 1);
   for (int i = tid; i < kRadixBins; i += blockDim.x) hist[0][i] = 0;
 
   // Z_g: log2-sum-exp2 over the summarised pages [0, nf) (group-mass
@@ -468,22 +471,31 @@ cudaError_t launch_select(const float *scores, const int32_t *seq_lens,
                       status);
   };
   const int gt = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : G <= 8 ? 8 : 16;
+  // one CTA per SM suffices when the units fit the GPU in one wave
+  static int n_sm = 0;
+  if (n_sm == 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  const bool own_sm = (long long)batch * h_kv <= n_sm;
+#define LOCKS_SELECT_CASES(SK, MB)                         \
+  switch (gt) {                                            \
+    case 1: return run(select_kernel<SK, 1, MB>);          \
+    case 2: return run(select_kernel<SK, 2, MB>);          \
+    case 4: return run(select_kernel<SK, 4, MB>);          \
+    case 8: return run(select_kernel<SK, 8, MB>);          \
+    default: return run(select_kernel<SK, 16, MB>);        \
+  }
   if (on_chip) {
-    switch (gt) {
-      case 1: return run(select_kernel<true, 1>);
-      case 2: return run(select_kernel<true, 2>);
-      case 4: return run(select_kernel<true, 4>);
-      case 8: return run(select_kernel<true, 8>);
-      default: return run(select_kernel<true, 16>);
-    }
+    if (own_sm) LOCKS_SELECT_CASES(true, 1)
+    LOCKS_SELECT_CASES(true, 2)
   }
-  switch (gt) {
-    case 1: return run(select_kernel<false, 1>);
-    case 2: return run(select_kernel<false, 2>);
-    case 4: return run(select_kernel<false, 4>);
-    case 8: return run(select_kernel<false, 8>);
-    default: return run(select_kernel<false, 16>);
-  }
+  if (own_sm) LOCKS_SELECT_CASES(false, 1)
+  LOCKS_SELECT_CASES(false, 2)
+#undef LOCKS_SELECT_CASES
 }
 
 }  // namespace locks
