@@ -789,9 +789,9 @@ def run_locks(args):
                        "d2h_bytes_per_step": q_bytes + batch * spec.h_q * 4 + 4,
                        "api": "locks_decoder_step_host (C ABI): one CUDA "
                               "graph per step: a kernel reading q from pinned "
-                              "host memory, the 4 step kernels, a kernel "
-                              "writing o, lse and the status word to pinned "
-                              "host memory"}
+                              "host memory, then the 4 step kernels, which "
+                              "write o, lse and the status word straight into "
+                              "pinned host memory"}
         # dense full-cache decode of the same shape, as context
         for _ in range(2):
             B.locks_sparse_decode(qs[0], wl.k_cache, wl.v_cache,

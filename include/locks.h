@@ -382,7 +382,6 @@ locks_status_t locks_append_kv_ex(const void *k_new, const void *v_new,
  *                  every step, so appends between steps take effect)
  *   q_dev         bf16 [batch][h_q][128] device staging buffer for the query
  *   idx           int32 [batch][h_kv][k] device buffer for the selection
- *   o_dev, lse_dev  bf16 [batch][h_q][128] and float [batch][h_q] device
  *   workspace     >= locks_workspace_size(batch, h_q, h_kv, max_pages, k)
  * It checks the arguments, creates a private non-blocking capture stream
  * and a 4-byte mapped page-locked host word, and allocates no device
@@ -396,8 +395,8 @@ locks_status_t locks_decoder_create(
     const void *k_cache, const void *v_cache, int64_t num_phys_pages,
     const int32_t *page_table, const void *summaries, const int32_t *seq_lens,
     int batch, int h_q, int h_kv, int max_pages, int k, void *q_dev,
-    int32_t *idx, void *o_dev, float *lse_dev, void *workspace,
-    size_t workspace_bytes, locks_decoder_t **out);
+    int32_t *idx, void *workspace, size_t workspace_bytes,
+    locks_decoder_t **out);
 
 /* One decode step from host buffers, synchronous:
  *   q_host    host bf16 [batch][h_q][128] query (page-locked)
@@ -410,16 +409,17 @@ locks_status_t locks_decoder_create(
  *             the legacy default stream) and the call returns when it is
  *             done (the stream is synchronised).
  * The first call records the whole step (a kernel that reads the query
- * from host memory into q_dev, the four kernels, a kernel that writes o,
- * lse and the status word to host memory) as one CUDA graph on the
- * decoder's capture stream, after one plain run of the same step that
- * completes first; every call then launches that graph once.  The host
- * buffers are accessed by those two kernels through their mapped device
- * addresses, so they must be page-locked (cudaHostAlloc, or
- * cudaHostRegister with mapping) with a 16-byte aligned device address;
- * anything else returns LOCKS_ERR_INVALID_ARG before anything runs.  Other
- * host buffers than the previous call's are patched into the two copy
- * kernels' graph nodes.
+ * from host memory into q_dev, the four kernels, the attention kernels
+ * writing o and lse straight into the host buffers and the merge kernel
+ * copying the status word out) as one CUDA graph on the decoder's capture
+ * stream, after one plain run of the same step that completes first; every
+ * call then launches that graph once.  The host buffers are reached through
+ * their mapped device addresses, so they must be page-locked
+ * (cudaHostAlloc, or cudaHostRegister with mapping) with a 16-byte aligned
+ * device address; anything else returns LOCKS_ERR_INVALID_ARG before
+ * anything runs.  Another query buffer than the previous call's is patched
+ * into the graph; other output buffers make the call record the graph
+ * again (keep them fixed for the fast path).
  * On LOCKS_ERR_CUDA, locks_decoder_last_cuda_error gives the cudaError_t.
  * Calls on one decoder must not overlap (one host thread at a time). */
 locks_status_t locks_decoder_step_host(locks_decoder_t *decoder,

@@ -77,8 +77,7 @@ _SIGS = {
     "locks_append_kv": (_I, [_P, _P, _P, _P, _I64, _I, _P, _I, _I, _P, _P, _P,
                              _P, _P]),
     "locks_decoder_create": (_I, [_P, _P, _I64, _P, _P, _P, _I, _I, _I, _I,
-                                  _I, _P, _P, _P, _P, _P, _SZ,
-                                  ctypes.POINTER(_P)]),
+                                  _I, _P, _P, _P, _SZ, ctypes.POINTER(_P)]),
     "locks_decoder_step_host": (_I, [_P, _P, _P, _P,
                                      ctypes.POINTER(ctypes.c_int32), _P]),
     "locks_decoder_last_cuda_error": (_I, [_P]),
@@ -527,8 +526,8 @@ class LocksDecoder:
                 _ptr(self.page_table), _ptr(self.summaries),
                 _ptr(self.seq_lens_dev), self.batch, self.h_q, self.h_kv,
                 self.max_pages, self.k, _ptr(self.q_dev), _ptr(self.idx),
-                _ptr(self.o), _ptr(self.lse), _ptr(self.workspace),
-                self.workspace.numel(), ctypes.byref(h)))
+                _ptr(self.workspace), self.workspace.numel(),
+                ctypes.byref(h)))
             self._native = h
         return self._native
 

@@ -102,7 +102,7 @@ locks_status_t locks::sparse_decode(
     int64_t num_phys_pages, const int32_t *page_table,
     const int32_t *seq_lens, const int32_t *idx, int k, int batch, int h_q,
     int h_kv, int max_pages, void *o_out, float *lse_out, void *workspace,
-    size_t workspace_bytes, cudaStream_t stream, bool out_dependent) {
+    size_t workspace_bytes, cudaStream_t stream, int32_t *status_mirror) {
   if (batch < 0 || max_pages < 1 || num_phys_pages < 1 || !heads_ok(h_q, h_kv))
     return LOCKS_ERR_INVALID_ARG;
   if (idx && k < 1) return LOCKS_ERR_INVALID_ARG;
@@ -133,7 +133,7 @@ locks_status_t locks::sparse_decode(
   cudaError_t e = launch_decode(
       q, k_cache, v_cache, num_phys_pages, page_table, seq_lens, idx, k, batch,
       h_kv, G, max_pages, max_warps, o_out, lse_out, o_part, lse_part, meta,
-      status, stream, out_dependent);
+      status, stream, status_mirror);
   return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
 }
 
@@ -366,7 +366,7 @@ locks_status_t locks_sparse_decode(
   return locks::sparse_decode(q, k_cache, v_cache, num_phys_pages, page_table,
                               seq_lens, idx, k, batch, h_q, h_kv, max_pages,
                               o_out, lse_out, workspace, workspace_bytes,
-                              (cudaStream_t)stream, false);
+                              (cudaStream_t)stream, nullptr);
 }
 
 locks_status_t locks_append_kv(const void *k_new, const void *v_new,

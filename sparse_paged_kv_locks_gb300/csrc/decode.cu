@@ -446,13 +446,15 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
                    const float *__restrict__ lse_part,
                    const int *__restrict__ meta, int batch, int h_kv, int k,
                    int dense, int G, __nv_bfloat16 *__restrict__ o_out,
-                   float *__restrict__ lse_out, int trigger) {
+                   float *__restrict__ lse_out,
+                   const int32_t *__restrict__ status_src,
+                   int32_t *status_mirror) {
   const int lane = threadIdx.x & 31;
-  // A dependent that only reads o and lse after its own wait (a copy of
-  // them to the host) may launch now.  Off for plain calls: a following
-  // decode launched early would hold its SM slots idle meanwhile.
-  if (trigger) pdl_trigger();
   pdl_wait();  // partials and layout of the decode kernel
+  // the step's device status word is final once the decode kernel is done
+  // (every kernel before it waited on its predecessor): copy it out
+  if (status_mirror && blockIdx.x == 0 && threadIdx.x == 0)
+    *status_mirror = *status_src;
   const long long row =
       (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
   if (row >= (long long)batch * h_kv * G) return;
@@ -540,7 +542,7 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
                           int G, int max_pages, int max_warps, void *o_out,
                           float *lse_out, float *o_part, float *lse_part,
                           int *meta, int32_t *status, cudaStream_t stream,
-                          bool out_dependent) {
+                          int32_t *status_mirror) {
   static bool attr_set = false;
   static int blocks_per_sm[2] = {0, 0};
   if (!attr_set) {
@@ -587,7 +589,7 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
                     dim3((unsigned)((rows + kCombineWarps - 1) / kCombineWarps)),
                     dim3(32 * kCombineWarps), 0, stream, o_part, lse_part,
                     (const int *)meta, batch, h_kv, k, idx ? 0 : 1, G, oo,
-                    lse_out, out_dependent ? 1 : 0);
+                    lse_out, (const int32_t *)status, status_mirror);
 }
 
 }  // namespace locks

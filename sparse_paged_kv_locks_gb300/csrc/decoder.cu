@@ -2,17 +2,18 @@
 // §2 Fig. 1 decode path: score the page summaries, select k pages, attend
 // over them) driven from host buffers.  The first step records, on a
 // private capture stream, a kernel that pulls the query from page-locked
-// host memory into the device staging buffer, the four kernels of
-// locks_score_select + locks_sparse_decode, and a kernel that pushes o, lse
-// and the device status word out to page-locked host memory, as one CUDA
-// graph; every later step is one graph launch on the caller's stream and
-// one stream synchronisation.  The host buffers are reached through their
+// host memory into the device staging buffer and the four kernels of
+// locks_score_select + locks_sparse_decode, the attention kernels writing
+// o and lse straight into the caller's page-locked output buffers and the
+// merge kernel copying the device status word out, as one CUDA graph;
+// every later step is one graph launch on the caller's stream and one
+// stream synchronisation.  The host buffers are reached through their
 // mapped device addresses (page-locked memory is mapped into the GPU's
 // address space under unified addressing; on Grace-Blackwell the accesses
 // cross NVLink-C2C), which costs a few microseconds less per step than
-// copy-engine transfers of these few hundred kilobytes.  When the caller
-// passes other host buffers than the ones recorded, the two copy kernels'
-// nodes in the instantiated graph are given the new addresses.
+// copy-engine transfers of these few hundred kilobytes.  Another query
+// buffer is patched into the copy kernel's graph node; other output
+// buffers make the next step record the graph again.
 #include <stdint.h>
 
 #include <new>
@@ -33,16 +34,14 @@ struct locks_decoder {
   int batch, h_q, h_kv, max_pages, k;
   void *q_dev;
   int32_t *idx;
-  void *o_dev;
-  float *lse_dev;
   void *workspace;
   size_t ws_bytes;
-  size_t q_bytes, o_bytes, lse_bytes;
+  size_t q_bytes;
   // runtime objects owned by the decoder
   cudaStream_t cap = nullptr;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
-  cudaGraphNode_t n_in = nullptr, n_out = nullptr;
+  cudaGraphNode_t n_in = nullptr;
   int32_t *st_host = nullptr;  // page-locked, one int32
   int32_t *st_map = nullptr;   // its mapped device address
   // host buffers the instantiated graph copies from / to, and their mapped
@@ -95,22 +94,7 @@ __global__ void __launch_bounds__(kCopyThreads)
     dst[i] = src[i];
 }
 
-// results out: o (16 bytes per thread), lse (one float per thread) and the
-// status word, device -> host (mapped)
-__global__ void __launch_bounds__(kCopyThreads)
-    host_out_kernel(const uint4 *__restrict__ o_dev, uint4 *__restrict__ o_host,
-                    long long n16, const float *__restrict__ lse_dev,
-                    float *__restrict__ lse_host, long long n_lse,
-                    const int32_t *__restrict__ status, int32_t *st_host) {
-  locks::pdl_wait();  // o and lse of the merge kernel
-  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = t; i < n16; i += stride) o_host[i] = o_dev[i];
-  for (long long i = t; i < n_lse; i += stride) lse_host[i] = lse_dev[i];
-  if (t == 0) *st_host = *status;
-}
-
-// One step's work on `s`: query in, score + select, sparse attention,
+// One step's work on `s`: query in, score + select, sparse attention with
 // (o, lse, status word) out.  q_map / o_map / lse_map are mapped device
 // addresses of the caller's host buffers.
 locks_status_t enqueue_step(locks_decoder *d, cudaStream_t s,
@@ -124,18 +108,11 @@ locks_status_t enqueue_step(locks_decoder *d, cudaStream_t s,
       d->q_dev, d->summaries, d->seq_lens, d->batch, d->h_q, d->h_kv,
       d->max_pages, d->k, d->idx, d->workspace, d->ws_bytes, s, true);
   if (st != LOCKS_OK) return st;
-  st = locks::sparse_decode(d->q_dev, d->k_cache, d->v_cache, d->num_phys,
-                            d->page_table, d->seq_lens, d->idx, d->k,
-                            d->batch, d->h_q, d->h_kv, d->max_pages, d->o_dev,
-                            d->lse_dev, d->workspace, d->ws_bytes, s, true);
-  if (st != LOCKS_OK) return st;
-  const long long n_lse = (long long)(d->lse_bytes / 4);
-  e = locks::launch_pdl(
-      host_out_kernel, dim3(copy_grid(n16)), dim3(kCopyThreads), 0, s,
-      static_cast<const uint4 *>(d->o_dev), static_cast<uint4 *>(o_map), n16,
-      static_cast<const float *>(d->lse_dev), lse_map, n_lse,
-      static_cast<const int32_t *>(d->workspace), d->st_map);
-  return e == cudaSuccess ? LOCKS_OK : fail(d, e);
+  return locks::sparse_decode(d->q_dev, d->k_cache, d->v_cache, d->num_phys,
+                              d->page_table, d->seq_lens, d->idx, d->k,
+                              d->batch, d->h_q, d->h_kv, d->max_pages, o_map,
+                              lse_map, d->workspace, d->ws_bytes, s,
+                              d->st_map);
 }
 
 void drop_graph(locks_decoder *d) {
@@ -143,12 +120,12 @@ void drop_graph(locks_decoder *d) {
   if (d->graph) cudaGraphDestroy(d->graph);
   d->exec = nullptr;
   d->graph = nullptr;
-  d->n_in = d->n_out = nullptr;
+  d->n_in = nullptr;
 }
 
 // Warm-up run ordered after the caller's stream (first launches set kernel
-// attributes), then capture and instantiate; finds the two copy kernels'
-// nodes by their functions.
+// attributes), then capture and instantiate; finds the query copy kernel's
+// node by its function.
 locks_status_t record(locks_decoder *d, cudaStream_t caller,
                       const void *q_map, void *o_map, float *lse_map) {
   cudaEvent_t ev;
@@ -197,49 +174,26 @@ locks_status_t record(locks_decoder *d, cudaStream_t caller,
     cudaKernelNodeParams p;
     if (cudaGraphKernelNodeGetParams(nodes[i], &p) != cudaSuccess) continue;
     if (p.func == reinterpret_cast<void *>(host_in_kernel)) d->n_in = nodes[i];
-    if (p.func == reinterpret_cast<void *>(host_out_kernel))
-      d->n_out = nodes[i];
   }
-  if (!d->n_in || !d->n_out) {
+  if (!d->n_in) {
     drop_graph(d);
     return LOCKS_ERR_UNSUPPORTED;
   }
   return LOCKS_OK;
 }
 
-locks_status_t retarget(locks_decoder *d, const void *q_map, void *o_map,
-                        float *lse_map) {
+locks_status_t retarget_query(locks_decoder *d, const void *q_map) {
   const long long n16 = (long long)(d->q_bytes / 16);
-  if (q_map != d->q_map) {
-    const void *src = q_map;
-    long long n = n16;
-    void *args[3] = {const_cast<void **>(&src), &d->q_dev, &n};
-    cudaKernelNodeParams p = {};
-    p.func = reinterpret_cast<void *>(host_in_kernel);
-    p.gridDim = dim3(copy_grid(n16));
-    p.blockDim = dim3(kCopyThreads);
-    p.kernelParams = args;
-    cudaError_t e = cudaGraphExecKernelNodeSetParams(d->exec, d->n_in, &p);
-    if (e != cudaSuccess) return fail(d, e);
-  }
-  if (o_map != d->o_map || lse_map != d->lse_map) {
-    const void *od = d->o_dev;
-    void *oh = o_map;
-    long long n = n16, nl = (long long)(d->lse_bytes / 4);
-    const float *ld = d->lse_dev;
-    float *lh = lse_map;
-    const void *stw = d->workspace;
-    void *args[8] = {&od, &oh, &n, &ld, &lh, &nl,
-                     const_cast<void **>(&stw), &d->st_map};
-    cudaKernelNodeParams p = {};
-    p.func = reinterpret_cast<void *>(host_out_kernel);
-    p.gridDim = dim3(copy_grid(n16));
-    p.blockDim = dim3(kCopyThreads);
-    p.kernelParams = args;
-    cudaError_t e = cudaGraphExecKernelNodeSetParams(d->exec, d->n_out, &p);
-    if (e != cudaSuccess) return fail(d, e);
-  }
-  return LOCKS_OK;
+  const void *src = q_map;
+  long long n = n16;
+  void *args[3] = {const_cast<void **>(&src), &d->q_dev, &n};
+  cudaKernelNodeParams p = {};
+  p.func = reinterpret_cast<void *>(host_in_kernel);
+  p.gridDim = dim3(copy_grid(n16));
+  p.blockDim = dim3(kCopyThreads);
+  p.kernelParams = args;
+  cudaError_t e = cudaGraphExecKernelNodeSetParams(d->exec, d->n_in, &p);
+  return e == cudaSuccess ? LOCKS_OK : fail(d, e);
 }
 
 }  // namespace
@@ -250,15 +204,15 @@ locks_status_t locks_decoder_create(
     const void *k_cache, const void *v_cache, int64_t num_phys_pages,
     const int32_t *page_table, const void *summaries, const int32_t *seq_lens,
     int batch, int h_q, int h_kv, int max_pages, int k, void *q_dev,
-    int32_t *idx, void *o_dev, float *lse_dev, void *workspace,
-    size_t workspace_bytes, locks_decoder_t **out) {
+    int32_t *idx, void *workspace, size_t workspace_bytes,
+    locks_decoder_t **out) {
   if (!out) return LOCKS_ERR_INVALID_ARG;
   *out = nullptr;
   if (batch < 1 || k < 2 || max_pages < 1 || num_phys_pages < 1 ||
       h_kv < 1 || h_q < h_kv || h_q % h_kv != 0)
     return LOCKS_ERR_INVALID_ARG;
   if (!k_cache || !v_cache || !page_table || !summaries || !seq_lens ||
-      !q_dev || !idx || !o_dev || !lse_dev || !workspace)
+      !q_dev || !idx || !workspace)
     return LOCKS_ERR_INVALID_ARG;
   size_t need = 0;
   locks_status_t st =
@@ -280,13 +234,9 @@ locks_status_t locks_decoder_create(
   d->k = k;
   d->q_dev = q_dev;
   d->idx = idx;
-  d->o_dev = o_dev;
-  d->lse_dev = lse_dev;
   d->workspace = workspace;
   d->ws_bytes = workspace_bytes;
   d->q_bytes = (size_t)batch * h_q * LOCKS_HEAD_DIM * 2;
-  d->o_bytes = d->q_bytes;
-  d->lse_bytes = (size_t)batch * h_q * sizeof(float);
   cudaError_t e = cudaStreamCreateWithFlags(&d->cap, cudaStreamNonBlocking);
   if (e == cudaSuccess)
     e = cudaHostAlloc(reinterpret_cast<void **>(&d->st_host), sizeof(int32_t),
@@ -316,9 +266,14 @@ locks_status_t locks_decoder_step_host(locks_decoder_t *d,
                        : static_cast<float *>(const_cast<void *>(
                              mapped(lse_host)));
   if (!q_map || !o_map || !lse_map) return LOCKS_ERR_INVALID_ARG;
-  locks_status_t st = d->exec ? retarget(d, q_map, o_map, lse_map)
-                              : record(d, (cudaStream_t)stream, q_map, o_map,
-                                       lse_map);
+  // the graph writes o and lse into the recorded output buffers: others
+  // need a new recording; another query buffer is patched in place
+  if (d->exec && (o_map != d->o_map || lse_map != d->lse_map)) drop_graph(d);
+  locks_status_t st = LOCKS_OK;
+  if (!d->exec)
+    st = record(d, (cudaStream_t)stream, q_map, o_map, lse_map);
+  else if (q_map != d->q_map)
+    st = retarget_query(d, q_map);
   if (st != LOCKS_OK) return st;
   d->q_host = q_host;
   d->o_host = o_host;

@@ -54,10 +54,11 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
                           int G, int max_pages, int max_warps, void *o_out,
                           float *lse_out, float *o_part, float *lse_part,
                           int *meta, int32_t *status, cudaStream_t stream,
-                          bool out_dependent = false);
+                          int32_t *status_mirror = nullptr);
 
-// locks_sparse_decode on a cudaStream_t; out_dependent: the merge kernel
-// lets a programmatic dependent that reads only o and lse launch early.
+// locks_sparse_decode on a cudaStream_t; status_mirror (optional): where
+// the merge kernel copies the device status word at the end of the step
+// (a mapped host word, for instance).
 locks_status_t sparse_decode(const void *q, const void *k_cache,
                              const void *v_cache, int64_t num_phys_pages,
                              const int32_t *page_table,
@@ -65,7 +66,7 @@ locks_status_t sparse_decode(const void *q, const void *k_cache,
                              int k, int batch, int h_q, int h_kv,
                              int max_pages, void *o_out, float *lse_out,
                              void *workspace, size_t workspace_bytes,
-                             cudaStream_t stream, bool out_dependent);
+                             cudaStream_t stream, int32_t *status_mirror);
 
 cudaError_t launch_exact(const void *q, const void *k_cache, int64_t num_phys,
                          const int32_t *pt, const int32_t *seq_lens,

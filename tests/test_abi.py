@@ -76,7 +76,7 @@ def test_host_validation_before_launch(L):
     # decoder object: argument and workspace checks before any CUDA call
     out = ctypes.c_void_p(123)
     args = [fake, fake, 10, fake, fake, fake, 2, 8, 2, 16, 4, fake, fake,
-            fake, fake, fake]
+            fake]
     assert L.locks_decoder_create(*args, 1 << 30, None) == 1
     assert L.locks_decoder_create(*args, 64, ctypes.byref(out)) == 3
     assert out.value is None
