@@ -776,21 +776,43 @@ def run_locks(args):
         o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         lse_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         n_e2e = max(10, min(args.steps, 500))
+        # the C ABI call with host buffers, as a C caller makes it: each
+        # step's query, output and status pointers are plain host pointers
+        import ctypes
+        step_host = B.lib().locks_decoder_step_host
+        handle = dec.handle()
+        q_ptrs = [ctypes.c_void_p(q_host[i].data_ptr()) for i in range(n_q)]
+        o_ptr = ctypes.c_void_p(o_host.data_ptr())
+        l_ptr = ctypes.c_void_p(lse_host.data_ptr())
+        dev_status = ctypes.c_int32(0)
+        st_ref = ctypes.byref(dev_status)
+        s_ptr = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
         for i in range(3):
-            dec.step_host(q_host[i % n_q], wl.seq_lens, o_host, lse_host)
+            assert step_host(handle, q_ptrs[i % n_q], o_ptr, l_ptr, st_ref,
+                             s_ptr) == 0
         barrier()
+        rcs = 0
         t0 = time.perf_counter()
         for i in range(n_e2e):
-            dec.step_host(q_host[i % n_q], wl.seq_lens, o_host, lse_host)
+            rcs |= step_host(handle, q_ptrs[i % n_q], o_ptr, l_ptr, st_ref,
+                             s_ptr)
         dt = reduce_max(time.perf_counter() - t0)
+        assert rcs == 0 and dev_status.value == 0, "e2e step failed"
+        # the same result the eager step gives for the last query
+        ref_o, ref_lse = B.LocksDecoder(
+            wl.k_cache, wl.v_cache, wl.page_table, store, spec.h_q,
+            k).step(qs[(n_e2e - 1) % n_q].contiguous(), wl.seq_lens)
+        assert torch.equal(ref_o.cpu(), o_host) and \
+            torch.equal(ref_lse.cpu(), lse_host), "e2e result differs"
         line["e2e"] = {"value": world * batch * n_e2e / dt, "unit": "tokens/s",
                        "steps": n_e2e,
                        "h2d_bytes_per_step": q_bytes,
                        "d2h_bytes_per_step": q_bytes + batch * spec.h_q * 4 + 4,
-                       "api": "locks_decoder_step_host (C ABI): one CUDA "
-                              "graph per step: a kernel reading q from pinned "
-                              "host memory, then the 4 step kernels, which "
-                              "write o, lse and the status word straight into "
+                       "api": "locks_decoder_step_host (C ABI, called "
+                              "with the step's host pointers): one CUDA graph "
+                              "per step: a kernel reading q from pinned host "
+                              "memory, then the 4 step kernels, which write "
+                              "o, lse and the status word straight into "
                               "pinned host memory"}
         # dense full-cache decode of the same shape, as context
         for _ in range(2):

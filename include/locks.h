@@ -419,7 +419,9 @@ locks_status_t locks_decoder_create(
  * device address; anything else returns LOCKS_ERR_INVALID_ARG before
  * anything runs.  Another query buffer than the previous call's is patched
  * into the graph; other output buffers make the call record the graph
- * again (keep them fixed for the fast path).
+ * again (keep them fixed for the fast path).  The decoder remembers the
+ * mapped addresses of the buffers it last used: a buffer must stay
+ * page-locked for as long as the decoder may still be given it.
  * On LOCKS_ERR_CUDA, locks_decoder_last_cuda_error gives the cudaError_t.
  * Calls on one decoder must not overlap (one host thread at a time). */
 locks_status_t locks_decoder_step_host(locks_decoder_t *decoder,

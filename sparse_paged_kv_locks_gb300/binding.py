@@ -474,6 +474,11 @@ class LocksDecoder:
         self.use_graph = graph
         self._graph = None
         self._native = None
+        self._out = None
+        self._stream_arg = None
+        self._st = ctypes.c_int32(0)
+        self._st_ref = ctypes.byref(self._st)
+        self._step_fn = lib().locks_decoder_step_host
 
     def _eager(self, q, seq_lens, stream=None):
         locks_score_select(q, self.summaries, seq_lens, self.k, self.idx,
@@ -517,6 +522,12 @@ class LocksDecoder:
         self._graph.replay()
         return self.o, self.lse
 
+    def handle(self):
+        """The C ABI decoder object (a locks_decoder_t *, as a ctypes
+        pointer) bound to this decoder's device buffers, for callers that
+        drive locks_decoder_step_host directly; owned by this object."""
+        return self._native_decoder()
+
     def _native_decoder(self):
         if self._native is None:
             h = ctypes.c_void_p(None)
@@ -533,7 +544,54 @@ class LocksDecoder:
 
     def step_host(self, q_host, seq_lens, o_host, lse_host, stream=None):
         """Pinned host query in, pinned host (o, lse) out (synchronises).
-        Returns (o_host, lse_host, device status word)."""
+        Returns (o_host, lse_host, device status word).
+
+        With graph=True the output buffers are checked once per distinct
+        pair and the query with a few attribute reads per call, so that the
+        per-step host cost stays small (the C call checks that every buffer
+        is page-locked)."""
+        if not self.use_graph:
+            self._check_host(q_host, o_host, lse_host)
+            s = torch.cuda.current_stream() if stream is None else stream
+            with torch.cuda.stream(s):
+                self.q_dev.copy_(q_host, non_blocking=True)
+                self._bind_lens(seq_lens, s)
+                self._eager(self.q_dev, self.seq_lens_dev, s)
+                o_host.copy_(self.o, non_blocking=True)
+                lse_host.copy_(self.lse, non_blocking=True)
+            s.synchronize()
+            return o_host, lse_host, self.status()
+        out = self._out
+        if out is None or out[0] is not o_host or out[1] is not lse_host:
+            self._check_host(q_host, o_host, lse_host)
+            out = self._out = (o_host, lse_host,
+                               ctypes.c_void_p(o_host.data_ptr()),
+                               ctypes.c_void_p(lse_host.data_ptr()))
+        elif (q_host.dtype is not torch.bfloat16 or q_host.is_cuda or
+              q_host.shape != self.q_dev.shape or
+              not q_host.is_contiguous()):
+            raise ValueError("q_host must be a contiguous bf16 host tensor "
+                             "[batch][h_q][128]")
+        if seq_lens is not None and seq_lens is not self.seq_lens_dev:
+            self._bind_lens(seq_lens, stream)
+        st = self._st
+        sc = self._stream_arg
+        if sc is None or sc[0] is not stream:
+            sc = self._stream_arg = (stream, _stream(stream)) \
+                if stream is not None else (None, None)
+        rc = self._step_fn(self._native_decoder(),
+                           ctypes.c_void_p(q_host.data_ptr()), out[2], out[3],
+                           self._st_ref,
+                           sc[1] if stream is not None else _stream(None))
+        if rc != 0:
+            L = lib()
+            raise LocksError(
+                f"locks_decoder_step_host: "
+                f"{L.locks_status_string(rc).decode()} (status {rc}, cuda "
+                f"error {L.locks_decoder_last_cuda_error(self._native)})")
+        return o_host, lse_host, int(st.value)
+
+    def _check_host(self, q_host, o_host, lse_host):
         for t, name, dt in ((q_host, "q_host", torch.bfloat16),
                             (o_host, "o_host", torch.bfloat16),
                             (lse_host, "lse_host", torch.float32)):
@@ -545,28 +603,6 @@ class LocksDecoder:
                 tuple(lse_host.shape) != (self.batch, self.h_q):
             raise ValueError("host buffers must be [batch][h_q][128] and "
                              "[batch][h_q]")
-        if not self.use_graph:
-            s = torch.cuda.current_stream() if stream is None else stream
-            with torch.cuda.stream(s):
-                self.q_dev.copy_(q_host, non_blocking=True)
-                self._bind_lens(seq_lens, s)
-                self._eager(self.q_dev, self.seq_lens_dev, s)
-                o_host.copy_(self.o, non_blocking=True)
-                lse_host.copy_(self.lse, non_blocking=True)
-            s.synchronize()
-            return o_host, lse_host, self.status()
-        self._bind_lens(seq_lens, stream)
-        st = ctypes.c_int32(0)
-        L = lib()
-        rc = L.locks_decoder_step_host(self._native_decoder(), _ptr(q_host),
-                                       _ptr(o_host), _ptr(lse_host),
-                                       ctypes.byref(st), _stream(stream))
-        if rc != 0:
-            raise LocksError(
-                f"locks_decoder_step_host: "
-                f"{L.locks_status_string(rc).decode()} (status {rc}, cuda "
-                f"error {L.locks_decoder_last_cuda_error(self._native)})")
-        return o_host, lse_host, int(st.value)
 
     def close(self):
         if self._native is not None:
