@@ -454,6 +454,44 @@ def test_variant_build_and_score_match_oracle(rank, vbits):
         assert (s_gpu[0, h, :, nf:] == 5.0).all()
 
 
+@pytest.mark.parametrize("G,h_kv,rank,vbits", [(1, 3, 4, 2), (3, 2, 8, 4),
+                                                (8, 1, 15, 8), (16, 1, 12, 2),
+                                                (4, 2, 15, 4)])
+def test_variant_score_group_sizes(G, h_kv, rank, vbits):
+    """Variant scores from the oracle's own variant records at several
+    group sizes, over enough pages for several CTAs and a ragged tail."""
+    spec = W.custom_spec(batch=2, h_q=G * h_kv, h_kv=h_kv, ctx=16 * 150 + 7,
+                         k=8, needles=0, seed=60 + G)
+    wl = W.generate(spec, "cpu", steps=1)
+    kc, _, pt, _ = host(wl)
+    lens = [16 * 150 + 7, 16 * 70]
+    batch, max_pages = pt.shape
+    seq, pg = full_pairs(lens)
+    keys = kc[pt[seq, pg]]                                 # [n][h_kv][16][128]
+    qo, _ = O.build_page_variant(keys, rank, vbits)
+    recs = B.new_variant_store(batch, h_kv, max_pages, rank, vbits, DEV)
+    recs[seq, :, pg] = torch.from_numpy(O.encode_variant(qo, rank, vbits)).to(
+        DEV)
+    q = wl.queries[0]
+    sc = torch.full((batch, h_kv, G, max_pages), 5.0, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.locks_score_variant(q.to(DEV), recs, rank, vbits, i32(lens), sc, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    mu, V, C = O.dequantize(qo)
+    qn = q.float().numpy()
+    s_gpu = sc.cpu().numpy()
+    seq, pg = np.asarray(seq), np.asarray(pg)
+    for b in range(batch):
+        nf = lens[b] // 16
+        sel = seq == b
+        for h in range(h_kv):
+            ref = O.score_from_summaries(qn[b, h * G:(h + 1) * G],
+                                         mu[sel, h], V[sel, h], C[sel, h])
+            assert np.abs(s_gpu[b, h, :, pg[sel]].T - ref).max() <= S_TOL
+            assert (s_gpu[b, h, :, nf:] == 5.0).all()
+
+
 # ---------------------------------------------------------------------------
 # select (Eq.(5) + sink/recent) from identical scores
 # ---------------------------------------------------------------------------
