@@ -8,7 +8,7 @@ separately).  Prints one JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W]
                     [--impl locks|reference] [--workload NAME] [--batch B]
-                    [--quick]
+                    [--quick [--ablation]] [--ctx T]
 
 Under torchrun every rank runs its own replica of the workload (the path
 shards by sequence with no exchange step), so `value` is the sum over ranks
@@ -54,6 +54,9 @@ def parse_args(argv=None):
     p.add_argument("--quick", action="store_true",
                    help="skip e2e, dense context, build timing and CPU "
                         "baseline (profiling runs)")
+    p.add_argument("--ablation", action="store_true",
+                   help="with --quick: run the rank / precision ablation "
+                        "as well (profiling the variant kernels)")
     return p.parse_args(argv)
 
 
@@ -307,6 +310,82 @@ def small_configs(B, W, dev, n_steps=200):
     return out
 
 
+def ragged_config(B, W, dev, peak_gbs, n_steps=50):
+    """The ragged serving batch (ragged_64: 64 sequences with lengths
+    U{4096..131072}, most ending in a partial page, 32q/8kv) over the
+    budget sweep k = 16..256 pages: the decode step (score + select +
+    sparse attention) timed back to back on the device; the summaries
+    (about 1.8 GB) are larger than L2 at every k.  Algorithmic bytes per
+    step as on the main workload: summaries of every full page, the
+    selected pages' valid K/V tokens, q and o."""
+    import torch
+    spec = W.SPECS["ragged_64"]
+    wl = W.generate(spec, dev)
+    lens = [int(x) for x in wl.seq_lens]
+    batch, max_pages = wl.page_table.shape
+    seq = torch.tensor([b for b in range(batch)
+                        for _ in range(lens[b] // 16)],
+                       dtype=torch.int32, device=dev)
+    pgs = torch.tensor([p for b in range(batch)
+                        for p in range(lens[b] // 16)],
+                       dtype=torch.int32, device=dev)
+    store = B.new_summary_store(batch, spec.h_kv, max_pages, dev)
+    B.locks_build_summaries(wl.k_cache, wl.page_table, seq, pgs, store)
+    k_max = max(spec.k_sweep)
+    ws = B.new_workspace(batch, spec.h_q, spec.h_kv, max_pages, k_max, dev)
+    o = torch.empty(batch, spec.h_q, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(batch, spec.h_q, dtype=torch.float32, device=dev)
+    qs = wl.queries
+    n_full = sum(L // 16 for L in lens)
+    score_bytes = n_full * spec.h_kv * RECORD_PAYLOAD
+    q_bytes = batch * spec.h_q * 128 * 2
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
+        enable_timing=True)
+    sweep = []
+    for k in spec.k_sweep:
+        idx = torch.empty(batch, spec.h_kv, k, dtype=torch.int32, device=dev)
+
+        def step(i):
+            q = qs[i % qs.shape[0]]
+            B.locks_score_select(q, store, wl.seq_lens, k, idx, ws)
+            B.locks_sparse_decode(q, wl.k_cache, wl.v_cache, wl.page_table,
+                                  wl.seq_lens, idx, k, o, lse, ws)
+
+        for i in range(5):
+            step(i)
+        torch.cuda.synchronize()
+        e0.record()
+        for i in range(n_steps):
+            step(i)
+        e1.record()
+        torch.cuda.synchronize()
+        assert B.locks_read_status(ws) == 0
+        ms = e0.elapsed_time(e1) / n_steps
+        # K/V bytes of the last step's selection (valid tokens only)
+        idx_h = idx.cpu().numpy()
+        kv_bytes = 0
+        for b in range(batch):
+            for h in range(spec.h_kv):
+                for p in idx_h[b, h]:
+                    if p >= 0:
+                        kv_bytes += min(16, lens[b] - 16 * int(p)) * 2 * 128 * 2
+        step_bytes = score_bytes + kv_bytes + 2 * q_bytes
+        gbs = step_bytes / (ms / 1e3) / 1e9
+        sweep.append({"k": k, "ms_per_step": round(ms, 4),
+                      "tokens_per_s": round(batch / (ms / 1e3)),
+                      "algorithmic_bytes": step_bytes,
+                      "gbs": round(gbs, 1),
+                      "frac_of_copy_peak": round(gbs / peak_gbs, 4)})
+    out = {"batch": batch, "h_q": spec.h_q, "h_kv": spec.h_kv,
+           "context_min": min(lens), "context_max": max(lens),
+           "context_mean": round(statistics.mean(lens)),
+           "partial_last_pages": sum(1 for L in lens if L % 16),
+           "steps": n_steps, "sweep": sweep}
+    del wl, store, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def append_config(B, W, dev, n_steps=64):
     """The append workload (llama70b_128k_append: 8 x 131072 tokens,
     64q/8kv, k = 128): every step appends one token per sequence (writing K
@@ -475,8 +554,9 @@ def rank_precision_ablation(B, wl, lens, k, h_q, peak_gbs, n_seqs=4,
     sequences of the workload: for every variant, carrier retention on the
     planted needles, exact coverage and page-score error against the exact
     LSE at budget k, with the variant's record bytes (the scoring stream's
-    bytes per page-head) and its build and scoring times; the scoring
-    stream's rate against the measured copy peak."""
+    bytes per page-head) and its build and scoring times (scoring: mean of
+    10 calls after warm-up, each after an L2 flush); the scoring stream's
+    rate against the measured copy peak."""
     import torch
     dev = wl.k_cache.device
     batch = min(n_seqs, wl.page_table.shape[0])
@@ -496,6 +576,9 @@ def rank_precision_ablation(B, wl, lens, k, h_q, peak_gbs, n_seqs=4,
     idx = torch.empty(batch, h_kv, k, dtype=torch.int32, device=dev)
     needles = wl.needle_pages[:batch].to(dev)
     e0, e1, e2 = (torch.cuda.Event(True) for _ in range(3))
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    n_time = 10
     out = []
     for rank in (4, 8, 12, 15):
         for vbits in (2, 4, 8):
@@ -512,11 +595,7 @@ def rank_precision_ablation(B, wl, lens, k, h_q, peak_gbs, n_seqs=4,
             for i in range(n_steps):
                 q = wl.queries[i, :batch].contiguous()
                 B.locks_exact_page_scores(q, wl.k_cache, pt, sl, ex, status)
-                e1.record()
                 B.locks_score_variant(q, rec, rank, vbits, sl, sc, status)
-                e2.record()
-                torch.cuda.synchronize()
-                score_ms.append(e1.elapsed_time(e2))
                 B.locks_select_pages(sc, sl, h_q, k, idx, ws)
                 kept = (idx[:, :, None, :] == needles[:, :, :, None]).any(-1)
                 hit += int((kept & (needles >= 0)).sum())
@@ -530,6 +609,18 @@ def rank_precision_ablation(B, wl, lens, k, h_q, peak_gbs, n_seqs=4,
                     cov.append(float((c * valid).sum(-1).mean()))
                     err.append((sc[b, :, :, :nf] - ex[b, :, :, :nf]).abs()
                                .flatten())
+            # scoring time: warm launches, then n_time calls each after an
+            # L2 flush (the smaller variant stores fit in L2)
+            q = wl.queries[0, :batch].contiguous()
+            for _ in range(3):
+                B.locks_score_variant(q, rec, rank, vbits, sl, sc, status)
+            for i in range(n_time):
+                flush.fill_(float(i))
+                e1.record()
+                B.locks_score_variant(q, rec, rank, vbits, sl, sc, status)
+                e2.record()
+                torch.cuda.synchronize()
+                score_ms.append(e1.elapsed_time(e2))
             assert int(status.item()) == 0 and B.locks_read_status(ws) == 0
             e = torch.cat(err).double()
             n_rec = int(seq.numel()) * h_kv
@@ -552,7 +643,8 @@ def rank_precision_ablation(B, wl, lens, k, h_q, peak_gbs, n_seqs=4,
                 "page_heads": n_rec})
             del rec
     return {"sequences": batch, "budget_pages": k, "steps": n_steps,
-            "variants": out,
+            "score_timing": f"mean of {n_time} calls, L2 flushed before "
+                            "each", "variants": out,
             "note": "variant records scored on CUDA cores (a warp per "
                     "record, lane-parallel over head dims); the shipped "
                     "(8, 4-bit) record is the tensor-core path"}
@@ -774,6 +866,9 @@ def run_locks(args):
                                              clk.get("sm_mhz") or
                                              clk.get("sm_max_mhz"))}
 
+    if args.quick and args.ablation:
+        line["quality"] = {"rank_precision_ablation": rank_precision_ablation(
+            B, wl, lens, k, spec.h_q, peak)}
     if not args.quick:
         # e2e: pinned host query in, pinned host (o, lse) out, every step,
         # through the C ABI decoder object: the query copy, the kernels and
@@ -844,6 +939,7 @@ def run_locks(args):
             "gbs": round(dense_bytes / (dms / 1e3) / 1e9, 1)}
         line["small_configs"] = small_configs(B, W, dev)
         line["append_config"] = append_config(B, W, dev)
+        line["ragged_config"] = ragged_config(B, W, dev, peak)
         line["quality"] = selection_quality(B, wl, store, scores, ws, lens,
                                             k, spec.h_q, n_records)
         line["quality"]["rank_precision_ablation"] = rank_precision_ablation(

@@ -177,8 +177,8 @@ locks_status_t locks_build_summaries_ex(
  * and zero padding to a 16-byte stride.  Quantiser as the shipped record
  * (symmetric, fp16 scale = fp16_rn(absmax / qmax), codes rint(x / s)
  * clamped).  The shipped 832-byte record carries the same values as the
- * (r = 8, 4-bit) variant in a tensor-core layout; variants are for the
- * ablation, scored on CUDA cores.
+ * (r = 8, 4-bit) variant in its own tensor-core layout; variants are for
+ * the ablation.
  * locks_variant_record_bytes: the stride (0 for an unsupported pair). */
 size_t locks_variant_record_bytes(int rank, int vbits);
 
@@ -197,7 +197,8 @@ locks_status_t locks_build_variant(
 /* Eq.(4) page scores of every full page from variant records, in the
  * layout of locks_score_pages (scores_out float [batch][h_kv][G][max_pages];
  * entries of pages that are not full are left untouched).  Feed them to
- * locks_select_pages for the variant's selection. */
+ * locks_select_pages for the variant's selection.  `records` must be
+ * 16-byte aligned (LOCKS_ERR_INVALID_ARG otherwise). */
 locks_status_t locks_score_variant(const void *q, const void *records,
                                    int rank, int vbits,
                                    const int32_t *seq_lens, int batch,

@@ -244,6 +244,7 @@ locks_status_t locks_score_variant(const void *q, const void *records,
     return LOCKS_ERR_UNSUPPORTED;
   if (batch == 0) return LOCKS_OK;
   if (!q || !records || !seq_lens || !scores_out) return LOCKS_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(records) & 15u) return LOCKS_ERR_INVALID_ARG;
   cudaError_t e = launch_score_variant(q, records, rank, vbits, seq_lens,
                                        batch, h_kv, h_q / h_kv, max_pages,
                                        scores_out, status,

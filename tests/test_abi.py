@@ -71,6 +71,11 @@ def test_host_validation_before_launch(L):
     assert L.locks_append_kv(fake, fake, fake, fake, 10, 33, fake, 1, 16,
                              fake, fake, None, None, s) == 2
     assert L.locks_pack_summaries(None, None, None, -1, None, s) == 1
+    # variant scoring: unsupported (rank, bits), records not 16-byte aligned
+    assert L.locks_score_variant(fake, fake, 7, 4, fake, 1, 8, 2, 16, fake,
+                                 None, s) == 1
+    assert L.locks_score_variant(fake, ctypes.c_void_p(24), 8, 4, fake, 1, 8,
+                                 2, 16, fake, None, s) == 1
     assert L.locks_clear_status(None, s) == 1
     assert L.locks_read_status(None, None, s) == 1
     # decoder object: argument and workspace checks before any CUDA call
