@@ -960,14 +960,13 @@ cudaError_t launch_append(const void *k_new, const void *v_new, void *k_cache,
                           int flags, int32_t *status, cudaStream_t stream) {
   if (batch == 0) return cudaSuccess;
   const size_t smem = sizeof(BuildSmem) * (size_t)h_kv;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(
-        append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        (int)(sizeof(BuildSmem) * 32));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static DeviceFlags attr_set;
+  cudaError_t e = once_per_device(attr_set, [] {
+    return cudaFuncSetAttribute(append_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(sizeof(BuildSmem) * 32));
+  });
+  if (e != cudaSuccess) return e;
   append_kernel<<<batch, 32 * h_kv, smem, stream>>>(
       static_cast<const __nv_bfloat16 *>(k_new),
       static_cast<const __nv_bfloat16 *>(v_new),

@@ -516,17 +516,6 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
 // --------------------------------------------------------------------------
 // launchers
 // --------------------------------------------------------------------------
-static int dec_sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
-}
-
 size_t decode_smem_bytes(int batch) {
   return (size_t)kDecRing + sizeof(int) * ((size_t)batch + 1);
 }
@@ -543,33 +532,32 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
                           float *lse_out, float *o_part, float *lse_part,
                           int *meta, int32_t *status, cudaStream_t stream,
                           int32_t *status_mirror) {
-  static bool attr_set = false;
-  static int blocks_per_sm[2] = {0, 0};
-  if (!attr_set) {
+  static DeviceFlags attr_set, blocks_narrow, blocks_wide;
+  cudaError_t ea = once_per_device(attr_set, [] {
     cudaError_t e = cudaFuncSetAttribute(
         decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         227 * 1024);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_kernel<true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             227 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return cudaFuncSetAttribute(decode_kernel<true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                227 * 1024);
+  });
+  if (ea != cudaSuccess) return ea;
   const size_t smem = decode_smem_bytes(batch);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   const int wide = G > 8 ? 1 : 0;
   // resident CTAs per SM at the common (small-batch) footprint; a larger
   // batch only lowers the count the hardware actually fits
-  if (blocks_per_sm[wide] == 0) {
-    int n = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &n, wide ? decode_kernel<true> : decode_kernel<false>, kDecThreads,
-        decode_smem_bytes(64));
-    if (e != cudaSuccess) return e;
-    blocks_per_sm[wide] = n > 0 ? n : 1;
-  }
-  long long warps = (long long)blocks_per_sm[wide] * dec_sm_count() * kDecWarps;
+  const int blocks_per_sm =
+      per_device_value(wide ? blocks_wide : blocks_narrow, [wide] {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &n, wide ? decode_kernel<true> : decode_kernel<false>,
+                kDecThreads, decode_smem_bytes(64)) != cudaSuccess)
+          return 0;
+        return n;
+      });
+  long long warps = (long long)blocks_per_sm * device_sm_count() * kDecWarps;
   if (warps > max_warps) warps = max_warps;
   if (warps < 1) warps = 1;
   const int n_warps = (int)warps;

@@ -229,33 +229,29 @@ cudaError_t launch_exact(const void *q, const void *k_cache, int64_t num_phys,
                          int batch, int h_kv, int G, int max_pages,
                          float *scores, int32_t *status,
                          cudaStream_t stream) {
-  static bool attr_set = false;
-  static int blocks_per_sm[2] = {0, 0};
-  if (!attr_set) {
+  static DeviceFlags attr_set, blocks_narrow, blocks_wide;
+  cudaError_t ea = once_per_device(attr_set, [] {
     cudaError_t e = cudaFuncSetAttribute(
         exact_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         227 * 1024);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(exact_kernel<true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               227 * 1024);
     if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return cudaFuncSetAttribute(exact_kernel<true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                227 * 1024);
+  });
+  if (ea != cudaSuccess) return ea;
   const size_t smem = exact_smem_bytes(batch);
   const int wide = G > 8 ? 1 : 0;
-  if (blocks_per_sm[wide] == 0) {
-    int n = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &n, wide ? exact_kernel<true> : exact_kernel<false>, kExThreads,
-        exact_smem_bytes(64));
-    if (e != cudaSuccess) return e;
-    blocks_per_sm[wide] = n > 0 ? n : 1;
-  }
-  int dev = 0, sms = 1;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  long long warps = (long long)blocks_per_sm[wide] * sms * kExWarps;
+  const int blocks_per_sm =
+      per_device_value(wide ? blocks_wide : blocks_narrow, [wide] {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &n, wide ? exact_kernel<true> : exact_kernel<false>,
+                kExThreads, exact_smem_bytes(64)) != cudaSuccess)
+          return 0;
+        return n;
+      });
+  long long warps = (long long)blocks_per_sm * device_sm_count() * kExWarps;
   const long long positions = (long long)batch * h_kv * max_pages;
   if (warps > positions) warps = positions;
   if (warps < 1) warps = 1;

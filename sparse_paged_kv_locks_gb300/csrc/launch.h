@@ -5,9 +5,63 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "locks.h"
 
 namespace locks {
+
+// Launch facts cached per CUDA device: function attributes are set per
+// device, and SM counts and occupancy are properties of the device, so a
+// process that launches on several GPUs keeps one entry for each.  The
+// caches are function-level statics (zero-initialised); concurrent first
+// calls compute the same value, so relaxed atomics suffice.
+constexpr int kMaxCachedDevices = 64;
+using DeviceFlags = std::atomic<int>[kMaxCachedDevices];
+
+inline int cached_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev >= 0 && dev < kMaxCachedDevices ? dev : -1;
+}
+
+// Runs `step` (returning cudaError_t, e.g. a cudaFuncSetAttribute) until it
+// has succeeded once on the current device.
+template <class F>
+cudaError_t once_per_device(DeviceFlags &done, F step) {
+  const int dev = cached_device();
+  if (dev >= 0 && done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  const cudaError_t e = step();
+  if (e == cudaSuccess && dev >= 0) done[dev].store(1, std::memory_order_relaxed);
+  return e;
+}
+
+// A positive per-device value (SM count, resident blocks per SM) computed by
+// `make` on the first call on each device; a `make` result below 1 is
+// returned as 1 and not cached.
+template <class F>
+int per_device_value(DeviceFlags &cache, F make) {
+  const int dev = cached_device();
+  int v = dev >= 0 ? cache[dev].load(std::memory_order_relaxed) : 0;
+  if (v > 0) return v;
+  v = make();
+  if (v < 1) return 1;
+  if (dev >= 0) cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+// Streaming multiprocessors of the current device (1 if the query fails).
+inline int device_sm_count() {
+  static DeviceFlags cache;
+  return per_device_value(cache, [] {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+            cudaSuccess)
+      return 0;
+    return n;
+  });
+}
 
 // locks_score_select on a cudaStream_t, with the scoring kernel optionally
 // launched after_query (see launch_score).

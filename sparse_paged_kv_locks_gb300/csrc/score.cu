@@ -709,17 +709,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // --------------------------------------------------------------------------
 // launchers
 // --------------------------------------------------------------------------
-static int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
-}
-
 size_t score_smem_bytes(int batch) {
   return (size_t)kRingBytes + sizeof(uint64_t) * kScoreWarps * kStages +
          sizeof(int) * (3 * (size_t)batch + 1);
@@ -737,8 +726,8 @@ cudaError_t launch_score(const void *q, const void *summaries,
                          int max_pages, float *s_hat, int32_t *status,
                          cudaStream_t stream, bool after_query) {
   const size_t smem = score_smem_bytes(batch);
-  static bool attr_set = false;
-  if (!attr_set) {
+  static DeviceFlags attr_set;
+  cudaError_t ea = once_per_device(attr_set, [] {
     cudaError_t e = cudaFuncSetAttribute(
         score_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         227 * 1024);
@@ -750,10 +739,10 @@ cudaError_t launch_score(const void *q, const void *summaries,
       e = cudaFuncSetAttribute(score_kernel<3>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                227 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  const int grid = sm_count();
+    return e;
+  });
+  if (ea != cudaSuccess) return ea;
+  const int grid = device_sm_count();
   auto *qq = static_cast<const __nv_bfloat16 *>(q);
   auto *ss = static_cast<const uint8_t *>(summaries);
   auto *kern = G > 8 ? score_kernel<3> : G > 4 ? score_kernel<2>

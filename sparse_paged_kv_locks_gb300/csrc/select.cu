@@ -472,15 +472,7 @@ cudaError_t launch_select(const float *scores, const int32_t *seq_lens,
   };
   const int gt = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : G <= 8 ? 8 : 16;
   // one CTA per SM suffices when the units fit the GPU in one wave
-  static int n_sm = 0;
-  if (n_sm == 0) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess)
-      e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-  }
-  const bool own_sm = (long long)batch * h_kv <= n_sm;
+  const bool own_sm = (long long)batch * h_kv <= device_sm_count();
 #define LOCKS_SELECT_CASES(SK, MB)                         \
   switch (gt) {                                            \
     case 1: return run(select_kernel<SK, 1, MB>);          \
