@@ -18,6 +18,20 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Sum of the per-warp values v[0..wid) (one per warp of the block, in
+// shared memory): a shuffle scan over the warps instead of a loop
+template <int NWARPS>
+__device__ __forceinline__ int warps_before(const int *v, int wid, int lane) {
+  const int x = lane < NWARPS ? v[lane] : 0;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < NWARPS; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  return __shfl_sync(0xffffffffu, incl - x, wid);
+}
+
 // block-wide exclusive scan of two counters (blockDim = kSelThreads)
 __device__ __forceinline__ void block_scan2(int a, int b, int &ea, int &eb,
                                             int *sh /* [2*32] */) {
@@ -118,7 +132,7 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
   __shared__ int sh_wcnt[2][32];
   __shared__ uint32_t red_u[2][32];
   __shared__ uint32_t sh_prefix, sh_mask;
-  __shared__ int sh_remaining, sh_varying;
+  __shared__ int sh_remaining, sh_varying, sh_slow;
 
   const int b = blockIdx.y, h = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -158,8 +172,57 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
   for (int i = tid; i < kRadixBins; i += blockDim.x) hist[0][i] = 0;
 
   // Z_g: log2-sum-exp2 over the summarised pages [0, nf) (group-mass
-  // pooling does not normalise per head and skips it)
+  // pooling does not normalise per head and skips it).  Common form: every
+  // thread sums 2^(x - r_g) against one reference per head, r_g = the score
+  // of page 0 (always summarised here, since n > k >= 2), so the block
+  // combine is a plain sum; a score more than 2^7 above r_g (the sum
+  // overflows) or a page-0 score that is not finite takes the general form
+  // below, with per-thread references.
   if (rule != LOCKS_MERGE_GROUP_MASS) {
+  float ref[GT];
+  bool finite = true;
+#pragma unroll
+  for (int g = 0; g < GT; ++g) {
+    ref[g] = g < G ? __ldg(sc + (size_t)g * max_pages) * kLog2e : 0.f;
+    finite = finite && !(fabsf(ref[g]) > 3.0e38f) && ref[g] == ref[g];
+  }
+  if (tid == 0) sh_slow = 0;
+  if (finite) {
+    float s[GT];
+#pragma unroll
+    for (int g = 0; g < GT; ++g) s[g] = 0.f;
+    for (int qd = tid; qd < nq; qd += R * blockDim.x) {
+      float x[R][GT][4];
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        load_quad<GT>(sc, max_pages, G, vec, 4 * (qd + r * blockDim.x), nf,
+                      -INFINITY, x[r]);
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int g = 0; g < GT; ++g)
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            s[g] += ex2_fast(fmaf(x[r][g][u], kLog2e, -ref[g]));
+    }
+#pragma unroll
+    for (int g = 0; g < GT; ++g) {
+      float sg = s[g];
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1)
+        sg += __shfl_xor_sync(0xffffffffu, sg, o);
+      if (lane == 0) red_s[wid][g] = sg;
+    }
+    __syncthreads();
+    if (tid < G) {
+      float sum = 0.f;
+      for (int w = 0; w < nwarps; ++w) sum += red_s[w][tid];
+      zs[tid] = __ldg(sc + (size_t)tid * max_pages) * kLog2e + lg2_fast(sum);
+      if (!(sum < INFINITY)) sh_slow = 1;
+    }
+    __syncthreads();
+  }
+  if (!finite || sh_slow) {
   {
     float m[GT], s[GT];
 #pragma unroll
@@ -224,6 +287,7 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
     zs[tid] = m + lg2_fast(s);
   }
   __syncthreads();
+  }
   } else {
     if (tid < G) zs[tid] = 0.f;
     __syncthreads();
@@ -237,51 +301,61 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
   float zreg[GT];
 #pragma unroll
   for (int g = 0; g < GT; ++g) zreg[g] = g < G ? zs[g] : 0.f;
-  for (int qd = tid; qd < nq; qd += R * blockDim.x) {
+  // last block of quads first: the normaliser pass just read them, so the
+  // part of the scores still in L1 is read before it is evicted
+  const int qstep = R * blockDim.x;
+  for (int it = (nq + qstep - 1) / qstep - 1; it >= 0; --it) {
+    const int qd = it * qstep + tid;
+    if (qd >= nq) continue;
     float x[R][GT][4];
+    // heads at or above G read -inf: no term, no maximum
 #pragma unroll
     for (int r = 0; r < R; ++r)
-      load_quad<GT>(sc, max_pages, G, vec, 4 * (qd + r * blockDim.x), nf, 0.f,
-                    x[r]);
+      load_quad<GT>(sc, max_pages, G, vec, 4 * (qd + r * blockDim.x), nf,
+                    -INFINITY, x[r]);
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int j0 = 4 * (qd + r * blockDim.x);
       if (j0 >= 4 * nq) break;
       uint32_t kq[4];
+      float key[4];
+      if (rule == LOCKS_MERGE_GROUP_MAX) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          key[u] = -INFINITY;
+#pragma unroll
+          for (int g = 0; g < GT; ++g)
+            key[u] = fmaxf(key[u], fmaf(x[r][g][u], kLog2e, -zreg[g]));
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float sum = 0.f;
+#pragma unroll
+          for (int g = 0; g < GT; ++g)
+            sum += ex2_fast(fmaf(x[r][g][u], kLog2e, -zreg[g]));
+          key[u] = lg2_fast(sum);
+          if (!(sum > 0.f && sum < INFINITY)) {
+            // every term underflowed (or, pooling raw masses, overflowed):
+            // subtract the largest first
+            float m = -INFINITY;
+#pragma unroll
+            for (int g = 0; g < GT; ++g)
+              m = fmaxf(m, fmaf(x[r][g][u], kLog2e, -zreg[g]));
+            float t = 0.f;
+#pragma unroll
+            for (int g = 0; g < GT; ++g)
+              t += ex2_fast(fmaf(x[r][g][u], kLog2e, -zreg[g]) - m);
+            key[u] = m + lg2_fast(t);
+          }
+        }
+      }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int j = j0 + u;
-        kq[u] = 0u;
-        if (j < 1 || j > n - 2) continue;
-        float key;
-        float sum = 0.f;
-        if (rule == LOCKS_MERGE_GROUP_MAX) {
-          key = -INFINITY;
-#pragma unroll
-          for (int g = 0; g < GT; ++g)
-            if (g < G) key = fmaxf(key, x[r][g][u] * kLog2e - zreg[g]);
-        } else {
-#pragma unroll
-          for (int g = 0; g < GT; ++g)
-            if (g < G) sum += ex2_fast(x[r][g][u] * kLog2e - zreg[g]);
-        }
-        if (rule == LOCKS_MERGE_GROUP_MAX) {
-        } else if (sum > 0.f && sum < INFINITY) {
-          key = lg2_fast(sum);
-        } else {  // every term underflowed (or, pooling raw masses,
-                  // overflowed): subtract the largest first
-          float m = -INFINITY;
-#pragma unroll
-          for (int g = 0; g < GT; ++g)
-            if (g < G) m = fmaxf(m, x[r][g][u] * kLog2e - zreg[g]);
-          float t = 0.f;
-#pragma unroll
-          for (int g = 0; g < GT; ++g)
-            if (g < G) t += ex2_fast(x[r][g][u] * kLog2e - zreg[g] - m);
-          key = m + lg2_fast(t);
-        }
-        kq[u] = order_key(key);
-        kmin = min(kmin, kq[u]);
+        // candidates are pages 1..n-2
+        const bool cand = (unsigned)(j0 + u - 1) <= (unsigned)(n - 3);
+        kq[u] = cand ? order_key(key[u]) : 0u;
+        kmin = min(kmin, cand ? kq[u] : 0xffffffffu);
         kmax = max(kmax, kq[u]);
       }
       if (kvec) {
@@ -358,8 +432,7 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
     }
     if (lane == 31) sh_wcnt[0][wid] = incl;
     __syncthreads();
-    int before = 0;
-    for (int w = 0; w < wid; ++w) before += sh_wcnt[0][w];
+    const int before = warps_before<nwarps>(sh_wcnt[0], wid, lane);
     const int mine = before + incl - cnt;  // count above this lane's digits
     if (mine < rem && rem <= mine + cnt) {
       const int c[8] = {c4.w, c4.z, c4.y, c4.x,
@@ -395,15 +468,22 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
     gt += __shfl_xor_sync(0xffffffffu, gt, o);
     eq += __shfl_xor_sync(0xffffffffu, eq, o);
   }
-  if (lane == 0) {
-    sh_wcnt[0][wid] = gt;
-    sh_wcnt[1][wid] = eq;
-  }
-  __syncthreads();
-  int gt_before = 0, eq_before = 0;
-  for (int w = 0; w < wid; ++w) {
-    gt_before += sh_wcnt[0][w];
-    eq_before += sh_wcnt[1][w];
+  int gt_before, eq_before;
+  if constexpr (SMEM_KEYS) {
+    // n <= 32768 pages: both counts and their sums stay below 2^15
+    if (lane == 0) sh_wcnt[0][wid] = (eq << 16) | gt;
+    __syncthreads();
+    const int ge_before = warps_before<nwarps>(sh_wcnt[0], wid, lane);
+    gt_before = ge_before & 0xffff;
+    eq_before = ge_before >> 16;
+  } else {
+    if (lane == 0) {
+      sh_wcnt[0][wid] = gt;
+      sh_wcnt[1][wid] = eq;
+    }
+    __syncthreads();
+    gt_before = warps_before<nwarps>(sh_wcnt[0], wid, lane);
+    eq_before = warps_before<nwarps>(sh_wcnt[1], wid, lane);
   }
   for (int base = w_lo; base < w_hi; base += 128) {
     const int j0 = base + 4 * lane;
