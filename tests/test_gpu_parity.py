@@ -525,6 +525,38 @@ def test_select_matches_oracle_on_same_scores():
             assert v == sorted(v) and len(set(v)) == len(v)
 
 
+@pytest.mark.parametrize("G", [1, 4, 16])
+def test_select_normaliser_fallback(G):
+    """Scores for which the normaliser's common reference (each head's
+    page-0 score) does not serve: page 0 at -inf, page 0 far below every
+    other page, one page far above page 0 (the sum against the reference
+    overflows).  The selection must still be the oracle's (Eq.(5) with the
+    normaliser over all full pages)."""
+    rng = np.random.default_rng(11 + G)
+    batch, h_kv, max_pages, k = 3, 2, 400, 20
+    lens = [16 * 400, 16 * 333 + 7, 16 * 400]
+    scores = rng.normal(0, 2, (batch, h_kv, G, max_pages)).astype(np.float32)
+    scores[0, 0, :, 0] = -np.inf
+    scores[0, 1, :, 0] = -200.0
+    scores[1, :, :, 0] = -120.0
+    scores[2, 1, 0, 5] = 90.0
+    ws = B.new_workspace(batch, G * h_kv, h_kv, max_pages, k, DEV)
+    idx = torch.zeros(batch, h_kv, k, dtype=torch.int32, device=DEV)
+    B.locks_select_pages(torch.from_numpy(scores).to(DEV), i32(lens),
+                         G * h_kv, k, idx, ws)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == 0
+    ig = idx.cpu().numpy()
+    io = O.select_store(scores.astype(np.float64), lens, k)
+    for b in range(batch):
+        for h in range(h_kv):
+            ok, _ = selection_agrees(ig[b, h], io[b, h],
+                                     scores[b, h].astype(np.float64),
+                                     lens[b], k, 1e-4)
+            assert ok, (b, h, ig[b, h], io[b, h])
+    assert 5 in ig[2, 1]
+
+
 # ---------------------------------------------------------------------------
 # sparse attention over the oracle's selection
 # ---------------------------------------------------------------------------
