@@ -14,7 +14,7 @@ Sources (cited by page title and section, equation or algorithm):
   [gist]   "Resumo Técnico: LOCKS – Sumários de Chaves Compactos por Página
            para Decodificação Eficiente de Contexto Longo" (gist.science), §2.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * quantiser: symmetric, fp16 scales (basis: one per column; coefficients:
     one per row; centroid: one per page), scale = fp16_rn(fp32(absmax)/qmax),
     code = clamp(rint_fp32(fp32(x)/fp32(scale)), -qmax, qmax), qmax = 7 for

@@ -1,6 +1,6 @@
 """GPU parity: every step of the CUDA path against the float64 oracle.
 
-Tolerances (from the LOCKS decode specification, the design doc lists them):
+Tolerances of the LOCKS decode path against the float64 oracle:
   * quantised bytes: bit-exact where both sides quantise the same fp32
     values (the pack entry point, the centroid); after the eigensolver,
     codes may differ by one step only where the oracle's value lies near a
