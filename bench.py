@@ -386,13 +386,14 @@ def ragged_config(B, W, dev, peak_gbs, n_steps=50):
     return out
 
 
-def append_config(B, W, dev, n_steps=64):
+def append_config(B, W, dev, sm_mhz, n_steps=64):
     """The append workload (llama70b_128k_append: 8 x 131072 tokens,
-    64q/8kv, k = 128): every step appends one token per sequence (writing K
-    and V and building the summary of a page the append fills, once every
-    16 steps here) and then runs the decode step; the incremental build is
-    part of the step.  CUDA events around the append and around the whole
-    step."""
+    64q/8kv, k = 128): the summary build of the whole cache at the
+    prefill/decode boundary (524,288 page-heads, timed on its own, warm), then
+    steps that each append one token per sequence (writing K and V and
+    building the summary of a page the append fills, once every 16 steps
+    here) and run the decode step; the incremental build is part of the
+    step.  CUDA events around the build, the append and the whole step."""
     import torch
     spec = W.SPECS["llama70b_128k_append"]
     wl = W.generate(spec, dev)
@@ -406,6 +407,14 @@ def append_config(B, W, dev, n_steps=64):
                        dtype=torch.int32, device=dev)
     store = B.new_summary_store(batch, spec.h_kv, max_pages, dev)
     B.locks_build_summaries(wl.k_cache, wl.page_table, seq, pgs, store)
+    b0, b1 = torch.cuda.Event(True), torch.cuda.Event(True)
+    torch.cuda.synchronize()
+    b0.record()
+    B.locks_build_summaries(wl.k_cache, wl.page_table, seq, pgs, store)
+    b1.record()
+    torch.cuda.synchronize()
+    build_ms = b0.elapsed_time(b1)
+    n_build = int(seq.numel()) * spec.h_kv
     ws = B.new_workspace(batch, spec.h_q, spec.h_kv, max_pages, spec.k, dev)
     idx = torch.empty(batch, spec.h_kv, spec.k, dtype=torch.int32,
                       device=dev)
@@ -439,7 +448,11 @@ def append_config(B, W, dev, n_steps=64):
            "append_filling_a_page_us": round(1e3 * statistics.median(
                [app[s] for s in fills]), 2) if fills else None,
            "step_ms": round(statistics.mean(step), 4),
-           "tokens_per_s": round(batch / (statistics.mean(step) / 1e3))}
+           "tokens_per_s": round(batch / (statistics.mean(step) / 1e3)),
+           "boundary_build": {
+               "page_heads": n_build, "ms": round(build_ms, 3),
+               "page_heads_per_s": round(n_build / (build_ms / 1e3)),
+               "roofline": build_issue(n_build, build_ms, sm_mhz)}}
     del wl, store, ws
     torch.cuda.empty_cache()
     return res
@@ -938,7 +951,8 @@ def run_locks(args):
             "ms_per_step": round(dms, 4),
             "gbs": round(dense_bytes / (dms / 1e3) / 1e9, 1)}
         line["small_configs"] = small_configs(B, W, dev)
-        line["append_config"] = append_config(B, W, dev)
+        line["append_config"] = append_config(
+            B, W, dev, clk.get("sm_mhz") or clk.get("sm_max_mhz"))
         line["ragged_config"] = ragged_config(B, W, dev, peak)
         line["quality"] = selection_quality(B, wl, store, scores, ws, lens,
                                             k, spec.h_q, n_records)
