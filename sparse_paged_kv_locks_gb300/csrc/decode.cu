@@ -180,7 +180,8 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
     __syncthreads();
     total = s_pre[batch];
   }
-  const int chunk = max(1, (total + n_warps - 1) / n_warps);
+  const int chunk =
+      (int)max(1LL, ((long long)total + n_warps - 1) / n_warps);
   const int gw = blockIdx.x * kDecWarps + wid;
   const bool active = gw < n_warps && (long long)gw * chunk < total;
   const int pb = active ? gw * chunk : 0, pe = min(total, pb + chunk);
@@ -448,7 +449,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
                    int dense, int G, __nv_bfloat16 *__restrict__ o_out,
                    float *__restrict__ lse_out,
                    const int32_t *__restrict__ status_src,
-                   int32_t *status_mirror) {
+                   int32_t *status_mirror, int chunk_hint) {
   const int lane = threadIdx.x & 31;
   pdl_wait();  // partials and layout of the decode kernel
   // the step's device status word is final once the decode kernel is done
@@ -460,7 +461,9 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
   if (row >= (long long)batch * h_kv * G) return;
   const int u = (int)(row / G), g = (int)(row - (long long)u * G);
   const Layout lay{meta + 1, batch, h_kv, dense ? 0 : h_kv * k};
-  const int chunk = meta[0];
+  // sparse decode: the run length is known at launch (saves a dependent
+  // load); dense decode reads it from the decode kernel's layout
+  const int chunk = chunk_hint > 0 ? chunk_hint : meta[0];
   const int2 sp = lay.span(u);
   uint2 *dst = reinterpret_cast<uint2 *>(o_out + row * kDim) + lane;
   float M = -INFINITY, wsum = 0.f;
@@ -573,11 +576,17 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
       lse_part, meta, status);
   if (e != cudaSuccess) return e;
   const long long rows = (long long)batch * h_kv * G;
+  // the decode kernel's run length for sparse decode (dense decode's
+  // depends on the sequence lengths and is read on the device)
+  const long long per_warp =
+      ((long long)batch * h_kv * k + n_warps - 1) / n_warps;
+  const int chunk_hint = idx ? (int)(per_warp > 1 ? per_warp : 1) : 0;
   return launch_pdl(combine_kernel,
                     dim3((unsigned)((rows + kCombineWarps - 1) / kCombineWarps)),
                     dim3(32 * kCombineWarps), 0, stream, o_part, lse_part,
                     (const int *)meta, batch, h_kv, k, idx ? 0 : 1, G, oo,
-                    lse_out, (const int32_t *)status, status_mirror);
+                    lse_out, (const int32_t *)status, status_mirror,
+                    chunk_hint);
 }
 
 }  // namespace locks
