@@ -658,9 +658,11 @@ def rank_precision_ablation(B, wl, lens, k, h_q, peak_gbs, n_seqs=4,
     return {"sequences": batch, "budget_pages": k, "steps": n_steps,
             "score_timing": f"mean of {n_time} calls, L2 flushed before "
                             "each", "variants": out,
-            "note": "variant records scored on CUDA cores (a warp per "
-                    "record, lane-parallel over head dims); the shipped "
-                    "(8, 4-bit) record is the tensor-core path"}
+            "note": "variant records scored by the variant kernel (a warp "
+                    "per record: codes decoded to a bf16 operand tile, "
+                    "projections on tensor cores, logits in fp32); the "
+                    "shipped (8, 4-bit) record has its own layout and "
+                    "scoring kernel"}
 
 
 def host_cores():
