@@ -981,6 +981,33 @@ def test_merge_rules_match_oracle(rule, G):
                     (rule, b, h, p)
 
 
+@pytest.mark.parametrize("G", [1, 8, 16])
+def test_select_more_units_than_sms(G):
+    """160 (sequence, KV head) units, more than a GB300 has SMs: the launch
+    takes the form compiled for two CTAs per SM (G <= 8) or the one-CTA-per-
+    SM form in two waves (G = 16); every unit must still match the oracle's
+    selection on the same scores."""
+    rng = np.random.default_rng(300 + G)
+    batch, h_kv, max_pages, k = 40, 4, 64, 12
+    lens = [int(x) for x in rng.integers(0, 16 * max_pages + 1, batch)]
+    lens[0], lens[1] = 16 * max_pages, 16 * k
+    scores = rng.normal(0, 3, (batch, h_kv, G, max_pages)).astype(np.float32)
+    ws = B.new_workspace(batch, G * h_kv, h_kv, max_pages, k, DEV)
+    idx = torch.zeros(batch, h_kv, k, dtype=torch.int32, device=DEV)
+    B.locks_select_pages(torch.from_numpy(scores).to(DEV), i32(lens),
+                         G * h_kv, k, idx, ws)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == 0
+    ig = idx.cpu().numpy()
+    io = O.select_store(scores.astype(np.float64), lens, k)
+    for b in range(batch):
+        for h in range(h_kv):
+            ok, _ = selection_agrees(ig[b, h], io[b, h],
+                                     scores[b, h].astype(np.float64),
+                                     lens[b], k, 1e-4)
+            assert ok, (b, h, ig[b, h], io[b, h])
+
+
 @pytest.mark.parametrize("G,max_pages", [(8, 300), (16, 97), (4, 33001),
                                          (2, 33004)])
 def test_select_group_sizes_and_long_tables(G, max_pages):
