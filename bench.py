@@ -169,10 +169,12 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def score_traffic(n_records):
+def score_traffic(n_records, group):
     """DRAM bytes per score launch from the committed ncu capture
     (profiles/score_kernel_traffic.json), scaled by records; None when the
-    scoring kernel's source changed since the capture."""
+    scoring kernel's source changed since the capture or when the workload's
+    GQA group size selects another form of the kernel than the captured
+    one."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles",
@@ -184,7 +186,7 @@ def score_traffic(n_records):
             digest = hashlib.sha256(f.read()).hexdigest()
     except (OSError, ValueError):
         return None
-    if d.get("score_cu_sha256") != digest:
+    if d.get("score_cu_sha256") != digest or d.get("group_size") != group:
         return None
     return round(float(d["dram_bytes_per_record"]) * n_records)
 
@@ -858,7 +860,7 @@ def run_locks(args):
             "bound": "hbm", "kernel": "score (summary stream)",
             "achieved": round(score_gbs, 1), "peak": peak, "unit": "GB/s",
             "frac": round(score_gbs / peak, 4),
-            "traffic": score_traffic(n_records),
+            "traffic": score_traffic(n_records, spec.h_q // spec.h_kv),
             "peak_source": peak_src,
             "algorithmic_bytes": score_bytes},
         "step_roofline": {
