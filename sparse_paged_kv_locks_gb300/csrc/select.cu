@@ -168,7 +168,9 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
   const bool kvec = SMEM_KEYS || (max_pages & 3) == 0;  // 16-byte key rows
   const int nq = (n + 3) >> 2;        // quads of pages covering [0, n)
   // quads a thread has in flight at once (what the registers allow)
-  constexpr int R = MINB == 1 ? (GT <= 8 ? 2 : 1) : (GT <= 4 ? 2 : 1);
+  // (at two CTAs per SM and G = 4 a second quad in flight measured slower,
+  // 16.6 against 16.2 us on 256 units, and spilled)
+  constexpr int R = MINB == 1 ? (GT <= 8 ? 2 : 1) : (GT <= 2 ? 2 : 1);
   for (int i = tid; i < kRadixBins; i += blockDim.x) hist[0][i] = 0;
 
   // Z_g: log2-sum-exp2 over the summarised pages [0, nf) (group-mass
