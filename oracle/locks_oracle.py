@@ -32,10 +32,11 @@ Readings taken where the pages are silent:
     sequence, sink included; sink = logical page 0, recent = the page holding
     the last token; ties in the share-average go to the lower page index.
 
-Pins (tests/test_oracle_pins.py): the §5.1 toy example in closed form, an SVD
-cross-check, orthonormal bases, exactness at r = rank, the Eckart-Young tail,
-Eq.(1) identity, Eq.(7) bound, brute-force top-k, k >= pages giving dense
-attention, and hand-written record fixtures.  Parity unpinned by the pages:
+Pins (tests/test_oracle_pins.py): the §5.1 toy example in closed form, a
+cross-check against the Gram-matrix eigensolver of Eq.(3), orthonormal
+bases, exactness at r = rank, the Eckart-Young tail, Eq.(1) identity, Eq.(7) bound, brute-force top-k, k >= pages giving dense
+attention, attention and page scores by token-position loops through the page
+table, and hand-written record fixtures.  Parity unpinned by the pages:
 the quantiser's scale dtype/granularity, rounding and sign rule are readings
 (pinned only by their own invariants and by hand-written byte fixtures).
 """
@@ -77,36 +78,42 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 # Build: notes §4.1 Eq.(2)-(3), §4.3 Algorithm 1
 # ----------------------------------------------------------------------------
 def page_summary(keys: np.ndarray, r: int = RANK):
-    """Unquantised per-page summary of Algorithm 1 for keys [..., B, d].
+    """Unquantised rank-r page summary of §4.1 for keys [..., B, d].
+
+    Eq.(2) centres the page on its mean; Eq.(3) takes the eigenpairs of the
+    token-space Gram matrix D D^T.  Those are the singular triplets of the
+    centred keys themselves: with D = U diag(sigma) W^T, the eigenvectors of
+    D D^T are the columns of U with eigenvalues sigma^2, the basis
+    V = D^T U_r Sigma_r^{-1} is W_r, and the coefficients c_i = V^T delta_i
+    are the rows of U_r Sigma_r.  This statement takes that route (one SVD
+    of D), so it does not repeat the Gram/eigensolver steps the kernels take.
 
     Returns dict with
       mu   [..., d]     page centroid (Eq.(2))
       D    [..., B, d]  centred deviations delta_i = k_i - mu
-      lam  [..., B]     eigenvalues of D D^T, descending (Eq.(3)), >= 0
-      U    [..., B, B]  matching eigenvectors (columns), sign-canonicalised
-      V    [..., d, r]  basis V = D^T U_r Sigma_r^{-1}
-      C    [..., B, r]  coefficients C = U_r Sigma_r  (c_i = V^T delta_i)
-      tau  [...]        spectral tail sum_{k>r} sigma_k^2
+      lam  [..., B]     sigma_k^2: eigenvalues of D D^T, descending
+      U    [..., B, B]  left singular vectors (columns), sign-canonicalised
+      V    [..., d, r]  orthonormal basis of the top-r directions
+      C    [..., B, r]  coefficients, c_i = V^T delta_i
+      tau  [...]        spectral tail sum_{k>r} sigma_k^2 (Eckart-Young)
     """
     K = np.asarray(keys, dtype=np.float64)
     mu = K.mean(axis=-2)                                  # Eq.(2)
     D = K - mu[..., None, :]                              # delta_i rows
-    gram = D @ np.swapaxes(D, -1, -2)                     # D D^T, B x B
-    lam, U = np.linalg.eigh(gram)                         # Eq.(3), ascending
-    lam = np.maximum(lam[..., ::-1], 0.0)
-    U = U[..., ::-1].copy()
-    # sign: entry of largest magnitude positive, lowest index on exact ties
+    U, sigma, Wt = np.linalg.svd(D, full_matrices=False)  # descending sigma
+    # sign: each u_k's entry of largest magnitude positive (lowest index on
+    # exact ties); w_k flips with it so that D = U diag(sigma) W^T still holds
     piv = np.argmax(np.abs(U), axis=-2)                   # [..., B]
     pv = np.take_along_axis(U, piv[..., None, :], axis=-2)[..., 0, :]
-    U = U * np.where(pv < 0, -1.0, 1.0)[..., None, :]
-    sigma = np.sqrt(lam)
+    flip = np.where(pv < 0, -1.0, 1.0)
+    U = U * flip[..., None, :]
+    Wt = Wt * flip[..., :, None]
+    lam = sigma * sigma
     lam1 = lam[..., :1]
     keep = (lam[..., :r] > ZERO_TOL * lam1) & (lam1 > 0)  # [..., r]
-    Ur, sr = U[..., :r], sigma[..., :r]
-    safe = np.where(keep, sr, 1.0)
-    V = (np.swapaxes(D, -1, -2) @ Ur) / safe[..., None, :]
-    V = np.where(keep[..., None, :], V, 0.0)
-    C = np.where(keep[..., None, :], Ur * sr[..., None, :], 0.0)
+    V = np.where(keep[..., None, :],
+                 np.ascontiguousarray(np.swapaxes(Wt[..., :r, :], -1, -2)), 0.0)
+    C = np.where(keep[..., None, :], U[..., :r] * sigma[..., None, :r], 0.0)
     tau = lam[..., r:].sum(axis=-1)
     return dict(mu=mu, D=D, lam=lam, U=U, V=V, C=C, tau=tau)
 

@@ -1,9 +1,9 @@
 """Pins of the float64 oracle against what the LOCKS pages and mathematics fix.
 
 None of these checks retypes an oracle formula: each compares the oracle with
-a closed form, an independent library routine (SVD instead of the Gram
-eigensolver), brute force on tiny inputs, an identity of the pages, or a
-hand-derived byte fixture.
+a closed form, an independent library routine (the Gram eigensolver of
+Eq.(3) against the oracle's SVD of the centred keys), brute force on tiny
+inputs, an identity of the pages, or a hand-derived byte fixture.
 """
 import itertools
 import json
@@ -68,25 +68,30 @@ def test_toy_example_closed_form(golden_dir):
 
 
 # --------------------------------------------------------------------------
-# Eq.(3) against an independent routine (SVD of D) and basis properties
+# Eq.(3) as printed (eigenpairs of the Gram matrix D D^T, a different library
+# routine from the oracle's SVD) and basis properties
 # --------------------------------------------------------------------------
-def test_gram_eigen_matches_svd():
+def test_summary_matches_gram_eigensolver():
     rng = _rng(1)
     keys = _pages(rng, 24)
     s = O.page_summary(keys, r=8)
     for j in range(keys.shape[0]):
         D = keys[j] - keys[j].mean(axis=0)
-        U_, S_, Vt_ = np.linalg.svd(D, full_matrices=False)
-        # eigenvalues of D D^T are the squared singular values of D (the zero
-        # one only to rounding of the squared scale)
-        assert s["lam"][j] == pytest.approx(S_ ** 2, rel=1e-9,
-                                            abs=1e-13 * S_[0] ** 2)
-        gaps = np.diff(S_[:9] ** 2)
+        lam, U = np.linalg.eigh(D @ D.T)
+        lam, U = lam[::-1], U[:, ::-1]
+        # the eigenvalues (the zero one only to rounding of the squared scale)
+        assert s["lam"][j] == pytest.approx(np.maximum(lam, 0), rel=1e-9,
+                                            abs=1e-13 * lam[0])
         for k in range(8):
-            if min(abs(gaps[k]) if k < 8 else 1, abs(gaps[k - 1]) if k else 1) \
-                    < 1e-6 * S_[0] ** 2:
+            gap = min(lam[k - 1] - lam[k] if k else np.inf, lam[k] - lam[k + 1])
+            if gap < 1e-6 * lam[0]:
                 continue
-            assert abs(s["V"][j][:, k] @ Vt_[k]) == pytest.approx(1, abs=1e-9)
+            # V = D^T U_r Sigma_r^{-1}, column by column, up to sign
+            v = D.T @ U[:, k] / math.sqrt(lam[k])
+            assert abs(s["V"][j][:, k] @ v) == pytest.approx(1, abs=1e-9)
+            # the sign rule: u_k's largest-magnitude entry is positive
+            u = s["C"][j][:, k] / math.sqrt(s["lam"][j][k])
+            assert u[np.argmax(np.abs(u))] > 0
         # C = U_r Sigma_r equals D V (c_i = V^T delta_i)
         assert s["C"][j] == pytest.approx(D @ s["V"][j], abs=1e-10)
 
@@ -439,6 +444,167 @@ def test_all_pages_selected_equals_dense():
     o1, l1 = O.sparse_decode(q, kc, vc, pt, lens, idx)
     o2, l2 = O.dense_decode(q, kc, vc, pt, lens)
     assert np.abs(o1 - o2).max() < 1e-12 and np.abs(l1 - l2).max() < 1e-12
+
+
+# --------------------------------------------------------------------------
+# Paged gather (notes §2 and Algorithm 2: attention over the selected pages'
+# tokens, found through the page table) and the full-page score cut (a
+# summary exists only for a page that has filled, notes §2 Fig. 1)
+# --------------------------------------------------------------------------
+def _paged_case(seed=71):
+    rng = _rng(seed)
+    P, h_kv, G, max_pages = 11, 2, 3, 5
+    kc = rng.normal(size=(P, h_kv, 16, 128))
+    vc = rng.normal(size=(P, h_kv, 16, 128))
+    # non-identity tables: no logical page maps to its own index
+    pt = np.array([[7, 2, 9, 4, 0],
+                   [3, 10, 6, 8, 1],
+                   [5, 1, 0, -1, -1],
+                   [8, 6, 7, 9, 2]], np.int32)
+    lens = np.array([16 * 3 + 5, 16 * 5, 0, 1])
+    q = rng.normal(size=(4, h_kv * G, 128))
+    # selections: out of order, -1 padded, the partial page included or not
+    idx = np.array([[[3, 0, 1, -1], [0, 2, 3, -1]],
+                    [[4, 0, 2, 1], [0, 4, -1, -1]],
+                    [[-1, -1, -1, -1], [-1, -1, -1, -1]],
+                    [[0, -1, -1, -1], [-1, 0, -1, -1]]], np.int32)
+    return kc, vc, pt, lens, q, idx, h_kv, G
+
+
+def _token_loop_attention(q, kc, vc, pt, L, pages, h, G):
+    """Attention by a loop over the sequence's token positions: token t lives
+    in logical page t // 16, slot t % 16, physical page pt[t // 16]; it is
+    attended when its logical page is selected."""
+    sel = {int(p) for p in pages if p >= 0}
+    toks = [t for t in range(int(L)) if t // 16 in sel]
+    o = np.zeros((G, 128))
+    lse = np.full(G, -np.inf)
+    for g in range(G):
+        if not toks:
+            continue
+        z = [float(np.dot(q[h * G + g], kc[pt[t // 16], h, t % 16]))
+             / math.sqrt(128) for t in toks]
+        m = max(z)
+        w = [math.exp(x - m) for x in z]
+        tot = sum(w)
+        lse[g] = m + math.log(tot)
+        for wi, t in zip(w, toks):
+            o[g] += (wi / tot) * vc[pt[t // 16], h, t % 16]
+    return o, lse
+
+
+def test_paged_gather_by_token_loop():
+    kc, vc, pt, lens, q, idx, h_kv, G = _paged_case()
+    o, lse = O.sparse_decode(q, kc, vc, pt, lens, idx)
+    od, ld = O.dense_decode(q, kc, vc, pt, lens)
+    for b in range(len(lens)):
+        n = -(-int(lens[b]) // 16)
+        for h in range(h_kv):
+            ro, rl = _token_loop_attention(q[b], kc, vc, pt[b], lens[b],
+                                           idx[b, h], h, G)
+            sl = slice(h * G, (h + 1) * G)
+            assert np.abs(o[b, sl] - ro).max() < 1e-12, (b, h)
+            assert np.array_equal(np.isinf(lse[b, sl]), np.isinf(rl))
+            fin = np.isfinite(rl)
+            assert np.abs(lse[b, sl][fin] - rl[fin]).max(initial=0) < 1e-12
+            ro, rl = _token_loop_attention(q[b], kc, vc, pt[b], lens[b],
+                                           range(n), h, G)
+            assert np.abs(od[b, sl] - ro).max() < 1e-12, (b, h)
+    # the empty sequence attends nothing: o = 0, lse = -inf
+    assert (o[2] == 0).all() and np.isneginf(lse[2]).all()
+    # a one-token sequence attends that token alone: o_g = v_0
+    assert np.abs(o[3, :G] - vc[pt[3, 0], 0, 0]).max() < 1e-12
+
+
+def _reconstructed_page_lse(q, rec):
+    """LSE over one page's tokens of q . k_hat_i / sqrt(d), with the keys
+    reconstructed from the record first: k_hat_i = mu_hat + V_hat c_hat_i."""
+    mu, V, C = O.dequantize(O.decode_records(rec))
+    z = [float(np.dot(q, mu + V @ C[i])) / math.sqrt(128) for i in range(16)]
+    m = max(z)
+    return m + math.log(sum(math.exp(x - m) for x in z))
+
+
+def test_score_store_cut_and_head_groups():
+    rng = _rng(72)
+    P, h_kv, G, max_pages = 9, 2, 3, 4
+    keys = np.stack([_pages(rng, h_kv) for _ in range(P)]).astype(np.float32)
+    pt = np.array([[4, 1, 7, 2], [8, 3, 0, 6], [5, 0, 1, 2]], np.int32)
+    lens = np.array([16 * 3 + 7, 16 * 4, 15])
+    seq_ids = [0, 0, 0, 0, 1, 1, 1, 1]
+    page_ids = [0, 1, 2, 3, 0, 1, 2, 3]
+    # records for every slot, the partial pages' too, so that a store read
+    # past the full pages would find a well-formed record
+    store, _ = O.build_summaries(keys, pt, seq_ids, page_ids, 3, max_pages)
+    store[2, :, 0] = store[0, :, 1]
+    q = rng.normal(size=(3, h_kv * G, 128))
+    s = O.score_store(q, store, lens)
+    assert s.shape == (3, h_kv, G, max_pages)
+    for b in range(3):
+        nf = int(lens[b]) // 16
+        for h in range(h_kv):
+            for g in range(G):
+                for j in range(max_pages):
+                    if j >= nf:
+                        assert np.isnan(s[b, h, g, j]), (b, h, g, j)
+                        continue
+                    ref = _reconstructed_page_lse(q[b, h * G + g],
+                                                  store[b, h, j])
+                    assert abs(s[b, h, g, j] - ref) < 1e-9, (b, h, g, j)
+
+
+def test_planted_gather_and_cut_mistakes_are_caught(monkeypatch):
+    orig_gather = O.gather_tokens
+
+    def gather_variant(ignore_table=False, extra=0, keep_pad=False):
+        def f(k_cache, v_cache, page_table, b, h, pages, seq_len):
+            Ks, Vs = [], []
+            for p in pages:
+                if p < 0 and not keep_pad:
+                    continue
+                ntok = min(16, int(seq_len) - 16 * int(p) + extra)
+                if ntok <= 0:
+                    continue
+                phys = int(p) if ignore_table else int(page_table[b][p])
+                Ks.append(np.asarray(k_cache[phys, h, :ntok], np.float64))
+                Vs.append(np.asarray(v_cache[phys, h, :ntok], np.float64))
+            if not Ks:
+                return np.zeros((0, 128)), np.zeros((0, 128))
+            return np.concatenate(Ks), np.concatenate(Vs)
+        return f
+
+    for plant in (dict(ignore_table=True), dict(extra=1), dict(extra=-1),
+                  dict(keep_pad=True)):
+        monkeypatch.setattr(O, "gather_tokens", gather_variant(**plant))
+        with pytest.raises(AssertionError):
+            test_paged_gather_by_token_loop()
+    monkeypatch.setattr(O, "gather_tokens", orig_gather)
+    test_paged_gather_by_token_loop()
+
+    def score_store_variant(ceil_cut=False, interleave=False):
+        def f(q, store, seq_lens):
+            q = np.asarray(q, np.float64)
+            batch, h_kv, max_pages, _ = store.shape
+            G = q.shape[1] // h_kv
+            out = np.full((batch, h_kv, G, max_pages), np.nan)
+            for b in range(batch):
+                L = int(seq_lens[b])
+                nf = -(-L // 16) if ceil_cut else L // 16
+                for h in range(h_kv):
+                    if nf == 0:
+                        continue
+                    mu, V, C = O.dequantize(O.decode_records(store[b, h, :nf]))
+                    heads = [g * h_kv + h for g in range(G)] if interleave \
+                        else list(range(h * G, (h + 1) * G))
+                    out[b, h, :, :nf] = O.score_from_summaries(
+                        q[b, heads], mu, V, C)
+            return out
+        return f
+
+    for plant in (dict(ceil_cut=True), dict(interleave=True)):
+        monkeypatch.setattr(O, "score_store", score_store_variant(**plant))
+        with pytest.raises(AssertionError):
+            test_score_store_cut_and_head_groups()
 
 
 # --------------------------------------------------------------------------
