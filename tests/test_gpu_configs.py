@@ -9,9 +9,11 @@
     and build every page the append fills
 
 (tiny_4k is covered end to end in test_gpu_parity.py, llama8b_128k in
-test_gpu_fullsize.py.)  As there, the oracle builds the sampled pairs'
-records, which replace the GPU-built records of those pairs, so scores and
-selections are compared on identical records; attention runs in the full
+test_gpu_fullsize.py.)  As there, the full-batch GPU build of the sampled
+pairs is first checked against the oracle's build of the same keys
+(tests/build_parity.py); then the oracle's records replace the GPU-built
+records of those pairs, so scores and selections are compared on identical
+records; attention runs in the full
 batch with the oracle's selection of the sampled pairs.  Tolerances are the
 specification's: scores 1e-3 absolute, selections identical except pages
 whose log share-average lies within 1e-3 of the boundary, attention
@@ -21,6 +23,7 @@ import numpy as np
 import pytest
 import torch
 
+from build_parity import check_build, check_full_size_build
 from oracle import locks_oracle as O
 from sparse_paged_kv_locks_gb300 import binding as B
 from sparse_paged_kv_locks_gb300 import workload as W
@@ -97,6 +100,7 @@ def run_sampled(spec, dev, samples, ks, q_step=1):
     batch, max_pages = wl.page_table.shape
     h_kv, G = spec.h_kv, spec.group
     store = build_all(wl, lens, dev)
+    check_full_size_build(B, wl, store, samples, dev, spec.name)
     q = wl.queries[q_step]
     qn = q.float().cpu().numpy()
     orc = {}
@@ -197,23 +201,39 @@ def test_llama70b_append_sampled_parity(dev):
             assert torch.equal(wl.v_cache[int(pt[b, pos // 16]), :, pos % 16],
                                wl.v_append[s, b])
     samples = [(0, 0), (5, 3), (7, 7)]
+    # every page the appends filled holds the record a fresh build of the
+    # final cache writes, byte for byte; on the sampled pairs that build
+    # matches the oracle's (the boundary build is checked the same way)
+    filled = [(b, p) for b in range(batch)
+              for p in range(lens0[b] // 16, lens1[b] // 16)]
+    fs = torch.tensor([b for b, _ in filled], dtype=torch.int32, device=dev)
+    fp = torch.tensor([p for _, p in filled], dtype=torch.int32, device=dev)
+    fresh = torch.zeros_like(store)
+    nfh = len(filled) * h_kv
+    unq = torch.zeros(nfh * B.UNQUANTISED_FLOATS, dtype=torch.float32,
+                      device=dev)
+    tau = torch.zeros(nfh, dtype=torch.float32, device=dev)
+    B.locks_build_summaries(wl.k_cache, wl.page_table, fs, fp, fresh, tau,
+                            unq, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for b, p in filled:
+        assert torch.equal(store[b, :, p], fresh[b, :, p]), (b, p)
+    unq = unq.view(len(filled), h_kv, -1).cpu().numpy()
+    tau = tau.view(len(filled), h_kv).cpu().numpy()
+    fsn = fs.cpu().numpy()
+    for b, h in samples:
+        rows = np.nonzero(fsn == b)[0]
+        phys = wl.page_table[b, fp[rows].long()].long()
+        check_build(fresh[b, h, fp[rows].long()].cpu().numpy(), unq[rows, h],
+                    tau[rows, h], wl.k_cache[phys, h].float().cpu().numpy(),
+                    f"append seq {b} head {h}")
+    check_full_size_build(B, wl, store, samples, dev, spec.name)
     q = wl.queries[steps - 1]
     qn = q.float().cpu().numpy()
-    got = store.cpu()
     orc = {}
     for b, h in samples:
         q8, rec, (mu, V, C) = oracle_pair(wl, lens1[b], b, h)
-        # pages filled by the appends: centroid bytes exact, reconstruction
-        # of the quantised summary as the small append test
-        for p in range(lens0[b] // 16, lens1[b] // 16):
-            gq = O.decode_records(got[b, h, p].numpy()[None])
-            oq = O.decode_records(rec[p][None])
-            assert (gq["mu8"] == oq["mu8"]).all()
-            assert (gq["smu"] == oq["smu"]).all()
-            _, Vg, Cg = O.dequantize(gq)
-            _, Vo, Co = O.dequantize(oq)
-            R, Ro = Cg @ np.swapaxes(Vg, -1, -2), Co @ np.swapaxes(Vo, -1, -2)
-            assert np.linalg.norm(R - Ro) <= 0.05 * np.linalg.norm(Ro), (b, h, p)
         store[b, h, :lens1[b] // 16] = torch.from_numpy(rec).to(dev)
         orc[(b, h)] = O.score_from_summaries(qn[b, h * G:(h + 1) * G], mu, V,
                                              C)

@@ -1,9 +1,11 @@
 """Parity at the 128K-context bench workload (batch 32, 32q/8kv, k=128), in
 the launch configuration bench.py times, on sampled outputs.
 
-For a few sampled (sequence, KV head) pairs the oracle builds the summary
-records itself; they replace the GPU-built records of those pairs in the
-full store, and the full-batch kernels then run.  Scores and selections of
+The full-batch GPU build is checked first: for sampled (sequence, KV head)
+pairs its records are compared with the oracle's build of the same keys
+(tests/build_parity.py).  Then the oracle's own records of those pairs
+replace the GPU-built ones in the full store, and the full-batch kernels
+run.  Scores and selections of
 the sampled pairs must match the oracle's exactly as on small cases; the
 attention outputs of the sampled pairs are checked with the oracle's
 selection fed to the full-batch decode.
@@ -12,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+from build_parity import check_full_size_build
 from oracle import locks_oracle as O
 from sparse_paged_kv_locks_gb300 import binding as B
 from sparse_paged_kv_locks_gb300 import workload as W
@@ -39,6 +42,9 @@ def test_full_size_sampled_parity():
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     samples = [(0, 0), (13, 5), (31, 7)]
+    stats = check_full_size_build(B, wl, store, samples, dev, "llama8b_128k")
+    for st in stats.values():
+        assert st["sub_ok"] > 0.8 and st["full"] > 0.5, st
     q = wl.queries[1]
     qn = q.float().cpu().numpy()
     orc = {}

@@ -3,13 +3,14 @@
 Tolerances of the LOCKS decode path against the float64 oracle:
   * quantised bytes: bit-exact where both sides quantise the same fp32
     values (the pack entry point, the centroid); after the eigensolver,
-    codes may differ by one step only where the oracle's value lies near a
-    rounding boundary, up to eigenvector sign
+    codes may differ by one step only inside the window that the measured
+    fp32 eigensolver error carries through the scale (tests/build_parity.py),
+    up to eigenvector sign
   * reconstructions C V^T (fp32, before quantisation): relative Frobenius
     error <= 1e-3, up to sign, on pages whose kept spectrum is separated
   * page scores from the same records: absolute error <= 1e-3
   * selections: identical except pages whose oracle log share-average lies
-    within the window of the k-th boundary
+    within 1e-3 of the k-th boundary's
   * attention: max |o - o_ref| <= 2e-2 * max |o_ref|; |lse - lse_ref| <= 1e-3
 Inputs flow only oracle -> GPU (records, indices), never the other way.
 """
@@ -19,6 +20,7 @@ import numpy as np
 import pytest
 import torch
 
+from build_parity import check_build
 from oracle import locks_oracle as O
 from sparse_paged_kv_locks_gb300 import binding as B
 from sparse_paged_kv_locks_gb300 import workload as W
@@ -167,79 +169,34 @@ def _degenerate_workload():
     return wl
 
 
-@pytest.mark.parametrize("which", ["tiny_4k", "degenerate"])
+def _ragged_decay_workload():
+    """Small pages with the ragged workload's spectra: per-page decay
+    rho ~ U(0.4, 0.8), so the kept spectrum reaches the noise floor and
+    near-degenerate tails occur."""
+    spec = W.custom_spec(batch=3, h_q=8, h_kv=2, ctx=16 * 300 + 5, k=8,
+                         steps=4, needles=1, seed=41, decay_range=(0.4, 0.8),
+                         ragged_min=16 * 120)
+    return W.generate(spec, "cpu")
+
+
+@pytest.mark.parametrize("which", ["tiny_4k", "degenerate", "ragged_decay"])
 def test_build_matches_oracle(which):
-    wl = W.generate(W.SPECS["tiny_4k"], "cpu") if which == "tiny_4k" \
-        else _degenerate_workload()
+    wl = {"tiny_4k": lambda: W.generate(W.SPECS["tiny_4k"], "cpu"),
+          "degenerate": _degenerate_workload,
+          "ragged_decay": _ragged_decay_workload}[which]()
     d = Dev(wl)
     kc, vc, pt, lens = host(wl)
-    batch, max_pages = pt.shape
     store, tau, unq, seq, pg = gpu_build(d, lens, want_unq=True)
     h_kv = kc.shape[1]
-    # oracle, same pages
-    keys = kc[pt[seq, pg]]                                  # [n][h_kv][16][128]
-    q8, s = O.build_page(keys)
-    orc = O.encode_records(q8)                               # [n][h_kv][832]
-    got = store.cpu().numpy()[seq, :, pg]                    # [n][h_kv][832]
-    gq = O.decode_records(got)
-    # centroid codes and scale: bit-exact (same fp32 rule on both sides)
-    assert (gq["mu8"] == q8["mu8"]).all()
-    assert (gq["smu"] == q8["smu"]).all()
-    # eigenvalues, basis, reconstructions
-    u = unq.view(len(seq), h_kv, -1).cpu().numpy().astype(np.float64)
-    lam_g = u[..., :16]
-    mu_g = u[..., 16:144]
-    V_g = u[..., 144:144 + 1024].reshape(len(seq), h_kv, 128, 8)
-    C_g = u[..., 1168:].reshape(len(seq), h_kv, 16, 8)
-    lam1 = s["lam"][..., :1]
-    assert np.abs(lam_g - s["lam"]).max() <= 1e-5 * max(1.0, lam1.max())
-    assert np.abs(mu_g - s["mu"]).max() < 1e-6
-    assert np.abs(tau.view(len(seq), h_kv).cpu().numpy() - s["tau"]).max() \
-        <= 1e-4 * max(1.0, lam1.max())
-    R_g = C_g @ np.swapaxes(V_g, -1, -2)
-    R_o = s["C"] @ np.swapaxes(s["V"], -1, -2)
-    gap = (s["lam"][..., 7] - s["lam"][..., 8]) / np.maximum(lam1[..., 0],
-                                                              1e-30)
-    nrm = np.linalg.norm(R_o, axis=(-2, -1))
-    err = np.linalg.norm(R_g - R_o, axis=(-2, -1)) / np.maximum(nrm, 1e-30)
-    zero = nrm < 1e-12
-    assert (np.linalg.norm(R_g, axis=(-2, -1))[zero] < 1e-6).all()
-    # the rank-8 subspace is determined to ~eps/gap: pages whose kept
-    # spectrum separates by >= 1e-3 lambda_1 meet 1e-3; closer gaps get the
-    # bound scaled by 1e-3/gap
-    ok = (gap > 1e-3) & ~zero
-    near = (gap > 1e-5) & (gap <= 1e-3) & ~zero
-    assert err[ok].max(initial=0) <= 1e-3, float(err[ok].max())
-    assert (err[near] <= 1e-3 * (1e-3 / gap[near])).all()
-    assert ok.mean() > 0.8 if which == "tiny_4k" else ok.sum() > 0
-    # kept basis columns orthonormal
-    keep = s["lam"][..., :8] > 1e-6 * lam1
-    VtV = np.swapaxes(V_g, -1, -2) @ V_g
-    for i, j in zip(*np.nonzero(keep.all(axis=-1))):
-        assert np.abs(VtV[i, j] - np.eye(8)).max() < 1e-4
-    # codes after sign alignment: off by at most one, only near a boundary
-    sgn = np.sign(np.einsum("nhdk,nhdk->nhk", V_g, s["V"]))
-    sgn[sgn == 0] = 1
-    lam = s["lam"]
-    above = np.concatenate([np.full(lam[..., :1].shape, np.inf),
-                            lam[..., :7]], -1)
-    rel_gap = np.minimum(above - lam[..., :8], lam[..., :8] - lam[..., 1:9])
-    rel_gap = rel_gap / np.maximum(lam1, 1e-30)
-    comp_ok = (rel_gap > 1e-3) & keep                       # [n][h][8]
-    V4g = gq["V4"].astype(np.int64) * sgn[..., None, :].astype(np.int64)
-    dv = np.abs(V4g - q8["V4"])
-    sv = q8["sV"].astype(np.float32)
-    xs = s["V"].astype(np.float32) / np.where(sv == 0, 1, sv)[..., None, :]
-    near = np.abs(np.abs(xs - np.floor(xs)) - 0.5) < 0.05
-    m = comp_ok[..., None, :] & np.ones_like(dv, bool)
-    assert dv[m].max(initial=0) <= 1
-    assert not ((dv > 0) & m & ~near).any()
-    assert (dv[m] > 0).mean() < 0.01
-    # coefficient codes on page-heads whose kept components all separate
-    full = comp_ok.all(axis=-1)
-    C8g = gq["C8"].astype(np.int64) * sgn[..., None, :].astype(np.int64)
-    dc = np.abs(C8g - q8["C8"])[full]
-    assert dc.max(initial=0) <= 1 and (dc > 0).mean() < 0.01
+    n = len(seq) * h_kv
+    keys = kc[pt[seq, pg]].reshape(n, 16, 128)
+    got = store.cpu().numpy()[seq, :, pg].reshape(n, 832)
+    stats = check_build(got, unq.view(n, -1).cpu().numpy(),
+                        tau.cpu().numpy(), keys, which)
+    if which != "degenerate":
+        assert stats["sub_ok"] > 0.8 and stats["full"] > 0.5, stats
+    else:
+        assert stats["sub_ok"] > 0
 
 
 def test_build_per_page_basis_scale():
@@ -649,43 +606,72 @@ def test_decode_many_short_units(G, mode):
 # ---------------------------------------------------------------------------
 # the whole step on the 4K-context workload, 8 decode steps
 # ---------------------------------------------------------------------------
-def test_end_to_end_tiny_workload():
-    spec = W.SPECS["tiny_4k"]
-    wl = W.generate(spec, "cpu")
+SEL_WIN = 1e-3
+
+
+@pytest.mark.parametrize("which", ["tiny_4k", "ragged_decay"])
+def test_end_to_end_workload(which):
+    """The whole product path (GPU build, then every decode step through the
+    decoder object: score, select, sparse attention) against the oracle's
+    own build, selection and attention on the same inputs.  Selections must
+    be identical except pages whose oracle log share-average lies within
+    1e-3 of the boundary candidate's; o and lse are compared for every
+    (step, query head): directly where the sets agree, and where they differ
+    within the window, by running the GPU decode on the oracle's selection."""
+    if which == "tiny_4k":
+        spec = W.SPECS["tiny_4k"]
+        wl = W.generate(spec, "cpu")
+    else:
+        wl = _ragged_decay_workload()
+        spec = wl.spec
     d = Dev(wl)
     kc, vc, pt, lens = host(wl)
     batch, max_pages = pt.shape
+    G = spec.group
     store, _, _, seq, pg = gpu_build(d, lens)
     ostore, _ = O.build_summaries(kc, pt, seq, pg, batch, max_pages)
     dec = B.LocksDecoder(d.k_cache, d.v_cache, d.page_table, store, spec.h_q,
                          spec.k)
-    n_same = 0
-    for step in range(spec.steps):
+    steps = min(spec.steps, 8)
+    n_diff = 0
+    for step in range(steps):
         o, lse = dec.step(d.queries[step], d.seq_lens)
         torch.cuda.synchronize()
         assert dec.status() == 0
         q = wl.queries[step].float().numpy()
         s_orc = O.score_store(q, ostore, lens)
-        s_gpu = s_hat_from_ws(dec.workspace, batch, spec.h_kv, spec.group,
-                              max_pages)
         idx_o = O.select_store(s_orc, lens, spec.k)
         ig = dec.idx.cpu().numpy()
-        o_ref, lse_ref = O.sparse_decode(q, kc, vc, pt, lens, idx_o)
         og, lg = o.float().cpu().numpy(), lse.cpu().numpy()
-        for h in range(spec.h_kv):
-            nf = lens[0] // 16
-            window = 2 * np.abs(s_gpu[0, h, :, :nf] - s_orc[0, h, :, :nf]).max() \
-                + 1e-3
-            ok, _ = selection_agrees(ig[0, h], idx_o[0, h], s_orc[0, h],
-                                     lens[0], spec.k, window)
-            assert ok
-            if set(ig[0, h]) == set(idx_o[0, h]):
-                n_same += 1
-                sl = slice(h * spec.group, (h + 1) * spec.group)
-                assert np.abs(og[0, sl] - o_ref[0, sl]).max() <= \
-                    O_TOL * np.abs(o_ref[0, sl]).max()
-                assert np.abs(lg[0, sl] - lse_ref[0, sl]).max() <= LSE_TOL
-    assert n_same >= spec.steps * spec.h_kv // 2
+        o_ref, lse_ref = O.sparse_decode(q, kc, vc, pt, lens, idx_o)
+        differs = np.zeros((batch, spec.h_kv), bool)
+        for b in range(batch):
+            for h in range(spec.h_kv):
+                ok, nd = selection_agrees(ig[b, h], idx_o[b, h], s_orc[b, h],
+                                          lens[b], spec.k, SEL_WIN)
+                assert ok, (step, b, h)
+                differs[b, h] = nd > 0
+        if differs.any():
+            n_diff += int(differs.sum())
+            o2 = torch.empty_like(o)
+            l2 = torch.empty_like(lse)
+            B.locks_sparse_decode(d.queries[step], d.k_cache, d.v_cache,
+                                  d.page_table, d.seq_lens, i32(idx_o),
+                                  spec.k, o2, l2, dec.workspace)
+            torch.cuda.synchronize()
+            assert dec.status() == 0
+            o2, l2 = o2.float().cpu().numpy(), l2.cpu().numpy()
+            for b, h in zip(*np.nonzero(differs)):
+                sl = slice(h * G, (h + 1) * G)
+                og[b, sl], lg[b, sl] = o2[b, sl], l2[b, sl]
+        for b in range(batch):
+            for h in range(spec.h_kv):
+                sl = slice(h * G, (h + 1) * G)
+                assert np.abs(og[b, sl] - o_ref[b, sl]).max() <= \
+                    O_TOL * np.abs(o_ref[b, sl]).max(), (step, b, h)
+                assert np.abs(lg[b, sl] - lse_ref[b, sl]).max() <= LSE_TOL
+    # the differing sets are rare: the boundary window is narrow
+    assert n_diff <= max(1, steps * batch * spec.h_kv // 10)
 
 
 @pytest.mark.parametrize("name", ["tiny_4k", "ragged"])
@@ -827,20 +813,29 @@ def test_append_builds_filled_pages():
             pos = lens0[b] + s
             kc[pt[b, pos // 16], :, pos % 16] = wl.k_append[s, b].float().numpy()
     assert np.array_equal(d.k_cache.float().cpu().numpy(), kc)
-    # every page full after the appends has the record Algorithm 1 gives
+    # every page the appends filled holds, byte for byte, the record a
+    # fresh build of the final cache writes, and that build (with its fp32
+    # values before quantisation) matches the oracle's build
     lens1 = [L + 20 for L in lens0]
     seq1, pg1 = full_pairs(lens1)
-    ostore, _ = O.build_summaries(kc, pt, seq1, pg1, batch, max_pages)
-    got = store.cpu().numpy()
-    for b, p in zip(seq1, pg1):
-        gq = O.decode_records(got[b, :, p])
-        oq = O.decode_records(ostore[b, :, p])
-        assert (gq["mu8"] == oq["mu8"]).all() and (gq["smu"] == oq["smu"]).all()
-        mu, V, C = O.dequantize(gq)
-        mo, Vo, Co = O.dequantize(oq)
-        R, Ro = C @ np.swapaxes(V, -1, -2), Co @ np.swapaxes(Vo, -1, -2)
-        rel = np.linalg.norm(R - Ro) / np.linalg.norm(Ro)
-        assert rel < 0.05, (b, p, rel)
+    filled = [(b, p) for b, p in zip(seq1, pg1) if p >= lens0[b] // 16]
+    assert len(filled) >= batch
+    fs = np.array([b for b, _ in filled], np.int32)
+    fp = np.array([p for _, p in filled], np.int32)
+    fresh = B.new_summary_store(batch, spec.h_kv, max_pages, DEV)
+    n = len(filled) * spec.h_kv
+    unq = torch.zeros(n * B.UNQUANTISED_FLOATS, dtype=torch.float32,
+                      device=DEV)
+    tau = torch.zeros(n, dtype=torch.float32, device=DEV)
+    B.locks_build_summaries(d.k_cache, d.page_table, i32(fs), i32(fp), fresh,
+                            tau, unq, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for b, p in filled:
+        assert torch.equal(store[b, :, p], fresh[b, :, p]), (b, p)
+    check_build(fresh.cpu().numpy()[fs, :, fp].reshape(n, 832),
+                unq.view(n, -1).cpu().numpy(), tau.cpu().numpy(),
+                kc[pt[fs, fp]].reshape(n, 16, 128), "append")
     # appended tokens are in the cache
     for s in (0, 7, 19):
         for b in range(batch):
