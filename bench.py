@@ -31,6 +31,15 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# The float64 oracle (CPU baseline and reference arm) runs its BLAS on every
+# core this process may use; set before numpy is first imported.
+try:
+    _CORES = len(os.sched_getaffinity(0))
+except AttributeError:
+    _CORES = os.cpu_count() or 1
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
 METRIC = ("decode tokens/s per layer (score+select+sparse attn) @128K; "
           "% HBM roofline")
 RECORD_PAYLOAD = 818          # algorithmic bytes of one page summary
@@ -169,26 +178,39 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def score_traffic(n_records, group):
-    """DRAM bytes per score launch from the committed ncu capture
-    (profiles/score_kernel_traffic.json), scaled by records; None when the
-    scoring kernel's source changed since the capture or when the workload's
-    GQA group size selects another form of the kernel than the captured
-    one."""
+def _sha256(path):
     import hashlib
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def step_traffic(units, group):
+    """DRAM bytes of one decode step from the committed small-case ncu
+    captures (profiles/step_traffic.json): for each kernel of the step,
+    dram__bytes_read.sum + dram__bytes_write.sum per unit of work (record,
+    score entry, selected page-head) times the units of this step.  Returns
+    (total, {kernel: bytes}) or (None, reason) when a kernel's source
+    changed since its capture or the group size selects another form of a
+    kernel than the captured one."""
     try:
-        with open(os.path.join(ROOT, "profiles",
-                               "score_kernel_traffic.json")) as f:
+        with open(os.path.join(ROOT, "profiles", "step_traffic.json")) as f:
             d = json.load(f)
-        src = os.path.join(ROOT, "sparse_paged_kv_locks_gb300", "csrc",
-                           "score.cu")
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
     except (OSError, ValueError):
-        return None
-    if d.get("score_cu_sha256") != digest or d.get("group_size") != group:
-        return None
-    return round(float(d["dram_bytes_per_record"]) * n_records)
+        return None, "no capture"
+    if d.get("group_size") != group:
+        return None, f"captured at group size {d.get('group_size')}"
+    out = {}
+    for name, k in d["kernels"].items():
+        src = os.path.join(ROOT, "sparse_paged_kv_locks_gb300", "csrc",
+                           k["source"])
+        try:
+            if _sha256(src) != k["source_sha256"]:
+                return None, f"{k['source']} changed since its capture"
+        except OSError:
+            return None, f"{k['source']} missing"
+        out[name] = round(float(k["dram_bytes_per_unit"]) *
+                          units[k["unit"]])
+    return sum(out.values()), out
 
 
 def build_issue(n_page_heads, build_ms, sm_mhz):
@@ -668,10 +690,30 @@ def rank_precision_ablation(B, wl, lens, k, h_q, peak_gbs, n_seqs=4,
 
 
 def host_cores():
+    return _CORES
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
     try:
-        return len(os.sched_getaffinity(0))
-    except AttributeError:
-        return os.cpu_count() or 1
+        out = subprocess.run(["lscpu"], capture_output=True, text=True,
+                             timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def blas_threads():
+    return int(os.environ.get("OPENBLAS_NUM_THREADS", _CORES))
 
 
 # ---------------------------------------------------------------------------
@@ -841,6 +883,11 @@ def run_locks(args):
     score_gbs = score_bytes / (score_ms / 1e3) / 1e9
     step_gbs = step_bytes / (total_ms / args.steps / 1e3) / 1e9
     decode_gbs = kv_bytes / (decode_ms / 1e3) / 1e9
+    traffic, per_kernel = step_traffic(
+        {"record": n_records,
+         "score_entry": batch * h_kv * G * max_pages,
+         "page_head": int((idx_h >= 0).sum())}, G)
+    step_ms = total_ms / args.steps
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -860,18 +907,30 @@ def run_locks(args):
                   f"{score_bytes / 1e9:.2f} GB of summaries and "
                   f"{kv_bytes / 1e6:.0f} MB of selected K/V",
             "parallelism": f"replicas x{world}"},
+        # the step's roofline as the method defines it: bytes of every
+        # summary, the selected pages' K/V, q and o over the step time
         "roofline": {
-            "bound": "hbm", "kernel": "score (summary stream)",
-            "achieved": round(score_gbs, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(score_gbs / peak, 4),
-            "traffic": score_traffic(n_records, spec.h_q // spec.h_kv),
-            "peak_source": peak_src,
-            "algorithmic_bytes": score_bytes},
-        "step_roofline": {
+            "bound": "hbm",
+            "kernel": "whole step (score + select + sparse decode + merge)",
             "achieved": round(step_gbs, 1), "peak": peak, "unit": "GB/s",
             "frac": round(step_gbs / peak, 4),
             "frac_of_8tbs": round(step_gbs / 8000.0, 4),
-            "algorithmic_bytes": step_bytes},
+            "traffic": traffic,
+            "traffic_per_kernel": per_kernel,
+            "traffic_source": "small-case ncu captures scaled per unit of "
+                              "work (profiles/step_traffic.json)",
+            "peak_source": peak_src,
+            "algorithmic_bytes": step_bytes,
+            "ms_per_step": round(step_ms, 4),
+            "dominant_kernel": {
+                "kernel": "score (summary stream)",
+                "achieved": round(score_gbs, 1),
+                "frac": round(score_gbs / peak, 4),
+                "algorithmic_bytes": score_bytes,
+                "traffic": (per_kernel or {}).get("score")
+                if traffic is not None else None,
+                "ms": round(score_ms, 4),
+                "share_of_step": round(score_ms / step_ms, 4)}},
         "kernels_ms": {"score": round(score_ms, 4),
                        "select": round(select_ms, 4),
                        "sparse_decode": round(decode_ms, 4),
@@ -979,12 +1038,14 @@ def run_locks(args):
                                          steps_cpu)
             line["cpu_baseline"] = {
                 "value": v_cpu, "unit": "tokens/s", "cores": host_cores(),
-                "kind": "oracle",
+                "kind": "oracle", "cpu_model": cpu_model(),
+                "blas_threads": blas_threads(),
                 "sample": f"sequence 0 of {batch} ({lens[b0]} tokens), all "
                           f"{h_kv} KV heads, {steps_cpu} decode steps (score "
                           "+ select + sparse attention) in "
                           f"{dt_cpu:.1f} s; oracle summaries built outside "
-                          "the timed region; numpy default threading"}
+                          "the timed region; extrapolated to the batch as "
+                          "tokens/s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -1048,6 +1109,8 @@ def run_reference(args):
                        "batch": spec.batch, "context": spec.ctx},
             "cpu_baseline": {"value": value, "unit": "tokens/s",
                              "cores": host_cores(), "kind": "oracle",
+                             "cpu_model": cpu_model(),
+                             "blas_threads": blas_threads(),
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s",
                     "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
