@@ -812,7 +812,6 @@ def run_locks(args):
     idx = torch.empty(batch, h_kv, k, dtype=torch.int32, device=dev)
     o = torch.empty(batch, spec.h_q, 128, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(batch, spec.h_q, dtype=torch.float32, device=dev)
-    norm = B.new_norm_partials(batch, spec.h_q, h_kv, dev)
     qs = wl.queries
     n_q = qs.shape[0]
 
@@ -822,12 +821,11 @@ def run_locks(args):
         q = qs[i % n_q]
         if evs:
             evs[0].record()
-        B.locks_score_pages_ex(q, store, wl.seq_lens, scores, norm,
-                               ws[:4].view(torch.int32))
+        B.locks_score_pages(q, store, wl.seq_lens, scores, ws[:4].view(
+            torch.int32))
         if evs:
             evs[1].record()
-        B.locks_select_pages_ex(scores, norm, wl.seq_lens, spec.h_q, k, idx,
-                                ws)
+        B.locks_select_pages(scores, wl.seq_lens, spec.h_q, k, idx, ws)
         if evs:
             evs[2].record()
         B.locks_sparse_decode(q, wl.k_cache, wl.v_cache, wl.page_table,

@@ -254,31 +254,6 @@ locks_status_t locks_score_pages(const void *q, const void *summaries,
                                  int h_kv, int max_pages, float *scores_out,
                                  int32_t *status, locks_stream_t stream);
 
-/* Bytes of the normaliser partials buffer that locks_score_pages_ex writes
- * and locks_select_pages_ex reads for these sizes (about
- * 8 * G * (batch * h_kv + 8192) bytes). */
-locks_status_t locks_norm_partials_size(int batch, int h_q, int h_kv,
-                                        size_t *bytes);
-
-/* locks_score_pages that also hands the selection the denominators of the
- * mass fractions (LOCKS reading notes §4.2 Eq.(5): for each (b, h, g), the
- * sum over every full page of exp(s_hat[g][j])), as partial sums of the
- * pages each scoring warp scored: locks_select_pages_ex then merges a few
- * partials instead of reading every score a second time.
- * locks_score_select = locks_score_pages_ex + locks_select_pages_ex.
- *   norm_out    nullable; 16-byte aligned device buffer of norm_bytes >=
- *               locks_norm_partials_size bytes (LOCKS_ERR_WORKSPACE when
- *               smaller), overwritten by every call; its contents are
- *               valid for these scores only, until the next call that
- *               writes it
- * Other arguments as locks_score_pages. */
-locks_status_t locks_score_pages_ex(const void *q, const void *summaries,
-                                    const int32_t *seq_lens, int batch,
-                                    int h_q, int h_kv, int max_pages,
-                                    float *scores_out, void *norm_out,
-                                    size_t norm_bytes, int32_t *status,
-                                    locks_stream_t stream);
-
 /* Exact page scores (LOCKS reading notes §4.2 Eq.(4), the quantity the
  * summaries estimate; ranking by it is the exact-mass selector of §6
  * Fig. 1(b) and Fig. 2, which reads every key): for every full page j of
@@ -339,18 +314,6 @@ locks_status_t locks_select_pages(const float *scores, const int32_t *seq_lens,
                                   int k, int32_t *idx_out, void *workspace,
                                   size_t workspace_bytes,
                                   locks_stream_t stream);
-
-/* locks_select_pages with the normaliser partials that
- * locks_score_pages_ex wrote for the same scores, seq_lens, batch and
- * heads (norm, 16-byte aligned; NULL = locks_select_pages).  The selection
- * is the one locks_select_pages makes, up to fp32 rounding of the
- * normalisers; a partial that is not finite falls back to the scores. */
-locks_status_t locks_select_pages_ex(const float *scores, const void *norm,
-                                     const int32_t *seq_lens, int batch,
-                                     int h_q, int h_kv, int max_pages, int k,
-                                     int32_t *idx_out, void *workspace,
-                                     size_t workspace_bytes,
-                                     locks_stream_t stream);
 
 /* locks_select_pages with the candidates ranked by another GQA merge rule
  * (LOCKS_MERGE_*; LOCKS_MERGE_SHARE_AVERAGE is locks_select_pages itself).

@@ -61,11 +61,6 @@ _SIGS = {
     "locks_score_select": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ,
                                 _P]),
     "locks_score_pages": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
-    "locks_norm_partials_size": (_I, [_I, _I, _I, ctypes.POINTER(_SZ)]),
-    "locks_score_pages_ex": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ,
-                                  _P, _P]),
-    "locks_select_pages_ex": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P,
-                                   _SZ, _P]),
     "locks_select_pages": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ,
                                 _P]),
     "locks_select_pages_merge": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
@@ -267,45 +262,6 @@ def locks_score_pages(q, summaries, seq_lens, scores_out, status=None,
         max_pages, _ptr(scores_out), _ptr(status), _stream(stream)))
 
 
-def locks_norm_partials_size(batch, h_q, h_kv) -> int:
-    out = _SZ(0)
-    _check("locks_norm_partials_size",
-           lib().locks_norm_partials_size(batch, h_q, h_kv,
-                                          ctypes.byref(out)))
-    return int(out.value)
-
-
-def new_norm_partials(batch, h_q, h_kv, device="cuda"):
-    """Buffer for the normaliser partials (uint8, 16-byte aligned)."""
-    return torch.zeros(locks_norm_partials_size(batch, h_q, h_kv),
-                       dtype=torch.uint8, device=device)
-
-
-def locks_score_pages_ex(q, summaries, seq_lens, scores_out, norm_out=None,
-                         status=None, stream=None):
-    """locks_score_pages that also writes the selection's normaliser
-    partials into norm_out (see new_norm_partials)."""
-    _req(q, "q", torch.bfloat16, 3)
-    _req(summaries, "summaries", torch.uint8, 4)
-    _req(seq_lens, "seq_lens", torch.int32, 1)
-    _req(scores_out, "scores_out", torch.float32, 4)
-    batch, h_q, d = q.shape
-    _, h_kv, max_pages, rb = summaries.shape
-    if d != HEAD_DIM or rb != RECORD_BYTES or summaries.shape[0] != batch:
-        raise ValueError("q [batch][h_q][128], summaries [batch][h_kv][P][832]")
-    if tuple(scores_out.shape) != (batch, h_kv, h_q // h_kv, max_pages):
-        raise ValueError("scores_out must be [batch][h_kv][G][max_pages]")
-    if norm_out is not None:
-        _req(norm_out, "norm_out", torch.uint8, 1)
-    if status is not None:
-        _req(status, "status", torch.int32)
-    _check("locks_score_pages_ex", lib().locks_score_pages_ex(
-        _ptr(q), _ptr(summaries), _ptr(seq_lens), batch, h_q, h_kv,
-        max_pages, _ptr(scores_out), _ptr(norm_out),
-        0 if norm_out is None else norm_out.numel(), _ptr(status),
-        _stream(stream)))
-
-
 def locks_exact_page_scores(q, k_cache, page_table, seq_lens, scores_out,
                             status=None, stream=None):
     """Exact page LSE of every full page (the exact-mass selector's scores),
@@ -385,26 +341,6 @@ def locks_select_pages(scores, seq_lens, h_q, k, idx_out, workspace,
     _check("locks_select_pages", lib().locks_select_pages(
         _ptr(scores), _ptr(seq_lens), batch, h_q, h_kv, max_pages, k,
         _ptr(idx_out), _ptr(workspace), workspace.numel(), _stream(stream)))
-
-
-def locks_select_pages_ex(scores, norm, seq_lens, h_q, k, idx_out, workspace,
-                          stream=None):
-    """locks_select_pages with the partials locks_score_pages_ex wrote."""
-    _req(scores, "scores", torch.float32, 4)
-    _req(seq_lens, "seq_lens", torch.int32, 1)
-    _req(idx_out, "idx_out", torch.int32, 3)
-    _req(workspace, "workspace", torch.uint8, 1)
-    if norm is not None:
-        _req(norm, "norm", torch.uint8, 1)
-    batch, h_kv, G, max_pages = scores.shape
-    if G * h_kv != h_q:
-        raise ValueError("scores must be [batch][h_kv][h_q/h_kv][max_pages]")
-    if tuple(idx_out.shape) != (batch, h_kv, k) or seq_lens.numel() != batch:
-        raise ValueError("idx_out must be [batch][h_kv][k]")
-    _check("locks_select_pages_ex", lib().locks_select_pages_ex(
-        _ptr(scores), _ptr(norm), _ptr(seq_lens), batch, h_q, h_kv,
-        max_pages, k, _ptr(idx_out), _ptr(workspace), workspace.numel(),
-        _stream(stream)))
 
 
 MERGE_SHARE_AVERAGE, MERGE_GROUP_MAX, MERGE_GROUP_MASS = 0, 1, 2

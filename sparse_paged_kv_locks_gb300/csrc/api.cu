@@ -17,19 +17,12 @@ static locks_status_t fail_cuda(cudaError_t e) {
 
 static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// bytes of the scoring region: s_hat [batch][h_kv][G][max_pages] float,
-// selection keys [batch][h_kv][max_pages] u32, and the normaliser partials
-// the scoring kernel passes to the selection kernel
-static size_t scores_bytes(int batch, int h_q, int h_kv, int max_pages) {
-  return round_up((size_t)batch * h_kv * (h_q / h_kv) * max_pages * 4, 256);
-}
-static size_t keys_bytes(int batch, int h_kv, int max_pages) {
-  return round_up((size_t)batch * h_kv * max_pages * 4, 256);
-}
+// bytes of the scoring region: s_hat [batch][h_kv][G][max_pages] float and
+// selection keys [batch][h_kv][max_pages] u32
 static size_t score_region(int batch, int h_q, int h_kv, int max_pages) {
-  return scores_bytes(batch, h_q, h_kv, max_pages) +
-         keys_bytes(batch, h_kv, max_pages) +
-         round_up(norm_bytes((long long)batch * h_kv, h_q / h_kv), 256);
+  const size_t G = (size_t)(h_q / h_kv);
+  return round_up((size_t)batch * h_kv * G * max_pages * 4, 256) +
+         round_up((size_t)batch * h_kv * max_pages * 4, 256);
 }
 
 // Decode partials: one slot per (unit, warp) piece, slot index unit + warp,
@@ -94,14 +87,12 @@ locks_status_t locks::score_select(const void *q, const void *summaries,
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   int32_t *status = reinterpret_cast<int32_t *>(ws);
   float *s_hat = reinterpret_cast<float *>(ws + kWsHeader);
-  const size_t sb = scores_bytes(batch, h_q, h_kv, max_pages);
-  uint32_t *keys = reinterpret_cast<uint32_t *>(ws + kWsHeader + sb);
-  uint8_t *norm = ws + kWsHeader + sb + keys_bytes(batch, h_kv, max_pages);
+  uint32_t *keys = reinterpret_cast<uint32_t *>(
+      ws + kWsHeader + round_up((size_t)batch * h_kv * G * max_pages * 4, 256));
   cudaError_t e = launch_score(q, summaries, seq_lens, batch, h_kv, G,
-                               max_pages, s_hat, norm, status, stream,
-                               after_query);
+                               max_pages, s_hat, status, stream, after_query);
   if (e != cudaSuccess) return fail_cuda(e);
-  e = launch_select(s_hat, norm, seq_lens, batch, h_kv, G, max_pages, k,
+  e = launch_select(s_hat, seq_lens, batch, h_kv, G, max_pages, k,
                     LOCKS_MERGE_SHARE_AVERAGE, idx_out, keys, status, stream);
   return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
 }
@@ -303,44 +294,8 @@ locks_status_t locks_score_pages(const void *q, const void *summaries,
     return LOCKS_ERR_INVALID_ARG;
   if (batch > score_max_batch()) return LOCKS_ERR_UNSUPPORTED;
   cudaError_t e = launch_score(q, summaries, seq_lens, batch, h_kv,
-                               h_q / h_kv, max_pages, scores_out, nullptr,
-                               status, (cudaStream_t)stream);
-  return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
-}
-
-locks_status_t locks_norm_partials_size(int batch, int h_q, int h_kv,
-                                        size_t *bytes) {
-  if (!bytes || batch < 0 || !heads_ok(h_q, h_kv))
-    return LOCKS_ERR_INVALID_ARG;
-  if (h_q / h_kv > kMaxGroup) return LOCKS_ERR_UNSUPPORTED;
-  *bytes = norm_bytes((long long)batch * h_kv, h_q / h_kv);
-  return LOCKS_OK;
-}
-
-locks_status_t locks_score_pages_ex(const void *q, const void *summaries,
-                                    const int32_t *seq_lens, int batch,
-                                    int h_q, int h_kv, int max_pages,
-                                    float *scores_out, void *norm_out,
-                                    size_t norm_bytes_avail, int32_t *status,
-                                    locks_stream_t stream) {
-  if (norm_out) {
-    if (reinterpret_cast<uintptr_t>(norm_out) & 15u)
-      return LOCKS_ERR_INVALID_ARG;
-    if (batch >= 0 && heads_ok(h_q, h_kv) && h_q / h_kv <= kMaxGroup &&
-        norm_bytes_avail < norm_bytes((long long)batch * h_kv, h_q / h_kv))
-      return LOCKS_ERR_WORKSPACE;
-  }
-  if (batch < 0 || max_pages < 1 || !heads_ok(h_q, h_kv))
-    return LOCKS_ERR_INVALID_ARG;
-  if (h_q / h_kv > kMaxGroup) return LOCKS_ERR_UNSUPPORTED;
-  if ((long long)max_pages * kPage > 0x7fffffffLL) return LOCKS_ERR_UNSUPPORTED;
-  if (batch == 0) return LOCKS_OK;
-  if (!q || !summaries || !seq_lens || !scores_out)
-    return LOCKS_ERR_INVALID_ARG;
-  if (batch > score_max_batch()) return LOCKS_ERR_UNSUPPORTED;
-  cudaError_t e = launch_score(q, summaries, seq_lens, batch, h_kv,
-                               h_q / h_kv, max_pages, scores_out, norm_out,
-                               status, (cudaStream_t)stream);
+                               h_q / h_kv, max_pages, scores_out, status,
+                               (cudaStream_t)stream);
   return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
 }
 
@@ -365,14 +320,13 @@ locks_status_t locks_exact_page_scores(
   return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
 }
 
-static locks_status_t select_pages(const float *scores, const void *norm,
-                                   const int32_t *seq_lens, int batch, int h_q,
-                                   int h_kv, int max_pages, int k, int rule,
-                                   int32_t *idx_out, void *workspace,
-                                   size_t workspace_bytes,
-                                   locks_stream_t stream) {
-  if (norm && (reinterpret_cast<uintptr_t>(norm) & 15u))
-    return LOCKS_ERR_INVALID_ARG;
+locks_status_t locks_select_pages_merge(const float *scores,
+                                        const int32_t *seq_lens, int batch,
+                                        int h_q, int h_kv, int max_pages,
+                                        int k, int rule, int32_t *idx_out,
+                                        void *workspace,
+                                        size_t workspace_bytes,
+                                        locks_stream_t stream) {
   if (rule != LOCKS_MERGE_SHARE_AVERAGE && rule != LOCKS_MERGE_GROUP_MAX &&
       rule != LOCKS_MERGE_GROUP_MASS)
     return LOCKS_ERR_INVALID_ARG;
@@ -387,33 +341,11 @@ static locks_status_t select_pages(const float *scores, const void *norm,
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   int32_t *status = reinterpret_cast<int32_t *>(ws);
   uint32_t *keys = reinterpret_cast<uint32_t *>(
-      ws + kWsHeader + scores_bytes(batch, h_q, h_kv, max_pages));
+      ws + kWsHeader + round_up((size_t)batch * h_kv * G * max_pages * 4, 256));
   cudaError_t e =
-      launch_select(scores, norm, seq_lens, batch, h_kv, G, max_pages, k,
-                    rule, idx_out, keys, status, (cudaStream_t)stream);
+      launch_select(scores, seq_lens, batch, h_kv, G, max_pages, k, rule,
+                    idx_out, keys, status, (cudaStream_t)stream);
   return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
-}
-
-locks_status_t locks_select_pages_ex(const float *scores, const void *norm,
-                                     const int32_t *seq_lens, int batch,
-                                     int h_q, int h_kv, int max_pages, int k,
-                                     int32_t *idx_out, void *workspace,
-                                     size_t workspace_bytes,
-                                     locks_stream_t stream) {
-  return select_pages(scores, norm, seq_lens, batch, h_q, h_kv, max_pages, k,
-                      LOCKS_MERGE_SHARE_AVERAGE, idx_out, workspace,
-                      workspace_bytes, stream);
-}
-
-locks_status_t locks_select_pages_merge(const float *scores,
-                                        const int32_t *seq_lens, int batch,
-                                        int h_q, int h_kv, int max_pages,
-                                        int k, int rule, int32_t *idx_out,
-                                        void *workspace,
-                                        size_t workspace_bytes,
-                                        locks_stream_t stream) {
-  return select_pages(scores, nullptr, seq_lens, batch, h_q, h_kv, max_pages,
-                      k, rule, idx_out, workspace, workspace_bytes, stream);
 }
 
 locks_status_t locks_select_pages(const float *scores, const int32_t *seq_lens,
@@ -421,9 +353,9 @@ locks_status_t locks_select_pages(const float *scores, const int32_t *seq_lens,
                                   int k, int32_t *idx_out, void *workspace,
                                   size_t workspace_bytes,
                                   locks_stream_t stream) {
-  return select_pages(scores, nullptr, seq_lens, batch, h_q, h_kv, max_pages,
-                      k, LOCKS_MERGE_SHARE_AVERAGE, idx_out, workspace,
-                      workspace_bytes, stream);
+  return locks_select_pages_merge(scores, seq_lens, batch, h_q, h_kv,
+                                  max_pages, k, LOCKS_MERGE_SHARE_AVERAGE,
+                                  idx_out, workspace, workspace_bytes, stream);
 }
 
 locks_status_t locks_sparse_decode(

@@ -305,71 +305,4 @@ __device__ __forceinline__ float lg2_fast(float x) {
   return y;
 }
 
-// ---------------------------------------------------------------------------
-// Normaliser partials (the denominators of the mass fractions of §4.2
-// Eq.(5)): the scoring kernel hands the selection kernel, per (sequence,
-// KV head) unit and per scoring warp that scored some of the unit's pages,
-// one (reference r, sum s) pair per query head with
-//   sum over those pages of 2^(s_hat_j * log2(e) - r),
-// so the selection merges a few pairs instead of re-reading every score.
-// Layout of the buffer (16-byte aligned):
-//   int hdr[4]          total 8-page tiles of the launch (-1: no partials),
-//                       warps of the scoring grid, 0, 0
-//   int tile0[units]    first tile of each unit in the scoring order
-//   float2 part[units + kNormMaxWarps][G]   at the next 16-byte boundary;
-//                       unit u's pair from warp w sits in slot u + w (a
-//                       warp's tiles are contiguous, so u + w is unique)
-// ---------------------------------------------------------------------------
-constexpr int kScoreTilePages = 8;
-constexpr int kScoreWarpsPerCta = 16;
-constexpr int kScoreMaxGrid = 512;
-constexpr int kNormMaxWarps = kScoreWarpsPerCta * kScoreMaxGrid;
-
-__host__ __device__ inline size_t norm_parts_offset(long long units) {
-  return ((size_t)(4 + units) * 4 + 15) / 16 * 16;
-}
-__host__ __device__ inline size_t norm_bytes(long long units, int G) {
-  return norm_parts_offset(units) +
-         (size_t)(units + kNormMaxWarps) * (size_t)G * sizeof(float2);
-}
-
-// The scoring warp that holds tile t when `warps` warps split `total` tiles
-// into contiguous ranges [w * total / warps, (w + 1) * total / warps).
-__host__ __device__ inline long long norm_warp_of_tile(long long t,
-                                                       long long total,
-                                                       long long warps) {
-  return ((t + 1) * warps + total - 1) / total - 1;
-}
-
-// Adds 2^v to (r, s); r is raised (and s rescaled) only when v passes it by
-// more than 2^6, so terms stay below 2^64.  A NaN makes r = +inf, which the
-// reader treats as "no usable partial".
-__device__ __forceinline__ void norm_add(float &r, float &s, float v) {
-  if (!(v > -INFINITY)) {  // -inf adds nothing
-    if (v != v) r = INFINITY;
-    return;
-  }
-  if (v > r + 64.f) {  // also the first value (r = -inf)
-    s = r == -INFINITY ? 0.f : s * ex2_fast(r - v);
-    r = v;
-  }
-  s += ex2_fast(v - r);
-}
-
-// (r, s) <- (r, s) + (r2, s2) in the same sense
-__device__ __forceinline__ void norm_merge(float &r, float &s, float r2,
-                                           float s2) {
-  const float m = fmaxf(r, r2);
-  if (m == -INFINITY) return;
-  s = (r == -INFINITY ? 0.f : s * ex2_fast(r - m)) +
-      (r2 == -INFINITY ? 0.f : s2 * ex2_fast(r2 - m));
-  r = m;
-}
-
-__device__ __forceinline__ void norm_merge_xor(float &r, float &s, int o) {
-  const float r2 = __shfl_xor_sync(0xffffffffu, r, o);
-  const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-  norm_merge(r, s, r2, s2);
-}
-
 }  // namespace locks

@@ -91,21 +91,15 @@ cudaError_t launch_append(const void *k_new, const void *v_new, void *k_cache,
 // after_query: launch as a programmatic dependent of the preceding kernel,
 // which may write only the query (the kernel reads seq_lens and the
 // summaries and starts its first copies before waiting on it).
-// norm (nullable): where the scoring kernel writes the normaliser partials
-// for the selection kernel (layout and size: common.cuh, norm_bytes).
 cudaError_t launch_score(const void *q, const void *summaries,
                          const int32_t *seq_lens, int batch, int h_kv, int G,
-                         int max_pages, float *s_hat, void *norm,
-                         int32_t *status, cudaStream_t stream,
-                         bool after_query = false);
+                         int max_pages, float *s_hat, int32_t *status,
+                         cudaStream_t stream, bool after_query = false);
 
-// norm (nullable): the partials the scoring kernel wrote for these scores;
-// without them the selection computes the normaliser from the scores.
-cudaError_t launch_select(const float *scores, const void *norm,
-                          const int32_t *seq_lens, int batch, int h_kv, int G,
-                          int max_pages, int k, int rule, int32_t *idx,
-                          uint32_t *keybuf, int32_t *status,
-                          cudaStream_t stream);
+cudaError_t launch_select(const float *scores, const int32_t *seq_lens,
+                          int batch, int h_kv, int G, int max_pages, int k,
+                          int rule, int32_t *idx, uint32_t *keybuf,
+                          int32_t *status, cudaStream_t stream);
 
 cudaError_t launch_decode(const void *q, const void *k_cache,
                           const void *v_cache, int64_t num_phys,

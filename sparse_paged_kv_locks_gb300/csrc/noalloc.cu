@@ -77,11 +77,10 @@ extern "C" locks_status_t locks_score_select_static(
   float *s_hat = static_cast<float *>(base);
   uint32_t *keys = reinterpret_cast<uint32_t *>(
       static_cast<unsigned char *>(base) + score_bytes);
-  cudaError_t e =
-      launch_score(q, summaries, seq_lens, batch, h_kv, G, max_pages, s_hat,
-                   nullptr, status, (cudaStream_t)stream);
+  cudaError_t e = launch_score(q, summaries, seq_lens, batch, h_kv, G,
+                               max_pages, s_hat, status, (cudaStream_t)stream);
   if (e != cudaSuccess) return LOCKS_ERR_CUDA;
-  e = launch_select(s_hat, nullptr, seq_lens, batch, h_kv, G, max_pages, k,
+  e = launch_select(s_hat, seq_lens, batch, h_kv, G, max_pages, k,
                     LOCKS_MERGE_SHARE_AVERAGE, idx_out, keys, status,
                     (cudaStream_t)stream);
   return e == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;

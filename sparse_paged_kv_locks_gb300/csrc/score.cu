@@ -17,9 +17,9 @@
 
 namespace locks {
 
-constexpr int kScoreWarps = kScoreWarpsPerCta;
+constexpr int kScoreWarps = 16;
 constexpr int kScoreThreads = 32 * kScoreWarps;
-constexpr int kTilePages = kScoreTilePages;
+constexpr int kTilePages = 8;
 constexpr int kTileBytes = kTilePages * kRec;  // 6656
 constexpr int kStages = 2;
 constexpr int kRingBytes = kScoreWarps * kStages * kTileBytes;
@@ -321,8 +321,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                  const uint8_t *__restrict__ summaries,
                  const int32_t *__restrict__ seq_lens, int batch, int h_kv,
                  int G, int max_pages, float *__restrict__ s_hat,
-                 uint8_t *__restrict__ norm, int32_t *status,
-                 int wait_query) {
+                 int32_t *status, int wait_query) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *ring = smem;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes);
@@ -375,22 +374,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const long long total = prefix[batch];
   const long long W = (long long)gridDim.x * kScoreWarps;
   const long long gw = (long long)blockIdx.x * kScoreWarps + wid;
-  const long long units = (long long)batch * h_kv;
-  float2 *norm_part = nullptr;
-  if (norm) {  // the tile order of this launch, for the selection kernel
-    int *hdr = reinterpret_cast<int *>(norm);
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-      hdr[0] = (int)total;
-      hdr[1] = (int)W;
-      hdr[2] = hdr[3] = 0;
-    }
-    for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-         u < units; u += (long long)gridDim.x * blockDim.x) {
-      const int ub = (int)(u / h_kv), uh = (int)(u % h_kv);
-      hdr[4 + u] = prefix[ub] + uh * tph[ub];
-    }
-    norm_part = reinterpret_cast<float2 *>(norm + norm_parts_offset(units));
-  }
   const long long t_begin = gw * total / W, t_end = (gw + 1) * total / W;
   // wait_query: the query comes from the preceding kernel (this one is its
   // programmatic dependent), so every thread waits for it before reading q
@@ -443,32 +426,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   // MODE 1: head gq & 3; MODE 2: head gq)
   float *lane_row = nullptr, *lane_row8 = nullptr;
   const int n_tiles = (int)(t_end - t_begin);
-  // normaliser partials of the current unit: (reference, sum of 2^(v - r))
-  // over this lane's scores of head (MODE 1: gq & 3, else gq) and, MODE 3,
-  // of head gq + 8
-  float nr0 = -INFINITY, ns0 = 0.f, nr1 = -INFINITY, ns1 = 0.f;
-  auto flush_norm = [&](int fb, int fh) {
-    norm_merge_xor(nr0, ns0, 1);
-    norm_merge_xor(nr0, ns0, 2);
-    if (MODE == 1) norm_merge_xor(nr0, ns0, 16);
-    if (MODE == 3) {
-      norm_merge_xor(nr1, ns1, 1);
-      norm_merge_xor(nr1, ns1, 2);
-    }
-    float2 *slot = norm_part + ((size_t)fb * h_kv + fh + gw) * G;
-    if (t4 == 0 && (MODE != 1 || gq < 4)) {
-      if (gq < G) slot[gq] = make_float2(nr0, ns0);
-      if (MODE == 3 && gq + 8 < G) slot[gq + 8] = make_float2(nr1, ns1);
-    }
-    nr0 = nr1 = -INFINITY;
-    ns0 = ns1 = 0.f;
-  };
 
   for (int it = 0; it < n_tiles; ++it) {
     const int stage = it & 1;
     const uint32_t phase = (uint32_t)((it >> 1) & 1);
     if (cur.b != cur_b || cur.h != cur_h) {
-      if (norm_part && cur_b >= 0) flush_norm(cur_b, cur_h);
       cur_b = cur.b;
       cur_h = cur.h;
       float *unit_rows =
@@ -616,11 +578,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const float smu = __half2float(__ushort_as_half(
             (unsigned short)lds16(base_s + pg * kRec + kOffSMu)));
         const float qmu = up ? qm_from_low : qm_lo;
-        if (head < G && pg < npg) {
-          const float v = keepA + qmu * smu * mscale;  // log2 units
-          st_keep(lane_row + page0 + pg, v * kLn2, keep);
-          if (norm_part) norm_add(nr0, ns0, v);
-        }
+        if (head < G && pg < npg)
+          st_keep(lane_row + page0 + pg, (keepA + qmu * smu * mscale) * kLn2,
+                  keep);
       } else {
         const int pg0 = 2 * t4, pg1 = pg0 + 1;
         const float sm0 = __half2float(__ushort_as_half(
@@ -628,16 +588,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const float sm1 = __half2float(__ushort_as_half(
             (unsigned short)lds16(base_s + pg1 * kRec + kOffSMu)));
         if (gq < G) {
-          if (pg0 < npg) {
-            const float v = keepA + qm_lo * sm0 * mscale;
-            st_keep(lane_row + page0 + pg0, v * kLn2, keep);
-            if (norm_part) norm_add(nr0, ns0, v);
-          }
-          if (pg1 < npg) {
-            const float v = keepB + qm_hi * sm1 * mscale;
-            st_keep(lane_row + page0 + pg1, v * kLn2, keep);
-            if (norm_part) norm_add(nr0, ns0, v);
-          }
+          if (pg0 < npg)
+            st_keep(lane_row + page0 + pg0,
+                    (keepA + qm_lo * sm0 * mscale) * kLn2, keep);
+          if (pg1 < npg)
+            st_keep(lane_row + page0 + pg1,
+                    (keepB + qm_hi * sm1 * mscale) * kLn2, keep);
         }
       }
     } else {
@@ -719,29 +675,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           (unsigned short)lds16(base_s + pg1 * kRec + kOffSMu)));
       if (gq < G) {
         float *dst = lane_row + page0;
-        if (pg0 < npg) {
-          const float v = o0 + (qm[0] + qm2[0]) * sm0 * mscale;
-          dst[pg0] = v * kLn2;
-          if (norm_part) norm_add(nr0, ns0, v);
-        }
-        if (pg1 < npg) {
-          const float v = o1 + (qm[1] + qm2[1]) * sm1 * mscale;
-          dst[pg1] = v * kLn2;
-          if (norm_part) norm_add(nr0, ns0, v);
-        }
+        if (pg0 < npg)
+          dst[pg0] = (o0 + (qm[0] + qm2[0]) * sm0 * mscale) * kLn2;
+        if (pg1 < npg)
+          dst[pg1] = (o1 + (qm[1] + qm2[1]) * sm1 * mscale) * kLn2;
       }
       if (gq + 8 < G) {
         float *dst = lane_row8 + page0;
-        if (pg0 < npg) {
-          const float v = o80 + (qm[2] + qm2[2]) * sm0 * mscale;
-          dst[pg0] = v * kLn2;
-          if (norm_part) norm_add(nr1, ns1, v);
-        }
-        if (pg1 < npg) {
-          const float v = o81 + (qm[3] + qm2[3]) * sm1 * mscale;
-          dst[pg1] = v * kLn2;
-          if (norm_part) norm_add(nr1, ns1, v);
-        }
+        if (pg0 < npg)
+          dst[pg0] = (o80 + (qm[2] + qm2[2]) * sm0 * mscale) * kLn2;
+        if (pg1 < npg)
+          dst[pg1] = (o81 + (qm[3] + qm2[3]) * sm1 * mscale) * kLn2;
       }
     }
     __syncwarp();
@@ -752,7 +696,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
     advance_cursor(cur, tph, batch, h_kv);
   }
-  if (norm_part && !failed && cur_b >= 0) flush_norm(cur_b, cur_h);
   if (failed) {
     if (lane == 0) set_status(status, LOCKS_DEV_TIMEOUT);
     // let copies still in flight land before the CTA's memory goes away
@@ -780,9 +723,8 @@ int score_max_batch() {
 
 cudaError_t launch_score(const void *q, const void *summaries,
                          const int32_t *seq_lens, int batch, int h_kv, int G,
-                         int max_pages, float *s_hat, void *norm,
-                         int32_t *status, cudaStream_t stream,
-                         bool after_query) {
+                         int max_pages, float *s_hat, int32_t *status,
+                         cudaStream_t stream, bool after_query) {
   const size_t smem = score_smem_bytes(batch);
   static DeviceFlags attr_set;
   cudaError_t ea = once_per_device(attr_set, [] {
@@ -800,19 +742,17 @@ cudaError_t launch_score(const void *q, const void *summaries,
     return e;
   });
   if (ea != cudaSuccess) return ea;
-  const int grid = device_sm_count() < kScoreMaxGrid ? device_sm_count()
-                                                    : kScoreMaxGrid;
+  const int grid = device_sm_count();
   auto *qq = static_cast<const __nv_bfloat16 *>(q);
-  auto *nb = static_cast<uint8_t *>(norm);
   auto *ss = static_cast<const uint8_t *>(summaries);
   auto *kern = G > 8 ? score_kernel<3> : G > 4 ? score_kernel<2>
                                                : score_kernel<1>;
   if (after_query)
     return launch_pdl(kern, dim3(grid), dim3(kScoreThreads), smem, stream, qq,
-                      ss, seq_lens, batch, h_kv, G, max_pages, s_hat, nb,
-                      status, 1);
+                      ss, seq_lens, batch, h_kv, G, max_pages, s_hat, status,
+                      1);
   kern<<<grid, kScoreThreads, smem, stream>>>(qq, ss, seq_lens, batch, h_kv, G,
-                                              max_pages, s_hat, nb, status, 0);
+                                              max_pages, s_hat, status, 0);
   return cudaGetLastError();
 }
 

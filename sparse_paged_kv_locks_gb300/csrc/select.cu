@@ -123,7 +123,6 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
     select_kernel(const float *__restrict__ scores,
                   const int32_t *__restrict__ seq_lens, int h_kv, int G,
                   int max_pages, int k, int rule,
-                  const uint8_t *__restrict__ norm,
                   int32_t *__restrict__ idx, uint32_t *__restrict__ keybuf,
                   int32_t *status) {
   extern __shared__ __align__(16) uint32_t sel_keys[];
@@ -182,67 +181,6 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
   // overflows) or a page-0 score that is not finite takes the general form
   // below, with per-thread references.
   if (rule != LOCKS_MERGE_GROUP_MASS) {
-  // The scoring kernel's partials, when given: (r, s) pairs of the warps
-  // that scored this unit's tiles, merged per head.
-  bool have_z = false;
-  if (norm) {
-    const int *hdr = reinterpret_cast<const int *>(norm);
-    const long long total = hdr[0], W = hdr[1];
-    const long long units = (long long)gridDim.y * h_kv;
-    const long long u = (long long)b * h_kv + h;
-    const long long t0 = hdr[4 + u];
-    const long long tiles = (nf + kScoreTilePages - 1) / kScoreTilePages;
-    if (total > 0 && W > 0 && tiles > 0) {
-      const long long wf = norm_warp_of_tile(t0, total, W);
-      const long long wl = norm_warp_of_tile(t0 + tiles - 1, total, W);
-      const float2 *part =
-          reinterpret_cast<const float2 *>(norm + norm_parts_offset(units)) +
-          (size_t)u * G;
-      float r[GT], sm[GT];
-#pragma unroll
-      for (int g = 0; g < GT; ++g) {
-        r[g] = -INFINITY;
-        sm[g] = 0.f;
-      }
-      for (long long w = wf + tid; w <= wl; w += blockDim.x) {
-        if (w * total / W == (w + 1) * total / W) continue;  // no tiles
-#pragma unroll
-        for (int g = 0; g < GT; ++g) {
-          if (g < G) {
-            const float2 p = __ldg(part + (size_t)w * G + g);
-            norm_merge(r[g], sm[g], p.x, p.y);
-          }
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < GT; ++g) {
-        float rg = r[g], sg = sm[g];
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) norm_merge_xor(rg, sg, o);
-        if (lane == 0) {
-          red_m[wid][g] = rg;
-          red_s[wid][g] = sg;
-        }
-      }
-      if (tid == 0) sh_slow = 0;
-      __syncthreads();
-      if (tid < G) {
-        float rg = -INFINITY, sg = 0.f;
-        for (int w = 0; w < nwarps; ++w)
-          norm_merge(rg, sg, red_m[w][tid], red_s[w][tid]);
-        // usable: a finite reference and a sum in [1, 2^126) (the pair of
-        // the page that set the reference contributes at least 1)
-        if (!(rg > -INFINITY && rg < INFINITY && sg >= 1.f &&
-              sg < 8.5e37f))
-          sh_slow = 1;
-        zs[tid] = rg + lg2_fast(sg);
-      }
-      __syncthreads();
-      have_z = sh_slow == 0;
-      __syncthreads();
-    }
-  }
-  if (!have_z) {
   float ref[GT];
   bool finite = true;
 #pragma unroll
@@ -351,7 +289,6 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
     zs[tid] = m + lg2_fast(s);
   }
   __syncthreads();
-  }
   }
   } else {
     if (tid < G) zs[tid] = 0.f;
@@ -600,11 +537,10 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
 // --------------------------------------------------------------------------
 constexpr int kSelSmemKeys = 32 * 1024;   // candidate keys held on chip
 
-cudaError_t launch_select(const float *scores, const void *norm,
-                          const int32_t *seq_lens, int batch, int h_kv, int G,
-                          int max_pages, int k, int rule, int32_t *idx,
-                          uint32_t *keybuf, int32_t *status,
-                          cudaStream_t stream) {
+cudaError_t launch_select(const float *scores, const int32_t *seq_lens,
+                          int batch, int h_kv, int G, int max_pages, int k,
+                          int rule, int32_t *idx, uint32_t *keybuf,
+                          int32_t *status, cudaStream_t stream) {
   dim3 grid(h_kv, batch);
   const bool on_chip = max_pages <= kSelSmemKeys;
   const size_t smem = on_chip ? (size_t)((max_pages + 3) & ~3) * 4 : 0;
@@ -613,8 +549,8 @@ cudaError_t launch_select(const float *scores, const void *norm,
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmemKeys * 4);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, grid, dim3(kSelThreads), smem, stream, scores,
-                      seq_lens, h_kv, G, max_pages, k, rule,
-                      static_cast<const uint8_t *>(norm), idx, keybuf, status);
+                      seq_lens, h_kv, G, max_pages, k, rule, idx, keybuf,
+                      status);
   };
   const int gt = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : G <= 8 ? 8 : 16;
   // one CTA per SM suffices when the units fit the GPU in one wave

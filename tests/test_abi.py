@@ -32,20 +32,10 @@ def test_record_and_status_strings(L):
     assert L.locks_last_cuda_error() == 0
 
 
-def _norm_bytes(units, G):
-    # int header[4] + int tile0[units], 16-byte aligned, then one float2
-    # pair per (unit + scoring warp, head), at most 16 x 512 warps
-    return -(-(4 + units) * 4 // 16) * 16 + (units + 16 * 512) * G * 8
-
-
 def test_workspace_size_rules(L):
-    # 256-byte header + max(score region, split-K region); the score region
-    # holds the scores, the selection keys and the normaliser partials
+    # 256-byte header + max(score region, split-K region)
     a = B.locks_workspace_size(32, 32, 8, 8192, 128)
-    assert a == 256 + 32 * 8 * 4 * 8192 * 4 + 32 * 8 * 8192 * 4 + \
-        -(-_norm_bytes(256, 4) // 256) * 256
-    assert B.locks_norm_partials_size(32, 32, 8) == _norm_bytes(256, 4)
-    assert B.locks_norm_partials_size(3, 16, 1) == _norm_bytes(3, 16)
+    assert a == 256 + 32 * 8 * 4 * 8192 * 4 + 32 * 8 * 8192 * 4
     b = B.locks_workspace_size(1, 8, 2, 256, 16)
     assert b >= 256 + 2 * 4 * 256 * 4
     out = ctypes.c_size_t(0)
@@ -68,17 +58,6 @@ def test_host_validation_before_launch(L):
                                 8, s) == 3
     assert L.locks_score_select(fake, fake, fake, 1, 64, 2, 16, 4, fake, fake,
                                 1 << 30, s) == 2
-    # score_pages_ex / select_pages_ex: misaligned or short partials buffer
-    odd = ctypes.c_void_p(24)
-    assert L.locks_score_pages_ex(fake, fake, fake, 1, 8, 2, 16, fake, odd,
-                                  1 << 20, None, s) == 1
-    assert L.locks_score_pages_ex(fake, fake, fake, 1, 8, 2, 16, fake, fake,
-                                  64, None, s) == 3
-    assert L.locks_select_pages_ex(fake, odd, fake, 1, 8, 2, 16, 4, fake,
-                                   fake, 1 << 30, s) == 1
-    out = ctypes.c_size_t(0)
-    assert L.locks_norm_partials_size(1, 7, 2, ctypes.byref(out)) == 1
-    assert L.locks_norm_partials_size(1, 34, 2, ctypes.byref(out)) == 2
     # sparse_decode
     assert L.locks_sparse_decode(fake, fake, fake, 0, fake, fake, fake, 4, 1,
                                  8, 2, 16, fake, fake, fake, 1 << 20, s) == 1

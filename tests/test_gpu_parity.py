@@ -482,60 +482,6 @@ def test_select_matches_oracle_on_same_scores():
             assert v == sorted(v) and len(set(v)) == len(v)
 
 
-@pytest.mark.parametrize("G,h_kv,batch,max_pages,k",
-                         [(4, 2, 1, 40, 8), (5, 2, 3, 300, 10),
-                          (16, 1, 2, 700, 16), (1, 4, 4, 129, 6),
-                          (8, 3, 5, 3001, 20), (4, 8, 9, 257, 32)])
-def test_select_with_normaliser_partials(G, h_kv, batch, max_pages, k):
-    """locks_score_pages_ex writes the mass-fraction denominators as
-    per-warp partials; locks_select_pages_ex merges them instead of
-    re-reading the scores.  The pages selected must equal those of the
-    normaliser pass over the scores (locks_select_pages) on the same
-    scores, and the fused locks_score_select must select the same pages
-    and write the same scores.  Shapes cover launches with fewer tiles than
-    scoring warps (most warps empty), warps whose tiles span two units,
-    every group size form, empty and one-page sequences."""
-    spec = W.custom_spec(batch=batch, h_q=G * h_kv, h_kv=h_kv,
-                         ctx=16 * max_pages, k=k, needles=0, seed=90 + G)
-    wl = W.generate(spec, "cpu")
-    _, _, pt, _ = host(wl)
-    rng = np.random.default_rng(G + batch)
-    lens = [int(x) for x in rng.integers(0, 16 * max_pages + 1, batch)]
-    lens[0] = 16 * max_pages
-    if batch > 2:
-        lens[1], lens[2] = 0, 9
-    seq, pg = full_pairs(lens)
-    store, _ = O.build_summaries(wl.k_cache.float().numpy(), pt, seq, pg,
-                                 batch, max_pages)
-    q = wl.queries[0].to(DEV)
-    st = torch.from_numpy(store).to(DEV)
-    sl = i32(lens)
-    scores = torch.full((batch, h_kv, G, max_pages), float("nan"),
-                        device=DEV)
-    norm = B.new_norm_partials(batch, G * h_kv, h_kv, DEV)
-    norm.fill_(0xFF)                     # stale contents must not matter
-    status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    B.locks_score_pages_ex(q, st, sl, scores, norm, status)
-    ws = B.new_workspace(batch, G * h_kv, h_kv, max_pages, k, DEV)
-    idx_p = torch.zeros(batch, h_kv, k, dtype=torch.int32, device=DEV)
-    idx_s = torch.zeros_like(idx_p)
-    idx_f = torch.zeros_like(idx_p)
-    B.locks_select_pages_ex(scores, norm, sl, G * h_kv, k, idx_p, ws)
-    B.locks_select_pages(scores, sl, G * h_kv, k, idx_s, ws)
-    ws2 = B.new_workspace(batch, G * h_kv, h_kv, max_pages, k, DEV)
-    B.locks_score_select(q, st, sl, k, idx_f, ws2)
-    torch.cuda.synchronize()
-    assert int(status.item()) == 0 and B.locks_read_status(ws) == 0
-    assert B.locks_read_status(ws2) == 0
-    assert torch.equal(idx_p, idx_s)
-    assert torch.equal(idx_f, idx_s)
-    n = batch * h_kv * G * max_pages
-    fused = ws2[256:256 + 4 * n].view(torch.float32).view(scores.shape)
-    for b in range(batch):
-        nf = lens[b] // 16
-        assert torch.equal(fused[b, :, :, :nf], scores[b, :, :, :nf])
-
-
 @pytest.mark.parametrize("G", [1, 4, 16])
 def test_select_normaliser_fallback(G):
     """Scores for which the normaliser's common reference (each head's
