@@ -290,7 +290,10 @@ locks_status_t locks_exact_page_scores(
  *     LOCKS_ERR_UNSUPPORTED and nothing is launched.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the life of the
+ *     process: do not call this entry point on a device after
+ *     cudaDeviceReset has been called for it (the array may then sit at
+ *     another address).
  *   - Every call shares the one array and it keeps the last call's contents;
  *     nothing in it needs to start at zero.  Calls that overlap on the GPU
  *     (on different streams) race on it.

@@ -14,7 +14,8 @@
 // a device address.  The device address is looked up once per device with
 // cudaGetSymbolAddress, with that device current, on the first call made on
 // that device (so that first call should happen before any stream capture),
-// and cached.
+// and cached for the life of the process; a cudaDeviceReset of that device
+// afterwards is not supported (the array may be placed elsewhere).
 #include <mutex>
 
 #include "common.cuh"
