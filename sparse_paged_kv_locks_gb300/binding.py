@@ -444,10 +444,16 @@ class LocksDecoder:
     the device length buffer the step reads (it is bound, so appends that
     update it in place take effect); otherwise the decoder keeps its own
     and copies the lengths passed to each step into it.  The library
-    allocates no device memory and the eager step never synchronises."""
+    allocates no device memory and the eager step never synchronises.
+
+    With append=True every `step` first appends one token per sequence
+    (k_new, v_new [batch][h_kv][128]) at the current length and builds the
+    summary of a page that this fills (locks_append_kv, the notes' §2
+    Fig. 1 build step), then decodes with the lengths it has grown; with
+    graph=True the append, with its page build, is part of the one graph."""
 
     def __init__(self, k_cache, v_cache, page_table, summaries, h_q, k,
-                 graph=False, seq_lens=None):
+                 graph=False, seq_lens=None, append=False):
         self.k_cache, self.v_cache = k_cache, v_cache
         self.page_table, self.summaries = page_table, summaries
         self.batch, self.h_kv, self.max_pages = summaries.shape[:3]
@@ -471,6 +477,11 @@ class LocksDecoder:
             if seq_lens.numel() != self.batch:
                 raise ValueError("seq_lens must have one entry per sequence")
             self.seq_lens_dev = seq_lens
+        self.append = append
+        if append:
+            self.k_new = torch.empty(self.batch, self.h_kv, HEAD_DIM,
+                                     dtype=torch.bfloat16, device=dev)
+            self.v_new = torch.empty_like(self.k_new)
         self.use_graph = graph
         self._graph = None
         self._native = None
@@ -480,7 +491,12 @@ class LocksDecoder:
         self._st_ref = ctypes.byref(self._st)
         self._step_fn = lib().locks_decoder_step_host
 
-    def _eager(self, q, seq_lens, stream=None):
+    def _eager(self, q, seq_lens, stream=None, k_new=None, v_new=None):
+        if self.append:
+            locks_append_kv(k_new, v_new, self.k_cache, self.v_cache,
+                            self.page_table, seq_lens, self.summaries,
+                            status=self.workspace[:4].view(torch.int32),
+                            stream=stream)
         locks_score_select(q, self.summaries, seq_lens, self.k, self.idx,
                            self.workspace, stream)
         locks_sparse_decode(q, self.k_cache, self.v_cache, self.page_table,
@@ -492,12 +508,27 @@ class LocksDecoder:
         side = torch.cuda.Stream()
         side.wait_stream(cur)
         with torch.cuda.stream(side):   # one-time setup outside the capture
-            self._eager(self.q_dev, self.seq_lens_dev)
+            self._eager(self.q_dev, self.seq_lens_dev, None, self.k_new_b,
+                        self.v_new_b)
+            if self.append:
+                # the warm-up appended this step's token; the replay that
+                # follows writes it (and any page build) again at the same
+                # position, so the lengths go back by one
+                self.seq_lens_dev.sub_(1)
         cur.wait_stream(side)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self._eager(self.q_dev, self.seq_lens_dev)
+            self._eager(self.q_dev, self.seq_lens_dev, None, self.k_new_b,
+                        self.v_new_b)
         self._graph = g
+
+    @property
+    def k_new_b(self):
+        return self.k_new if self.append else None
+
+    @property
+    def v_new_b(self):
+        return self.v_new if self.append else None
 
     def _bind_lens(self, seq_lens, stream=None):
         if seq_lens is not None and seq_lens is not self.seq_lens_dev:
@@ -506,16 +537,30 @@ class LocksDecoder:
             with torch.cuda.stream(s):
                 self.seq_lens_dev.copy_(seq_lens, non_blocking=True)
 
-    def step(self, q, seq_lens=None, stream=None):
-        """Device-resident query -> (o, lse) on the device."""
+    def step(self, q, seq_lens=None, stream=None, k_new=None, v_new=None):
+        """Device-resident query -> (o, lse) on the device (append mode:
+        after appending k_new, v_new)."""
+        if self.append:
+            if k_new is None or v_new is None:
+                raise ValueError("an appending decoder needs k_new and v_new")
+            _req(k_new, "k_new", torch.bfloat16, 3)
+            _req(v_new, "v_new", torch.bfloat16, 3)
+            if tuple(k_new.shape) != tuple(self.k_new.shape) or \
+                    tuple(v_new.shape) != tuple(self.k_new.shape):
+                raise ValueError("k_new, v_new must be [batch][h_kv][128]")
         if not self.use_graph:
             self._eager(q, self.seq_lens_dev if seq_lens is None else seq_lens,
-                        stream)
+                        stream, k_new, v_new)
             return self.o, self.lse
         if stream is not None:
             raise ValueError("graph replay runs on the current stream")
         if q is not self.q_dev:
             self.q_dev.copy_(q, non_blocking=True)
+        if self.append:
+            if k_new is not self.k_new:
+                self.k_new.copy_(k_new, non_blocking=True)
+            if v_new is not self.v_new:
+                self.v_new.copy_(v_new, non_blocking=True)
         self._bind_lens(seq_lens)
         if self._graph is None:
             self._capture()

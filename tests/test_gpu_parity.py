@@ -703,6 +703,47 @@ def test_decoder_graph_replay_matches_eager(name):
     assert graph._graph is not None
 
 
+def test_decoder_append_graph_matches_eager():
+    """The decode step with its append (the new token written at the
+    current length and, when that fills a page, the page's summary built)
+    captured into one CUDA graph gives the eager step's bytes: o, lse and
+    indices every step, and the same caches, summary store and lengths
+    after 20 steps that fill a page of every sequence."""
+    spec = W.custom_spec(batch=3, h_q=16, h_kv=4, ctx=16 * 40 + 9, k=8,
+                         steps=20, needles=1, seed=23, append_steps=20,
+                         ragged_min=16 * 30)
+    wl = W.generate(spec, "cpu")
+    d = Dev(wl)
+    batch, max_pages = wl.page_table.shape
+    lens0 = [int(x) for x in wl.seq_lens]
+    seq, pg = full_pairs(lens0)
+    store = B.new_summary_store(batch, spec.h_kv, max_pages, DEV)
+    B.locks_build_summaries(d.k_cache, d.page_table, i32(seq), i32(pg), store)
+    kc2, vc2, st2 = d.k_cache.clone(), d.v_cache.clone(), store.clone()
+    lens_e, lens_g = d.seq_lens.clone(), d.seq_lens.clone()
+    eager = B.LocksDecoder(d.k_cache, d.v_cache, d.page_table, store,
+                           spec.h_q, spec.k, seq_lens=lens_e, append=True)
+    graph = B.LocksDecoder(kc2, vc2, d.page_table, st2, spec.h_q, spec.k,
+                           graph=True, seq_lens=lens_g, append=True)
+    ka, va = wl.k_append.to(DEV), wl.v_append.to(DEV)
+    for s in range(spec.append_steps):
+        q = d.queries[s]
+        oe, le = eager.step(q, k_new=ka[s], v_new=va[s])
+        oe, le, ie = oe.clone(), le.clone(), eager.idx.clone()
+        og, lg = graph.step(q, k_new=ka[s], v_new=va[s])
+        torch.cuda.synchronize()
+        assert eager.status() == 0 and graph.status() == 0, s
+        assert torch.equal(ie, graph.idx), s
+        assert torch.equal(oe, og) and torch.equal(le, lg), s
+    assert graph._graph is not None
+    assert lens_g.cpu().tolist() == [L + spec.append_steps for L in lens0]
+    assert torch.equal(lens_e, lens_g)
+    assert torch.equal(d.k_cache, kc2) and torch.equal(d.v_cache, vc2)
+    assert torch.equal(store, st2)
+    # every sequence filled at least one page during the appends
+    assert all((L + spec.append_steps) // 16 > L // 16 for L in lens0)
+
+
 def test_native_host_decoder_matches_eager():
     """locks_decoder_step_host (query copy in, five kernels, copies of o,
     lse and the status word out, replayed as one CUDA graph) returns the
