@@ -89,6 +89,15 @@ locks_status_t locks::score_select(const void *q, const void *summaries,
   float *s_hat = reinterpret_cast<float *>(ws + kWsHeader);
   uint32_t *keys = reinterpret_cast<uint32_t *>(
       ws + kWsHeader + round_up((size_t)batch * h_kv * G * max_pages * 4, 256));
+  // short page lists on fewer units than SMs: one launch, the selection
+  // done by the cluster that scored the unit
+  const int cluster = fused_cluster_size(batch, h_kv, G, max_pages);
+  if (cluster > 0) {
+    const cudaError_t e = launch_score_select_fused(
+        q, summaries, seq_lens, batch, h_kv, G, max_pages, k, cluster, s_hat,
+        idx_out, status, stream, after_query);
+    return e == cudaSuccess ? LOCKS_OK : fail_cuda(e);
+  }
   cudaError_t e = launch_score(q, summaries, seq_lens, batch, h_kv, G,
                                max_pages, s_hat, status, stream, after_query);
   if (e != cudaSuccess) return fail_cuda(e);

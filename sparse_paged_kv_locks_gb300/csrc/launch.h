@@ -96,6 +96,19 @@ cudaError_t launch_score(const void *q, const void *summaries,
                          int max_pages, float *s_hat, int32_t *status,
                          cudaStream_t stream, bool after_query = false);
 
+// Single-launch score and select (share-average rule) for units with short
+// page lists: one cluster of `cluster` CTAs per (sequence, KV head).
+// fused_cluster_size: the cluster size for these sizes on the current
+// device, 0 when the fused form does not apply (G > 8, more than 8192
+// pages, more units than SMs, or the clusters cannot all be resident).
+int fused_cluster_size(int batch, int h_kv, int G, int max_pages);
+cudaError_t launch_score_select_fused(const void *q, const void *summaries,
+                                      const int32_t *seq_lens, int batch,
+                                      int h_kv, int G, int max_pages, int k,
+                                      int cluster, float *s_hat, int32_t *idx,
+                                      int32_t *status, cudaStream_t stream,
+                                      bool after_query);
+
 cudaError_t launch_select(const float *scores, const int32_t *seq_lens,
                           int batch, int h_kv, int G, int max_pages, int k,
                           int rule, int32_t *idx, uint32_t *keybuf,

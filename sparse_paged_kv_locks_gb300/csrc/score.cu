@@ -14,6 +14,7 @@
 // each lane's mma fragments come from one 16-byte shared-memory read.
 #include "common.cuh"
 #include "launch.h"
+#include "select_top.cuh"
 
 namespace locks {
 
@@ -315,13 +316,185 @@ __device__ __forceinline__ void issue_tile(const Cursor &c, const int *nfull,
   }
 }
 
+// Running sums of 2^v (v in log2 units) as (reference r, sum s of
+// 2^(v - r)): r is raised, and s rescaled, only when v passes it by more
+// than 2^6, so every term stays below 2^64.  A NaN makes r = +inf.
+__device__ __forceinline__ void norm_add(float &r, float &s, float v) {
+  if (!(v > -INFINITY)) {  // -inf adds nothing
+    if (v != v) r = INFINITY;
+    return;
+  }
+  if (v > r + 64.f) {  // also the first value (r = -inf)
+    s = r == -INFINITY ? 0.f : s * ex2_fast(r - v);
+    r = v;
+  }
+  s += ex2_fast(v - r);
+}
+
+// (r, s) <- (r, s) + (r2, s2) in the same sense
+__device__ __forceinline__ void norm_merge(float &r, float &s, float r2,
+                                           float s2) {
+  const float m = fmaxf(r, r2);
+  if (m == -INFINITY) return;
+  s = (r == -INFINITY ? 0.f : s * ex2_fast(r - m)) +
+      (r2 == -INFINITY ? 0.f : s2 * ex2_fast(r2 - m));
+  r = m;
+}
+
+__device__ __forceinline__ void norm_merge_xor(float &r, float &s, int o) {
+  const float r2 = __shfl_xor_sync(0xffffffffu, r, o);
+  const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+  norm_merge(r, s, r2, s2);
+}
+
+// Longest page list the fused form takes: its CTA 0 keeps the unit's keys
+// and the radix scratch in the (by then idle) tile ring.
+constexpr int kFusedMaxPages = 8192;
+static_assert(kFusedMaxPages * 4 + sizeof(SelectScratch) + 16 <= kRingBytes,
+              "fused keys and scratch must fit the tile ring");
+
+// The selection of the fused form, after the cluster's warps scored unit
+// (b, h) into s_hat.  (nr, ns): this lane's running pair of its head
+// (MODE 1: gq & 3, else gq).  Every thread of every CTA of the cluster
+// calls it.
 template <int MODE>
+__device__ __forceinline__ void fused_select_epilogue(
+    float nr, float ns, const float *s_hat, const int32_t *seq_lens,
+    int h_kv, int G, int max_pages, int k, int b, int h, int rank, int csize,
+    int tiles, uint8_t *smem, int32_t *idx_out, int32_t *status) {
+  __shared__ float f_r[kScoreWarps][kMaxGroup], f_s[kScoreWarps][kMaxGroup];
+  __shared__ float f_pr[kMaxGroup], f_ps[kMaxGroup], f_z[kMaxGroup];
+  __shared__ uint32_t f_red[2][kScoreWarps];
+  __shared__ uint32_t f_kmm[2][8];  // CTA 0: (kmin, kmax) of every rank
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int gq = lane >> 2, t4 = lane & 3;
+  // this CTA's pair per head: lanes of a head, then warps
+  norm_merge_xor(nr, ns, 1);
+  norm_merge_xor(nr, ns, 2);
+  if (MODE == 1) norm_merge_xor(nr, ns, 16);
+  if (t4 == 0 && (MODE != 1 || gq < 4) && gq < G) {
+    f_r[wid][gq] = nr;
+    f_s[wid][gq] = ns;
+  }
+  __syncthreads();
+  if (tid < G) {
+    float r = -INFINITY, sm = 0.f;
+    for (int w = 0; w < kScoreWarps; ++w) norm_merge(r, sm, f_r[w][tid], f_s[w][tid]);
+    f_pr[tid] = r;
+    f_ps[tid] = sm;
+  }
+  cluster_sync();  // every CTA scored its pages and holds its pairs
+  // Z_g (log2 units): the cluster's pairs merged in rank order, the same
+  // value in every CTA
+  if (tid < G) {
+    float r = -INFINITY, sm = 0.f;
+    for (int c = 0; c < csize; ++c)
+      norm_merge(r, sm, ld_cluster_f32(mapa_shared(smem_u32(&f_pr[tid]), c)),
+                 ld_cluster_f32(mapa_shared(smem_u32(&f_ps[tid]), c)));
+    f_z[tid] = r + lg2_fast(sm);
+  }
+  int L = seq_lens[b];
+  L = max(0, min(L, max_pages * kPage));
+  const int n = (L + kPage - 1) / kPage, nf = L / kPage;
+  // CTA 0's tile ring, idle now: keys of the unit's pages, then the radix
+  // scratch
+  uint32_t *keys = reinterpret_cast<uint32_t *>(smem);
+  SelectScratch &sel = *reinterpret_cast<SelectScratch *>(
+      smem + ((size_t)max_pages * 4 + 15) / 16 * 16);
+  const uint32_t keys_s = smem_u32(keys);
+  if (rank == 0) {
+    for (int j = nf + tid; j < n; j += blockDim.x) keys[j] = 0u;
+    for (int i = tid; i < kRadixBins; i += blockDim.x) sel.hist[0][i] = 0;
+  }
+  __syncthreads();
+  // keys of this CTA's full pages (the tiles its warps scored):
+  // log2 sum_g 2^(s_gj - Z_g), the share-average up to the factor 1/G
+  const long long nwc = (long long)csize * kScoreWarps;
+  const int p0 = (int)((long long)rank * kScoreWarps * tiles / nwc) *
+                 kTilePages;
+  const int p1 = min(nf, (int)((long long)(rank + 1) * kScoreWarps * tiles /
+                               nwc) * kTilePages);
+  const float *sc = s_hat + ((size_t)b * h_kv + h) * G * (size_t)max_pages;
+  constexpr float kLog2e = 1.4426950408889634f;
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  for (int j = p0 + tid; j < p1; j += blockDim.x) {
+    float sum = 0.f, m = -INFINITY;
+    for (int g = 0; g < G; ++g) {
+      const float x = fmaf(sc[(size_t)g * max_pages + j], kLog2e, -f_z[g]);
+      sum += ex2_fast(x);
+      m = fmaxf(m, x);
+    }
+    float key = lg2_fast(sum);
+    if (!(sum > 0.f && sum < INFINITY)) {  // every term underflowed
+      float t = 0.f;
+      for (int g = 0; g < G; ++g)
+        t += ex2_fast(fmaf(sc[(size_t)g * max_pages + j], kLog2e, -f_z[g]) -
+                      m);
+      key = m + lg2_fast(t);
+    }
+    const bool cand = (unsigned)(j - 1) <= (unsigned)(n - 3);
+    const uint32_t kq = cand ? order_key(key) : 0u;
+    st_cluster_u32(mapa_shared(keys_s + 4u * (uint32_t)j, 0), kq);
+    if (cand) {
+      kmin = min(kmin, kq);
+      kmax = max(kmax, kq);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  if (lane == 0) {
+    f_red[0][wid] = kmin;
+    f_red[1][wid] = kmax;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < kScoreWarps; ++w) {
+      kmin = min(kmin, f_red[0][w]);
+      kmax = max(kmax, f_red[1][w]);
+    }
+    st_cluster_u32(mapa_shared(smem_u32(&f_kmm[0][rank]), 0), kmin);
+    st_cluster_u32(mapa_shared(smem_u32(&f_kmm[1][rank]), 0), kmax);
+  }
+  cluster_sync();  // CTA 0 holds every key and every rank's bounds
+  if (rank != 0) return;
+  int32_t *out = idx_out + ((size_t)b * h_kv + h) * k;
+  if (n <= k) {
+    for (int i = tid; i < k; i += blockDim.x) out[i] = i < n ? i : -1;
+    return;
+  }
+  if (k == 2) {  // only the sink and the recent page
+    if (tid == 0) {
+      out[0] = 0;
+      out[1] = n - 1;
+    }
+    return;
+  }
+  uint32_t a = 0xffffffffu, z = 0u;
+  if (tid == 0)
+    for (int c = 0; c < csize; ++c) {
+      a = min(a, f_kmm[0][c]);
+      z = max(z, f_kmm[1][c]);
+    }
+  select_top<true, kScoreWarps>(keys, true, n, k, a, z, out, status, sel);
+}
+
+// FUSED: the single-launch score-and-select form for short page lists.
+// The grid is one cluster of C CTAs per (sequence, KV head) unit; the C x
+// 16 warps of a cluster split that unit's tiles, and after scoring the
+// cluster forms the mass-fraction denominators from per-CTA partial sums
+// (distributed shared memory), each CTA computes its pages' selection keys
+// into CTA 0's shared memory, and CTA 0 selects (select_top) into idx_out.
+template <int MODE, bool FUSED = false>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_kernel(const __nv_bfloat16 *__restrict__ q,
                  const uint8_t *__restrict__ summaries,
                  const int32_t *__restrict__ seq_lens, int batch, int h_kv,
                  int G, int max_pages, float *__restrict__ s_hat,
-                 int32_t *status, int wait_query) {
+                 int32_t *status, int wait_query, int k,
+                 int32_t *__restrict__ idx_out) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *ring = smem;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes);
@@ -371,42 +544,62 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   }
   __syncthreads();
 
-  const long long total = prefix[batch];
-  const long long W = (long long)gridDim.x * kScoreWarps;
-  const long long gw = (long long)blockIdx.x * kScoreWarps + wid;
-  const long long t_begin = gw * total / W, t_end = (gw + 1) * total / W;
-  // wait_query: the query comes from the preceding kernel (this one is its
-  // programmatic dependent), so every thread waits for it before reading q
-  // or exiting.
-  if (t_begin >= t_end) {
-    if (wait_query) pdl_wait();
-    return;
+  long long t_begin, t_end;
+  int fu_b = 0, fu_h = 0, fu_rank = 0, fu_size = 1;  // FUSED: the unit
+  if constexpr (FUSED) {
+    fu_rank = (int)cluster_ctarank();
+    fu_size = (int)cluster_nctarank();
+    const int u = (int)(blockIdx.x / fu_size);
+    fu_b = u / h_kv;
+    fu_h = u - fu_b * h_kv;
+    const long long t0 = prefix[fu_b] + (long long)fu_h * tph[fu_b];
+    const long long nt = tph[fu_b];
+    const long long lw = (long long)fu_rank * kScoreWarps + wid;
+    const long long nw = (long long)fu_size * kScoreWarps;
+    t_begin = t0 + lw * nt / nw;
+    t_end = t0 + (lw + 1) * nt / nw;
+  } else {
+    const long long total = prefix[batch];
+    const long long W = (long long)gridDim.x * kScoreWarps;
+    const long long gw = (long long)blockIdx.x * kScoreWarps + wid;
+    t_begin = gw * total / W;
+    t_end = (gw + 1) * total / W;
+    // wait_query: the query comes from the preceding kernel (this one is
+    // its programmatic dependent), so every thread waits for it before
+    // reading q or exiting.
+    if (t_begin >= t_end) {
+      if (wait_query) pdl_wait();
+      return;
+    }
   }
   uint8_t *my_ring = ring + (size_t)wid * kStages * kTileBytes;
   const uint32_t ring_s = smem_u32(my_ring);
   uint64_t *my_bar = bars + wid * kStages;
 
-  Cursor cur;
-  {  // largest b with prefix[b] <= t_begin
-    int lo = 0, hi = batch;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (prefix[mid] <= t_begin) lo = mid; else hi = mid;
-    }
-    const int rem = (int)(t_begin - prefix[lo]);
-    const int tb = tph[lo];
-    cur.b = lo;
-    cur.h = rem / tb;
-    cur.j = rem - cur.h * tb;
-  }
+  Cursor cur{0, 0, 0};
   Cursor nxt = cur;
-  issue_tile(nxt, nfull, summaries, h_kv, max_pages, my_ring, &my_bar[0],
-             lane);
-  advance_cursor(nxt, tph, batch, h_kv);
-  if (t_begin + 1 < t_end) {
-    issue_tile(nxt, nfull, summaries, h_kv, max_pages, my_ring + kTileBytes,
-               &my_bar[1], lane);
+  if (t_begin < t_end) {
+    {  // largest b with prefix[b] <= t_begin
+      int lo = 0, hi = batch;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= t_begin) lo = mid; else hi = mid;
+      }
+      const int rem = (int)(t_begin - prefix[lo]);
+      const int tb = tph[lo];
+      cur.b = lo;
+      cur.h = rem / tb;
+      cur.j = rem - cur.h * tb;
+    }
+    nxt = cur;
+    issue_tile(nxt, nfull, summaries, h_kv, max_pages, my_ring, &my_bar[0],
+               lane);
     advance_cursor(nxt, tph, batch, h_kv);
+    if (t_begin + 1 < t_end) {
+      issue_tile(nxt, nfull, summaries, h_kv, max_pages, my_ring + kTileBytes,
+                 &my_bar[1], lane);
+      advance_cursor(nxt, tph, batch, h_kv);
+    }
   }
   if (wait_query) pdl_wait();  // first two tiles in flight; q is read next
 
@@ -426,6 +619,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   // MODE 1: head gq & 3; MODE 2: head gq)
   float *lane_row = nullptr, *lane_row8 = nullptr;
   const int n_tiles = (int)(t_end - t_begin);
+  // FUSED: this lane's running (reference, sum of 2^(v - reference)) over
+  // the scores it writes (log2 units), for head gq & 3 (MODE 1) or gq
+  float nr = -INFINITY, ns = 0.f;
 
   for (int it = 0; it < n_tiles; ++it) {
     const int stage = it & 1;
@@ -542,6 +738,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
     const uint32_t base_s = ring_s + stage * kTileBytes;
     if constexpr (MODE != 3) {
+      // An odd page count leaves the second page of the last pair unused:
+      // its slot is zeroed (a zero record scores to a finite constant) so
+      // that what the ring held before cannot take part in the overflow
+      // vote below and change how the tile's pages are computed.
+      if (npg & 1) {
+        uint4 *slot = reinterpret_cast<uint4 *>(my_ring + stage * kTileBytes +
+                                                npg * kRec);
+        for (int i = lane; i < kRec / 16; i += 32)
+          slot[i] = make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+      }
       float keepA = 0.f, keepB = 0.f;
       // first pass without per-pair overflow checks; a second, max-
       // subtracted pass only when some quad sum left the normal range
@@ -578,9 +785,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const float smu = __half2float(__ushort_as_half(
             (unsigned short)lds16(base_s + pg * kRec + kOffSMu)));
         const float qmu = up ? qm_from_low : qm_lo;
-        if (head < G && pg < npg)
-          st_keep(lane_row + page0 + pg, (keepA + qmu * smu * mscale) * kLn2,
-                  keep);
+        if (head < G && pg < npg) {
+          const float v = keepA + qmu * smu * mscale;  // log2 units
+          st_keep(lane_row + page0 + pg, v * kLn2, keep);
+          if constexpr (FUSED) norm_add(nr, ns, v);
+        }
       } else {
         const int pg0 = 2 * t4, pg1 = pg0 + 1;
         const float sm0 = __half2float(__ushort_as_half(
@@ -588,12 +797,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const float sm1 = __half2float(__ushort_as_half(
             (unsigned short)lds16(base_s + pg1 * kRec + kOffSMu)));
         if (gq < G) {
-          if (pg0 < npg)
-            st_keep(lane_row + page0 + pg0,
-                    (keepA + qm_lo * sm0 * mscale) * kLn2, keep);
-          if (pg1 < npg)
-            st_keep(lane_row + page0 + pg1,
-                    (keepB + qm_hi * sm1 * mscale) * kLn2, keep);
+          if (pg0 < npg) {
+            const float v = keepA + qm_lo * sm0 * mscale;
+            st_keep(lane_row + page0 + pg0, v * kLn2, keep);
+            if constexpr (FUSED) norm_add(nr, ns, v);
+          }
+          if (pg1 < npg) {
+            const float v = keepB + qm_hi * sm1 * mscale;
+            st_keep(lane_row + page0 + pg1, v * kLn2, keep);
+            if constexpr (FUSED) norm_add(nr, ns, v);
+          }
         }
       }
     } else {
@@ -704,6 +917,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     mbar_wait(&my_bar[0], 1, 1u << 16);
     mbar_wait(&my_bar[1], 1, 1u << 16);
   }
+  if constexpr (FUSED)
+    fused_select_epilogue<MODE>(nr, ns, s_hat, seq_lens, h_kv, G, max_pages,
+                                k, fu_b, fu_h, fu_rank, fu_size,
+                                tph[fu_b], smem, idx_out, status);
 }
 
 // --------------------------------------------------------------------------
@@ -750,10 +967,103 @@ cudaError_t launch_score(const void *q, const void *summaries,
   if (after_query)
     return launch_pdl(kern, dim3(grid), dim3(kScoreThreads), smem, stream, qq,
                       ss, seq_lens, batch, h_kv, G, max_pages, s_hat, status,
-                      1);
+                      1, 0, (int32_t *)nullptr);
   kern<<<grid, kScoreThreads, smem, stream>>>(qq, ss, seq_lens, batch, h_kv, G,
-                                              max_pages, s_hat, status, 0);
+                                              max_pages, s_hat, status, 0, 0,
+                                              nullptr);
   return cudaGetLastError();
+}
+
+static_assert(kScoreThreads == kSelThreads,
+              "the fused form runs select_top on the scoring block");
+
+static cudaError_t fused_attributes() {
+  static DeviceFlags attr_set;
+  return once_per_device(attr_set, [] {
+    cudaError_t e = cudaFuncSetAttribute(
+        score_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        227 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(score_kernel<2, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               227 * 1024);
+    return e;
+  });
+}
+
+int fused_cluster_size(int batch, int h_kv, int G, int max_pages) {
+  if (G > 8 || max_pages > kFusedMaxPages || batch > score_max_batch())
+    return 0;
+  if (fused_attributes() != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  const long long units = (long long)batch * h_kv;
+  const int sms = device_sm_count();
+  if (units < 1 || units > sms) return 0;
+  int C = 8;
+  while (C > 1 && units * C > sms) C >>= 1;
+  // every cluster must be resident at once (one CTA per SM, C SMs of a
+  // GPC each): ask the occupancy calculator, once per device and form
+  static DeviceFlags fits[2][4];
+  const int form = G > 4 ? 1 : 0;
+  int lc = 0;
+  for (int c = C; c > 1; c >>= 1) ++lc;
+  for (; C >= 1; C >>= 1, --lc) {
+    const int maxc = per_device_value(fits[form][lc], [&] {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(units * C));
+      cfg.blockDim = dim3(kScoreThreads);
+      cfg.dynamicSmemBytes = score_smem_bytes(batch);
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = C;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(
+              &n, form ? score_kernel<2, true> : score_kernel<1, true>,
+              &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+      return n + 1;  // cached values are >= 1
+    });
+    if (maxc - 1 >= units) return C;
+  }
+  return 0;
+}
+
+cudaError_t launch_score_select_fused(const void *q, const void *summaries,
+                                      const int32_t *seq_lens, int batch,
+                                      int h_kv, int G, int max_pages, int k,
+                                      int cluster, float *s_hat, int32_t *idx,
+                                      int32_t *status, cudaStream_t stream,
+                                      bool after_query) {
+  const cudaError_t ea = fused_attributes();
+  if (ea != cudaSuccess) return ea;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((long long)batch * h_kv * cluster));
+  cfg.blockDim = dim3(kScoreThreads);
+  cfg.dynamicSmemBytes = score_smem_bytes(batch);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_query ? 2 : 1;
+  auto *qq = static_cast<const __nv_bfloat16 *>(q);
+  auto *ss = static_cast<const uint8_t *>(summaries);
+  return cudaLaunchKernelEx(&cfg,
+                            G > 4 ? score_kernel<2, true> : score_kernel<1, true>,
+                            qq, ss, seq_lens, batch, h_kv, G, max_pages, s_hat,
+                            status, after_query ? 1 : 0, k, idx);
 }
 
 }  // namespace locks

@@ -5,33 +5,13 @@
 // share (ties to the lower page).
 #include "common.cuh"
 #include "launch.h"
+#include "select_top.cuh"
 
 namespace locks {
 
 // ---------------------------------------------------------------------------
 // selection: one CTA per (sequence, KV head)
 // ---------------------------------------------------------------------------
-constexpr int kSelThreads = 512;
-
-__device__ __forceinline__ uint32_t order_key(float x) {
-  const uint32_t u = __float_as_uint(x);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Sum of the per-warp values v[0..wid) (one per warp of the block, in
-// shared memory): a shuffle scan over the warps instead of a loop
-template <int NWARPS>
-__device__ __forceinline__ int warps_before(const int *v, int wid, int lane) {
-  const int x = lane < NWARPS ? v[lane] : 0;
-  int incl = x;
-#pragma unroll
-  for (int o = 1; o < NWARPS; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  return __shfl_sync(0xffffffffu, incl - x, wid);
-}
-
 // block-wide exclusive scan of two counters (blockDim = kSelThreads)
 __device__ __forceinline__ void block_scan2(int a, int b, int &ea, int &eb,
                                             int *sh /* [2*32] */) {
@@ -96,25 +76,9 @@ __device__ __forceinline__ void load_quad(const float *sc, int max_pages,
   }
 }
 
-// Keys j0..j0+3 (16-byte aligned when `kvec`); keys at or past `lim` read 0.
-__device__ __forceinline__ uint4 load_keys4(const uint32_t *keys, int j0,
-                                            int lim, bool kvec) {
-  if (kvec && j0 + 3 < lim) return *reinterpret_cast<const uint4 *>(keys + j0);
-  uint4 v;
-  v.x = j0 < lim ? keys[j0] : 0u;
-  v.y = j0 + 1 < lim ? keys[j0 + 1] : 0u;
-  v.z = j0 + 2 < lim ? keys[j0 + 2] : 0u;
-  v.w = j0 + 3 < lim ? keys[j0 + 3] : 0u;
-  return v;
-}
-
 // Keys live in shared memory when they fit (SMEM_KEYS), else in the
 // workspace.  Keys are indexed by page; the sink, the recent page and pages
 // past the candidates hold key 0, which is below every real key.
-constexpr int kRadixBits = 12;
-constexpr int kRadixBins = 1 << kRadixBits;
-constexpr int kBinsPerWarp = kRadixBins / (kSelThreads / 32);  // 256
-
 // MINB: resident CTAs per SM the registers are sized for.  2 when there are
 // more (sequence, KV head) units than SMs; 1 when every unit has an SM of
 // its own, which leaves registers for more pages in flight per thread.
@@ -128,11 +92,9 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
   extern __shared__ __align__(16) uint32_t sel_keys[];
   __shared__ float zs[kMaxGroup];
   __shared__ float red_m[32][kMaxGroup], red_s[32][kMaxGroup];
-  __shared__ __align__(16) int hist[2][kRadixBins];
-  __shared__ int sh_wcnt[2][32];
+  __shared__ __align__(16) SelectScratch sel;
   __shared__ uint32_t red_u[2][32];
-  __shared__ uint32_t sh_prefix, sh_mask;
-  __shared__ int sh_remaining, sh_varying, sh_slow;
+  __shared__ int sh_slow;
 
   const int b = blockIdx.y, h = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -171,7 +133,7 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
   // (at two CTAs per SM and G = 4 a second quad in flight measured slower,
   // 16.6 against 16.2 us on 256 units, and spilled)
   constexpr int R = MINB == 1 ? (GT <= 8 ? 2 : 1) : (GT <= 2 ? 2 : 1);
-  for (int i = tid; i < kRadixBins; i += blockDim.x) hist[0][i] = 0;
+  for (int i = tid; i < kRadixBins; i += blockDim.x) sel.hist[0][i] = 0;
 
   // Z_g: log2-sum-exp2 over the summarised pages [0, nf) (group-mass
   // pooling does not normalise per head and skips it).  Common form: every
@@ -380,156 +342,14 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
     red_u[1][wid] = kmax;
   }
   __syncthreads();
+  uint32_t a = 0xffffffffu, z = 0u;
   if (tid == 0) {
-    uint32_t a = 0xffffffffu, z = 0u;
     for (int w = 0; w < nwarps; ++w) {
       a = min(a, red_u[0][w]);
       z = max(z, red_u[1][w]);
     }
-    // bits above the highest one where min and max differ are common to
-    // every candidate key
-    const int varying = (a == z) ? 0 : 32 - __clz(a ^ z);
-    const uint32_t msk = varying == 32 ? 0u : ~((1u << varying) - 1u);
-    sh_prefix = z & msk;
-    sh_mask = msk;
-    sh_remaining = k - 2;
-    sh_varying = varying;
   }
-  __syncthreads();
-
-  // radix select of the (k-2)-th largest key over the varying bits,
-  // 12-bit digits from the top; key 0 never matches a candidate prefix.
-  // Histograms alternate between two buffers so the next one is cleared
-  // while the current one fills.
-  const int varying = sh_varying;
-  const int nk4 = (n + 3) >> 2;
-  for (int top = varying, pass = 0; top > 0; top -= kRadixBits, ++pass) {
-    const int width = min(kRadixBits, top), shift = top - width;
-    const uint32_t dmask = (1u << width) - 1u;
-    int *hc = hist[pass & 1];
-    int *hn = hist[(pass & 1) ^ 1];
-    const uint32_t pre = sh_prefix, msk = sh_mask;
-    const int rem = sh_remaining;
-    for (int i = tid; i < kRadixBins; i += blockDim.x) hn[i] = 0;
-    for (int qd = tid; qd < nk4; qd += blockDim.x) {
-      const uint4 v = load_keys4(keys, 4 * qd, n, kvec);
-      const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (kv[u] != 0u && (kv[u] & msk) == pre)
-          atomicAdd(&hc[(kv[u] >> shift) & dmask], 1);
-    }
-    __syncthreads();
-    // warp w covers digits [bins-256(w+1), bins-256w), lane l its eight
-    // digits from the top; counts are scanned from the largest digit down
-    const int hi = kRadixBins - 1 - kBinsPerWarp * wid - 8 * lane;
-    const int4 c4 = *reinterpret_cast<const int4 *>(hc + hi - 3);
-    const int4 d4 = *reinterpret_cast<const int4 *>(hc + hi - 7);
-    const int cnt = c4.x + c4.y + c4.z + c4.w + d4.x + d4.y + d4.z + d4.w;
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    if (lane == 31) sh_wcnt[0][wid] = incl;
-    __syncthreads();
-    const int before = warps_before<nwarps>(sh_wcnt[0], wid, lane);
-    const int mine = before + incl - cnt;  // count above this lane's digits
-    if (mine < rem && rem <= mine + cnt) {
-      const int c[8] = {c4.w, c4.z, c4.y, c4.x,
-                        d4.w, d4.z, d4.y, d4.x};  // digits hi, hi-1, ...
-      int acc = mine;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (acc < rem && rem <= acc + c[i]) {
-          sh_prefix = pre | ((uint32_t)(hi - i) << shift);
-          sh_mask = msk | (dmask << shift);
-          sh_remaining = rem - acc;
-        }
-        acc += c[i];
-      }
-    }
-    __syncthreads();
-  }
-  const uint32_t T = sh_prefix;
-  const int need_eq = sh_remaining;  // keys equal to T to keep (lowest j)
-
-  // ordered compaction: warp w owns pages [w*seg, (w+1)*seg), walked 128 at
-  // a time (four per lane); warps' counts are scanned once
-  const int seg = ((n + nwarps - 1) / nwarps + 127) & ~127;
-  const int w_lo = min(n, wid * seg), w_hi = min(n, w_lo + seg);
-  int gt = 0, eq = 0;
-  for (int j0 = w_lo + 4 * lane; j0 < w_hi; j0 += 128) {
-    const uint4 v = load_keys4(keys, j0, w_hi, kvec);
-    gt += (v.x > T) + (v.y > T) + (v.z > T) + (v.w > T);
-    eq += (v.x == T) + (v.y == T) + (v.z == T) + (v.w == T);
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    gt += __shfl_xor_sync(0xffffffffu, gt, o);
-    eq += __shfl_xor_sync(0xffffffffu, eq, o);
-  }
-  int gt_before, eq_before;
-  if constexpr (SMEM_KEYS) {
-    // n <= 32768 pages: both counts and their sums stay below 2^15
-    if (lane == 0) sh_wcnt[0][wid] = (eq << 16) | gt;
-    __syncthreads();
-    const int ge_before = warps_before<nwarps>(sh_wcnt[0], wid, lane);
-    gt_before = ge_before & 0xffff;
-    eq_before = ge_before >> 16;
-  } else {
-    if (lane == 0) {
-      sh_wcnt[0][wid] = gt;
-      sh_wcnt[1][wid] = eq;
-    }
-    __syncthreads();
-    gt_before = warps_before<nwarps>(sh_wcnt[0], wid, lane);
-    eq_before = warps_before<nwarps>(sh_wcnt[1], wid, lane);
-  }
-  for (int base = w_lo; base < w_hi; base += 128) {
-    const int j0 = base + 4 * lane;
-    const uint4 v = load_keys4(keys, j0, w_hi, kvec);
-    const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
-    int ngt = 0, neq = 0;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      ngt += kv[u] > T;
-      neq += kv[u] == T;
-    }
-    // most groups of 128 hold no key at or above the threshold
-    if (!__any_sync(0xffffffffu, ngt + neq > 0)) continue;
-    // exclusive scan of (eq << 16 | gt) over the lanes
-    const int packed = (neq << 16) | ngt;
-    int incl = packed;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const int tot = __shfl_sync(0xffffffffu, incl, 31);
-    int my_gt = gt_before + ((incl - packed) & 0xffff);
-    int my_eq = eq_before + ((incl - packed) >> 16);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const bool is_gt = kv[u] > T, is_eq = kv[u] == T;
-      if (is_gt || (is_eq && my_eq < need_eq)) {
-        const int pos = 1 + my_gt + min(my_eq, need_eq);
-        if (pos >= 1 && pos < k - 1)
-          out[pos] = j0 + u;
-        else
-          set_status(status, LOCKS_DEV_BAD_INDEX);
-      }
-      my_gt += is_gt;
-      my_eq += is_eq;
-    }
-    gt_before += tot & 0xffff;
-    eq_before += tot >> 16;
-  }
-  if (tid == 0) {
-    out[0] = 0;
-    out[k - 1] = n - 1;
-  }
+  select_top<SMEM_KEYS, nwarps>(keys, kvec, n, k, a, z, out, status, sel);
 }
 
 // --------------------------------------------------------------------------

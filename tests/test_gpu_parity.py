@@ -482,6 +482,68 @@ def test_select_matches_oracle_on_same_scores():
             assert v == sorted(v) and len(set(v)) == len(v)
 
 
+@pytest.mark.parametrize("G,h_kv,batch,max_pages,k",
+                         [(4, 2, 1, 40, 8), (8, 4, 3, 700, 12),
+                          (4, 8, 8, 2048, 64), (1, 1, 2, 300, 6),
+                          (5, 2, 5, 129, 10), (4, 8, 4, 8192, 128),
+                          (8, 8, 19, 64, 2), (4, 2, 3, 90, 200)])
+def test_fused_score_select_matches_two_kernels(G, h_kv, batch, max_pages, k):
+    """Short page lists on at most one unit per SM take the single-launch
+    score and select (one thread-block cluster per (sequence, KV head)):
+    locks_score_select then writes the scores locks_score_pages writes,
+    bit for bit, and selects what the oracle selects from them (identical
+    sets except pages within 1e-3 of the boundary in log share-average);
+    the two-kernel path (locks_score_pages + locks_select_pages) on the
+    same records agrees with it the same way.  Shapes: clusters of 8, 4, 2
+    and 1 CTAs, both scoring forms (G <= 4, G <= 8), 8,192 pages, empty and
+    one-page sequences, k = 2 and k above every sequence's pages."""
+    spec = W.custom_spec(batch=batch, h_q=G * h_kv, h_kv=h_kv,
+                         ctx=16 * max_pages, k=max(k, 2), needles=1,
+                         seed=300 + G + batch)
+    wl = W.generate(spec, "cpu")
+    kc, _, pt, _ = host(wl)
+    rng = np.random.default_rng(G * 7 + batch)
+    lens = [int(x) for x in rng.integers(0, 16 * max_pages + 1, batch)]
+    lens[0] = 16 * max_pages
+    if batch > 2:
+        lens[1], lens[2] = 0, 16 + 3
+    seq, pg = full_pairs(lens)
+    store, _ = O.build_summaries(kc, pt, seq, pg, batch, max_pages)
+    q = wl.queries[0].to(DEV)
+    st = torch.from_numpy(store).to(DEV)
+    sl = i32(lens)
+    ws_f = B.new_workspace(batch, G * h_kv, h_kv, max_pages, k, DEV)
+    ws_t = B.new_workspace(batch, G * h_kv, h_kv, max_pages, k, DEV)
+    idx_f = torch.zeros(batch, h_kv, k, dtype=torch.int32, device=DEV)
+    idx_t = torch.zeros_like(idx_f)
+    B.locks_score_select(q, st, sl, k, idx_f, ws_f)
+    n = batch * h_kv * G * max_pages
+    sc_t = ws_t[256:256 + 4 * n].view(torch.float32).view(
+        batch, h_kv, G, max_pages)
+    B.locks_score_pages(q, st, sl, sc_t, ws_t[:4].view(torch.int32))
+    B.locks_select_pages(sc_t, sl, G * h_kv, k, idx_t, ws_t)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws_f) == 0 and B.locks_read_status(ws_t) == 0
+    sc_f = ws_f[256:256 + 4 * n].view(torch.float32).view(sc_t.shape)
+    s_orc = O.score_store(wl.queries[0].float().numpy(), store, lens)
+    idx_o = O.select_store(s_orc, lens, k)
+    i_f, i_t = idx_f.cpu().numpy(), idx_t.cpu().numpy()
+    for b in range(batch):
+        nf = lens[b] // 16
+        assert torch.equal(sc_f[b, :, :, :nf], sc_t[b, :, :, :nf]), b
+        for h in range(h_kv):
+            for ig in (i_f, i_t):
+                ok, _ = selection_agrees(ig[b, h], idx_o[b, h], s_orc[b, h],
+                                         lens[b], k, 1e-3)
+                assert ok, (b, h, ig[b, h], idx_o[b, h])
+            v = [x for x in i_f[b, h] if x >= 0]
+            assert v == sorted(v) and len(set(v)) == len(v)
+            if set(i_f[b, h]) != set(i_t[b, h]):
+                ok, _ = selection_agrees(i_f[b, h], i_t[b, h], s_orc[b, h],
+                                         lens[b], k, 1e-3)
+                assert ok, (b, h)
+
+
 @pytest.mark.parametrize("G", [1, 4, 16])
 def test_select_normaliser_fallback(G):
     """Scores for which the normaliser's common reference (each head's
