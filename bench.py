@@ -201,13 +201,13 @@ def step_traffic(units, group):
         return None, f"captured at group size {d.get('group_size')}"
     out = {}
     for name, k in d["kernels"].items():
-        src = os.path.join(ROOT, "sparse_paged_kv_locks_gb300", "csrc",
-                           k["source"])
-        try:
-            if _sha256(src) != k["source_sha256"]:
-                return None, f"{k['source']} changed since its capture"
-        except OSError:
-            return None, f"{k['source']} missing"
+        for f in k["sources"]:
+            src = os.path.join(ROOT, "sparse_paged_kv_locks_gb300", "csrc", f)
+            try:
+                if _sha256(src) != k["source_sha256"][f]:
+                    return None, f"{f} changed since the {name} capture"
+            except OSError:
+                return None, f"{f} missing"
         out[name] = round(float(k["dram_bytes_per_unit"]) *
                           units[k["unit"]])
     return sum(out.values()), out
