@@ -165,20 +165,36 @@ locks_status_t locks_build_summaries_ex(
 /* Rank / precision variants of the page summary (LOCKS reading notes §6
  * ablation "rank and quantisation precision": int8, int4 and int2 bases at
  * several ranks).  A variant record of rank r in {4, 8, 12, 15} with a
- * basis of vbits in {2, 4, 8} bits holds, at byte offsets
- *   0                basis codes [128][r], element (d, k) at index d*r + k,
- *                    vbits bits each, packed little-endian from bit 0,
- *                    two's complement (qmax = 2^(vbits-1) - 1)
- *   16 r vbits       int8 C [16][r] row-major (c_i = row i)
- *   + 16 r           int8 mu [128]
- *   + 128            fp16 sV [r] (one scale per basis column)
- *   + 2 r            fp16 sC [16] (one scale per coefficient row)
- *   + 32             fp16 smu
- * and zero padding to a 16-byte stride.  Quantiser as the shipped record
- * (symmetric, fp16 scale = fp16_rn(absmax / qmax), codes rint(x / s)
- * clamped).  The shipped 832-byte record carries the same values as the
- * (r = 8, 4-bit) variant in its own tensor-core layout; variants are for
- * the ablation.
+ * basis of vbits in {2, 4, 8} bits is laid out, like the shipped record, so
+ * that each scoring lane finds its tensor-core fragments in aligned words;
+ * the (r = 8, 4-bit) variant record is the shipped 832-byte record, byte
+ * for byte.  With t = (d%8)/2, e = d%2, h = (d%16)/8, s = d/16 for head dim
+ * d, g = i%8 for token i, and C_OFF = 16 r vbits:
+ *   [0, C_OFF)  basis codes V[d][k]: the 32 codes of component k with the
+ *               same t form slot 4k + t (4*vbits bytes at 4*vbits*(4k + t));
+ *               inside the slot, as little-endian u32 words,
+ *                 vbits 4: word s/2, bit 16e + 8(s%2) + 4h, two's complement
+ *                 vbits 2: word s/4, bit 16e + 2(2(s%4) + h), two's complement
+ *                 vbits 8: byte 4s + 2h + e, excess-128 (byte = code + 128)
+ *   C_OFF       int8 C[i][k], excess-128, at C_OFF plus
+ *                 r <= 8: 4(g r/2 + k/2) + 2(i/8) + k%2            (16 r B)
+ *                 r = 15: 32g + 8t' + 4(i/8) + 2(k/8) + k%2       (256 B)
+ *                 r = 12: 24g + 8t' + 4(i/8) + 2(k/8) + k%2, but
+ *                         24g + 16 + 4(t'-2) + 2(i/8) + k%2 when t' >= 2
+ *                                                                 (192 B)
+ *               with t' = (k%8)/2; unused bytes hold code 0 (byte 128)
+ *   MU_OFF      int8 mu[128], excess-128, in the shipped record's order
+ *               (MU_OFF = C_OFF + coefficient bytes)
+ *   S_OFF       64-byte fp16 scale block (S_OFF = MU_OFF + 128): group t
+ *               (16 bytes at S_OFF + 16t) holds sV[2t], sV[2t+1], sC[2t],
+ *               sC[2t+1], sC[8+2t], sC[9+2t], then for r <= 8 sMU (group 0,
+ *               byte 12) and zeros, for r > 8 sV[8+2t], sV[9+2t] (sMU in the
+ *               sV[15] slot, byte 62); scales of absent components are 0
+ * Record stride S_OFF + 64: 384, 512, 768 (r 4); 576, 832, 1344 (r 8);
+ * 768, 1152, 1920 (r 12); 928, 1408, 2368 (r 15) bytes for 2-, 4-, 8-bit
+ * bases.  Quantiser as the shipped record (symmetric, fp16 scale =
+ * fp16_rn(absmax / qmax), qmax = 2^(vbits-1) - 1, codes rint(x / s)
+ * clamped).
  * locks_variant_record_bytes: the stride (0 for an unsupported pair). */
 size_t locks_variant_record_bytes(int rank, int vbits);
 
@@ -198,7 +214,9 @@ locks_status_t locks_build_variant(
  * layout of locks_score_pages (scores_out float [batch][h_kv][G][max_pages];
  * entries of pages that are not full are left untouched).  Feed them to
  * locks_select_pages for the variant's selection.  `records` must be
- * 16-byte aligned (LOCKS_ERR_INVALID_ARG otherwise). */
+ * 16-byte aligned (LOCKS_ERR_INVALID_ARG otherwise); batch is limited by
+ * the per-sequence tables kept on chip beside the record ring (about 1600
+ * sequences, LOCKS_ERR_UNSUPPORTED above). */
 locks_status_t locks_score_variant(const void *q, const void *records,
                                    int rank, int vbits,
                                    const int32_t *seq_lens, int batch,

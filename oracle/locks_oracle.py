@@ -221,62 +221,134 @@ def build_page_variant(keys_bf16_as_f32, r, vbits):
 
 def variant_layout(r, vbits):
     """Byte offsets of a variant record (include/locks.h, variant records):
-    basis codes [128][r] d-major, bit-packed little-endian; int8 C [16][r];
-    int8 mu [128]; fp16 sV [r], sC [16], smu; 16-byte stride."""
+    basis codes in per-(component, lane) slots; coefficient codes in the
+    order of the scorer's lanes (16 r bytes for r <= 8, 192 for r = 12,
+    256 for r = 15); the centroid codes; the 64-byte fp16 scale block.
+    `payload` counts the quantised summary's own bytes (codes and scales),
+    `stride` the record with its layout padding."""
     off = {"V": 0}
     off["C"] = 16 * r * vbits
-    off["MU"] = off["C"] + 16 * r
-    off["SV"] = off["MU"] + HEAD_DIM
-    off["SC"] = off["SV"] + 2 * r
-    off["SMU"] = off["SC"] + 2 * PAGE
-    off["payload"] = off["SMU"] + 2
-    off["stride"] = -(-off["payload"] // 16) * 16
+    off["MU"] = off["C"] + (16 * r if r <= 8 else 192 if r == 12 else 256)
+    off["S"] = off["MU"] + HEAD_DIM
+    off["SMU"] = off["S"] + (12 if r <= 8 else 62)
+    off["stride"] = off["S"] + 64
+    off["payload"] = 16 * r * vbits + 16 * r + HEAD_DIM + 2 * r + 2 * PAGE + 2
     return off
+
+
+def _variant_v_bits(r, vbits):
+    """First bit (within the record) of the basis code V[d][k], [128][r]:
+    slot 4k + t holds the 32 codes of dims 16s + 2t + e + 8h (t = (d%8)/2,
+    e = d%2, h = (d%16)/8, s = d/16) in 4*vbits bytes; inside the slot, a
+    4-bit code sits in word s/2 at bit 16e + 8(s%2) + 4h, a 2-bit code in
+    word s/4 at bit 16e + 2(2(s%4) + h), an 8-bit code in byte 4s + 2h + e."""
+    d = np.arange(HEAD_DIM)[:, None]
+    k = np.arange(r)[None, :]
+    t, e, h, s = (d % 8) // 2, d % 2, (d % 16) // 8, d // 16
+    base = 32 * vbits * (4 * k + t)
+    if vbits == 4:
+        inner = 32 * (s // 2) + 16 * e + 8 * (s % 2) + 4 * h
+    elif vbits == 2:
+        inner = 32 * (s // 4) + 16 * e + 2 * (2 * (s % 4) + h)
+    else:
+        inner = 8 * (4 * s + 2 * h + e)
+    return base + inner
+
+
+def _variant_c_offsets(r):
+    """Byte (within the coefficient region) of C[i][k], [16][r]: the word of
+    lane (g = i%8, t) of the scorer.  r <= 8: 4(g r/2 + k/2) + 2(i/8) + k%2;
+    r = 15: 32g + 8t + 4(i/8) + 2(k/8) + k%2 with t = (k%8)/2; r = 12: the
+    same with 24 bytes per g, except components 4..7, at
+    24g + 16 + 4(t-2) + 2(i/8) + k%2."""
+    i = np.arange(PAGE)[:, None]
+    k = np.arange(r)[None, :]
+    g, hi, t = i % 8, i // 8, (k % 8) // 2
+    if r <= 8:
+        return 4 * (g * (r // 2) + k // 2) + 2 * hi + k % 2
+    per = 24 if r == 12 else 32
+    main = per * g + 8 * t + 4 * hi + 2 * (k // 8) + k % 2
+    if r == 12:
+        main = np.where(t >= 2, 24 * g + 16 + 4 * (t - 2) + 2 * hi + k % 2,
+                        main)
+    return main
+
+
+def _variant_scale_offsets(r):
+    """Bytes (within the scale block) of sV[k] and sC[i]: group t (16 bytes)
+    holds sV[2t], sV[2t+1], sC[2t], sC[2t+1], sC[8+2t], sC[9+2t], and for
+    r > 8 sV[8+2t], sV[9+2t] in its last four bytes."""
+    k = np.arange(r)
+    sv = np.where(k < 8, 16 * (k // 2) + 2 * (k % 2),
+                  16 * ((k - 8) // 2) + 12 + 2 * (k % 2))
+    i = np.arange(PAGE)
+    sc = 16 * ((i % 8) // 2) + 4 + 2 * (i % 2) + 4 * (i // 8)
+    return sv, sc
 
 
 def encode_variant(q, r, vbits):
     off = variant_layout(r, vbits)
     Vq = np.asarray(q["Vq"], np.int64)
     lead = Vq.shape[:-2]
-    out = np.zeros(lead + (off["stride"],), np.uint8)
-    codes = (Vq.reshape(lead + (-1,)) & ((1 << vbits) - 1)).astype(np.uint64)
-    per = 8 // vbits
-    codes = codes.reshape(lead + (-1, per))
-    byte = np.zeros(lead + (codes.shape[-2],), np.uint64)
-    for t in range(per):
-        byte |= codes[..., t] << np.uint64(t * vbits)
-    out[..., off["V"]:off["C"]] = byte.astype(np.uint8)
-    out[..., off["C"]:off["MU"]] = np.asarray(q["C8"], np.int8).reshape(
-        lead + (-1,)).view(np.uint8)
-    out[..., off["MU"]:off["SV"]] = np.asarray(q["mu8"], np.int8).view(
-        np.uint8)
-    out[..., off["SV"]:off["SC"]] = np.ascontiguousarray(
-        np.asarray(q["sV"], np.float16)).view(np.uint8)
-    out[..., off["SC"]:off["SMU"]] = np.ascontiguousarray(
-        np.asarray(q["sC"], np.float16)).view(np.uint8)
-    out[..., off["SMU"]:off["payload"]] = np.ascontiguousarray(
-        np.asarray(q["smu"], np.float16)[..., None]).view(np.uint8)
-    return out
+    n = int(np.prod(lead)) if lead else 1
+    out = np.zeros((n, off["stride"]), np.uint8)
+    # basis codes: two's complement (2, 4 bits) or excess-128 (8 bits)
+    codes = Vq.reshape(n, HEAD_DIM * r)
+    codes = codes + 128 if vbits == 8 else codes & ((1 << vbits) - 1)
+    bits = _variant_v_bits(r, vbits).reshape(-1)
+    n_words = 4 * r * vbits
+    words = np.zeros((n, n_words), np.uint64)
+    for j in range(bits.size):       # codes never overlap inside a word
+        words[:, bits[j] // 32] |= (codes[:, j].astype(np.uint64)
+                                    << np.uint64(bits[j] % 32))
+    out[:, :off["C"]] = np.ascontiguousarray(words.astype("<u4")).view(
+        np.uint8).reshape(n, -1)
+    # coefficient and centroid codes, excess-128 (padding = code 0)
+    out[:, off["C"]:off["MU"]] = 128
+    c8 = (np.asarray(q["C8"], np.int16).reshape(n, PAGE * r) + 128)
+    out[:, off["C"] + _variant_c_offsets(r).reshape(-1)] = c8.astype(np.uint8)
+    mu8 = np.asarray(q["mu8"], np.int16).reshape(n, HEAD_DIM) + 128
+    out[:, off["MU"] + MU8_OFF - OFF_MU8] = mu8.astype(np.uint8)
+    sv_off, sc_off = _variant_scale_offsets(r)
+    for offs, key, cnt in ((off["S"] + sv_off, "sV", r),
+                           (off["S"] + sc_off, "sC", PAGE),
+                           (np.array([off["SMU"]]), "smu", 1)):
+        f16 = np.ascontiguousarray(np.asarray(q[key], np.float16).reshape(
+            n, cnt).astype("<f2")).view(np.uint8).reshape(n, cnt, 2)
+        out[:, offs] = f16[..., 0]
+        out[:, offs + 1] = f16[..., 1]
+    return out.reshape(lead + (off["stride"],))
 
 
 def decode_variant(rec, r, vbits):
     off = variant_layout(r, vbits)
     rec = np.ascontiguousarray(np.asarray(rec, np.uint8))
     lead = rec.shape[:-1]
-    byte = rec[..., off["V"]:off["C"]].astype(np.int64)
-    per = 8 // vbits
-    mask = (1 << vbits) - 1
-    codes = np.stack([(byte >> (t * vbits)) & mask for t in range(per)], -1)
-    codes = codes.reshape(lead + (HEAD_DIM, r))
-    codes = np.where(codes >= (1 << (vbits - 1)), codes - (1 << vbits), codes)
+    n = int(np.prod(lead)) if lead else 1
+    x = rec.reshape(n, off["stride"])
+    words = x[:, :off["C"]].copy().view("<u4").astype(np.int64)
+    bits = _variant_v_bits(r, vbits)
+    raw = (words[:, bits // 32] >> (bits % 32)) & ((1 << vbits) - 1)
+    if vbits == 8:
+        codes = raw - 128
+    else:
+        codes = np.where(raw >= (1 << (vbits - 1)), raw - (1 << vbits), raw)
+    C8 = x[:, off["C"] + _variant_c_offsets(r)].astype(np.int16) - 128
+    mu8 = x[:, off["MU"] + MU8_OFF - OFF_MU8].astype(np.int16) - 128
+    sv_off, sc_off = _variant_scale_offsets(r)
+
+    def halves(offs):
+        lo = x[:, offs].astype(np.uint16)
+        hi = x[:, offs + 1].astype(np.uint16)
+        return (lo | (hi << 8)).view(np.float16)
+    c = np.ascontiguousarray
     return dict(
-        Vq=codes.astype(np.int8),
-        C8=rec[..., off["C"]:off["MU"]].copy().view(np.int8).reshape(
-            lead + (PAGE, r)),
-        mu8=rec[..., off["MU"]:off["SV"]].copy().view(np.int8),
-        sV=rec[..., off["SV"]:off["SC"]].copy().view(np.float16),
-        sC=rec[..., off["SC"]:off["SMU"]].copy().view(np.float16),
-        smu=rec[..., off["SMU"]:off["payload"]].copy().view(np.float16)[..., 0],
+        Vq=c(codes.astype(np.int8).reshape(lead + (HEAD_DIM, r))),
+        C8=c(C8.astype(np.int8).reshape(lead + (PAGE, r))),
+        mu8=c(mu8.astype(np.int8).reshape(lead + (HEAD_DIM,))),
+        sV=c(halves(off["S"] + sv_off).reshape(lead + (r,))),
+        sC=c(halves(off["S"] + sc_off).reshape(lead + (PAGE,))),
+        smu=c(halves(np.array([off["SMU"]]))[:, 0].reshape(lead)),
         vbits=vbits)
 
 

@@ -23,7 +23,8 @@ LIBDIR = os.path.join(PKG, "lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIB = os.path.join(LIBDIR, "liblocks.so")
 SOURCES = ["api.cu", "build.cu", "score.cu", "select.cu", "decode.cu",
-           "exact.cu", "variant.cu", "noalloc.cu", "decoder.cu"]
+           "exact.cu", "variant.cu", "variant_b2.cu", "variant_b4.cu",
+           "variant_b8.cu", "noalloc.cu", "decoder.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -248,7 +248,7 @@ locks_status_t locks_score_variant(const void *q, const void *records,
   if (batch < 0 || max_pages < 1 || !heads_ok(h_q, h_kv))
     return LOCKS_ERR_INVALID_ARG;
   if (h_q / h_kv > kMaxGroup) return LOCKS_ERR_UNSUPPORTED;
-  if (batch > 65535 || h_kv > 65535 ||
+  if (batch > variant_max_batch(rank, vbits) || h_kv > 65535 ||
       (long long)max_pages * kPage > 0x7fffffffLL)
     return LOCKS_ERR_UNSUPPORTED;
   if (batch == 0) return LOCKS_OK;

@@ -19,6 +19,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "variant_layout.cuh"
 
 namespace locks {
 
@@ -746,21 +747,16 @@ __global__ void append_kernel(const __nv_bfloat16 *__restrict__ k_new,
 
 // --------------------------------------------------------------------------
 // rank / precision variants (notes §6 ablation): Algorithm 1 at rank R with
-// a `vbits`-bit basis, written as a variant record (include/locks.h):
-// basis codes [128][R] d-major, bit-packed little-endian; int8 C [16][R];
-// int8 mu; fp16 sV [R], sC [16], smu; zero padding to the 16-byte stride.
+// a `vbits`-bit basis, written as a variant record (variant_layout.cuh,
+// include/locks.h): codes are quantised per lane into shared memory, then
+// each lane assembles whole words of the fragment-ordered record.
 // --------------------------------------------------------------------------
 struct VariantSmem {
   float cv[16], cc[16];
   float Cf[16][16];
+  int8_t vq[kDim][16];  // basis codes [d][k]
+  int8_t cq[16][16];    // coefficient codes [i][k]
 };
-
-__device__ __forceinline__ int variant_payload(int r, int vbits) {
-  return 16 * r * vbits + 16 * r + kDim + 2 * r + 2 * kPage + 2;
-}
-__device__ __forceinline__ int variant_stride(int r, int vbits) {
-  return (variant_payload(r, vbits) + 15) / 16 * 16;
-}
 
 template <int R>
 __device__ float summarize_variant(const __nv_bfloat16 *page, BuildSmem &sm,
@@ -794,51 +790,41 @@ __device__ float summarize_variant(const __nv_bfloat16 *page, BuildSmem &sm,
     const int i = e / R, k = e - i * R;
     vs.Cf[i][k] = sm.post.U[i][sm.perm[k]] * vs.cc[k];
   }
+  const int off_c = var_off_c(R, vbits), off_mu = var_off_mu(R, vbits);
+  const int off_s = var_off_s(R, vbits);
+  // the scale block and the coefficient region start as zero scales and
+  // zero codes (excess-128), so padding entries are defined
+  for (int b = lane; b < 64; b += 32) rec[off_s + b] = 0;
+  for (int b = lane; b < var_coeff_bytes(R); b += 32) rec[off_c + b] = 128;
   __syncwarp();
-  const int off_c = 16 * R * vbits, off_mu = off_c + 16 * R;
-  const int off_sv = off_mu + kDim, off_sc = off_sv + 2 * R;
-  const int off_smu = off_sc + 2 * kPage;
   const float qv = (float)((1 << (vbits - 1)) - 1);
-  const uint32_t cmask = (1u << vbits) - 1u;
-  // basis: one scale per column; this lane's 4 dims x R codes are bits
-  // [4R vbits lane, 4R vbits (lane + 1)) of the code array
-  uint32_t acc = 0;
-  int nbits = 0, pos = lane * R * vbits / 2;
+  // basis: one scale per column; this lane's dims 4 lane .. 4 lane + 3
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int k = 0; k < R; ++k) {
+    float a = fmaxf(fmaxf(fabsf(V[0][k]), fabsf(V[1][k])),
+                    fmaxf(fabsf(V[2][k]), fabsf(V[3][k])));
+    a = warp_max(a);
+    const __half h = quant_scale(a, qv);
+    if (lane == k)
+      *reinterpret_cast<__half *>(rec + off_s + var_sv_off(k)) = h;
+    const float sc = __half2float(h);
 #pragma unroll
-    for (int k = 0; k < R; ++k) {
-      float a = 0.f;
-      if (j == 0) {  // scale of column k (same for every j)
-        a = fmaxf(fmaxf(fabsf(V[0][k]), fabsf(V[1][k])),
-                  fmaxf(fabsf(V[2][k]), fabsf(V[3][k])));
-        a = warp_max(a);
-        const __half h = quant_scale(a, qv);
-        if (lane == k) *reinterpret_cast<__half *>(rec + off_sv + 2 * k) = h;
-        vs.cv[k] = __half2float(h);  // reuse: per-column float scale
-      }
-      __syncwarp();
-      const int c = quant_code(V[j][k], vs.cv[k], (int)qv);
-      acc |= ((uint32_t)c & cmask) << nbits;
-      nbits += vbits;
-      if (nbits >= 8) {
-        rec[pos++] = (uint8_t)(acc & 0xFFu);
-        acc >>= 8;
-        nbits -= 8;
-      }
-    }
+    for (int j = 0; j < 4; ++j)
+      vs.vq[4 * lane + j][k] = (int8_t)quant_code(V[j][k], sc, (int)qv);
   }
-  // centroid: one scale, int8 codes
+  // centroid: one scale, int8 codes (excess-128)
   {
     float a = fmaxf(fmaxf(fabsf(mu[0]), fabsf(mu[1])),
                     fmaxf(fabsf(mu[2]), fabsf(mu[3])));
     a = warp_max(a);
     const __half h = quant_scale(a, 127.f);
     const float sc = __half2float(h);
-    if (lane == 0) *reinterpret_cast<__half *>(rec + off_smu) = h;
+    if (lane == 0)
+      *reinterpret_cast<__half *>(rec + var_off_smu(R, vbits)) = h;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      rec[off_mu + 4 * lane + j] = (uint8_t)(int8_t)quant_code(mu[j], sc, 127);
+      rec[off_mu + var_mu_off(4 * lane + j)] =
+          (uint8_t)(quant_code(mu[j], sc, 127) + 128);
   }
   // coefficients: one scale per row (token), int8 codes
   if (lane < 16) {
@@ -846,13 +832,33 @@ __device__ float summarize_variant(const __nv_bfloat16 *page, BuildSmem &sm,
     for (int k = 0; k < R; ++k) a = fmaxf(a, fabsf(vs.Cf[lane][k]));
     const __half h = quant_scale(a, 127.f);
     const float sc = __half2float(h);
-    *reinterpret_cast<__half *>(rec + off_sc + 2 * lane) = h;
-    for (int k = 0; k < R; ++k)
-      rec[off_c + lane * R + k] =
-          (uint8_t)(int8_t)quant_code(vs.Cf[lane][k], sc, 127);
+    *reinterpret_cast<__half *>(rec + off_s + var_sc_off(lane)) = h;
+    for (int k = 0; k < R; ++k) {
+      const int c = quant_code(vs.Cf[lane][k], sc, 127);
+      rec[off_c + var_c_off(R, lane, k)] = (uint8_t)(c + 128);
+    }
   }
-  const int pay = off_smu + 2, stride = variant_stride(R, vbits);
-  for (int b = pay + lane; b < stride; b += 32) rec[b] = 0;
+  __syncwarp();
+  // basis words: word wi of slot (k, t) = (wi / vbits) holds the codes of
+  // the dims var_v_bit places there
+  const uint32_t cmask = (1u << vbits) - 1u;
+  const int n_words = 4 * R * vbits;
+  for (int wi = lane; wi < n_words; wi += 32) {
+    const int slot = wi / vbits, w = wi - slot * vbits;
+    const int k = slot >> 2, t = slot & 3;
+    const int spw = 8 / vbits;  // k-steps per word
+    uint32_t word = 0;
+    for (int s = w * spw; s < (w + 1) * spw; ++s)
+      for (int e = 0; e < 2; ++e)
+        for (int h = 0; h < 2; ++h) {
+          const int d = 16 * s + 2 * t + e + 8 * h;
+          const int c = vs.vq[d][k];
+          const uint32_t u = vbits == 8 ? (uint32_t)(c + 128)
+                                        : (uint32_t)c & cmask;
+          word |= u << (var_v_bit(vbits, d, k) - 32 * wi);
+        }
+    reinterpret_cast<uint32_t *>(rec)[wi] = word;
+  }
   __syncwarp();
   return tau;
 }
@@ -869,7 +875,7 @@ __global__ void __launch_bounds__(32 * kBuildWarps, 4)
   __shared__ BuildSmem smem[kBuildWarps];
   __shared__ VariantSmem vsm[kBuildWarps];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const size_t stride = (size_t)variant_stride(R, vbits);
+  const size_t stride = (size_t)var_stride(R, vbits);
   const long long total = (long long)n_pairs * h_kv;
   for (long long w = (long long)blockIdx.x * kBuildWarps + wid; w < total;
        w += (long long)gridDim.x * kBuildWarps) {

@@ -154,7 +154,16 @@ cudaError_t launch_score_variant(const void *q, const void *records,
                                  int G, int max_pages, float *scores,
                                  int32_t *status, cudaStream_t stream);
 
+// the scorer of one basis width (variant_b2.cu, variant_b4.cu, variant_b8.cu)
+template <int VB>
+cudaError_t launch_variant_bits(int rank, const void *q, const void *records,
+                                const int32_t *seq_lens, int batch, int h_kv,
+                                int G, int max_pages, float *scores,
+                                int32_t *status, cudaStream_t stream);
+
 size_t variant_record_bytes(int rank, int vbits);
+// largest batch whose per-sequence tables fit beside the variant's ring
+int variant_max_batch(int rank, int vbits);
 
 int score_max_batch();
 int exact_max_batch();

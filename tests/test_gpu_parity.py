@@ -334,8 +334,8 @@ def test_exact_page_scores_match_oracle(G, h_kv):
 # rank / precision variants (notes §6 ablation)
 # ---------------------------------------------------------------------------
 def test_variant_r8_int4_build_equals_shipped_build():
-    """On the GPU, the (r = 8, 4-bit) variant record carries exactly the
-    shipped record's codes and scales (one eigensolver, one quantiser)."""
+    """On the GPU, the (r = 8, 4-bit) variant record is the shipped record
+    byte for byte (one eigensolver, one quantiser, one layout rule)."""
     wl = W.generate(W.SPECS["tiny_4k"], "cpu")
     d = Dev(wl)
     _, _, pt, lens = host(wl)
@@ -343,22 +343,17 @@ def test_variant_r8_int4_build_equals_shipped_build():
     batch, max_pages = pt.shape
     h_kv = d.k_cache.shape[1]
     var = B.new_variant_store(batch, h_kv, max_pages, 8, 4, DEV)
+    assert var.shape[-1] == store.shape[-1] == 832
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     B.locks_build_variant(d.k_cache, d.page_table, i32(seq), i32(pg), var, 8,
                           4, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    a = O.decode_records(store.cpu().numpy()[seq, :, pg])
-    v = O.decode_variant(var.cpu().numpy()[seq, :, pg], 8, 4)
-    assert (a["V4"] == v["Vq"]).all() and (a["C8"] == v["C8"]).all()
-    assert (a["mu8"] == v["mu8"]).all()
-    for key in ("sV", "sC", "smu"):
-        assert (np.asarray(a[key]).view(np.uint16) ==
-                np.asarray(v[key]).view(np.uint16)).all()
+    assert torch.equal(var[seq, :, pg], store[seq, :, pg])
 
 
-@pytest.mark.parametrize("rank,vbits", [(4, 2), (4, 8), (8, 2), (8, 8),
-                                        (12, 4), (15, 2), (15, 4), (15, 8)])
+@pytest.mark.parametrize("rank,vbits", [(r, b) for r in O.VARIANT_RANKS
+                                        for b in O.VARIANT_BITS])
 def test_variant_build_and_score_match_oracle(rank, vbits):
     wl = W.generate(W.SPECS["tiny_4k"], "cpu", steps=1)
     d = Dev(wl)
@@ -411,9 +406,18 @@ def test_variant_build_and_score_match_oracle(rank, vbits):
         assert (s_gpu[0, h, :, nf:] == 5.0).all()
 
 
-@pytest.mark.parametrize("G,h_kv,rank,vbits", [(1, 3, 4, 2), (3, 2, 8, 4),
-                                                (8, 1, 15, 8), (16, 1, 12, 2),
-                                                (4, 2, 15, 4)])
+# every (rank, head form) of the variant scorer: G <= 4 with ranks 4 and 8
+# pairs pages in the coefficient product, G <= 8 keeps heads in its rows,
+# G > 8 runs it per half of the heads; strides above 832 bytes take 4-page
+# tiles
+VARIANT_GROUP_CASES = [
+    (1, 3, 4, 2), (4, 2, 4, 4), (3, 2, 8, 4), (2, 1, 8, 8), (4, 2, 8, 2),
+    (8, 1, 4, 8), (6, 1, 4, 2), (8, 1, 8, 4), (5, 2, 8, 2), (4, 1, 12, 4),
+    (8, 1, 12, 8), (8, 1, 15, 8), (4, 2, 15, 4), (2, 2, 15, 2),
+    (16, 1, 12, 2), (12, 1, 4, 4), (9, 1, 8, 8), (16, 1, 15, 4)]
+
+
+@pytest.mark.parametrize("G,h_kv,rank,vbits", VARIANT_GROUP_CASES)
 def test_variant_score_group_sizes(G, h_kv, rank, vbits):
     """Variant scores from the oracle's own variant records at several
     group sizes, over enough pages for several CTAs and a ragged tail."""
@@ -446,6 +450,48 @@ def test_variant_score_group_sizes(G, h_kv, rank, vbits):
             ref = O.score_from_summaries(qn[b, h * G:(h + 1) * G],
                                          mu[sel, h], V[sel, h], C[sel, h])
             assert np.abs(s_gpu[b, h, :, pg[sel]].T - ref).max() <= S_TOL
+            assert (s_gpu[b, h, :, nf:] == 5.0).all()
+
+
+@pytest.mark.parametrize("G,rank,vbits", [(4, 8, 4), (8, 15, 8), (4, 4, 2)])
+def test_variant_score_many_tiles_per_warp(G, rank, vbits):
+    """More tiles than warps in the grid: every warp streams several tiles
+    across (sequence, KV head) boundaries through its double-buffered ring;
+    scores against the oracle's own records on sampled pages of every unit
+    and on every page of the last one."""
+    h_kv, n_pages = 8, 2600
+    lens = [16 * n_pages - 3, 16 * (n_pages // 2) + 8]
+    spec = W.custom_spec(batch=2, h_q=G * h_kv, h_kv=h_kv,
+                         ctx=16 * n_pages, k=8, needles=0, seed=90 + rank)
+    wl = W.generate(spec, "cpu", steps=1)
+    kc, _, pt, _ = host(wl)
+    batch, max_pages = pt.shape
+    seq, pg = full_pairs(lens)
+    seq, pg = np.asarray(seq), np.asarray(pg)
+    keys = kc[pt[seq, pg]]
+    qo, _ = O.build_page_variant(keys, rank, vbits)
+    recs = B.new_variant_store(batch, h_kv, max_pages, rank, vbits, DEV)
+    recs[torch.as_tensor(seq), :, torch.as_tensor(pg)] = torch.from_numpy(
+        O.encode_variant(qo, rank, vbits)).to(DEV)
+    q = wl.queries[0]
+    sc = torch.full((batch, h_kv, G, max_pages), 5.0, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.locks_score_variant(q.to(DEV), recs, rank, vbits, i32(lens), sc, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    mu, V, C = O.dequantize(qo)
+    qn = q.float().numpy()
+    s_gpu = sc.cpu().numpy()
+    rng = np.random.default_rng(rank)
+    for b in range(batch):
+        nf = lens[b] // 16
+        rows = np.flatnonzero(seq == b)
+        for h in range(h_kv):
+            pick = rows if (b, h) == (batch - 1, h_kv - 1) else \
+                np.sort(rng.choice(rows, 64, replace=False))
+            ref = O.score_from_summaries(qn[b, h * G:(h + 1) * G],
+                                         mu[pick, h], V[pick, h], C[pick, h])
+            assert np.abs(s_gpu[b, h, :, pg[pick]].T - ref).max() <= S_TOL
             assert (s_gpu[b, h, :, nf:] == 5.0).all()
 
 

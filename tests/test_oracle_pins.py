@@ -295,29 +295,93 @@ def test_share_average_maximises_group_coverage():
 
 
 def test_variant_record_bytes_by_hand():
-    """Variant record codec against bytes written out by hand: rank 4 with
-    a 2-bit basis packs the codes of dimension 0 (components 0..3) into byte
-    0, two bits each from the low end, two's complement."""
+    """Variant record codec against bytes worked out by hand from the
+    layout rule (include/locks.h, variant records): rank 4 with a 2-bit
+    basis puts the codes of dims 0, 8, 16, 24 of component 0 into byte 0
+    (two bits each: e = 0, h = 0/1, k-steps 0/1), dim 1 (e = 1) into byte 2,
+    component 1's slot 32 bytes further on; coefficients go by scorer lane,
+    centroid codes in the shipped order, scales in the 64-byte block."""
     r, vb = 4, 2
     off = O.variant_layout(r, vb)
-    assert (off["C"], off["MU"], off["SV"], off["SC"], off["SMU"],
-            off["payload"], off["stride"]) == (128, 192, 320, 328, 360, 362,
-                                               368)
+    assert (off["C"], off["MU"], off["S"], off["SMU"], off["payload"],
+            off["stride"]) == (128, 192, 320, 332, 362, 384)
     Vq = np.zeros((128, r), np.int8)
-    Vq[0] = [1, -1, 0, 1]          # 0b01, 0b11, 0b00, 0b01
-    Vq[1] = [-1, -1, -1, -1]       # all 0b11
+    Vq[0] = [1, -1, 0, 1]      # 0b01, 0b11, 0b00, 0b01
+    Vq[8, 0] = -1              # 0b11 at bits 2-3 of byte 0
+    Vq[16, 0] = 1              # 0b01 at bits 4-5
+    Vq[1, 0] = -2              # 0b10 at bits 0-1 of byte 2
+    Vq[64, 0] = 1              # k-step 4: second word of the slot, byte 4
+    Vq[2, 0] = -1              # t = 1: the next slot, byte 8
     q = dict(Vq=Vq, C8=np.arange(-32, 32, dtype=np.int8).reshape(16, r),
              mu8=np.full(128, -3, np.int8),
              sV=np.array([1, 2, 0.5, 0.25], np.float16),
-             sC=np.full(16, 0.125, np.float16), smu=np.float16(3.0))
+             sC=np.arange(16, dtype=np.float16) / 8,
+             smu=np.float16(3.0))
     rec = O.encode_variant(q, r, vb)
-    assert rec[0] == 0b01001101 and rec[1] == 0xFF and rec[2] == 0
-    assert rec[128] == 256 - 32 and rec[129] == 256 - 31     # C8 row 0
-    assert rec[192] == 253                                    # mu8[0] = -3
-    assert rec[320:322].tobytes() == np.float16(1).tobytes()  # sV[0]
-    assert rec[360:362].tobytes() == np.float16(3).tobytes()  # smu
+    assert rec[0] == 0b00011101 and rec[2] == 0b10 and rec[4] == 1
+    assert rec[8] == 0b11 and rec[32] == 0b11 and rec[64] == 0
+    assert rec[96] == 1
+    # C[0][0..2], C[8][0], C[1][0] (excess-128)
+    assert (rec[128], rec[129], rec[132], rec[130], rec[136]) == (
+        96, 97, 98, 128, 100)
+    assert (rec[192:320] == 125).all()                        # mu = -3
+    f16 = lambda x: np.float16(x).tobytes()
+    assert rec[320:322].tobytes() == f16(1)                   # sV[0]
+    assert rec[336:338].tobytes() == f16(0.5)                 # sV[2]
+    assert rec[324:326].tobytes() == f16(0)                   # sC[0]
+    assert rec[328:330].tobytes() == f16(1)                   # sC[8]
+    assert rec[340:342].tobytes() == f16(0.25)                # sC[2]
+    assert rec[332:334].tobytes() == f16(3)                   # smu
     d = O.decode_variant(rec, r, vb)
-    assert (d["Vq"] == Vq).all() and (d["C8"] == q["C8"]).all()
+    for key in ("Vq", "C8", "mu8"):
+        assert (d[key] == q[key]).all()
+    assert (d["sC"] == q["sC"]).all() and d["smu"] == q["smu"]
+
+    # rank 15, 8-bit basis: one byte per code (excess-128), 32 bytes of
+    # coefficients per lane row g, sV[8..14] in the groups' last bytes
+    r, vb = 15, 8
+    off = O.variant_layout(r, vb)
+    assert (off["C"], off["MU"], off["S"], off["SMU"], off["stride"]) == (
+        1920, 2176, 2304, 2366, 2368)
+    Vq = np.zeros((128, r), np.int8)
+    Vq[0, 0], Vq[1, 0], Vq[8, 0], Vq[16, 0], Vq[2, 0] = 5, 6, 7, 8, 9
+    Vq[0, 14] = -127
+    C8 = np.zeros((16, r), np.int8)
+    C8[0, 14], C8[9, 9] = 11, -12
+    q = dict(Vq=Vq, C8=C8, mu8=np.zeros(128, np.int8),
+             sV=np.arange(1, 16, dtype=np.float16),
+             sC=np.ones(16, np.float16), smu=np.float16(0.5))
+    rec = O.encode_variant(q, r, vb)
+    assert (rec[0], rec[1], rec[2], rec[4], rec[32], rec[1792]) == (
+        133, 134, 135, 136, 137, 1)
+    assert rec[1920 + 26] == 139 and rec[1920 + 39] == 116
+    assert rec[1920 + 27] == 128                   # component 15: padding
+    assert rec[2364:2366].tobytes() == f16(15)     # sV[14]
+    assert rec[2318:2320].tobytes() == f16(10)     # sV[9]
+    assert rec[2366:2368].tobytes() == f16(0.5)    # smu
+    d = O.decode_variant(rec, r, vb)
+    assert (d["Vq"] == Vq).all() and (d["C8"] == C8).all()
+    assert (d["sV"] == q["sV"]).all()
+
+    # rank 12, 4-bit basis: components 4..7 of a coefficient row share one
+    # word per lane for both tokens g and g + 8
+    r, vb = 12, 4
+    off = O.variant_layout(r, vb)
+    assert (off["C"], off["MU"], off["S"], off["SMU"], off["stride"]) == (
+        768, 960, 1088, 1150, 1152)
+    Vq = np.zeros((128, r), np.int8)
+    Vq[0, 0], Vq[8, 0], Vq[16, 0], Vq[1, 0] = 3, -2, -7, 1
+    C8 = np.zeros((16, r), np.int8)
+    C8[8, 6], C8[3, 9] = 21, -22
+    q = dict(Vq=Vq, C8=C8, mu8=np.zeros(128, np.int8),
+             sV=np.ones(r, np.float16), sC=np.ones(16, np.float16),
+             smu=np.float16(1))
+    rec = O.encode_variant(q, r, vb)
+    # byte 0: dim 0 low nibble, dim 8 (h = 1) high nibble; byte 1: dim 16
+    assert rec[0] == 0x3 | (0xE << 4) and rec[1] == 0x9 and rec[2] == 1
+    assert rec[768 + 22] == 149 and rec[768 + 75] == 106
+    d = O.decode_variant(rec, r, vb)
+    assert (d["Vq"] == Vq).all() and (d["C8"] == C8).all()
 
 
 def test_variant_r8_int4_is_the_shipped_summary():
@@ -333,6 +397,8 @@ def test_variant_r8_int4_is_the_shipped_summary():
     for a in ("sV", "sC", "smu"):
         assert (np.asarray(q8[a]).view(np.uint16) ==
                 np.asarray(qv[a]).view(np.uint16)).all()
+    # the (8, 4) variant record is the shipped record, byte for byte
+    assert np.array_equal(O.encode_variant(qv, 8, 4), O.encode_records(q8))
     qh = rng.normal(size=(4, 128))
     rec = O.decode_variant(O.encode_variant(qv, 8, 4), 8, 4)
     assert np.array_equal(O.score_from_summaries(qh, *O.dequantize(q8)),
