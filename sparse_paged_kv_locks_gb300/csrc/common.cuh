@@ -56,6 +56,29 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block,
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// launch_pdl with thread-block clusters of `cluster` CTAs along x
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid,
+                                      dim3 block, size_t smem,
+                                      cudaStream_t stream, int cluster,
+                                      Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------------------
 // quantiser (storage paragraph of §4.1): symmetric, fp16 scale
 // ---------------------------------------------------------------------------
@@ -200,6 +223,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank) {
 }
 __device__ __forceinline__ void st_cluster_u32(uint32_t a, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;\n" ::"r"(a), "r"(v)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t a, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(a),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
 __device__ __forceinline__ void st_cluster_f32(uint32_t a, float v) {

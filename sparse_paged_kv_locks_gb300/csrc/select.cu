@@ -82,7 +82,12 @@ __device__ __forceinline__ void load_quad(const float *sc, int max_pages,
 // MINB: resident CTAs per SM the registers are sized for.  2 when there are
 // more (sequence, KV head) units than SMs; 1 when every unit has an SM of
 // its own, which leaves registers for more pages in flight per thread.
-template <bool SMEM_KEYS, int GT, int MINB>
+// CL > 1: a thread-block cluster of CL CTAs per unit (few units): each CTA
+// takes 1/CL of the unit's pages through the normaliser and key passes, the
+// per-head sums are merged through distributed shared memory in rank order
+// (the same Z_g in every CTA), the keys go to CTA 0's shared memory and
+// CTA 0 selects.
+template <bool SMEM_KEYS, int GT, int MINB, int CL = 1>
 __global__ void __launch_bounds__(kSelThreads, MINB)
     select_kernel(const float *__restrict__ scores,
                   const int32_t *__restrict__ seq_lens, int h_kv, int G,
@@ -95,8 +100,14 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
   __shared__ __align__(16) SelectScratch sel;
   __shared__ uint32_t red_u[2][32];
   __shared__ int sh_slow;
+  // CL > 1: this CTA's per-head sums (fast and general normaliser forms)
+  // and, in CTA 0, every rank's (kmin, kmax)
+  __shared__ float c_s[kMaxGroup], c_m2[kMaxGroup], c_s2[kMaxGroup];
+  __shared__ uint32_t c_kmm[2][CL];
+  static_assert(!(CL > 1) || SMEM_KEYS, "clusters keep the keys on chip");
 
-  const int b = blockIdx.y, h = blockIdx.x;
+  const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
+  const int b = blockIdx.y, h = CL > 1 ? (int)blockIdx.x / CL : blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   constexpr int nwarps = kSelThreads / 32;
   pdl_trigger();
@@ -109,11 +120,12 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
   int32_t *out = idx + ((size_t)b * h_kv + h) * k;
   pdl_wait();  // scores of the scoring kernel; idx may still be read before
   if (n <= k) {
-    for (int i = tid; i < k; i += blockDim.x) out[i] = i < n ? i : -1;
+    if (rank == 0)
+      for (int i = tid; i < k; i += blockDim.x) out[i] = i < n ? i : -1;
     return;
   }
   if (k == 2) {  // only the sink and the recent page
-    if (tid == 0) {
+    if (tid == 0 && rank == 0) {
       out[0] = 0;
       out[1] = n - 1;
     }
@@ -129,6 +141,10 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
                    ((reinterpret_cast<uintptr_t>(scores) & 15u) == 0);
   const bool kvec = SMEM_KEYS || (max_pages & 3) == 0;  // 16-byte key rows
   const int nq = (n + 3) >> 2;        // quads of pages covering [0, n)
+  // this CTA's quads [qa, qb) (the whole unit when CL = 1)
+  const int qper = (nq + CL - 1) / CL;
+  const int qa = min(nq, rank * qper), qb = min(nq, qa + qper);
+  const int nlim = min(nf, 4 * qb);   // summarised pages of this CTA's range
   // quads a thread has in flight at once (what the registers allow)
   // (at two CTAs per SM and G = 4 a second quad in flight measured slower,
   // 16.6 against 16.2 us on 256 units, and spilled)
@@ -155,11 +171,11 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
     float s[GT];
 #pragma unroll
     for (int g = 0; g < GT; ++g) s[g] = 0.f;
-    for (int qd = tid; qd < nq; qd += R * blockDim.x) {
+    for (int qd = qa + tid; qd < qb; qd += R * blockDim.x) {
       float x[R][GT][4];
 #pragma unroll
       for (int r = 0; r < R; ++r)
-        load_quad<GT>(sc, max_pages, G, vec, 4 * (qd + r * blockDim.x), nf,
+        load_quad<GT>(sc, max_pages, G, vec, 4 * (qd + r * blockDim.x), nlim,
                       -INFINITY, x[r]);
 #pragma unroll
       for (int r = 0; r < R; ++r)
@@ -178,9 +194,19 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
       if (lane == 0) red_s[wid][g] = sg;
     }
     __syncthreads();
-    if (tid < G) {
-      float sum = 0.f;
+    float sum = 0.f;
+    if (tid < G)
       for (int w = 0; w < nwarps; ++w) sum += red_s[w][tid];
+    if constexpr (CL > 1) {  // the cluster's sums, in rank order
+      if (tid < G) c_s[tid] = sum;
+      cluster_sync();
+      if (tid < G) {
+        sum = 0.f;
+        for (int c = 0; c < CL; ++c)
+          sum += ld_cluster_f32(mapa_shared(smem_u32(&c_s[tid]), c));
+      }
+    }
+    if (tid < G) {
       zs[tid] = __ldg(sc + (size_t)tid * max_pages) * kLog2e + lg2_fast(sum);
       if (!(sum < INFINITY)) sh_slow = 1;
     }
@@ -198,11 +224,11 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
     // (and the sum rescaled) only when a quad's maximum passes it by more
     // than 2^6, so the common step is one exponential per score; terms stay
     // below 2^64 and the sum below 2^77.
-    for (int qd = tid; qd < nq; qd += R * blockDim.x) {
+    for (int qd = qa + tid; qd < qb; qd += R * blockDim.x) {
       float x[R][GT][4];
 #pragma unroll
       for (int r = 0; r < R; ++r)
-        load_quad<GT>(sc, max_pages, G, vec, 4 * (qd + r * blockDim.x), nf,
+        load_quad<GT>(sc, max_pages, G, vec, 4 * (qd + r * blockDim.x), nlim,
                       -INFINITY, x[r]);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
@@ -241,15 +267,34 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
     }
   }
   __syncthreads();
+  float m = -INFINITY, s = 0.f;
   if (tid < G) {
-    float m = -INFINITY;
     for (int w = 0; w < nwarps; ++w) m = fmaxf(m, red_m[w][tid]);
-    float s = 0.f;
     for (int w = 0; w < nwarps; ++w)
       if (red_m[w][tid] != -INFINITY)
         s += red_s[w][tid] * ex2_fast(red_m[w][tid] - m);
-    zs[tid] = m + lg2_fast(s);
   }
+  if constexpr (CL > 1) {  // the cluster's (m, s) pairs, in rank order
+    if (tid < G) {
+      c_m2[tid] = m;
+      c_s2[tid] = s;
+    }
+    cluster_sync();
+    if (tid < G) {
+      m = -INFINITY;
+      s = 0.f;
+      for (int c = 0; c < CL; ++c) {
+        const float m2 = ld_cluster_f32(mapa_shared(smem_u32(&c_m2[tid]), c));
+        const float s2 = ld_cluster_f32(mapa_shared(smem_u32(&c_s2[tid]), c));
+        const float mm = fmaxf(m, m2);
+        if (mm == -INFINITY) continue;
+        s = (m == -INFINITY ? 0.f : s * ex2_fast(m - mm)) +
+            (m2 == -INFINITY ? 0.f : s2 * ex2_fast(m2 - mm));
+        m = mm;
+      }
+    }
+  }
+  if (tid < G) zs[tid] = m + lg2_fast(s);
   __syncthreads();
   }
   } else {
@@ -268,9 +313,9 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
   // last block of quads first: the normaliser pass just read them, so the
   // part of the scores still in L1 is read before it is evicted
   const int qstep = R * blockDim.x;
-  for (int it = (nq + qstep - 1) / qstep - 1; it >= 0; --it) {
-    const int qd = it * qstep + tid;
-    if (qd >= nq) continue;
+  for (int it = (qb - qa + qstep - 1) / qstep - 1; it >= 0; --it) {
+    const int qd = qa + it * qstep + tid;
+    if (qd >= qb) continue;
     float x[R][GT][4];
     // heads at or above G read -inf: no term, no maximum
 #pragma unroll
@@ -280,7 +325,7 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int j0 = 4 * (qd + r * blockDim.x);
-      if (j0 >= 4 * nq) break;
+      if (j0 >= 4 * qb) break;
       uint32_t kq[4];
       float key[4];
       if (rule == LOCKS_MERGE_GROUP_MAX) {
@@ -322,7 +367,10 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
         kmin = min(kmin, cand ? kq[u] : 0xffffffffu);
         kmax = max(kmax, kq[u]);
       }
-      if (kvec) {
+      if (CL > 1) {  // into CTA 0's key array
+        st_cluster_v4(mapa_shared(smem_u32(keys + j0), 0),
+                      make_uint4(kq[0], kq[1], kq[2], kq[3]));
+      } else if (kvec) {
         *reinterpret_cast<uint4 *>(keys + j0) =
             make_uint4(kq[0], kq[1], kq[2], kq[3]);
       } else {
@@ -349,6 +397,19 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
       z = max(z, red_u[1][w]);
     }
   }
+  if constexpr (CL > 1) {
+    if (tid == 0) {
+      st_cluster_u32(mapa_shared(smem_u32(&c_kmm[0][rank]), 0), a);
+      st_cluster_u32(mapa_shared(smem_u32(&c_kmm[1][rank]), 0), z);
+    }
+    cluster_sync();  // CTA 0 holds every key and every rank's bounds
+    if (rank != 0) return;
+    if (tid == 0)
+      for (int c = 0; c < CL; ++c) {
+        a = min(a, c_kmm[0][c]);
+        z = max(z, c_kmm[1][c]);
+      }
+  }
   select_top<SMEM_KEYS, nwarps>(keys, kvec, n, k, a, z, out, status, sel);
 }
 
@@ -356,6 +417,22 @@ __global__ void __launch_bounds__(kSelThreads, MINB)
 // launcher
 // --------------------------------------------------------------------------
 constexpr int kSelSmemKeys = 32 * 1024;   // candidate keys held on chip
+
+// CTAs per (sequence, KV head) unit: 4 or 2 when that many clusters fit the
+// SMs in one wave and the lists are long, else 1.  Measured on GB300 (graph
+// replay): 64 units of 8,208 pages at G = 8, 15.6 -> 14.0 us with clusters
+// of 2; 64 units of 2,048 pages at G = 4, 7.4 -> 8.2 us (the cluster
+// barriers and the remote key stores cost more than the halved passes save),
+// hence the 4,096-page floor.
+constexpr int kSelClusterMinPages = 4096;
+
+int select_cluster_size(long long units, int max_pages) {
+  const int sms = device_sm_count();
+  if (max_pages < kSelClusterMinPages) return 1;
+  if (units * 4 <= sms) return 4;
+  if (units * 2 <= sms) return 2;
+  return 1;
+}
 
 cudaError_t launch_select(const float *scores, const int32_t *seq_lens,
                           int batch, int h_kv, int G, int max_pages, int k,
@@ -374,7 +451,32 @@ cudaError_t launch_select(const float *scores, const int32_t *seq_lens,
   };
   const int gt = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : G <= 8 ? 8 : 16;
   // one CTA per SM suffices when the units fit the GPU in one wave
-  const bool own_sm = (long long)batch * h_kv <= device_sm_count();
+  const long long units = (long long)batch * h_kv;
+  const bool own_sm = units <= device_sm_count();
+  // with few units, a cluster of CTAs per unit shares its passes
+  const int cl = on_chip ? select_cluster_size(units, max_pages) : 1;
+  if (cl > 1) {
+    auto run_cl = [&](auto kern) -> cudaError_t {
+      cudaError_t e = cudaFuncSetAttribute(
+          kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmemKeys * 4);
+      if (e != cudaSuccess) return e;
+      return launch_pdl_cluster(kern, dim3(h_kv * cl, batch),
+                                dim3(kSelThreads), smem, stream, cl, scores,
+                                seq_lens, h_kv, G, max_pages, k, rule, idx,
+                                keybuf, status);
+    };
+#define LOCKS_SELECT_CL(C)                                   \
+  switch (gt) {                                              \
+    case 1: return run_cl(select_kernel<true, 1, 1, C>);     \
+    case 2: return run_cl(select_kernel<true, 2, 1, C>);     \
+    case 4: return run_cl(select_kernel<true, 4, 1, C>);     \
+    case 8: return run_cl(select_kernel<true, 8, 1, C>);     \
+    default: return run_cl(select_kernel<true, 16, 1, C>);   \
+  }
+    if (cl == 4) LOCKS_SELECT_CL(4)
+    LOCKS_SELECT_CL(2)
+#undef LOCKS_SELECT_CL
+  }
   // G > 8 always runs the one-CTA-per-SM form: with two per SM its
   // registers spill (on 256 units of 8,192 pages, 74 us against 50 us)
 #define LOCKS_SELECT_CASES(SK, MB)                         \

@@ -622,6 +622,77 @@ def test_select_normaliser_fallback(G):
     assert 5 in ig[2, 1]
 
 
+# Few units of at least 4,096 pages take the selection's cluster form (4 or
+# 2 CTAs per unit, the passes split by page range, the normaliser's sums
+# merged across the cluster, CTA 0 selecting): every head-count width, the
+# three merge rules, the normaliser's fallback form, k = 2, ragged and empty
+# lists, page counts that split unevenly; one case below the floor.
+SELECT_CLUSTER_CASES = [
+    (1, 2, 3, 4100, 40, "share_average", False),
+    (2, 4, 4, 4096, 16, "group_max", False),
+    (4, 8, 9, 8192, 128, "share_average", False),
+    (2, 8, 5, 4500, 50, "group_mass", False),
+    (8, 4, 3, 4097, 128, "group_mass", False),
+    (16, 1, 5, 5030, 20, "share_average", False),
+    (4, 2, 3, 4777, 30, "share_average", True),
+    (8, 1, 3, 4900, 25, "group_max", True),
+    (3, 2, 2, 4099, 2, "share_average", False),
+    (4, 8, 8, 2048, 64, "share_average", False),
+]
+
+
+@pytest.mark.parametrize("G,h_kv,batch,max_pages,k,rule,extreme",
+                         SELECT_CLUSTER_CASES)
+def test_select_cluster_forms(G, h_kv, batch, max_pages, k, rule, extreme):
+    rng = np.random.default_rng(500 + G * 11 + max_pages)
+    lens = [int(x) for x in rng.integers(16 * k, 16 * max_pages + 1, batch)]
+    lens[0] = 16 * max_pages
+    if batch > 2:
+        lens[1] = 16 * (max_pages - 3) + 5       # partial last page
+        lens[2] = 16 * (k - 1)                   # fewer pages than k
+    if batch > 4:
+        lens[4] = 0
+    scores = (rng.normal(0, 3, (batch, h_kv, G, max_pages)) +
+              rng.normal(0, 4, (batch, h_kv, 1, max_pages))).astype(np.float32)
+    if extreme:  # the normaliser's common reference does not serve
+        scores[0, 0, :, 0] = -np.inf
+        scores[0, h_kv - 1, :, 0] = -200.0
+        scores[1, 0, 0, 7] = 95.0
+        scores[1, :, :, max_pages - 40] = 60.0
+    sd = torch.from_numpy(scores).to(DEV)
+    ws = B.new_workspace(batch, h_kv * G, h_kv, max_pages, k, DEV)
+    idx = torch.zeros(batch, h_kv, k, dtype=torch.int32, device=DEV)
+    B.locks_select_pages_merge(sd, i32(lens), h_kv * G, k, rule, idx, ws)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == 0
+    ig = idx.cpu().numpy()
+    s64 = scores.astype(np.float64)
+    for b in range(batch):
+        n = -(-lens[b] // 16)
+        for h in range(h_kv):
+            row = [int(x) for x in ig[b, h]]
+            valid = [x for x in row if x >= 0]
+            assert valid == sorted(valid) and len(set(valid)) == len(valid)
+            want = set(O.select_one_rule(s64[b, h], lens[b], k, rule))
+            got = set(valid)
+            if n <= k:
+                assert row == list(range(n)) + [-1] * (k - n), (b, h)
+                continue
+            if got == want:
+                continue
+            nf = lens[b] // 16
+            lk = O.merge_key(s64[b, h], nf, rule)
+            lk = lk if rule == "group_mass" else np.log(lk)
+            cand = np.arange(1, n - 1)
+            order = cand[np.lexsort((cand, -lk[cand]))]
+            edge = lk[order[k - 3]]
+            for p in got ^ want:
+                assert p not in (0, n - 1) and abs(lk[p] - edge) <= 1e-4, \
+                    (rule, b, h, p)
+    if extreme:
+        assert 7 in ig[1, 0] or rule == "group_max"
+
+
 # ---------------------------------------------------------------------------
 # sparse attention over the oracle's selection
 # ---------------------------------------------------------------------------
