@@ -31,6 +31,10 @@ constexpr int kDecRing = kDecWarps * kDecStages * 2 * kKvTile;      // 64 KB
 // resident CTAs per SM the register budget is sized for (G > 8 keeps a
 // second row of accumulators and takes two)
 constexpr int kDecMinBlocks = 3;
+// Sparse decode: fewest list positions per warp.  Graph-replayed decode +
+// merge on GB300: 64 units x 128 pages (G = 8) 17.5 -> 14.0 us, 64 x 64
+// (G = 4) 11.6 -> 10.5 us; 256 x 128 unchanged (already above 8 per warp).
+constexpr int kDecMinRun = 8;
 constexpr float kDecScale = 0.12751743074602467f;  // log2(e)/sqrt(d)
 constexpr float kLn2f = 0.69314718055994531f;
 
@@ -562,6 +566,14 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
       });
   long long warps = (long long)blocks_per_sm * device_sm_count() * kDecWarps;
   if (warps > max_warps) warps = max_warps;
+  if (idx) {
+    // at least kDecMinRun list positions per warp, so that a unit is split
+    // into fewer pieces for the merge, unless that leaves fewer than two
+    // warps per SM
+    long long cap = ((long long)batch * h_kv * k + kDecMinRun - 1) / kDecMinRun;
+    if (cap < 2LL * device_sm_count()) cap = 2LL * device_sm_count();
+    if (warps > cap) warps = cap;
+  }
   if (warps < 1) warps = 1;
   const int n_warps = (int)warps;
   const int grid = (n_warps + kDecWarps - 1) / kDecWarps;
