@@ -114,6 +114,13 @@ const char *locks_status_string(locks_status_t s);
 /* cudaError_t of the last failing CUDA call in this thread (0 if none). */
 int locks_last_cuda_error(void);
 
+/* Kernels this process has launched through the library: every kernel
+ * launch call (including one recorded into a stream capture) plus, for
+ * every replay of a decoder's graph (locks_decoder_step_host), the kernels
+ * the graph holds.  Monotone; read it before and after a region to count
+ * the region's launches. */
+long long locks_kernel_launches(void);
+
 /* Bytes per summary record (832: 818 B payload + 14 B padding). */
 size_t locks_summary_record_bytes(void);
 

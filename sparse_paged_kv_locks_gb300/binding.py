@@ -47,6 +47,7 @@ _SZ = ctypes.c_size_t
 _SIGS = {
     "locks_status_string": (ctypes.c_char_p, [_I]),
     "locks_last_cuda_error": (_I, []),
+    "locks_kernel_launches": (_I64, []),
     "locks_summary_record_bytes": (_SZ, []),
     "locks_workspace_size": (_I, [_I, _I, _I, _I, _I,
                                   ctypes.POINTER(_SZ)]),
@@ -148,6 +149,11 @@ def _req(t, name, dtype, ndim=None, device="cuda"):
 # ---------------------------------------------------------------------------
 def locks_summary_record_bytes() -> int:
     return int(lib().locks_summary_record_bytes())
+
+
+def locks_kernel_launches() -> int:
+    """Kernels this process has launched through the library so far."""
+    return int(lib().locks_kernel_launches())
 
 
 def locks_workspace_size(batch, h_q, h_kv, max_pages, k) -> int:

@@ -8,6 +8,10 @@
 
 using namespace locks;
 
+namespace locks {
+std::atomic<long long> g_kernel_launches{0};
+}
+
 static thread_local int g_last_cuda = 0;
 
 static locks_status_t fail_cuda(cudaError_t e) {
@@ -160,6 +164,10 @@ const char *locks_status_string(locks_status_t s) {
 }
 
 int locks_last_cuda_error(void) { return g_last_cuda; }
+
+long long locks_kernel_launches(void) {
+  return g_kernel_launches.load(std::memory_order_relaxed);
+}
 
 size_t locks_summary_record_bytes(void) { return (size_t)kRec; }
 

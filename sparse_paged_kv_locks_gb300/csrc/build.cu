@@ -920,7 +920,7 @@ cudaError_t launch_build(const void *k_cache, int64_t num_phys, int h_kv,
       static_cast<const __nv_bfloat16 *>(k_cache), num_phys, h_kv, pt, batch,
       max_pages, seq_ids, page_ids, n_pairs,
       static_cast<uint8_t *>(summaries), tau_out, unq_out, flags, status);
-  return cudaGetLastError();
+  return launched();
 }
 
 cudaError_t launch_build_variant(const void *k_cache, int64_t num_phys,
@@ -947,7 +947,7 @@ cudaError_t launch_build_variant(const void *k_cache, int64_t num_phys,
     default: return cudaErrorInvalidValue;
   }
 #undef LOCKS_BUILD_VARIANT
-  return cudaGetLastError();
+  return launched();
 }
 
 cudaError_t launch_pack(const float *mu, const float *basis,
@@ -956,7 +956,7 @@ cudaError_t launch_pack(const float *mu, const float *basis,
   if (n == 0) return cudaSuccess;
   pack_kernel<<<grid_for(n, kBuildWarps), 32 * kBuildWarps, 0, stream>>>(
       mu, basis, coeffs, n, static_cast<uint8_t *>(records), flags);
-  return cudaGetLastError();
+  return launched();
 }
 
 cudaError_t launch_append(const void *k_new, const void *v_new, void *k_cache,
@@ -979,7 +979,7 @@ cudaError_t launch_append(const void *k_new, const void *v_new, void *k_cache,
       static_cast<__nv_bfloat16 *>(k_cache),
       static_cast<__nv_bfloat16 *>(v_cache), num_phys, h_kv, pt, max_pages,
       seq_lens, static_cast<uint8_t *>(summaries), tau_out, flags, status);
-  return cudaGetLastError();
+  return launched();
 }
 
 }  // namespace locks

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "locks.h"
 
 namespace locks {
@@ -39,6 +41,19 @@ __device__ __forceinline__ void pdl_trigger() {
 }
 
 // Launch with programmatic stream serialisation allowed (host side).
+// kernels this process launched through the library (api.cu; read by
+// locks_kernel_launches)
+extern std::atomic<long long> g_kernel_launches;
+inline void note_launches(long long n = 1) {
+  g_kernel_launches.fetch_add(n, std::memory_order_relaxed);
+}
+// after a <<<...>>> launch: its error, counting it when it succeeded
+inline cudaError_t launched() {
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launches();
+  return e;
+}
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block,
                               size_t smem, cudaStream_t stream,
@@ -53,7 +68,10 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  if (e == cudaSuccess) note_launches();
+  return e;
 }
 
 // launch_pdl with thread-block clusters of `cluster` CTAs along x
@@ -76,7 +94,10 @@ inline cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid,
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  if (e == cudaSuccess) note_launches();
+  return e;
 }
 
 // ---------------------------------------------------------------------------

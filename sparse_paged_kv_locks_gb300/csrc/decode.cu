@@ -18,6 +18,13 @@
 // split across warps leaves one normalised partial (o, lse) per warp in
 // slot (unit + warp) -- distinct for distinct (unit, warp) pieces because
 // both grow along the positions -- and a second small kernel merges them.
+//
+// Unit form (sparse decode with at least one (sequence, KV head) unit per
+// SM): every unit has exactly k list positions, so one CTA takes one unit,
+// its four warps a quarter of the list each with a three-stage ring (two
+// CTAs per SM: the same 24 pages in flight per SM), and the four partials
+// are merged in shared memory at the end: no partials in the workspace and
+// no merge launch.
 #include "common.cuh"
 #include "launch.h"
 
@@ -35,6 +42,7 @@ constexpr int kDecMinBlocks = 3;
 // merge on GB300: 64 units x 128 pages (G = 8) 17.5 -> 14.0 us, 64 x 64
 // (G = 4) 11.6 -> 10.5 us; 256 x 128 unchanged (already above 8 per warp).
 constexpr int kDecMinRun = 8;
+constexpr int kDecUnitStages = 3;  // unit form: stages per warp
 constexpr float kDecScale = 0.12751743074602467f;  // log2(e)/sqrt(d)
 constexpr float kLn2f = 0.69314718055994531f;
 
@@ -130,8 +138,9 @@ __device__ __forceinline__ Entry resolve(int p, int pe, const Layout &lay,
   return e;
 }
 
-template <bool WIDE>
-__global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
+template <bool WIDE, bool UNIT = false>
+__global__ void __launch_bounds__(kDecThreads,
+                                  UNIT ? 2 : (WIDE ? 2 : kDecMinBlocks))
     decode_kernel(const __nv_bfloat16 *__restrict__ q,
                   const __nv_bfloat16 *__restrict__ k_cache,
                   const __nv_bfloat16 *__restrict__ v_cache, int64_t num_phys,
@@ -143,8 +152,11 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
                   float *__restrict__ lse_out, float *__restrict__ o_part,
                   float *__restrict__ lse_part, int *__restrict__ meta,
                   int32_t *status) {
+  constexpr int STG = UNIT ? kDecUnitStages : kDecStages;
+  constexpr int kWarpRing = STG * 2 * kKvTile;
   extern __shared__ __align__(128) uint8_t smem[];
-  int *s_pre = reinterpret_cast<int *>(smem + kDecRing);  // [batch + 1]
+  int *s_pre =
+      reinterpret_cast<int *>(smem + kDecWarps * kWarpRing);  // [batch + 1]
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int gq = lane >> 2, t4 = lane & 3;
   const int h_q = h_kv * G;
@@ -187,10 +199,20 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
   const int chunk =
       (int)max(1LL, ((long long)total + n_warps - 1) / n_warps);
   const int gw = blockIdx.x * kDecWarps + wid;
-  const bool active = gw < n_warps && (long long)gw * chunk < total;
-  const int pb = active ? gw * chunk : 0, pe = min(total, pb + chunk);
+  bool active;
+  int pb, pe;
+  if constexpr (UNIT) {  // a quarter of unit blockIdx.x's k positions
+    const int u0 = blockIdx.x;
+    pb = u0 * k + wid * k / kDecWarps;
+    pe = u0 * k + (wid + 1) * k / kDecWarps;
+    active = pe > pb;
+  } else {
+    active = gw < n_warps && (long long)gw * chunk < total;
+    pb = active ? gw * chunk : 0;
+    pe = min(total, pb + chunk);
+  }
 
-  uint8_t *wbase = smem + wid * (kDecStages * 2 * kKvTile);
+  uint8_t *wbase = smem + wid * kWarpRing;
   const uint32_t wbase_s = smem_u32(wbase);
 
   // query A fragments (bf16) of unit u, rows = heads of the group
@@ -209,18 +231,19 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
   };
   // the query is an input of the step: fetch it while the selection kernel
   // may still run
-  int cur_u = active ? lay.unit_of(pb) : 0;
+  int cur_u = UNIT ? (int)blockIdx.x : active ? lay.unit_of(pb) : 0;
   if (active) load_q(cur_u);
   // the page lists come from the selection kernel, and the workspace may
   // still be read by it
   pdl_wait();
-  if (blockIdx.x == 0) {  // layout for the merge kernel
+  if (!UNIT && blockIdx.x == 0) {  // layout for the merge kernel
     if (threadIdx.x == 0) meta[0] = chunk;
     if (!idx)
       for (int b = threadIdx.x; b <= batch; b += blockDim.x)
         meta[1 + b] = s_pre[b];
   }
-  if (!active) return;
+  // (unit form: an empty quarter still takes part in the CTA's merge)
+  if (!UNIT && !active) return;
   bool q_ready = true;
 
   // window of 32 positions: this lane's entry and the valid ones not yet
@@ -275,7 +298,7 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
     l8 += __shfl_xor_sync(0xffffffffu, l8, 1);
     l8 += __shfl_xor_sync(0xffffffffu, l8, 2);
     const int2 sp = lay.span(u);
-    const bool whole = sp.x >= pb && sp.y <= pe;
+    const bool whole = !UNIT && sp.x >= pb && sp.y <= pe;
     const int b = u / h_kv, h = u - b * h_kv;
 #pragma unroll
     for (int half = 0; half < (WIDE ? 2 : 1); ++half) {
@@ -294,13 +317,18 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
                 pack_bf2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
           if (t4 == 0) lse_out[row] = lse;
         } else {
-          const size_t slot = ((size_t)u + gw) * G + g;
-          float2 *dst = reinterpret_cast<float2 *>(o_part + slot * kDim);
+          // partial: slot (unit + warp) of the workspace, or (unit form)
+          // row g of this warp's ring region, drained by then
+          float *po = UNIT ? reinterpret_cast<float *>(wbase) + g * kDim
+                           : o_part + (((size_t)u + gw) * G + g) * kDim;
+          float *pl = UNIT ? reinterpret_cast<float *>(wbase) + 16 * kDim + g
+                           : lse_part + ((size_t)u + gw) * G + g;
+          float2 *dst = reinterpret_cast<float2 *>(po);
 #pragma unroll
           for (int nt = 0; nt < 16; ++nt)
             dst[(nt * 8 + 2 * t4) >> 1] =
                 make_float2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
-          if (t4 == 0) lse_part[slot] = lse;
+          if (t4 == 0) *pl = lse;
         }
       }
     }
@@ -322,9 +350,9 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
 
   // pages in flight, oldest first (qp < 0: none); the oldest sits in shared
   // memory stage `st`, the next ones in the stages after it
-  int qp[kDecStages], qn[kDecStages], qu[kDecStages];
+  int qp[STG], qn[STG], qu[STG];
 #pragma unroll
-  for (int i = 0; i < kDecStages; ++i) {
+  for (int i = 0; i < STG; ++i) {
     qn[i] = 0;
     qu[i] = 0;
     next_valid(qp[i], qn[i], qu[i]);
@@ -332,7 +360,7 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
     cp_async_commit();
   }
 
-  for (int st = 0;; st = st + 1 == kDecStages ? 0 : st + 1) {
+  for (int st = 0;; st = st + 1 == STG ? 0 : st + 1) {
     const int phys = qp[0];
     if (phys < 0) break;
     const int ntok = qn[0];
@@ -342,7 +370,7 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
       load_q(cur_u);
       q_ready = true;
     }
-    cp_async_wait<kDecStages - 1>();
+    cp_async_wait<STG - 1>();
     __syncwarp();
     const uint32_t kb_s = wbase_s + st * 2 * kKvTile, vb_s = kb_s + kKvTile;
 
@@ -418,24 +446,74 @@ __global__ void __launch_bounds__(kDecThreads, WIDE ? 2 : kDecMinBlocks)
     }
     __syncwarp();
 #pragma unroll
-    for (int i = 0; i + 1 < kDecStages; ++i) {
+    for (int i = 0; i + 1 < STG; ++i) {
       qp[i] = qp[i + 1];
       qn[i] = qn[i + 1];
       qu[i] = qu[i + 1];
     }
-    qn[kDecStages - 1] = 0;
-    qu[kDecStages - 1] = 0;
-    next_valid(qp[kDecStages - 1], qn[kDecStages - 1], qu[kDecStages - 1]);
-    if (qp[kDecStages - 1] >= 0) issue(st, qp[kDecStages - 1], qu[kDecStages - 1]);
+    qn[STG - 1] = 0;
+    qu[STG - 1] = 0;
+    next_valid(qp[STG - 1], qn[STG - 1], qu[STG - 1]);
+    if (qp[STG - 1] >= 0) issue(st, qp[STG - 1], qu[STG - 1]);
     cp_async_commit();
   }
   cp_async_wait<0>();
-  // close the units up to the one holding the run's last position
-  {
+  __syncwarp();
+  if constexpr (!UNIT) {
+    // close the units up to the one holding the run's last position
     const int u_last = lay.unit_of(pe - 1);
     advance_to(u_last);
     flush(u_last);
+  } else {
+    // the four quarters of unit blockIdx.x, merged row by row: warp w
+    // takes heads w, w + 4, ...; lane l dims 4l .. 4l + 3
+    const int u = (int)blockIdx.x;
+    flush(u);
+    __syncthreads();
+    const int b = u / h_kv, h = u - b * h_kv;
+    for (int g = wid; g < G; g += kDecWarps) {
+      float l[kDecWarps];
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        l[w] = reinterpret_cast<const float *>(smem + w * kWarpRing)[16 * kDim + g];
+        M = fmaxf(M, l[w]);
+      }
+      const size_t row = (size_t)b * h_q + (size_t)h * G + g;
+      uint2 *dst = reinterpret_cast<uint2 *>(o_out + row * kDim) + lane;
+      if (M == -INFINITY) {  // no tokens
+        *dst = make_uint2(0u, 0u);
+        if (lane == 0) lse_out[row] = -INFINITY;
+        continue;
+      }
+      float wsum = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        if (l[w] == -INFINITY) continue;
+        const float f = expf(l[w] - M);
+        const float4 v = reinterpret_cast<const float4 *>(
+            smem + w * kWarpRing)[g * (kDim / 4) + lane];
+        wsum += f;
+        acc.x += f * v.x;
+        acc.y += f * v.y;
+        acc.z += f * v.z;
+        acc.w += f * v.w;
+      }
+      const float inv = 1.f / wsum;
+      *dst = make_uint2(pack_bf2(acc.x * inv, acc.y * inv),
+                        pack_bf2(acc.z * inv, acc.w * inv));
+      if (lane == 0) lse_out[row] = M + logf(wsum);
+    }
   }
+}
+
+// the step's device status word, copied where the host reads it once the
+// decode kernel is done (unit form, which launches no merge kernel)
+__global__ void status_mirror_kernel(const int32_t *__restrict__ src,
+                                     int32_t *dst) {
+  pdl_wait();
+  *dst = *src;
 }
 
 // Merge of the partials of units split across warps; also writes the
@@ -527,6 +605,11 @@ size_t decode_smem_bytes(int batch) {
   return (size_t)kDecRing + sizeof(int) * ((size_t)batch + 1);
 }
 
+static size_t decode_unit_smem_bytes(int batch) {
+  return (size_t)kDecWarps * kDecUnitStages * 2 * kKvTile +
+         sizeof(int) * ((size_t)batch + 1);
+}
+
 int decode_max_batch() {
   return (int)((227 * 1024 - (size_t)kDecRing - 64) / sizeof(int));
 }
@@ -553,6 +636,36 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
   const size_t smem = decode_smem_bytes(batch);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   const int wide = G > 8 ? 1 : 0;
+  auto *qq = static_cast<const __nv_bfloat16 *>(q);
+  auto *kc = static_cast<const __nv_bfloat16 *>(k_cache);
+  auto *vc = static_cast<const __nv_bfloat16 *>(v_cache);
+  auto *oo = static_cast<__nv_bfloat16 *>(o_out);
+  // unit form: sparse decode with every SM holding at least one unit
+  const long long units = (long long)batch * h_kv;
+  if (idx && units >= device_sm_count() && units <= 0x7fffffffLL / kDecWarps) {
+    static DeviceFlags unit_attr;
+    cudaError_t eu = once_per_device(unit_attr, [] {
+      cudaError_t e = cudaFuncSetAttribute(
+          decode_kernel<false, true>,
+          cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      if (e != cudaSuccess) return e;
+      return cudaFuncSetAttribute(decode_kernel<true, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  227 * 1024);
+    });
+    if (eu != cudaSuccess) return eu;
+    const size_t usmem = decode_unit_smem_bytes(batch);
+    if (usmem > 227 * 1024) return cudaErrorInvalidValue;
+    cudaError_t e = launch_pdl(
+        wide ? decode_kernel<true, true> : decode_kernel<false, true>,
+        dim3((unsigned)units), dim3(kDecThreads), usmem, stream, qq, kc, vc,
+        num_phys, pt, seq_lens, idx, k, batch, h_kv, G, max_pages,
+        (int)(units * kDecWarps), oo, lse_out, o_part, lse_part, meta,
+        status);
+    if (e != cudaSuccess || !status_mirror) return e;
+    return launch_pdl(status_mirror_kernel, dim3(1), dim3(1), 0, stream,
+                      (const int32_t *)status, status_mirror);
+  }
   // resident CTAs per SM at the common (small-batch) footprint; a larger
   // batch only lowers the count the hardware actually fits
   const int blocks_per_sm =
@@ -577,10 +690,6 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
   if (warps < 1) warps = 1;
   const int n_warps = (int)warps;
   const int grid = (n_warps + kDecWarps - 1) / kDecWarps;
-  auto *qq = static_cast<const __nv_bfloat16 *>(q);
-  auto *kc = static_cast<const __nv_bfloat16 *>(k_cache);
-  auto *vc = static_cast<const __nv_bfloat16 *>(v_cache);
-  auto *oo = static_cast<__nv_bfloat16 *>(o_out);
   cudaError_t e = launch_pdl(
       wide ? decode_kernel<true> : decode_kernel<false>, dim3(grid),
       dim3(kDecThreads), smem, stream, qq, kc, vc, num_phys, pt, seq_lens,

@@ -42,6 +42,7 @@ struct locks_decoder {
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
   cudaGraphNode_t n_in = nullptr;
+  int graph_kernels = 0;  // kernel nodes of the instantiated step
   int32_t *st_host = nullptr;  // page-locked, one int32
   int32_t *st_map = nullptr;   // its mapped device address
   // host buffers the instantiated graph copies from / to, and their mapped
@@ -102,7 +103,7 @@ locks_status_t enqueue_step(locks_decoder *d, cudaStream_t s,
   const long long n16 = (long long)(d->q_bytes / 16);
   host_in_kernel<<<copy_grid(n16), kCopyThreads, 0, s>>>(
       static_cast<const uint4 *>(q_map), static_cast<uint4 *>(d->q_dev), n16);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = locks::launched();
   if (e != cudaSuccess) return fail(d, e);
   locks_status_t st = locks::score_select(
       d->q_dev, d->summaries, d->seq_lens, d->batch, d->h_q, d->h_kv,
@@ -121,6 +122,7 @@ void drop_graph(locks_decoder *d) {
   d->exec = nullptr;
   d->graph = nullptr;
   d->n_in = nullptr;
+  d->graph_kernels = 0;
 }
 
 // Warm-up run ordered after the caller's stream (first launches set kernel
@@ -171,6 +173,7 @@ locks_status_t record(locks_decoder *d, cudaStream_t caller,
     if (cudaGraphNodeGetType(nodes[i], &t) != cudaSuccess ||
         t != cudaGraphNodeTypeKernel)
       continue;
+    ++d->graph_kernels;
     cudaKernelNodeParams p;
     if (cudaGraphKernelNodeGetParams(nodes[i], &p) != cudaSuccess) continue;
     if (p.func == reinterpret_cast<void *>(host_in_kernel)) d->n_in = nodes[i];
@@ -282,7 +285,10 @@ locks_status_t locks_decoder_step_host(locks_decoder_t *d,
   d->o_map = o_map;
   d->lse_map = lse_map;
   cudaError_t e = cudaGraphLaunch(d->exec, (cudaStream_t)stream);
-  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e == cudaSuccess) {
+    locks::note_launches(d->graph_kernels);
+    e = cudaStreamSynchronize((cudaStream_t)stream);
+  }
   if (e != cudaSuccess) return fail(d, e);
   if (status_out) *status_out = *d->st_host;
   return LOCKS_OK;

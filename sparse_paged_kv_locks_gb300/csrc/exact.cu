@@ -267,7 +267,7 @@ cudaError_t launch_exact(const void *q, const void *k_cache, int64_t num_phys,
     exact_kernel<false><<<grid, kExThreads, smem, stream>>>(
         qq, kc, num_phys, pt, seq_lens, batch, h_kv, G, max_pages, n_warps,
         scores, status);
-  return cudaGetLastError();
+  return launched();
 }
 
 }  // namespace locks

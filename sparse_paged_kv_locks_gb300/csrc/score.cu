@@ -812,7 +812,7 @@ cudaError_t launch_score(const void *q, const void *summaries,
   kern<<<grid, kScoreThreads, smem, stream>>>(qq, ss, seq_lens, batch, h_kv, G,
                                               max_pages, s_hat, status, 0, 0,
                                               nullptr);
-  return cudaGetLastError();
+  return launched();
 }
 
 static_assert(kScoreThreads == kSelThreads,
@@ -901,10 +901,12 @@ cudaError_t launch_score_select_fused(const void *q, const void *summaries,
   cfg.numAttrs = after_query ? 2 : 1;
   auto *qq = static_cast<const __nv_bfloat16 *>(q);
   auto *ss = static_cast<const uint8_t *>(summaries);
-  return cudaLaunchKernelEx(&cfg,
-                            G > 4 ? score_kernel<2, true> : score_kernel<1, true>,
-                            qq, ss, seq_lens, batch, h_kv, G, max_pages, s_hat,
-                            status, after_query ? 1 : 0, k, idx);
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, G > 4 ? score_kernel<2, true> : score_kernel<1, true>, qq, ss,
+      seq_lens, batch, h_kv, G, max_pages, s_hat, status,
+      after_query ? 1 : 0, k, idx);
+  if (e == cudaSuccess) note_launches();
+  return e;
 }
 
 }  // namespace locks

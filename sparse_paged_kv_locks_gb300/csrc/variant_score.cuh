@@ -637,7 +637,7 @@ cudaError_t launch_variant_mode(const void *q, const void *records,
           static_cast<const __nv_bfloat16 *>(q),
           static_cast<const uint8_t *>(records), seq_lens, batch, h_kv, G,
           max_pages, scores, status);
-  return cudaGetLastError();
+  return launched();
 }
 
 template <int R, int VB>

@@ -27,6 +27,12 @@ def test_exports_every_declared_function(L):
 
 def test_record_and_status_strings(L):
     assert B.locks_summary_record_bytes() == 832
+    # rejected calls launch nothing
+    n0 = B.locks_kernel_launches()
+    assert n0 >= 0
+    assert L.locks_score_select(None, None, None, 1, 8, 2, 16, 4, None, None,
+                                0, None) == 1
+    assert B.locks_kernel_launches() == n0
     assert L.locks_status_string(0) == b"ok"
     assert L.locks_status_string(3) == b"workspace too small"
     assert L.locks_last_cuda_error() == 0

@@ -737,6 +737,82 @@ def test_sparse_decode_matches_oracle(G, h_kv, k):
             assert np.abs(lg[b] - rl[b]).max() <= LSE_TOL
 
 
+# at least one (sequence, KV head) unit per SM: sparse decode takes its unit
+# form (a CTA per unit, four warps on a quarter of the list each, merged in
+# shared memory); k not a multiple of 4, k = 3 (an empty quarter), lists
+# with -1 padding, partial pages and empty sequences, G = 16
+@pytest.mark.parametrize("G,k", [(4, 7), (8, 3), (16, 10), (1, 64)])
+def test_decode_unit_form_matches_oracle(G, k):
+    h_kv, batch, n_pages = 4, 40, 24
+    spec = W.custom_spec(batch=batch, h_q=G * h_kv, h_kv=h_kv,
+                         ctx=16 * n_pages, k=k, needles=0, seed=140 + G + k)
+    wl = W.generate(spec, "cpu")
+    kc, vc, pt, _ = host(wl)
+    rng = np.random.default_rng(G * 3 + k)
+    lens = [int(x) for x in rng.integers(1, 16 * n_pages + 1, batch)]
+    lens[0], lens[1], lens[2], lens[3] = 16 * n_pages, 0, 5, 16 * 2 + 9
+    max_pages = pt.shape[1]
+    s_hat = rng.normal(0, 2, (batch, h_kv, G, max_pages))
+    idx_o = O.select_store(s_hat, lens, k)
+    q = wl.queries[0].float().numpy()
+    o_ref, lse_ref = O.sparse_decode(q, kc, vc, pt, lens, idx_o)
+    d = Dev(wl)
+    ws = B.new_workspace(batch, spec.h_q, h_kv, max_pages, k, DEV)
+    o = torch.empty(batch, spec.h_q, 128, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(batch, spec.h_q, dtype=torch.float32, device=DEV)
+    B.locks_sparse_decode(d.queries[0], d.k_cache, d.v_cache, d.page_table,
+                          i32(lens), i32(idx_o), k, o, lse, ws)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == 0
+    og, lg = o.float().cpu().numpy(), lse.cpu().numpy()
+    for b in range(batch):
+        if lens[b] == 0:
+            assert (og[b] == 0).all() and np.isneginf(lg[b]).all()
+            continue
+        assert np.abs(og[b] - o_ref[b]).max() <= O_TOL * np.abs(o_ref[b]).max()
+        assert np.abs(lg[b] - lse_ref[b]).max() <= LSE_TOL
+
+
+def test_native_decoder_unit_form_status():
+    """The host-buffer decoder on 160 (sequence, KV head) units (the unit
+    form of the decode, whose status word reaches the host through its own
+    copy kernel): o and lse equal the eager step's bytes, and a page table
+    entry outside the cache comes back in the step's status."""
+    spec = W.custom_spec(batch=40, h_q=16, h_kv=4, ctx=16 * 20 + 3, k=6,
+                         needles=0, seed=151)
+    wl = W.generate(spec, "cpu", steps=3)
+    d = Dev(wl)
+    batch = wl.page_table.shape[0]
+    lens = [16 * 20 + 3] * batch
+    lens[5] = 0
+    lens_dev = i32(lens)
+    store, _, _, _, _ = gpu_build(d, lens)
+    pt = d.page_table.clone()
+    native = B.LocksDecoder(d.k_cache, d.v_cache, pt, store, spec.h_q,
+                            spec.k, graph=True, seq_lens=lens_dev)
+    eager = B.LocksDecoder(d.k_cache, d.v_cache, pt, store, spec.h_q, spec.k)
+    shape = (batch, spec.h_q, 128)
+    qh = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+    oh = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty(batch, spec.h_q).pin_memory()
+    for step in range(3):
+        if step == 1:        # the recent page of sequence 7: always selected
+            pt[7, 20] = d.k_cache.shape[0] + 11
+        if step == 2:
+            pt[7, 20] = int(d.page_table[7, 20])
+            B.locks_clear_status(native.workspace)
+            B.locks_clear_status(eager.workspace)
+        qh.copy_(wl.queries[step])
+        oe, le = eager.step(qh.to(DEV), lens_dev)
+        torch.cuda.synchronize()
+        _, _, st = native.step_host(qh, lens_dev, oh, lh)
+        assert st == (B.DEV_BAD_PAGE_ID if step == 1 else 0), (step, st)
+        assert st == eager.status()
+        assert torch.equal(oe.cpu(), oh) and torch.equal(le.cpu(), lh)
+        assert (oh[5] == 0).all() and torch.isinf(lh[5]).all()
+    native.close()
+
+
 @pytest.mark.parametrize("G,mode", [(4, "sparse"), (4, "dense"),
                                     (16, "sparse"), (2, "dense")])
 def test_decode_many_short_units(G, mode):
