@@ -261,6 +261,14 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t a) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ float4 ld_cluster_v4f(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
 // every thread of every CTA of the cluster; orders the shared-memory
 // (local and distributed) accesses before it against those after it
 __device__ __forceinline__ void cluster_sync() {

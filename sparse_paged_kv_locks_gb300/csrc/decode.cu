@@ -19,12 +19,13 @@
 // slot (unit + warp) -- distinct for distinct (unit, warp) pieces because
 // both grow along the positions -- and a second small kernel merges them.
 //
-// Unit form (sparse decode with at least one (sequence, KV head) unit per
-// SM): every unit has exactly k list positions, so one CTA takes one unit,
-// its four warps a quarter of the list each with a three-stage ring (two
-// CTAs per SM: the same 24 pages in flight per SM), and the four partials
-// are merged in shared memory at the end: no partials in the workspace and
-// no merge launch.
+// Unit form (sparse decode): every unit has exactly k list positions, so a
+// cluster of C CTAs takes one unit (C = 1 with at least one unit per SM),
+// its 4C warps a slice of the list each with a three-stage ring (two CTAs
+// per SM: the same 24 pages in flight per SM), and the 4C partials are
+// merged at the end in shared memory, across the cluster through
+// distributed shared memory: no partials in the workspace and no merge
+// launch.
 #include "common.cuh"
 #include "launch.h"
 
@@ -43,6 +44,7 @@ constexpr int kDecMinBlocks = 3;
 // (G = 4) 11.6 -> 10.5 us; 256 x 128 unchanged (already above 8 per warp).
 constexpr int kDecMinRun = 8;
 constexpr int kDecUnitStages = 3;  // unit form: stages per warp
+constexpr int kDecClusterMinRun = 4;  // unit form in clusters: positions per warp
 constexpr float kDecScale = 0.12751743074602467f;  // log2(e)/sqrt(d)
 constexpr float kLn2f = 0.69314718055994531f;
 
@@ -201,10 +203,14 @@ __global__ void __launch_bounds__(kDecThreads,
   const int gw = blockIdx.x * kDecWarps + wid;
   bool active;
   int pb, pe;
-  if constexpr (UNIT) {  // a quarter of unit blockIdx.x's k positions
-    const int u0 = blockIdx.x;
-    pb = u0 * k + wid * k / kDecWarps;
-    pe = u0 * k + (wid + 1) * k / kDecWarps;
+  // unit form: CTAs per unit (the cluster) and this CTA's rank in it
+  const int ucl = UNIT ? (int)cluster_nctarank() : 1;
+  const int urank = UNIT && ucl > 1 ? (int)cluster_ctarank() : 0;
+  if constexpr (UNIT) {  // slice urank * 4 + wid of the unit's k positions
+    const int u0 = (int)blockIdx.x / ucl;
+    const int sl = urank * kDecWarps + wid, nsl = ucl * kDecWarps;
+    pb = u0 * k + (int)((long long)sl * k / nsl);
+    pe = u0 * k + (int)((long long)(sl + 1) * k / nsl);
     active = pe > pb;
   } else {
     active = gw < n_warps && (long long)gw * chunk < total;
@@ -231,7 +237,7 @@ __global__ void __launch_bounds__(kDecThreads,
   };
   // the query is an input of the step: fetch it while the selection kernel
   // may still run
-  int cur_u = UNIT ? (int)blockIdx.x : active ? lay.unit_of(pb) : 0;
+  int cur_u = UNIT ? (int)blockIdx.x / ucl : active ? lay.unit_of(pb) : 0;
   if (active) load_q(cur_u);
   // the page lists come from the selection kernel, and the workspace may
   // still be read by it
@@ -465,46 +471,92 @@ __global__ void __launch_bounds__(kDecThreads,
     advance_to(u_last);
     flush(u_last);
   } else {
-    // the four quarters of unit blockIdx.x, merged row by row: warp w
-    // takes heads w, w + 4, ...; lane l dims 4l .. 4l + 3
-    const int u = (int)blockIdx.x;
+    // the 4C slices of the unit, merged row by row: CTA r of the cluster
+    // takes heads r, r + C, ..., warp w of it every fourth of those; lane l
+    // dims 4l .. 4l + 3.  Slice (c, w) is warp w's ring region in CTA c.
+    const int u = (int)blockIdx.x / ucl;
     flush(u);
-    __syncthreads();
+    if (ucl > 1)
+      cluster_sync();
+    else
+      __syncthreads();
     const int b = u / h_kv, h = u - b * h_kv;
-    for (int g = wid; g < G; g += kDecWarps) {
-      float l[kDecWarps];
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) {
-        l[w] = reinterpret_cast<const float *>(smem + w * kWarpRing)[16 * kDim + g];
-        M = fmaxf(M, l[w]);
-      }
+    const int nsl = ucl * kDecWarps;
+    const uint32_t base_s = smem_u32(smem);
+    // shared::cluster address of float `i` of slice s's region
+    auto at = [&](int s2, int i) -> uint32_t {
+      return mapa_shared(
+          base_s + (uint32_t)((s2 % kDecWarps) * kWarpRing + 4 * i),
+          (uint32_t)(s2 / kDecWarps));
+    };
+    constexpr int kMaxSlices = 8 * kDecWarps;  // clusters of up to 8 CTAs
+    for (int g = urank + ucl * wid; g < G; g += ucl * kDecWarps) {
       const size_t row = (size_t)b * h_q + (size_t)h * G + g;
       uint2 *dst = reinterpret_cast<uint2 *>(o_out + row * kDim) + lane;
+      float wsum = 0.f, M = -INFINITY;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ucl == 1) {  // the CTA's own four slices
+        float l[kDecWarps];
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) {
+          l[w] = reinterpret_cast<const float *>(smem + w * kWarpRing)[16 * kDim + g];
+          M = fmaxf(M, l[w]);
+        }
+        if (M > -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kDecWarps; ++w) {
+            if (l[w] == -INFINITY) continue;
+            const float f = expf(l[w] - M);
+            const float4 v = reinterpret_cast<const float4 *>(
+                smem + w * kWarpRing)[g * (kDim / 4) + lane];
+            wsum += f;
+            acc.x += f * v.x;
+            acc.y += f * v.y;
+            acc.z += f * v.z;
+            acc.w += f * v.w;
+          }
+        }
+      } else {  // every slice of the cluster: all loads issued before use
+        float l[kMaxSlices];
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxSlices; ++s2)
+          l[s2] = s2 < nsl ? ld_cluster_f32(at(s2, 16 * kDim + g)) : -INFINITY;
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxSlices; ++s2) M = fmaxf(M, l[s2]);
+        if (M > -INFINITY) {
+#pragma unroll
+          for (int h0 = 0; h0 < kMaxSlices; h0 += 16) {
+            float4 v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              v[j] = h0 + j < nsl && l[h0 + j] > -INFINITY
+                         ? ld_cluster_v4f(at(h0 + j, g * kDim + 4 * lane))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float f =
+                  l[h0 + j] > -INFINITY ? expf(l[h0 + j] - M) : 0.f;
+              wsum += f;
+              acc.x += f * v[j].x;
+              acc.y += f * v[j].y;
+              acc.z += f * v[j].z;
+              acc.w += f * v[j].w;
+            }
+          }
+        }
+      }
       if (M == -INFINITY) {  // no tokens
         *dst = make_uint2(0u, 0u);
         if (lane == 0) lse_out[row] = -INFINITY;
         continue;
-      }
-      float wsum = 0.f;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) {
-        if (l[w] == -INFINITY) continue;
-        const float f = expf(l[w] - M);
-        const float4 v = reinterpret_cast<const float4 *>(
-            smem + w * kWarpRing)[g * (kDim / 4) + lane];
-        wsum += f;
-        acc.x += f * v.x;
-        acc.y += f * v.y;
-        acc.z += f * v.z;
-        acc.w += f * v.w;
       }
       const float inv = 1.f / wsum;
       *dst = make_uint2(pack_bf2(acc.x * inv, acc.y * inv),
                         pack_bf2(acc.z * inv, acc.w * inv));
       if (lane == 0) lse_out[row] = M + logf(wsum);
     }
+    // no CTA leaves while another may still read its slices
+    if (ucl > 1) cluster_sync();
   }
 }
 
@@ -640,9 +692,25 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
   auto *kc = static_cast<const __nv_bfloat16 *>(k_cache);
   auto *vc = static_cast<const __nv_bfloat16 *>(v_cache);
   auto *oo = static_cast<__nv_bfloat16 *>(o_out);
-  // unit form: sparse decode with every SM holding at least one unit
+  // unit form: sparse decode with every SM holding at least one unit, or a
+  // cluster of 8 or 4 CTAs per unit when all of them fit two per SM and
+  // every warp keeps at least kDecClusterMinRun positions.  Graph-replayed
+  // decode on GB300 against the split form and its merge: 64 units x 128
+  // pages (G = 8, clusters of 4) 14.1 -> 12.7 us, 64 x 64 (G = 4, clusters
+  // of 4) 10.5 -> 9.1 us; clusters of 2 lost (11.2 against 10.5 us).
   const long long units = (long long)batch * h_kv;
-  if (idx && units >= device_sm_count() && units <= 0x7fffffffLL / kDecWarps) {
+  const int sms = device_sm_count();
+  int ucl = 0;
+  if (idx && units <= 0x7fffffffLL / (8 * kDecWarps)) {
+    if (units >= sms) {
+      ucl = 1;
+    } else {
+      for (int c = 8; c >= 4 && !ucl; c >>= 1)
+        if (units * c <= 2LL * sms && k >= c * kDecWarps * kDecClusterMinRun)
+          ucl = c;
+    }
+  }
+  if (ucl > 0) {
     static DeviceFlags unit_attr;
     cudaError_t eu = once_per_device(unit_attr, [] {
       cudaError_t e = cudaFuncSetAttribute(
@@ -656,12 +724,19 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
     if (eu != cudaSuccess) return eu;
     const size_t usmem = decode_unit_smem_bytes(batch);
     if (usmem > 227 * 1024) return cudaErrorInvalidValue;
-    cudaError_t e = launch_pdl(
-        wide ? decode_kernel<true, true> : decode_kernel<false, true>,
-        dim3((unsigned)units), dim3(kDecThreads), usmem, stream, qq, kc, vc,
-        num_phys, pt, seq_lens, idx, k, batch, h_kv, G, max_pages,
-        (int)(units * kDecWarps), oo, lse_out, o_part, lse_part, meta,
-        status);
+    auto *ukern = wide ? decode_kernel<true, true> : decode_kernel<false, true>;
+    const dim3 ugrid((unsigned)(units * ucl));
+    const int uwarps = (int)(units * ucl * kDecWarps);
+    cudaError_t e =
+        ucl > 1 ? launch_pdl_cluster(ukern, ugrid, dim3(kDecThreads), usmem,
+                                     stream, ucl, qq, kc, vc, num_phys, pt,
+                                     seq_lens, idx, k, batch, h_kv, G,
+                                     max_pages, uwarps, oo, lse_out, o_part,
+                                     lse_part, meta, status)
+                : launch_pdl(ukern, ugrid, dim3(kDecThreads), usmem, stream,
+                             qq, kc, vc, num_phys, pt, seq_lens, idx, k,
+                             batch, h_kv, G, max_pages, uwarps, oo, lse_out,
+                             o_part, lse_part, meta, status);
     if (e != cudaSuccess || !status_mirror) return e;
     return launch_pdl(status_mirror_kernel, dim3(1), dim3(1), 0, stream,
                       (const int32_t *)status, status_mirror);

@@ -741,16 +741,26 @@ def test_sparse_decode_matches_oracle(G, h_kv, k):
 # form (a CTA per unit, four warps on a quarter of the list each, merged in
 # shared memory); k not a multiple of 4, k = 3 (an empty quarter), lists
 # with -1 padding, partial pages and empty sequences, G = 16
-@pytest.mark.parametrize("G,k", [(4, 7), (8, 3), (16, 10), (1, 64)])
-def test_decode_unit_form_matches_oracle(G, k):
-    h_kv, batch, n_pages = 4, 40, 24
+# (fewer units than SMs: clusters of 4 or 8 CTAs per unit, the partials
+# merged across the cluster; too few positions per warp: the split form
+# and its merge)
+@pytest.mark.parametrize("G,k,batch", [(4, 7, 40), (8, 3, 40), (16, 10, 40),
+                                       (1, 64, 40), (4, 64, 3), (8, 128, 16),
+                                       (16, 128, 5), (2, 256, 2), (4, 32, 3),
+                                       (4, 40, 16), (2, 16, 3)])
+def test_decode_unit_form_matches_oracle(G, k, batch):
+    h_kv, n_pages = 4, max(24, k + 8)
     spec = W.custom_spec(batch=batch, h_q=G * h_kv, h_kv=h_kv,
                          ctx=16 * n_pages, k=k, needles=0, seed=140 + G + k)
     wl = W.generate(spec, "cpu")
     kc, vc, pt, _ = host(wl)
     rng = np.random.default_rng(G * 3 + k)
     lens = [int(x) for x in rng.integers(1, 16 * n_pages + 1, batch)]
-    lens[0], lens[1], lens[2], lens[3] = 16 * n_pages, 0, 5, 16 * 2 + 9
+    lens[0] = 16 * n_pages
+    if batch > 1:
+        lens[1] = 0
+    if batch > 3:
+        lens[2], lens[3] = 5, 16 * 2 + 9
     max_pages = pt.shape[1]
     s_hat = rng.normal(0, 2, (batch, h_kv, G, max_pages))
     idx_o = O.select_store(s_hat, lens, k)
