@@ -44,7 +44,7 @@ constexpr int kDecMinBlocks = 3;
 // (G = 4) 11.6 -> 10.5 us; 256 x 128 unchanged (already above 8 per warp).
 constexpr int kDecMinRun = 8;
 constexpr int kDecUnitStages = 3;  // unit form: stages per warp
-constexpr int kDecClusterMinRun = 4;  // unit form in clusters: positions per warp
+constexpr int kDecClusterMinRun = 1;  // unit form in clusters: positions per warp
 constexpr float kDecScale = 0.12751743074602467f;  // log2(e)/sqrt(d)
 constexpr float kLn2f = 0.69314718055994531f;
 
@@ -694,10 +694,12 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
   auto *oo = static_cast<__nv_bfloat16 *>(o_out);
   // unit form: sparse decode with every SM holding at least one unit, or a
   // cluster of 8 or 4 CTAs per unit when all of them fit two per SM and
-  // every warp keeps at least kDecClusterMinRun positions.  Graph-replayed
-  // decode on GB300 against the split form and its merge: 64 units x 128
-  // pages (G = 8, clusters of 4) 14.1 -> 12.7 us, 64 x 64 (G = 4, clusters
-  // of 4) 10.5 -> 9.1 us; clusters of 2 lost (11.2 against 10.5 us).
+  // every warp has a list position.  Graph-replayed decode on GB300 against
+  // the split form and its merge: 64 units x 128 pages (G = 8, clusters of
+  // 4) 14.1 -> 12.7 us, 64 x 64 (G = 4, clusters of 4) 10.5 -> 9.1 us,
+  // 2 x 16 (clusters of 4, one page per warp) 6.7 -> 6.3 us and the whole
+  // step 19.7 -> 17.5 us (no merge launch on the chain); clusters of 2 lost
+  // (11.2 against 10.5 us).
   const long long units = (long long)batch * h_kv;
   const int sms = device_sm_count();
   int ucl = 0;
