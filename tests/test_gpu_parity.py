@@ -783,18 +783,20 @@ def test_decode_unit_form_matches_oracle(G, k, batch):
         assert np.abs(lg[b] - lse_ref[b]).max() <= LSE_TOL
 
 
-def test_native_decoder_unit_form_status():
-    """The host-buffer decoder on 160 (sequence, KV head) units (the unit
-    form of the decode, whose status word reaches the host through its own
-    copy kernel): o and lse equal the eager step's bytes, and a page table
-    entry outside the cache comes back in the step's status."""
-    spec = W.custom_spec(batch=40, h_q=16, h_kv=4, ctx=16 * 20 + 3, k=6,
-                         needles=0, seed=151)
+@pytest.mark.parametrize("batch,h_kv,k", [(40, 4, 6), (4, 2, 16)])
+def test_native_decoder_unit_form_status(batch, h_kv, k):
+    """The host-buffer decoder with the decode's unit form (160 units: a CTA
+    per unit; 8 units of 16 list positions: clusters of 4 CTAs), whose
+    status word reaches the host through its own copy kernel: o and lse
+    equal the eager step's bytes, and a page table entry outside the cache
+    comes back in the step's status."""
+    spec = W.custom_spec(batch=batch, h_q=4 * h_kv, h_kv=h_kv,
+                         ctx=16 * 20 + 3, k=k, needles=0, seed=151 + batch)
     wl = W.generate(spec, "cpu", steps=3)
     d = Dev(wl)
-    batch = wl.page_table.shape[0]
     lens = [16 * 20 + 3] * batch
-    lens[5] = 0
+    empty, bad = (5, 7) if batch > 7 else (batch - 1, 1)
+    lens[empty] = 0
     lens_dev = i32(lens)
     store, _, _, _, _ = gpu_build(d, lens)
     pt = d.page_table.clone()
@@ -806,10 +808,10 @@ def test_native_decoder_unit_form_status():
     oh = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
     lh = torch.empty(batch, spec.h_q).pin_memory()
     for step in range(3):
-        if step == 1:        # the recent page of sequence 7: always selected
-            pt[7, 20] = d.k_cache.shape[0] + 11
+        if step == 1:        # the recent page of sequence `bad`: always selected
+            pt[bad, 20] = d.k_cache.shape[0] + 11
         if step == 2:
-            pt[7, 20] = int(d.page_table[7, 20])
+            pt[bad, 20] = int(d.page_table[bad, 20])
             B.locks_clear_status(native.workspace)
             B.locks_clear_status(eager.workspace)
         qh.copy_(wl.queries[step])
@@ -819,7 +821,7 @@ def test_native_decoder_unit_form_status():
         assert st == (B.DEV_BAD_PAGE_ID if step == 1 else 0), (step, st)
         assert st == eager.status()
         assert torch.equal(oe.cpu(), oh) and torch.equal(le.cpu(), lh)
-        assert (oh[5] == 0).all() and torch.isinf(lh[5]).all()
+        assert (oh[empty] == 0).all() and torch.isinf(lh[empty]).all()
     native.close()
 
 
