@@ -657,9 +657,10 @@ size_t decode_smem_bytes(int batch) {
   return (size_t)kDecRing + sizeof(int) * ((size_t)batch + 1);
 }
 
-static size_t decode_unit_smem_bytes(int batch) {
-  return (size_t)kDecWarps * kDecUnitStages * 2 * kKvTile +
-         sizeof(int) * ((size_t)batch + 1);
+// the unit form keeps only the warps' rings (no per-sequence table: it is
+// sparse decode only), so its footprint does not grow with the batch
+static size_t decode_unit_smem_bytes() {
+  return (size_t)kDecWarps * kDecUnitStages * 2 * kKvTile;
 }
 
 int decode_max_batch() {
@@ -724,8 +725,7 @@ cudaError_t launch_decode(const void *q, const void *k_cache,
                                   227 * 1024);
     });
     if (eu != cudaSuccess) return eu;
-    const size_t usmem = decode_unit_smem_bytes(batch);
-    if (usmem > 227 * 1024) return cudaErrorInvalidValue;
+    const size_t usmem = decode_unit_smem_bytes();
     auto *ukern = wide ? decode_kernel<true, true> : decode_kernel<false, true>;
     const dim3 ugrid((unsigned)(units * ucl));
     const int uwarps = (int)(units * ucl * kDecWarps);
