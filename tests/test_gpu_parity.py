@@ -1192,6 +1192,45 @@ def test_device_status_flags():
     assert B.locks_read_status(ws) == B.DEV_BAD_PAGE_ID
 
 
+@pytest.mark.parametrize("batch,k", [(2, 16), (160, 4)])
+def test_device_status_flags_unit_form(batch, k):
+    """The same data errors through the decode's unit form (2 units of 16
+    list positions: clusters of 4 CTAs; 160 units: a CTA per unit): a
+    selected page outside the sequence, a length above the page table, a
+    page table entry outside the cache; the step still finishes."""
+    spec = W.custom_spec(batch=batch, h_q=4, h_kv=1, ctx=16 * 20, k=k,
+                         needles=0, seed=5)
+    wl = W.generate(spec, "cpu")
+    d = Dev(wl)
+    max_pages = wl.page_table.shape[1]
+    P = d.k_cache.shape[0]
+    ws = B.new_workspace(batch, 4, 1, max_pages, max_pages, DEV)
+    o = torch.empty(batch, 4, 128, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(batch, 4, dtype=torch.float32, device=DEV)
+    good = np.tile(np.arange(k, dtype=np.int32), (batch, 1, 1))
+    idx = good.copy()
+    idx[0, 0, 1] = 50                          # beyond the 20 pages
+    B.locks_sparse_decode(d.queries[0], d.k_cache, d.v_cache, d.page_table,
+                          d.seq_lens, i32(idx), k, o, lse, ws)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == B.DEV_BAD_INDEX
+    B.locks_clear_status(ws)
+    long = d.seq_lens.clone()
+    long[batch - 1] = 16 * max_pages + 1
+    B.locks_sparse_decode(d.queries[0], d.k_cache, d.v_cache, d.page_table,
+                          long, i32(good), k, o, lse, ws)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) & B.DEV_BAD_SEQ_LEN
+    B.locks_clear_status(ws)
+    bad_pt = d.page_table.clone()
+    bad_pt[batch - 1, 2] = P + 5
+    B.locks_sparse_decode(d.queries[0], d.k_cache, d.v_cache, bad_pt,
+                          d.seq_lens, i32(good), k, o, lse, ws)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == B.DEV_BAD_PAGE_ID
+    assert torch.isfinite(lse).all()
+
+
 def test_native_decoder_status_wide_group_and_empty_sequence():
     """The host-buffer decoder with a group of 16 query heads: an empty
     sequence gives o = 0 and lse = -inf, a page table entry outside the
