@@ -70,7 +70,11 @@ typedef struct CUstream_st *locks_stream_t; /* same type as cudaStream_t */
 typedef enum {
   LOCKS_OK = 0,
   LOCKS_ERR_INVALID_ARG = 1, /* null pointer, bad size, k < 2, ...      */
-  LOCKS_ERR_UNSUPPORTED = 2, /* G outside 1..16, size above a limit      */
+  LOCKS_ERR_UNSUPPORTED = 2, /* G outside 1..16, size above a limit:
+                                batch above 1594 for the scoring and
+                                selection calls (their per-sequence tables
+                                sit on chip beside the summary ring),
+                                above 41712 for sparse decode           */
   LOCKS_ERR_WORKSPACE = 3,   /* workspace smaller than locks_workspace_size */
   LOCKS_ERR_CUDA = 4         /* a CUDA call failed: locks_last_cuda_error */
 } locks_status_t;

@@ -100,6 +100,16 @@ def test_host_validation_before_launch(L):
     assert L.locks_decoder_step_host(None, fake, fake, fake, None, s) == 1
     assert L.locks_decoder_last_cuda_error(None) == 0
     L.locks_decoder_destroy(None)
+    # batch limits (per-sequence tables on chip): refused above them, the
+    # argument checks go on below them (here: the workspace is too small)
+    assert L.locks_score_select(fake, fake, fake, 1595, 8, 2, 16, 4, fake,
+                                fake, 64, s) == 2
+    assert L.locks_score_select(fake, fake, fake, 1594, 8, 2, 16, 4, fake,
+                                fake, 64, s) == 3
+    assert L.locks_sparse_decode(fake, fake, fake, 10, fake, fake, fake, 4,
+                                 41713, 8, 2, 16, fake, fake, fake, 64, s) == 2
+    assert L.locks_sparse_decode(fake, fake, fake, 10, fake, fake, fake, 4,
+                                 41712, 8, 2, 16, fake, fake, fake, 64, s) == 3
     # empty batches launch nothing and succeed
     assert L.locks_score_select(None, None, None, 0, 8, 2, 16, 4, None, None,
                                 0, s) == 0

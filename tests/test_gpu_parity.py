@@ -825,6 +825,55 @@ def test_native_decoder_unit_form_status(batch, h_kv, k):
     native.close()
 
 
+def test_step_at_the_largest_batch():
+    """The step at the scoring and selection calls' batch limit (1594
+    sequences, whose per-sequence tables fill the on-chip space beside the
+    summary ring): scores from the oracle's records against the oracle on
+    every page, selections within the 1e-3 window, outputs of the decode's
+    unit form (1594 units) against the oracle's attention over the GPU's
+    selection."""
+    batch, G, k = 1594, 4, 3
+    spec = W.custom_spec(batch=batch, h_q=G, h_kv=1, ctx=16 * 5 + 7, k=k,
+                         needles=0, seed=1594)
+    wl = W.generate(spec, "cpu", steps=1)
+    kc, vc, pt, _ = host(wl)
+    rng = np.random.default_rng(1594)
+    lens = [int(x) for x in rng.integers(16 * 4, 16 * 5 + 8, batch)]
+    max_pages = pt.shape[1]
+    seq, pg = full_pairs(lens)
+    store, _ = O.build_summaries(kc, pt, seq, pg, batch, max_pages)
+    q = wl.queries[0]
+    st = torch.from_numpy(store).to(DEV)
+    ws = B.new_workspace(batch, G, 1, max_pages, k, DEV)
+    idx = torch.zeros(batch, 1, k, dtype=torch.int32, device=DEV)
+    B.locks_score_select(q.to(DEV), st, i32(lens), k, idx, ws)
+    n = batch * G * max_pages
+    sc = ws[256:256 + 4 * n].view(torch.float32).view(batch, 1, G,
+                                                      max_pages).clone()
+    d = Dev(wl)
+    o = torch.empty(batch, G, 128, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(batch, G, dtype=torch.float32, device=DEV)
+    B.locks_sparse_decode(d.queries[0], d.k_cache, d.v_cache, d.page_table,
+                          i32(lens), idx, k, o, lse, ws)
+    torch.cuda.synchronize()
+    assert B.locks_read_status(ws) == 0
+    s_orc = O.score_store(q.float().numpy(), store, lens)
+    s_gpu = sc.cpu().numpy()
+    full = ~np.isnan(s_orc)
+    assert np.abs(s_gpu[full] - s_orc[full]).max() <= S_TOL
+    ig = idx.cpu().numpy()
+    io = O.select_store(s_orc, lens, k)
+    for b in range(batch):
+        ok, _ = selection_agrees(ig[b, 0], io[b, 0], s_orc[b, 0], lens[b], k,
+                                 1e-3)
+        assert ok, (b, ig[b, 0], io[b, 0])
+    o_ref, lse_ref = O.sparse_decode(q.float().numpy(), kc, vc, pt, lens, ig)
+    og, lg = o.float().cpu().numpy(), lse.cpu().numpy()
+    scale = np.abs(o_ref).max(axis=(1, 2))
+    assert (np.abs(og - o_ref).max(axis=(1, 2)) <= O_TOL * scale).all()
+    assert np.abs(lg - lse_ref).max() <= LSE_TOL
+
+
 @pytest.mark.parametrize("G,mode", [(4, "sparse"), (4, "dense"),
                                     (16, "sparse"), (2, "dense")])
 def test_decode_many_short_units(G, mode):
