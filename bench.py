@@ -885,11 +885,11 @@ def run_locks(args):
         step(i)
     torch.cuda.synchronize()
     assert B.locks_read_status(ws) == 0, "decode reported a device error"
-    # per-kernel events on every fourth timed step: an event between two
+    # per-kernel events on every sixteenth timed step: an event between two
     # kernels stops the second from launching early (programmatic
     # dependent launch), so the other steps run with none, as a step does
     # in production
-    EV_EVERY = 4
+    EV_EVERY = 16
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
            if i % EV_EVERY == 0 else None for i in range(args.steps)]
     clocks = ClockSampler(torch.cuda.current_device())
